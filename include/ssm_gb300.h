@@ -1,0 +1,164 @@
+/*
+ * ssm_gb300.h -- C ABI of the GB300 (sm_103a) Mamba-1 selective-scan library.
+ *
+ * The library computes the hot path of the Mamba-1 (S6) block described by the
+ * CPU reference src/training/mamba1_cpu.ts (page "@seanhogg/builderforce-memory-
+ * engine 2026.7.12 -> 2026.9.27"): the selective scan forward (mamba1CpuForward
+ * steps 8-9) and backward (mamba1CpuBackward steps 9-8), and the causal
+ * depthwise conv1d + SiLU (forward steps 4-5, backward steps 5-4), plus the
+ * primitives of src/training/cpu_ops.ts they use (softplus, silu, sigmoid).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout (the pages' "Layout conventions"): activations are row-major
+ *    (M, width) with M = batch*seqlen and row r = b*seqlen + t.  Every
+ *    activation tensor has its own row stride (ld_*, in ELEMENTS), so column
+ *    slices of a wider projection (x | z of in_proj, dt | B | C of x_proj) are
+ *    passed as base pointer + row stride, without a copy.  A stride of 0 means
+ *    "packed" (dinner for (M, dinner) tensors, dstate for (M, dstate) tensors).
+ *  - Ownership: the caller allocates and owns every buffer (inputs, outputs,
+ *    saved context, workspace).  The library never allocates or frees memory.
+ *    All pointers are DEVICE pointers unless stated otherwise.
+ *  - Asynchrony: every call validates its arguments on the host, then enqueues
+ *    its kernels on `stream` and returns; results are ready when the stream
+ *    reaches that point.  Calls on one stream are ordered.
+ *  - Errors: arguments are validated on the host before anything is launched;
+ *    any status other than SSM_OK means NOTHING was enqueued, except
+ *    SSM_ERR_LAUNCH, which reports a failed launch (cudaGetLastError) and may
+ *    leave outputs partially written.  No kernel traps or asserts.
+ *  - Outputs and gradients are WRITTEN, not accumulated.  (The pages add
+ *    parameter gradients into a caller-owned accumulator; adding is the
+ *    caller's job here.)
+ *  - Alignment: every pointer to an (M, dinner) activation must be 16-byte
+ *    aligned and its row stride times the element size must be a multiple of
+ *    16 bytes; otherwise SSM_ERR_ALIGN.  B/C (and dB/dC) and the fp32
+ *    parameter vectors need only natural alignment.
+ *  - Arithmetic: fp32 state and accumulation in every case; SSM_BF16 changes
+ *    only the storage type of the activations and their gradients (rounded to
+ *    nearest even from fp32).
+ */
+#ifndef SSM_GB300_H
+#define SSM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSM_GB300_ABI_VERSION 1
+#define SSM_MAX_DSTATE 16
+
+typedef enum ssm_status {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,       /* a required pointer is NULL */
+    SSM_ERR_SHAPE = 2,      /* a size or stride is out of range */
+    SSM_ERR_ALIGN = 3,      /* a pointer or row stride breaks the alignment rule */
+    SSM_ERR_DTYPE = 4,      /* unknown dtype or discretisation */
+    SSM_ERR_WORKSPACE = 5,  /* context or workspace smaller than required */
+    SSM_ERR_LAUNCH = 6,     /* a kernel launch failed (see ssm_last_cuda_error) */
+    SSM_ERR_DEVICE = 7      /* the current device is not an sm_103 GPU */
+} ssm_status;
+
+/* Storage type of the activations and their gradients. */
+typedef enum ssm_dtype { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Discretisation of B (the input matrix).
+ *  SSM_DISC_EULER: beta = delta * B          -> h_t = exp(delta A) h_{t-1} + delta B_t u_t
+ *  SSM_DISC_ZOH:   beta = (exp(delta A) - 1) / A * B, as mamba1_cpu.ts step 8
+ *                  writes it (evaluated without cancellation for small delta*A). */
+typedef enum ssm_disc { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_disc;
+
+/* Shape, types and row strides of one selective-scan problem.
+ *   u, delta_raw, z, out, dout, du, ddelta_raw, dz : (M, dinner), dtype
+ *   B, C, dB, dC                                   : (M, dstate), dtype
+ *   A_log : (dinner, dstate) fp32, packed;  D : (dinner) fp32
+ * 0 <= dstate <= 16.  batch, seqlen or dinner may be 0 (empty problem). */
+typedef struct ssm_scan_desc {
+    int32_t batch, seqlen, dinner, dstate;
+    int32_t dtype;  /* ssm_dtype */
+    int32_t disc;   /* ssm_disc  */
+    int64_t ld_u, ld_delta, ld_z, ld_B, ld_C, ld_out;
+    int64_t ld_dout, ld_du, ld_ddelta, ld_dz, ld_dB, ld_dC;
+} ssm_scan_desc;
+
+/* Bytes of the saved context that ssm_scan_fwd writes for ssm_scan_bwd: the
+ * fp32 scan state h at every chunk boundary (the backward recomputes h inside
+ * each chunk instead of reading an (M, dinner, dstate) history). */
+size_t ssm_scan_ctx_bytes(const ssm_scan_desc* desc);
+
+/* Bytes of device scratch that ssm_scan_fwd / ssm_scan_bwd need. */
+size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);
+size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* desc);
+
+/* Selective scan forward (mamba1_cpu.ts mamba1CpuForward steps 8-9):
+ *   delta = softplus(delta_raw)                        (cpu_ops.ts softplus)
+ *   A     = -exp(clamp(A_log, -10, 5))                 (A_LOG_CLAMP_LO/HI)
+ *   h_t   = exp(delta_t A) * h_{t-1} + beta_t * u_t,   h_{-1} = 0 per batch row
+ *   y_t   = sum_n C_t[n] h_t[n] + D * u_t
+ *   out_t = y_t * silu(z_t)     (or y_t when z == NULL: no gate)
+ * D may be NULL (no skip term).  ctx may be NULL (inference: nothing saved);
+ * otherwise it must hold ssm_scan_ctx_bytes(desc) bytes and is read by
+ * ssm_scan_bwd.  workspace must hold ssm_scan_fwd_workspace_bytes(desc)
+ * (may be NULL when that is 0). */
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
+                        const void* u, const void* delta_raw, const float* A_log,
+                        const void* B, const void* C, const float* D, const void* z,
+                        void* out, void* ctx, size_t ctx_bytes,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Selective scan backward (mamba1_cpu.ts mamba1CpuBackward steps 9-8), given
+ * dout = dL/dout and the context of the matching ssm_scan_fwd call (same
+ * inputs).  Writes
+ *   du, ddelta_raw, dz (M, dinner) dtype;  dB, dC (M, dstate) dtype;
+ *   dA_log (dinner, dstate) fp32 -- exactly 0 where A_log <= -10 or >= 5;
+ *   dD (dinner) fp32 (may be NULL when D is NULL).
+ * dz is required iff z != NULL.  workspace must hold
+ * ssm_scan_bwd_workspace_bytes(desc) bytes. */
+ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
+                        const void* u, const void* delta_raw, const float* A_log,
+                        const void* B, const void* C, const float* D, const void* z,
+                        const void* dout, const void* ctx, size_t ctx_bytes,
+                        void* du, void* ddelta_raw, float* dA_log, void* dB, void* dC,
+                        float* dD, void* dz,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Causal depthwise conv1d + SiLU (mamba1_cpu.ts forward steps 4-5):
+ *   out[r, d] = silu(bias[d] + sum_{k < kconv, t >= k} w[d*kconv + k] * x[r - k, d])
+ * x and out are (M, dinner) fp32 with row strides ld_x, ld_out (0 = packed);
+ * w is (dinner, kconv) fp32 with tap k = 0 on the CURRENT step (the reverse of
+ * torch.nn.Conv1d's weight order); bias (dinner) fp32 may be NULL.
+ * 1 <= kconv <= 8. */
+ssm_status ssm_conv1d_silu(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                           const float* x, int64_t ld_x, const float* w, const float* bias,
+                           float* out, int64_t ld_out, cudaStream_t stream);
+
+/* Backward of ssm_conv1d_silu (mamba1_cpu.ts backward steps 5-4): given
+ * dout = dL/d(out) (ld_dout), writes dx (ld_dx), dw (dinner, kconv) and dbias
+ * (dinner; may be NULL).  workspace must hold
+ * ssm_conv1d_silu_bwd_workspace_bytes(...) bytes. */
+size_t ssm_conv1d_silu_bwd_workspace_bytes(int32_t batch, int32_t seqlen, int32_t dinner,
+                                           int32_t kconv);
+ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                               const float* x, int64_t ld_x, const float* w, const float* bias,
+                               const float* dout, int64_t ld_dout,
+                               float* dx, int64_t ld_dx, float* dw, float* dbias,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* ssm_status_string(ssm_status status);
+
+/* The cudaError_t of the most recent SSM_ERR_LAUNCH / SSM_ERR_DEVICE on the
+ * calling thread (cudaSuccess if none). */
+int ssm_last_cuda_error(void);
+
+/* SSM_GB300_ABI_VERSION of the built library. */
+int ssm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_GB300_H */

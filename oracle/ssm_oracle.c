@@ -1,0 +1,529 @@
+/*
+ * ssm_oracle.c -- plain, slow, sequential fp64 CPU oracle for the Mamba-1 (S6)
+ * selective scan, its causal depthwise conv1d+SiLU, and the whole Mamba-1 block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * Source of every formula: the page "@seanhogg/builderforce-memory-engine
+ * 2026.7.12 -> 2026.9.27" (diff of src/training/mamba1_cpu.ts) and the page
+ * "@seanhogg/builderforce-memory-engine 2026.7.14 -> 2026.9.28" (diff of
+ * src/training/cpu_ops.ts).  Section names below refer to those files:
+ *   cpu_ops.ts      sigmoid / silu / siluGrad / softplus / linearForward /
+ *                   linearBackward / rmsNormForward / rmsNormBackward
+ *   mamba1_cpu.ts   mamba1CpuForward steps 1-11, mamba1CpuBackward steps 11-1,
+ *                   A_LOG_CLAMP_LO / A_LOG_CLAMP_HI.
+ *
+ * Layouts (the pages' convention): activations are row-major (M, width) with
+ * M = batch*seqlen and row r = b*seqlen + t.  A_log is (dinner, dstate).
+ *
+ * Readings where the pages leave a step open:
+ *   - disc = 0 ("Euler" B): beta = delta*B, the form h_t = a*h_{t-1} + delta*B*u
+ *     of the simplified S6 recurrence.  disc = 1 ("ZOH" B): beta =
+ *     (exp(delta*A) - 1)/A * B exactly as mamba1_cpu.ts step 8 writes it, with
+ *     exp(x) - 1 evaluated by expm1 so the fp64 value is not cancelled away.
+ *   - The scan gate z is optional (NULL = no gate); the pages gate separately.
+ *   - Gradients are WRITTEN (zeroed first, then summed); the pages add into a
+ *     caller-owned accumulator, which is the same thing from zero.
+ *
+ * Loop order: the scan is walked one (batch row, channel) chain at a time
+ * (b -> d -> t -> n).  The pages walk b -> t -> d -> n with a full (M, D, N)
+ * cache; the chains of different channels never interact, and every sum over
+ * d (dB, dC), over (b, t) (dA_log, dD) or over n (y) is taken in the same
+ * index order as the pages' loops, so the results are the same numbers.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define A_LOG_CLAMP_LO (-10.0)  /* mamba1_cpu.ts A_LOG_CLAMP_LO */
+#define A_LOG_CLAMP_HI (5.0)    /* mamba1_cpu.ts A_LOG_CLAMP_HI */
+#define RMSNORM_EPS (1e-6)      /* cpu_ops.ts RMSNORM_EPS */
+
+/* ---------------- cpu_ops.ts scalar primitives ---------------- */
+
+static double sigmoid_(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double silu_(double x) { return x / (1.0 + exp(-x)); }
+static double silu_grad_(double x) {
+    double s = sigmoid_(x);
+    return s * (1.0 + x * (1.0 - s));
+}
+/* max(x,0) + log1p(exp(-|x|)); no threshold branch (cpu_ops.ts softplus). */
+static double softplus_(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+
+/* A = -exp(clamp(A_log, LO, HI))  (mamba1_cpu.ts step 8, aCont). */
+static double a_cont_(double a_log) {
+    double c = a_log < A_LOG_CLAMP_LO ? A_LOG_CLAMP_LO : a_log;
+    c = c > A_LOG_CLAMP_HI ? A_LOG_CLAMP_HI : c;
+    return -exp(c);
+}
+
+/* Discretisation of one (t, d, n) element and its partial derivatives.
+ *   a    = exp(dt*A)
+ *   bcoef = beta/B: dt (Euler) or expm1(dt*A)/A (ZOH)
+ *   da_ddt, da_dA            partials of a
+ *   db_ddt, db_dA            partials of beta/B (multiply by B for beta)   */
+typedef struct { double a, bcoef, da_ddt, da_dA, db_ddt, db_dA; } disc_t;
+
+static disc_t discretise_(double dt, double A, int zoh) {
+    disc_t r;
+    r.a = exp(dt * A);
+    r.da_ddt = A * r.a;
+    r.da_dA = dt * r.a;
+    if (zoh) {
+        double em1 = expm1(dt * A);
+        r.bcoef = em1 / A;
+        r.db_ddt = r.a;                                  /* d/d dt of (e^{dt A}-1)/A */
+        r.db_dA = (dt * r.a * A - em1) / (A * A);        /* d/dA, mamba1_cpu.ts backward */
+    } else {
+        r.bcoef = dt;
+        r.db_ddt = 1.0;
+        r.db_dA = 0.0;
+    }
+    return r;
+}
+
+/* ---------------- one chain of the selective scan ---------------- */
+
+/*
+ * Forward (and optionally backward) of one (batch row b, channel d) chain over
+ * all seqlen steps and all dstate states: mamba1_cpu.ts step 8 (scan) and
+ * step 9 (gate) forward, and steps 9 and 8 of the backward.
+ *
+ * Inputs are strided views: element t of u/dt_raw/z/dout is at [t*ld], element
+ * (t, n) of B/C is at [t*ldbc + n].  A_log points at the channel's dstate row.
+ * Forward outputs (length seqlen, stride ld, each may be NULL): out (gated),
+ * y (pre-gate).  If dout != NULL the backward runs too: du, ddt_raw, dz (stride ld,
+ * WRITTEN; dz only if z != NULL), and dA_log (dstate), dD (1), dB/dC
+ * (seqlen x dstate, stride ldbc) are ADDED INTO.
+ * Returns 0, or -1 if scratch allocation fails.
+ */
+int ssm_oracle_scan_chain(int seqlen, int dstate, int disc,
+                          const double* u, const double* dt_raw, const double* A_log,
+                          const double* B, const double* C, double Dskip,
+                          const double* z, long ld, long ldbc,
+                          double* out, double* y,
+                          const double* dout, double* du, double* ddt_raw, double* dz,
+                          double* dA_log, double* dD, double* dB, double* dC) {
+    const int L = seqlen, N = dstate, zoh = (disc == 1);
+    double* h = (double*)calloc((size_t)L * N, sizeof(double));      /* h_t for every t */
+    double* A = (double*)malloc((size_t)N * sizeof(double));
+    double* ys = (double*)malloc((size_t)L * sizeof(double));
+    double* dh_next = (double*)calloc((size_t)N, sizeof(double));
+    double* dA_acc = (double*)calloc((size_t)N, sizeof(double));
+    if (!h || !A || !ys || !dh_next || !dA_acc) {
+        free(h); free(A); free(ys); free(dh_next); free(dA_acc);
+        return -1;
+    }
+    for (int n = 0; n < N; ++n) A[n] = a_cont_(A_log[n]);
+
+    /* forward: h_t = a*h_{t-1} + beta*u_t ; y_t = sum_n C h + D u ; out = y*silu(z) */
+    for (int t = 0; t < L; ++t) {
+        double dv = softplus_(dt_raw[t * ld]);
+        double uv = u[t * ld];
+        double acc = Dskip * uv;
+        for (int n = 0; n < N; ++n) {
+            disc_t q = discretise_(dv, A[n], zoh);
+            double hprev = (t == 0) ? 0.0 : h[(size_t)(t - 1) * N + n];
+            double hv = q.a * hprev + q.bcoef * B[t * ldbc + n] * uv;
+            h[(size_t)t * N + n] = hv;
+            acc += C[t * ldbc + n] * hv;
+        }
+        ys[t] = acc;
+        if (y) y[t * ld] = acc;
+        if (out) out[t * ld] = z ? acc * silu_(z[t * ld]) : acc;
+    }
+
+    if (dout) {
+        /* backward, walked from t = L-1 down to 0; dh after the last step is 0 */
+        for (int t = L - 1; t >= 0; --t) {
+            double g = dout[t * ld];
+            double dy = z ? g * silu_(z[t * ld]) : g;
+            if (z) dz[t * ld] = g * ys[t] * silu_grad_(z[t * ld]);
+            double xr = dt_raw[t * ld];
+            double dv = softplus_(xr);
+            double uv = u[t * ld];
+            *dD += dy * uv;                        /* skip connection */
+            double du_acc = dy * Dskip;
+            double ddv = 0.0;
+            for (int n = 0; n < N; ++n) {
+                disc_t q = discretise_(dv, A[n], zoh);
+                double bv = B[t * ldbc + n];
+                double hv = h[(size_t)t * N + n];
+                double hprev = (t == 0) ? 0.0 : h[(size_t)(t - 1) * N + n];
+                dC[t * ldbc + n] += dy * hv;        /* y = sum_n C h */
+                double dh = dy * C[t * ldbc + n] + dh_next[n];
+                double d_abar = dh * hprev;          /* h = abar*hprev + bbar*u */
+                double d_bbar = dh * uv;
+                du_acc += dh * q.bcoef * bv;
+                dh_next[n] = dh * q.a;
+                ddv += d_abar * q.da_ddt + d_bbar * bv * q.db_ddt;
+                dA_acc[n] += d_abar * q.da_dA + d_bbar * bv * q.db_dA;
+                dB[t * ldbc + n] += d_bbar * q.bcoef;
+            }
+            du[t * ld] = du_acc;
+            ddt_raw[t * ld] = ddv * sigmoid_(xr);   /* softplus' = sigmoid */
+        }
+        /* dA/dA_log = A inside the clamp, exactly 0 at or beyond its bounds */
+        for (int n = 0; n < N; ++n) {
+            double al = A_log[n];
+            if (al <= A_LOG_CLAMP_LO || al >= A_LOG_CLAMP_HI) continue;
+            dA_log[n] += dA_acc[n] * A[n];
+        }
+    }
+    free(h); free(A); free(ys); free(dh_next); free(dA_acc);
+    return 0;
+}
+
+/* Whole scan forward: every chain.  u, dt_raw, z, out, y are (M, dinner);
+ * B, C are (M, dstate); A_log (dinner, dstate); Dv (dinner).  z, y may be NULL. */
+int ssm_oracle_scan_fwd(int batch, int seqlen, int dinner, int dstate, int disc,
+                        const double* u, const double* dt_raw, const double* A_log,
+                        const double* B, const double* C, const double* Dv,
+                        const double* z, double* out, double* y) {
+    for (int b = 0; b < batch; ++b) {
+        size_t r0 = (size_t)b * seqlen;
+        for (int d = 0; d < dinner; ++d) {
+            size_t o = r0 * dinner + d;
+            int rc = ssm_oracle_scan_chain(seqlen, dstate, disc, u + o, dt_raw + o,
+                                           A_log + (size_t)d * dstate, B + r0 * dstate,
+                                           C + r0 * dstate, Dv[d], z ? z + o : NULL,
+                                           dinner, dstate, out + o, y ? y + o : NULL,
+                                           NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
+            if (rc) return rc;
+        }
+    }
+    return 0;
+}
+
+/* Whole scan backward (the forward is recomputed inside).  Every gradient is
+ * written: du, ddt_raw, dz (M, dinner); dA_log (dinner, dstate); dB, dC
+ * (M, dstate); dD (dinner).  dz is untouched when z == NULL. */
+int ssm_oracle_scan_bwd(int batch, int seqlen, int dinner, int dstate, int disc,
+                        const double* u, const double* dt_raw, const double* A_log,
+                        const double* B, const double* C, const double* Dv,
+                        const double* z, const double* dout,
+                        double* du, double* ddt_raw, double* dA_log, double* dB,
+                        double* dC, double* dD, double* dz) {
+    size_t M = (size_t)batch * seqlen;
+    memset(dA_log, 0, (size_t)dinner * dstate * sizeof(double));
+    memset(dB, 0, M * dstate * sizeof(double));
+    memset(dC, 0, M * dstate * sizeof(double));
+    memset(dD, 0, (size_t)dinner * sizeof(double));
+    for (int b = 0; b < batch; ++b) {
+        size_t r0 = (size_t)b * seqlen;
+        for (int d = 0; d < dinner; ++d) {
+            size_t o = r0 * dinner + d;
+            int rc = ssm_oracle_scan_chain(seqlen, dstate, disc, u + o, dt_raw + o,
+                                           A_log + (size_t)d * dstate, B + r0 * dstate,
+                                           C + r0 * dstate, Dv[d], z ? z + o : NULL,
+                                           dinner, dstate, NULL, NULL,
+                                           dout + o, du + o, ddt_raw + o, z ? dz + o : NULL,
+                                           dA_log + (size_t)d * dstate, dD + d,
+                                           dB + r0 * dstate, dC + r0 * dstate);
+            if (rc) return rc;
+        }
+    }
+    return 0;
+}
+
+/* ---------------- causal depthwise conv1d + SiLU ---------------- */
+
+/* mamba1_cpu.ts steps 4-5: pre[r,d] = bias[d] + sum_{k<K, t>=k} w[d*K+k] * x[r-k, d]
+ * (tap k = 0 is the current step), out = silu(pre).  x, out, pre are (M, dinner)
+ * with row stride ld; pre may be NULL. */
+int ssm_oracle_conv1d_silu_fwd(int batch, int seqlen, int dinner, int kconv, long ld,
+                               const double* x, const double* w, const double* bias,
+                               double* out, double* pre) {
+    for (int b = 0; b < batch; ++b)
+        for (int t = 0; t < seqlen; ++t) {
+            size_t r = (size_t)b * seqlen + t;
+            for (int d = 0; d < dinner; ++d) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int k = 0; k < kconv; ++k)
+                    if (t >= k) acc += w[(size_t)d * kconv + k] * x[(r - k) * ld + d];
+                if (pre) pre[r * ld + d] = acc;
+                out[r * ld + d] = silu_(acc);
+            }
+        }
+    return 0;
+}
+
+/* mamba1_cpu.ts backward steps 5-4.  dout is dL/d(silu output).  dx (M, dinner)
+ * is written; dw (dinner, kconv) and dbias (dinner) are written (from zero). */
+int ssm_oracle_conv1d_silu_bwd(int batch, int seqlen, int dinner, int kconv, long ld,
+                               const double* x, const double* w, const double* bias,
+                               const double* dout, double* dx, double* dw, double* dbias) {
+    size_t M = (size_t)batch * seqlen;
+    for (size_t r = 0; r < M; ++r)
+        for (int d = 0; d < dinner; ++d) dx[r * ld + d] = 0.0;
+    memset(dw, 0, (size_t)dinner * kconv * sizeof(double));
+    if (dbias) memset(dbias, 0, (size_t)dinner * sizeof(double));
+    for (int b = 0; b < batch; ++b)
+        for (int t = 0; t < seqlen; ++t) {
+            size_t r = (size_t)b * seqlen + t;
+            for (int d = 0; d < dinner; ++d) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int k = 0; k < kconv; ++k)
+                    if (t >= k) acc += w[(size_t)d * kconv + k] * x[(r - k) * ld + d];
+                double g = dout[r * ld + d] * silu_grad_(acc);
+                if (dbias) dbias[d] += g;
+                for (int k = 0; k < kconv; ++k) {
+                    if (t < k) continue;
+                    dw[(size_t)d * kconv + k] += g * x[(r - k) * ld + d];
+                    dx[(r - k) * ld + d] += g * w[(size_t)d * kconv + k];
+                }
+            }
+        }
+    return 0;
+}
+
+/* ---------------- the whole Mamba-1 block ---------------- */
+
+/* cpu_ops.ts linearForward: Y (M,Nout) = X (M,K) W^T + b, W (Nout,K). */
+static void linear_fwd_(const double* X, const double* W, const double* b,
+                        size_t M, int K, int Nout, double* Y) {
+    for (size_t r = 0; r < M; ++r)
+        for (int n = 0; n < Nout; ++n) {
+            double acc = b ? b[n] : 0.0;
+            const double* xr = X + r * K;
+            const double* wn = W + (size_t)n * K;
+            for (int k = 0; k < K; ++k) acc += xr[k] * wn[k];
+            Y[r * Nout + n] = acc;
+        }
+}
+
+/* cpu_ops.ts linearBackward: dX written; dW, db added into. */
+static void linear_bwd_(const double* dY, const double* X, const double* W,
+                        size_t M, int K, int Nout, double* dX, double* dW, double* db) {
+    memset(dX, 0, M * K * sizeof(double));
+    for (size_t r = 0; r < M; ++r)
+        for (int n = 0; n < Nout; ++n) {
+            double g = dY[r * Nout + n];
+            if (g == 0.0) continue;
+            db[n] += g;
+            const double* xr = X + r * K;
+            const double* wn = W + (size_t)n * K;
+            double* dxr = dX + r * K;
+            double* dwn = dW + (size_t)n * K;
+            for (int k = 0; k < K; ++k) {
+                dxr[k] += g * wn[k];
+                dwn[k] += g * xr[k];
+            }
+        }
+}
+
+/* cpu_ops.ts rmsNormForward: inv = 1/sqrt(mean(x^2)+eps); y = x*inv*w. */
+static void rmsnorm_fwd_(const double* x, const double* w, size_t M, int Dm,
+                         double* y, double* inv) {
+    for (size_t r = 0; r < M; ++r) {
+        double sq = 0.0;
+        for (int i = 0; i < Dm; ++i) sq += x[r * Dm + i] * x[r * Dm + i];
+        double iv = 1.0 / sqrt(sq / Dm + RMSNORM_EPS);
+        inv[r] = iv;
+        for (int i = 0; i < Dm; ++i) y[r * Dm + i] = x[r * Dm + i] * iv * w[i];
+    }
+}
+
+/* cpu_ops.ts rmsNormBackward: dx and dw added into. */
+static void rmsnorm_bwd_(const double* dY, const double* x, const double* w, const double* inv,
+                         size_t M, int Dm, double* dx, double* dw) {
+    for (size_t r = 0; r < M; ++r) {
+        double iv = inv[r], dot = 0.0;
+        for (int i = 0; i < Dm; ++i) {
+            double g = dY[r * Dm + i] * w[i];
+            dot += g * x[r * Dm + i];
+            dw[i] += dY[r * Dm + i] * x[r * Dm + i] * iv;
+        }
+        double scale = iv * iv * iv / Dm;
+        for (int i = 0; i < Dm; ++i) {
+            double g = dY[r * Dm + i] * w[i];
+            dx[r * Dm + i] += g * iv - scale * dot * x[r * Dm + i];
+        }
+    }
+}
+
+/* Block weights, in the pages' parameter order (mamba1_cpu.ts Mamba1CpuWeights). */
+typedef struct {
+    const double *wInProj, *bInProj, *wConv, *bConv, *wXProj, *bXProj,
+                 *wDtProj, *bDtProj, *A_log, *D_vec, *wOutProj, *bOutProj, *normWeight;
+} ssm_oracle_block_weights;
+typedef struct {
+    double *wInProj, *bInProj, *wConv, *bConv, *wXProj, *bXProj,
+           *wDtProj, *bDtProj, *A_log, *D_vec, *wOutProj, *bOutProj, *normWeight;
+} ssm_oracle_block_grads;
+typedef struct { int dmodel, dstate, dconv, dinner, dtrank, batch, seqlen; } ssm_oracle_block_dims;
+
+/* Forward activations kept for the backward (mamba1_cpu.ts Mamba1CpuCache,
+ * minus the (M, D, N) arrays, which the chain routine recomputes). */
+typedef struct {
+    double *normInv, *normOut, *inProj, *xConvIn, *z, *convOut, *u, *xProj,
+           *dtRaw, *bRaw, *cRaw, *deltaFull, *scanY, *gated;
+} block_cache_;
+
+static void free_cache_(block_cache_* c) {
+    free(c->normInv); free(c->normOut); free(c->inProj); free(c->xConvIn); free(c->z);
+    free(c->convOut); free(c->u); free(c->xProj); free(c->dtRaw); free(c->bRaw);
+    free(c->cRaw); free(c->deltaFull); free(c->scanY); free(c->gated);
+}
+
+static int block_forward_(const ssm_oracle_block_dims* dm, int disc, const double* x,
+                          const ssm_oracle_block_weights* w, double* output, block_cache_* c) {
+    const int Dm = dm->dmodel, N = dm->dstate, K = dm->dconv, D = dm->dinner, R = dm->dtrank;
+    const int B = dm->batch, L = dm->seqlen;
+    const size_t M = (size_t)B * L;
+    const int P = R + 2 * N;
+    c->normInv = malloc(M * sizeof(double));
+    c->normOut = malloc(M * Dm * sizeof(double));
+    c->inProj = malloc(M * 2 * D * sizeof(double));
+    c->xConvIn = malloc(M * D * sizeof(double));
+    c->z = malloc(M * D * sizeof(double));
+    c->convOut = malloc(M * D * sizeof(double));
+    c->u = malloc(M * D * sizeof(double));
+    c->xProj = malloc(M * P * sizeof(double));
+    c->dtRaw = malloc(M * R * sizeof(double));
+    c->bRaw = malloc(M * N * sizeof(double));
+    c->cRaw = malloc(M * N * sizeof(double));
+    c->deltaFull = malloc(M * D * sizeof(double));
+    c->scanY = malloc(M * D * sizeof(double));
+    c->gated = malloc(M * D * sizeof(double));
+    if (!c->normInv || !c->normOut || !c->inProj || !c->xConvIn || !c->z || !c->convOut ||
+        !c->u || !c->xProj || !c->dtRaw || !c->bRaw || !c->cRaw || !c->deltaFull ||
+        !c->scanY || !c->gated) {
+        free_cache_(c);
+        return -1;
+    }
+    /* 1. RMSNorm  2. in_proj  3. column split (x, z) */
+    rmsnorm_fwd_(x, w->normWeight, M, Dm, c->normOut, c->normInv);
+    linear_fwd_(c->normOut, w->wInProj, w->bInProj, M, Dm, 2 * D, c->inProj);
+    for (size_t r = 0; r < M; ++r)
+        for (int d = 0; d < D; ++d) {
+            c->xConvIn[r * D + d] = c->inProj[r * 2 * D + d];
+            c->z[r * D + d] = c->inProj[r * 2 * D + D + d];
+        }
+    /* 4. causal depthwise conv1d  5. SiLU */
+    ssm_oracle_conv1d_silu_fwd(B, L, D, K, D, c->xConvIn, w->wConv, w->bConv, c->u, c->convOut);
+    /* 6. x_proj -> (dt_raw | B | C) column slices  7. dt_proj */
+    linear_fwd_(c->u, w->wXProj, w->bXProj, M, D, P, c->xProj);
+    for (size_t r = 0; r < M; ++r) {
+        for (int i = 0; i < R; ++i) c->dtRaw[r * R + i] = c->xProj[r * P + i];
+        for (int n = 0; n < N; ++n) {
+            c->bRaw[r * N + n] = c->xProj[r * P + R + n];
+            c->cRaw[r * N + n] = c->xProj[r * P + R + N + n];
+        }
+    }
+    linear_fwd_(c->dtRaw, w->wDtProj, w->bDtProj, M, R, D, c->deltaFull);
+    /* 8-9. selective scan with the SiLU(z) gate */
+    int rc = ssm_oracle_scan_fwd(B, L, D, N, disc, c->u, c->deltaFull, w->A_log, c->bRaw,
+                                 c->cRaw, w->D_vec, c->z, c->gated, c->scanY);
+    if (rc) { free_cache_(c); return rc; }
+    /* 10. out_proj  11. residual */
+    linear_fwd_(c->gated, w->wOutProj, w->bOutProj, M, D, Dm, output);
+    for (size_t i = 0; i < M * Dm; ++i) output[i] += x[i];
+    return 0;
+}
+
+/* Block forward: output (M, dmodel) = block(x). */
+int ssm_oracle_block_fwd(const ssm_oracle_block_dims* dm, int disc, const double* x,
+                         const ssm_oracle_block_weights* w, double* output) {
+    block_cache_ c;
+    int rc = block_forward_(dm, disc, x, w, output, &c);
+    if (rc) return rc;
+    free_cache_(&c);
+    return 0;
+}
+
+/* Block backward (forward recomputed inside).  dx (M, dmodel) and every
+ * parameter gradient are written (from zero). */
+int ssm_oracle_block_bwd(const ssm_oracle_block_dims* dm, int disc, const double* x,
+                         const ssm_oracle_block_weights* w, const double* dout,
+                         double* dx, ssm_oracle_block_grads* g) {
+    const int Dm = dm->dmodel, N = dm->dstate, K = dm->dconv, D = dm->dinner, R = dm->dtrank;
+    const int B = dm->batch, L = dm->seqlen;
+    const size_t M = (size_t)B * L;
+    const int P = R + 2 * N;
+    double* output = malloc(M * Dm * sizeof(double));
+    if (!output) return -1;
+    block_cache_ c;
+    int rc = block_forward_(dm, disc, x, w, output, &c);
+    free(output);
+    if (rc) return rc;
+
+    memset(g->wInProj, 0, (size_t)2 * D * Dm * sizeof(double));
+    memset(g->bInProj, 0, (size_t)2 * D * sizeof(double));
+    memset(g->wConv, 0, (size_t)D * K * sizeof(double));
+    memset(g->bConv, 0, (size_t)D * sizeof(double));
+    memset(g->wXProj, 0, (size_t)P * D * sizeof(double));
+    memset(g->bXProj, 0, (size_t)P * sizeof(double));
+    memset(g->wDtProj, 0, (size_t)D * R * sizeof(double));
+    memset(g->bDtProj, 0, (size_t)D * sizeof(double));
+    memset(g->A_log, 0, (size_t)D * N * sizeof(double));
+    memset(g->D_vec, 0, (size_t)D * sizeof(double));
+    memset(g->wOutProj, 0, (size_t)Dm * D * sizeof(double));
+    memset(g->bOutProj, 0, (size_t)Dm * sizeof(double));
+    memset(g->normWeight, 0, (size_t)Dm * sizeof(double));
+
+    double* dGated = malloc(M * D * sizeof(double));
+    double* du = malloc(M * D * sizeof(double));
+    double* dDelta = malloc(M * D * sizeof(double));
+    double* dz = malloc(M * D * sizeof(double));
+    double* dBr = malloc(M * N * sizeof(double));
+    double* dCr = malloc(M * N * sizeof(double));
+    double* dDtRaw = malloc(M * R * sizeof(double));
+    double* dXProj = malloc(M * P * sizeof(double));
+    double* duX = malloc(M * D * sizeof(double));
+    double* dXConvIn = malloc(M * D * sizeof(double));
+    double* dInProj = malloc(M * 2 * D * sizeof(double));
+    double* dNormOut = malloc(M * Dm * sizeof(double));
+    double* tw = malloc((size_t)D * K * sizeof(double));
+    double* tb = malloc((size_t)D * sizeof(double));
+    rc = -1;
+    if (!dGated || !du || !dDelta || !dz || !dBr || !dCr || !dDtRaw || !dXProj || !duX ||
+        !dXConvIn || !dInProj || !dNormOut || !tw || !tb)
+        goto done;
+
+    /* 11. residual: dx starts as dout */
+    memcpy(dx, dout, M * Dm * sizeof(double));
+    /* 10. out_proj */
+    linear_bwd_(dout, c.gated, w->wOutProj, M, D, Dm, dGated, g->wOutProj, g->bOutProj);
+    /* 9-8. gate and selective scan (dt_raw here is deltaFull) */
+    rc = ssm_oracle_scan_bwd(B, L, D, N, disc, c.u, c.deltaFull, w->A_log, c.bRaw, c.cRaw,
+                             w->D_vec, c.z, dGated, du, dDelta, g->A_log, dBr, dCr,
+                             g->D_vec, dz);
+    if (rc) goto done;
+    /* 7. dt_proj */
+    linear_bwd_(dDelta, c.dtRaw, w->wDtProj, M, R, D, dDtRaw, g->wDtProj, g->bDtProj);
+    /* 6. x_proj: reassemble the column slices, one linear backward */
+    for (size_t r = 0; r < M; ++r) {
+        for (int i = 0; i < R; ++i) dXProj[r * P + i] = dDtRaw[r * R + i];
+        for (int n = 0; n < N; ++n) {
+            dXProj[r * P + R + n] = dBr[r * N + n];
+            dXProj[r * P + R + N + n] = dCr[r * N + n];
+        }
+    }
+    linear_bwd_(dXProj, c.u, w->wXProj, M, D, P, duX, g->wXProj, g->bXProj);
+    for (size_t i = 0; i < M * D; ++i) du[i] += duX[i];
+    /* 5-4. SiLU and the causal conv */
+    rc = ssm_oracle_conv1d_silu_bwd(B, L, D, K, D, c.xConvIn, w->wConv, w->bConv, du,
+                                    dXConvIn, tw, tb);
+    if (rc) goto done;
+    for (int i = 0; i < D * K; ++i) g->wConv[i] += tw[i];
+    for (int i = 0; i < D; ++i) g->bConv[i] += tb[i];
+    /* 3. un-split (x, z)  2. in_proj */
+    for (size_t r = 0; r < M; ++r)
+        for (int d = 0; d < D; ++d) {
+            dInProj[r * 2 * D + d] = dXConvIn[r * D + d];
+            dInProj[r * 2 * D + D + d] = dz[r * D + d];
+        }
+    linear_bwd_(dInProj, c.normOut, w->wInProj, M, Dm, 2 * D, dNormOut, g->wInProj, g->bInProj);
+    /* 1. RMSNorm, added into the residual gradient */
+    rmsnorm_bwd_(dNormOut, x, w->normWeight, c.normInv, M, Dm, dx, g->normWeight);
+    rc = 0;
+done:
+    free(dGated); free(du); free(dDelta); free(dz); free(dBr); free(dCr); free(dDtRaw);
+    free(dXProj); free(duX); free(dXConvIn); free(dInProj); free(dNormOut); free(tw); free(tb);
+    free_cache_(&c);
+    return rc;
+}
