@@ -114,7 +114,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc,
  * inputs).  Writes
  *   du, ddelta_raw, dz (M, dinner) dtype;  dB, dC (M, dstate) dtype;
  *   dA_log (dinner, dstate) fp32 -- exactly 0 where A_log <= -10 or >= 5;
- *   dD (dinner) fp32 (may be NULL when D is NULL).
+ *   dD (dinner) fp32 (may be NULL: not written).
  * dz is required iff z != NULL.  workspace must hold
  * ssm_scan_bwd_workspace_bytes(desc) bytes. */
 ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
@@ -156,6 +156,14 @@ int ssm_last_cuda_error(void);
 
 /* SSM_GB300_ABI_VERSION of the built library. */
 int ssm_abi_version(void);
+
+/* Fault bits recorded by the kernels since the last call, then cleared:
+ * every wait of a kernel on an asynchronous copy is bounded, and a wait that
+ * gives up sets a bit here (1: forward copy wait, 2: backward copy wait,
+ * 4: drain after a failed wait) instead of hanging; that call's outputs are
+ * then invalid.  Synchronous: call it after the work has completed.  Returns
+ * 0 when no sm_103 device is current. */
+unsigned ssm_device_faults(void);
 
 #ifdef __cplusplus
 }

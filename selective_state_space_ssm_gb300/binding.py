@@ -23,6 +23,7 @@ __all__ = [
     "ssm_scan_ctx_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv1d_silu", "ssm_conv1d_silu_bwd",
     "ssm_conv1d_silu_bwd_workspace_bytes", "ssm_status_string", "ssm_abi_version",
+    "ssm_device_faults",
     "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "EXPORTED_SYMBOLS",
 ]
 
@@ -38,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "ssm_scan_ctx_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv1d_silu", "ssm_conv1d_silu_bwd_workspace_bytes",
     "ssm_conv1d_silu_bwd", "ssm_status_string", "ssm_last_cuda_error", "ssm_abi_version",
+    "ssm_device_faults",
 )
 
 
@@ -77,8 +79,11 @@ def load():
             "ssm_scan_ctx_bytes": (sz, [dp]),
             "ssm_scan_fwd_workspace_bytes": (sz, [dp]),
             "ssm_scan_bwd_workspace_bytes": (sz, [dp]),
-            "ssm_scan_fwd": (ctypes.c_int, [dp] + [vp] * 8 + [sz, vp, sz, vp]),
-            "ssm_scan_bwd": (ctypes.c_int, [dp] + [vp] * 9 + [sz] + [vp] * 8 + [vp, sz, vp]),
+            # desc, u, delta_raw, A_log, B, C, D, z, out, ctx | ctx_bytes | ws, ws_bytes, stream
+            "ssm_scan_fwd": (ctypes.c_int, [dp] + [vp] * 9 + [sz, vp, sz, vp]),
+            # desc, u, delta_raw, A_log, B, C, D, z, dout, ctx | ctx_bytes |
+            # du, ddelta_raw, dA_log, dB, dC, dD, dz, ws | ws_bytes | stream
+            "ssm_scan_bwd": (ctypes.c_int, [dp] + [vp] * 9 + [sz] + [vp] * 8 + [sz, vp]),
             "ssm_conv1d_silu": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp, vp, i64, vp]),
             "ssm_conv1d_silu_bwd_workspace_bytes": (sz, [i32, i32, i32, i32]),
             "ssm_conv1d_silu_bwd": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp, vp, i64,
@@ -86,6 +91,7 @@ def load():
             "ssm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "ssm_last_cuda_error": (ctypes.c_int, []),
             "ssm_abi_version": (ctypes.c_int, []),
+            "ssm_device_faults": (ctypes.c_uint, []),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -114,7 +120,7 @@ def _check(fn, status):
 
 
 def _ld(t):
-    if t is None:
+    if t is None or t.numel() == 0:
         return 0
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError("activations must be 2-D with unit column stride")
@@ -203,6 +209,10 @@ def ssm_status_string(status: int) -> str:
 
 def ssm_abi_version() -> int:
     return load().ssm_abi_version()
+
+
+def ssm_device_faults() -> int:
+    return load().ssm_device_faults()
 
 
 # ----------------------------------------------------------------- allocating helpers

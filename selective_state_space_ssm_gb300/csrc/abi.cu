@@ -1,0 +1,485 @@
+// abi.cu -- the extern "C" entry points of libssm_gb300 (declared in
+// include/ssm_gb300.h): host-side argument validation, TMA descriptor
+// encoding, workspace layout and kernel launches.  Nothing here allocates
+// device memory; every buffer belongs to the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "conv_args.cuh"
+#include "scan_args.cuh"
+#include "ssm_gb300.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ssm_status fail_cuda(cudaError_t e, ssm_status s = SSM_ERR_LAUNCH) {
+    g_last_cuda_error = static_cast<int>(e);
+    return s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// ---- device check: the kernels are built for sm_103a only
+ssm_status check_device() {
+    static std::mutex mu;
+    static int cached[64];   // 0 unknown, 1 ok, 2 wrong arch
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, SSM_ERR_DEVICE);
+    if (dev < 0 || dev >= 64) return SSM_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return fail_cuda(e, SSM_ERR_DEVICE);
+        cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return cached[dev] == 1 ? SSM_OK : SSM_ERR_DEVICE;
+}
+
+// ---- TMA descriptors, encoded through the runtime's driver entry point (the
+// library does not link libcuda, so it loads on machines without a driver).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// (M, dinner) activation viewed as [batch][seqlen][dinner] with row stride ld;
+// box = 32 channels x box_rows steps x 1 batch row; out-of-range reads fill 0.
+bool encode_act(CUtensorMap* m, const void* ptr, int dtype, int dinner, int seqlen, int batch,
+                int64_t ld, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const size_t es = dtype == SSM_BF16 ? 2 : 4;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(dinner), static_cast<cuuint64_t>(seqlen),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es,
+                             static_cast<cuuint64_t>(ld) * es * static_cast<cuuint64_t>(seqlen)};
+    cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(m, dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ---- descriptor validation
+struct Lds {
+    int64_t u, delta, z, B, C, out, dout, du, ddelta, dz, dB, dC;
+};
+
+int64_t pick(int64_t ld, int64_t packed) { return ld == 0 ? packed : ld; }
+
+ssm_status validate(const ssm_scan_desc* d, Lds& r) {
+    if (!d) return SSM_ERR_NULL;
+    if (d->batch < 0 || d->seqlen < 0 || d->dinner < 0 || d->dstate < 0 ||
+        d->dstate > SSM_MAX_DSTATE)
+        return SSM_ERR_SHAPE;
+    if (d->dtype != SSM_F32 && d->dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (d->disc != SSM_DISC_EULER && d->disc != SSM_DISC_ZOH) return SSM_ERR_DTYPE;
+    const int64_t D = d->dinner, N = d->dstate;
+    r.u = pick(d->ld_u, D);
+    r.delta = pick(d->ld_delta, D);
+    r.z = pick(d->ld_z, D);
+    r.out = pick(d->ld_out, D);
+    r.dout = pick(d->ld_dout, D);
+    r.du = pick(d->ld_du, D);
+    r.ddelta = pick(d->ld_ddelta, D);
+    r.dz = pick(d->ld_dz, D);
+    r.B = pick(d->ld_B, N);
+    r.C = pick(d->ld_C, N);
+    r.dB = pick(d->ld_dB, N);
+    r.dC = pick(d->ld_dC, N);
+    const int64_t acts[] = {r.u, r.delta, r.z, r.out, r.dout, r.du, r.ddelta, r.dz};
+    for (int64_t v : acts)
+        if (v < D || v > (int64_t(1) << 31)) return SSM_ERR_SHAPE;
+    const int64_t bcs[] = {r.B, r.C, r.dB, r.dC};
+    for (int64_t v : bcs)
+        if (v < N || v > (int64_t(1) << 31)) return SSM_ERR_SHAPE;
+    // every flat index must fit comfortably in 64 bits and TMA coordinates in int32
+    if (static_cast<int64_t>(d->batch) * d->seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    const int64_t es = d->dtype == SSM_BF16 ? 2 : 4;
+    if ((D * es) % 16 != 0) return SSM_ERR_ALIGN;
+    for (int64_t v : acts)
+        if ((v * es) % 16 != 0) return SSM_ERR_ALIGN;
+    return SSM_OK;
+}
+
+int nt_of(int dstate) { return dstate <= 8 ? 8 : 16; }
+int64_t nchunks_of(int seqlen) { return (static_cast<int64_t>(seqlen) + ssm::kChunk - 1) / ssm::kChunk; }
+int64_t nck_of(int seqlen) { return seqlen > 0 ? nchunks_of(seqlen) - 1 : 0; }
+
+// Saved context: fp32 checkpoints [batch][nck][NT][dinner], then the pre-gate
+// y (M, dinner) in the activation dtype (read by the backward for dz).
+size_t ctx_ck_bytes(const ssm_scan_desc* d) {
+    return static_cast<size_t>(d->batch) * nck_of(d->seqlen) * nt_of(d->dstate) * d->dinner *
+           sizeof(float);
+}
+size_t ctx_y_offset(const ssm_scan_desc* d) { return align256(ctx_ck_bytes(d)); }
+size_t ctx_total_bytes(const ssm_scan_desc* d) {
+    const size_t es = d->dtype == SSM_BF16 ? 2 : 4;
+    return ctx_y_offset(d) + static_cast<size_t>(d->batch) * d->seqlen * d->dinner * es;
+}
+
+bool encode_ck(CUtensorMap* m, const void* ptr, int dinner, int64_t rows, int nt) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(dinner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(dinner) * 4};
+    cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(nt)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// (M, dstate) B or C viewed as [batch][seqlen][dstate]; box = NT states x
+// box_rows steps (states past dstate read as 0).
+bool encode_bc(CUtensorMap* m, const void* ptr, int dtype, int dstate, int seqlen, int batch,
+               int64_t ld, int nt, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const size_t es = dtype == SSM_BF16 ? 2 : 4;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(dstate), static_cast<cuuint64_t>(seqlen),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es,
+                             static_cast<cuuint64_t>(ld) * es * static_cast<cuuint64_t>(seqlen)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(nt), static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+              3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// B and C travel by TMA when both rows start on 16-byte boundaries; otherwise
+// the kernels read them with plain loads.
+bool bc_tma_ok(const ssm_scan_desc* d, const void* B, const void* C, int64_t ldB, int64_t ldC) {
+    const int64_t es = d->dtype == SSM_BF16 ? 2 : 4;
+    return d->dstate > 0 && B && C && aligned16(B) && aligned16(C) && (ldB * es) % 16 == 0 &&
+           (ldC * es) % 16 == 0;
+}
+
+struct BwdLayout {
+    int cluster, ncl;
+    size_t off_bc, off_dA, off_dD, total;
+};
+
+BwdLayout bwd_layout(const ssm_scan_desc* d) {
+    BwdLayout l{};
+    const int64_t tiles = (static_cast<int64_t>(d->dinner) + 31) / 32;
+    l.cluster = tiles >= ssm::kBwdCluster ? ssm::kBwdCluster : 1;
+    l.ncl = static_cast<int>((tiles + l.cluster - 1) / l.cluster);
+    const size_t M = static_cast<size_t>(d->batch) * d->seqlen;
+    const size_t NT = nt_of(d->dstate);
+    l.off_bc = 0;
+    l.off_dA = align256(static_cast<size_t>(l.ncl) * M * 2 * NT * sizeof(float));
+    l.off_dD = l.off_dA + align256(static_cast<size_t>(d->batch) * d->dinner * NT * sizeof(float));
+    l.total = l.off_dD + align256(static_cast<size_t>(d->batch) * d->dinner * sizeof(float));
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_ctx_bytes(const ssm_scan_desc* d) {
+    Lds r;
+    if (validate(d, r) != SSM_OK) return 0;
+    return ctx_total_bytes(d);
+}
+
+size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
+    (void)d;
+    return 0;
+}
+
+size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
+    Lds r;
+    if (validate(d, r) != SSM_OK) return 0;
+    return bwd_layout(d).total;
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                        const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, void* out, void* ctx, size_t ctx_bytes, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    Lds r;
+    ssm_status st = validate(d, r);
+    if (st != SSM_OK) return st;
+    const int64_t M = static_cast<int64_t>(d->batch) * d->seqlen;
+    if (M == 0 || d->dinner == 0) return SSM_OK;
+    if (!u || !delta_raw || !out) return SSM_ERR_NULL;
+    if (d->dstate > 0 && (!B || !C || !A_log)) return SSM_ERR_NULL;
+    if (!aligned16(u) || !aligned16(delta_raw) || !aligned16(out) || (z && !aligned16(z)))
+        return SSM_ERR_ALIGN;
+    if (ctx) {
+        if (ctx_bytes < ssm_scan_ctx_bytes(d)) return SSM_ERR_WORKSPACE;
+        if (!aligned16(ctx)) return SSM_ERR_ALIGN;
+    }
+    if ((st = check_device()) != SSM_OK) return st;
+
+    ssm::FwdMaps maps;
+    const int nt = nt_of(d->dstate);
+    const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
+    if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile) ||
+        !encode_act(&maps.dr, delta_raw, d->dtype, d->dinner, d->seqlen, d->batch, r.delta,
+                    ssm::kFwdTile) ||
+        !encode_act(&maps.z, z ? z : u, d->dtype, d->dinner, d->seqlen, d->batch, z ? r.z : r.u,
+                    ssm::kFwdTile) ||
+        !(bct ? encode_bc(&maps.B, B, d->dtype, d->dstate, d->seqlen, d->batch, r.B, nt, ssm::kFwdTile)
+              : encode_act(&maps.B, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)) ||
+        !(bct ? encode_bc(&maps.C, C, d->dtype, d->dstate, d->seqlen, d->batch, r.C, nt, ssm::kFwdTile)
+              : encode_act(&maps.C, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)))
+        return SSM_ERR_DEVICE;
+    ssm::ScanFwdArgs a{};
+    a.B = B;
+    a.C = C;
+    a.A_log = A_log;
+    a.D = D;
+    a.out = out;
+    a.ctx = static_cast<float*>(ctx);
+    a.ysave = ctx ? static_cast<char*>(ctx) + ctx_y_offset(d) : nullptr;
+    a.batch = d->batch;
+    a.seqlen = d->seqlen;
+    a.dinner = d->dinner;
+    a.dstate = d->dstate;
+    a.ld_B = r.B;
+    a.ld_C = r.C;
+    a.ld_out = r.out;
+    a.nck = static_cast<int>(nck_of(d->seqlen));
+    a.bc_tma = bct ? 1 : 0;
+    cudaError_t e = ssm::launch_scan_fwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                        const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, const void* dout, const void* ctx, size_t ctx_bytes,
+                        void* du, void* ddelta_raw, float* dA_log, void* dB, void* dC, float* dD,
+                        void* dz, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Lds r;
+    ssm_status st = validate(d, r);
+    if (st != SSM_OK) return st;
+    const int64_t M = static_cast<int64_t>(d->batch) * d->seqlen;
+    const bool any_work = M > 0 && d->dinner > 0;
+    const bool any_out = (M > 0 && d->dstate > 0) || (d->dinner > 0);
+    if (!any_out) return SSM_OK;
+    if (any_work) {
+        if (!u || !delta_raw || !dout || !du || !ddelta_raw) return SSM_ERR_NULL;
+        if (z && !dz) return SSM_ERR_NULL;
+        if (!aligned16(u) || !aligned16(delta_raw) || !aligned16(dout) || !aligned16(du) ||
+            !aligned16(ddelta_raw) || (z && !aligned16(z)) || (dz && !aligned16(dz)))
+            return SSM_ERR_ALIGN;
+        if (nck_of(d->seqlen) > 0 || z) {
+            if (!ctx) return SSM_ERR_NULL;
+            if (ctx_bytes < ssm_scan_ctx_bytes(d)) return SSM_ERR_WORKSPACE;
+            if (!aligned16(ctx)) return SSM_ERR_ALIGN;
+        }
+    }
+    if (d->dinner > 0 && d->dstate > 0 && !A_log) return SSM_ERR_NULL;
+    if (d->dinner > 0 && d->dstate > 0 && !dA_log) return SSM_ERR_NULL;
+    if (M > 0 && d->dstate > 0 && (!B || !C || !dB || !dC)) return SSM_ERR_NULL;
+    const BwdLayout lay = bwd_layout(d);
+    if (workspace_bytes < lay.total || (lay.total > 0 && !workspace)) return SSM_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return SSM_ERR_ALIGN;
+    if ((st = check_device()) != SSM_OK) return st;
+
+    char* ws = static_cast<char*>(workspace);
+    const int nt = nt_of(d->dstate);
+    if (any_work) {
+        ssm::BwdMaps maps;
+        const int64_t nck = nck_of(d->seqlen);
+        const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
+        const bool ysaved = z != nullptr && ctx != nullptr;
+        const void* ybuf = ysaved ? static_cast<const char*>(ctx) + ctx_y_offset(d) : u;
+        if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk) ||
+            !encode_act(&maps.dr, delta_raw, d->dtype, d->dinner, d->seqlen, d->batch, r.delta,
+                        ssm::kChunk) ||
+            !encode_act(&maps.dout, dout, d->dtype, d->dinner, d->seqlen, d->batch, r.dout,
+                        ssm::kChunk) ||
+            !encode_act(&maps.z, z ? z : u, d->dtype, d->dinner, d->seqlen, d->batch, z ? r.z : r.u,
+                        ssm::kChunk) ||
+            !encode_act(&maps.y, ybuf, d->dtype, d->dinner, d->seqlen, d->batch,
+                        ysaved ? d->dinner : r.u, ssm::kChunk) ||
+            !(nck > 0 ? encode_ck(&maps.ck, ctx, d->dinner, static_cast<int64_t>(d->batch) * nck * nt, nt)
+                      : encode_act(&maps.ck, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u,
+                                   ssm::kChunk)) ||
+            !(bct ? encode_bc(&maps.B, B, d->dtype, d->dstate, d->seqlen, d->batch, r.B, nt, ssm::kChunk)
+                  : encode_act(&maps.B, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk)) ||
+            !(bct ? encode_bc(&maps.C, C, d->dtype, d->dstate, d->seqlen, d->batch, r.C, nt, ssm::kChunk)
+                  : encode_act(&maps.C, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk)))
+            return SSM_ERR_DEVICE;
+        ssm::ScanBwdArgs a{};
+        a.B = B;
+        a.C = C;
+        a.A_log = A_log;
+        a.D = D;
+        a.du = du;
+        a.ddelta = ddelta_raw;
+        a.dz = dz;
+        a.ws_bc = reinterpret_cast<float*>(ws + lay.off_bc);
+        a.ws_dA = reinterpret_cast<float*>(ws + lay.off_dA);
+        a.ws_dD = reinterpret_cast<float*>(ws + lay.off_dD);
+        a.batch = d->batch;
+        a.seqlen = d->seqlen;
+        a.dinner = d->dinner;
+        a.dstate = d->dstate;
+        a.ld_B = r.B;
+        a.ld_C = r.C;
+        a.ld_du = r.du;
+        a.ld_ddelta = r.ddelta;
+        a.ld_dz = r.dz;
+        a.nck = static_cast<int>(nck_of(d->seqlen));
+        a.ncl = lay.ncl;
+        a.bc_tma = bct ? 1 : 0;
+        cudaError_t e = ssm::launch_scan_bwd(d->dtype, nt, d->disc, z != nullptr, maps, a,
+                                             lay.cluster, stream);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    ssm::ScanReduceArgs ra{};
+    ra.ws_bc = reinterpret_cast<const float*>(ws + lay.off_bc);
+    ra.ws_dA = reinterpret_cast<const float*>(ws + lay.off_dA);
+    ra.ws_dD = reinterpret_cast<const float*>(ws + lay.off_dD);
+    ra.A_log = A_log;
+    ra.dB = dB;
+    ra.dC = dC;
+    ra.dA_log = dA_log;
+    ra.dD = dD;
+    ra.batch = d->batch;
+    ra.seqlen = d->seqlen;
+    ra.dinner = d->dinner;
+    ra.dstate = d->dstate;
+    ra.nt = nt;
+    ra.ncl = any_work ? lay.ncl : 0;
+    ra.nb_sum = any_work ? d->batch : 0;
+    ra.ld_dB = r.dB;
+    ra.ld_dC = r.dC;
+    ra.is_bf16 = d->dtype == SSM_BF16;
+    cudaError_t e = ssm::launch_scan_reduce(ra, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+ssm_status ssm_conv1d_silu(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                           const float* x, int64_t ld_x, const float* w, const float* bias,
+                           float* out, int64_t ld_out, cudaStream_t stream) {
+    if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
+    ld_x = ld_x ? ld_x : dinner;
+    ld_out = ld_out ? ld_out : dinner;
+    if (ld_x < dinner || ld_out < dinner) return SSM_ERR_SHAPE;
+    if (static_cast<int64_t>(batch) * seqlen == 0 || dinner == 0) return SSM_OK;
+    if (!x || !w || !out) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || ld_out % 4 || !aligned16(x) || !aligned16(out) ||
+        (bias && !aligned16(bias)))
+        return SSM_ERR_ALIGN;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    ssm::ConvArgs a{};
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.out = out;
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.dinner = dinner;
+    a.kconv = kconv;
+    a.ld_x = ld_x;
+    a.ld_out = ld_out;
+    cudaError_t e = ssm::launch_conv1d_fwd(a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+size_t ssm_conv1d_silu_bwd_workspace_bytes(int32_t batch, int32_t seqlen, int32_t dinner,
+                                           int32_t kconv) {
+    if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return 0;
+    return ssm::conv1d_bwd_workspace_bytes(batch, seqlen, dinner, kconv);
+}
+
+ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                               const float* x, int64_t ld_x, const float* w, const float* bias,
+                               const float* dout, int64_t ld_dout, float* dx, int64_t ld_dx,
+                               float* dw, float* dbias, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
+    ld_x = ld_x ? ld_x : dinner;
+    ld_dout = ld_dout ? ld_dout : dinner;
+    ld_dx = ld_dx ? ld_dx : dinner;
+    if (ld_x < dinner || ld_dout < dinner || ld_dx < dinner) return SSM_ERR_SHAPE;
+    if (dinner == 0) return SSM_OK;
+    if (!w || !dw) return SSM_ERR_NULL;
+    const bool rows = static_cast<int64_t>(batch) * seqlen > 0;
+    if (rows && (!x || !dout || !dx)) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || ld_dout % 4 || ld_dx % 4 || (x && !aligned16(x)) ||
+        (dout && !aligned16(dout)) || (dx && !aligned16(dx)) || (bias && !aligned16(bias)))
+        return SSM_ERR_ALIGN;
+    const size_t need = ssm::conv1d_bwd_workspace_bytes(batch, seqlen, dinner, kconv);
+    if (workspace_bytes < need || (need && !workspace)) return SSM_ERR_WORKSPACE;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    ssm::ConvArgs a{};
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.dout = dout;
+    a.dx = dx;
+    a.dw = dw;
+    a.dbias = dbias;
+    a.ws = static_cast<float*>(workspace);
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.dinner = dinner;
+    a.kconv = kconv;
+    a.ld_x = ld_x;
+    a.ld_dout = ld_dout;
+    a.ld_dx = ld_dx;
+    cudaError_t e = ssm::launch_conv1d_bwd(a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+const char* ssm_status_string(ssm_status s) {
+    switch (s) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_NULL: return "required pointer is NULL";
+        case SSM_ERR_SHAPE: return "size or stride out of range";
+        case SSM_ERR_ALIGN: return "pointer or row stride breaks the 16-byte alignment rule";
+        case SSM_ERR_DTYPE: return "unknown dtype or discretisation";
+        case SSM_ERR_WORKSPACE: return "context or workspace too small";
+        case SSM_ERR_LAUNCH: return "kernel launch failed";
+        case SSM_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+int ssm_last_cuda_error(void) { return g_last_cuda_error; }
+
+int ssm_abi_version(void) { return SSM_GB300_ABI_VERSION; }
+
+unsigned ssm_device_faults(void) {
+    unsigned f1 = 0, f2 = 0;
+    if (check_device() != SSM_OK) return 0;
+    ssm::read_clear_fault_fwd(&f1);
+    ssm::read_clear_fault_bwd(&f2);
+    return f1 | f2;
+}
+
+}  // extern "C"

@@ -1,0 +1,248 @@
+// conv1d.cu -- causal depthwise conv1d + SiLU, forward and backward, for sm_103a.
+//
+// mamba1_cpu.ts (page "@seanhogg/builderforce-memory-engine 2026.7.12 ->
+// 2026.9.27"), mamba1CpuForward steps 4-5 and mamba1CpuBackward steps 5-4:
+//   pre[r, d] = bias[d] + sum_{k < K, t >= k} w[d*K + k] * x[r - k, d]
+//   out       = silu(pre)
+//   dpre      = dout * silu'(pre);  dbias[d] = sum_r dpre;  dw[d,k] = sum_r dpre[r] x[r-k]
+//   dx[r, d]  = sum_{k < K, t + k < L} w[d*K + k] * dpre[r + k, d]
+// Tap k = 0 multiplies the CURRENT step.
+//
+// Design: the op is bound by HBM (one read of x and one write of out per
+// element).  A thread owns 4 adjacent channels (one 16-byte access per row,
+// 512 contiguous bytes per warp) and walks a run of kRun rows, keeping the
+// last K rows of x (and, backward, of dpre) in registers, so each element is
+// read from HBM once plus a (K-1)/kRun halo.
+#include <algorithm>
+
+#include "conv_args.cuh"
+#include "ssm_common.cuh"
+
+namespace ssm {
+
+constexpr int kConvMaxK = 8;
+constexpr int kConvThreads = 128;
+
+__device__ __forceinline__ float silu_f(float x) { return x * rcp(1.0f + ex2(-x * kLog2e)); }
+__device__ __forceinline__ float silu_grad_f(float x) {
+    const float s = rcp(1.0f + ex2(-x * kLog2e));
+    return s * (1.0f + x * (1.0f - s));
+}
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+template <int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_silu_fwd_kernel(const ConvArgs a) {
+    const int nq = a.dinner / 4;
+    const int runs = (a.seqlen + kConvRun - 1) / kConvRun;
+    const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long total = static_cast<long long>(nq) * runs * a.batch;
+    if (gid >= total) return;
+    const int q = static_cast<int>(gid % nq);
+    const long long rest = gid / nq;
+    const int run = static_cast<int>(rest % runs);
+    const int b = static_cast<int>(rest / runs);
+    const int d0 = 4 * q;
+    float4 w[kConvMaxK];
+#pragma unroll
+    for (int k = 0; k < kConvMaxK; ++k)
+        w[k] = k < K ? make_float4(a.w[(d0 + 0) * K + k], a.w[(d0 + 1) * K + k],
+                                   a.w[(d0 + 2) * K + k], a.w[(d0 + 3) * K + k])
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 bias = a.bias ? ld4(a.bias + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t0 = run * kConvRun;
+    const int t1 = min(a.seqlen, t0 + kConvRun);
+    const size_t row0 = static_cast<size_t>(b) * a.seqlen;
+    float4 xw[kConvMaxK];   // xw[k] = x[t - k]
+#pragma unroll
+    for (int k = 0; k < kConvMaxK; ++k) xw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // halo: rows t0-K+1 .. t0-1
+    for (int t = max(0, t0 - K + 1); t < t0; ++t) {
+#pragma unroll
+        for (int k = kConvMaxK - 1; k > 0; --k) xw[k] = xw[k - 1];
+        xw[0] = ld4(a.x + (row0 + t) * a.ld_x + d0);
+    }
+    for (int t = t0; t < t1; ++t) {
+#pragma unroll
+        for (int k = kConvMaxK - 1; k > 0; --k) xw[k] = xw[k - 1];
+        xw[0] = ld4(a.x + (row0 + t) * a.ld_x + d0);
+        float4 acc = bias;
+#pragma unroll
+        for (int k = 0; k < kConvMaxK; ++k) {
+            acc.x = fmaf(w[k].x, xw[k].x, acc.x);
+            acc.y = fmaf(w[k].y, xw[k].y, acc.y);
+            acc.z = fmaf(w[k].z, xw[k].z, acc.z);
+            acc.w = fmaf(w[k].w, xw[k].w, acc.w);
+        }
+        st4(a.out + (row0 + t) * a.ld_out + d0,
+            make_float4(silu_f(acc.x), silu_f(acc.y), silu_f(acc.z), silu_f(acc.w)));
+    }
+}
+
+// Backward: per run, dx for its rows and partial dw / dbias (written to the
+// workspace, reduced over runs by conv1d_reduce_kernel).
+template <int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_silu_bwd_kernel(const ConvArgs a) {
+    const int nq = a.dinner / 4;
+    const int runs = (a.seqlen + kConvRun - 1) / kConvRun;
+    const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long total = static_cast<long long>(nq) * runs * a.batch;
+    if (gid >= total) return;
+    const int q = static_cast<int>(gid % nq);
+    const long long rest = gid / nq;
+    const int run = static_cast<int>(rest % runs);
+    const int b = static_cast<int>(rest / runs);
+    const int d0 = 4 * q;
+    const int L = a.seqlen;
+    float4 w[kConvMaxK];
+#pragma unroll
+    for (int k = 0; k < kConvMaxK; ++k)
+        w[k] = k < K ? make_float4(a.w[(d0 + 0) * K + k], a.w[(d0 + 1) * K + k],
+                                   a.w[(d0 + 2) * K + k], a.w[(d0 + 3) * K + k])
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 bias = a.bias ? ld4(a.bias + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t0 = run * kConvRun;
+    const int t1 = min(L, t0 + kConvRun);
+    const size_t row0 = static_cast<size_t>(b) * L;
+    float4 xw[kConvMaxK], gw[kConvMaxK];   // xw[k] = x[s-k], gw[k] = dpre[s-k]
+#pragma unroll
+    for (int k = 0; k < kConvMaxK; ++k) xw[k] = gw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 dwa[kConvMaxK], dba = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kConvMaxK; ++k) dwa[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int s = max(0, t0 - K + 1); s < t1 + K - 1; ++s) {
+#pragma unroll
+        for (int k = kConvMaxK - 1; k > 0; --k) {
+            xw[k] = xw[k - 1];
+            gw[k] = gw[k - 1];
+        }
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < L) {
+            xw[0] = ld4(a.x + (row0 + s) * a.ld_x + d0);
+            if (s >= t0) {
+                float4 p = bias;
+#pragma unroll
+                for (int k = 0; k < kConvMaxK; ++k) {
+                    p.x = fmaf(w[k].x, xw[k].x, p.x);
+                    p.y = fmaf(w[k].y, xw[k].y, p.y);
+                    p.z = fmaf(w[k].z, xw[k].z, p.z);
+                    p.w = fmaf(w[k].w, xw[k].w, p.w);
+                }
+                const float4 go = ld4(a.dout + (row0 + s) * a.ld_dout + d0);
+                g = make_float4(go.x * silu_grad_f(p.x), go.y * silu_grad_f(p.y),
+                                go.z * silu_grad_f(p.z), go.w * silu_grad_f(p.w));
+                if (s < t1) {
+                    dba.x += g.x; dba.y += g.y; dba.z += g.z; dba.w += g.w;
+#pragma unroll
+                    for (int k = 0; k < kConvMaxK; ++k) {
+                        dwa[k].x = fmaf(g.x, xw[k].x, dwa[k].x);
+                        dwa[k].y = fmaf(g.y, xw[k].y, dwa[k].y);
+                        dwa[k].z = fmaf(g.z, xw[k].z, dwa[k].z);
+                        dwa[k].w = fmaf(g.w, xw[k].w, dwa[k].w);
+                    }
+                }
+            }
+        } else {
+            xw[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        gw[0] = g;
+        const int r = s - (K - 1);   // dx[r] = sum_k w[k] dpre[r+k] is complete now
+        if (r >= t0 && r < t1) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kConvMaxK; ++k) {
+                if (k < K) {   // dpre[r + k] sits in gw[K - 1 - k]
+                    const float4 gv = gw[K - 1 - k];
+                    acc.x = fmaf(w[k].x, gv.x, acc.x);
+                    acc.y = fmaf(w[k].y, gv.y, acc.y);
+                    acc.z = fmaf(w[k].z, gv.z, acc.z);
+                    acc.w = fmaf(w[k].w, gv.w, acc.w);
+                }
+            }
+            st4(a.dx + (row0 + r) * a.ld_dx + d0, acc);
+        }
+    }
+    // partial dw | dbias of this run: ws[(b*runs + run)][d][K+1]
+    float* wsr = a.ws + (static_cast<size_t>(b) * runs + run) * a.dinner * (K + 1);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float* dst = wsr + static_cast<size_t>(d0 + c) * (K + 1);
+#pragma unroll
+        for (int k = 0; k < kConvMaxK; ++k)
+            if (k < K) dst[k] = c == 0 ? dwa[k].x : c == 1 ? dwa[k].y : c == 2 ? dwa[k].z : dwa[k].w;
+        dst[K] = c == 0 ? dba.x : c == 1 ? dba.y : c == 2 ? dba.z : dba.w;
+    }
+}
+
+__global__ void conv1d_reduce_kernel(const ConvArgs a, int nparts) {
+    const int K = a.kconv;
+    const int total = a.dinner * (K + 1);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        float s = 0.0f;
+        for (int p = 0; p < nparts; ++p) s += a.ws[static_cast<size_t>(p) * total + i];
+        const int d = i / (K + 1), k = i % (K + 1);
+        if (k < K) a.dw[d * K + k] = s;
+        else if (a.dbias) a.dbias[d] = s;
+    }
+}
+
+static unsigned blocks_for(long long n) {
+    return static_cast<unsigned>((n + kConvThreads - 1) / kConvThreads);
+}
+
+template <template <int> class Sel>
+static cudaError_t dispatch_k(int k, const ConvArgs& a, unsigned blocks, cudaStream_t st) {
+    switch (k) {
+        case 1: Sel<1>::run(a, blocks, st); break;
+        case 2: Sel<2>::run(a, blocks, st); break;
+        case 3: Sel<3>::run(a, blocks, st); break;
+        case 4: Sel<4>::run(a, blocks, st); break;
+        case 5: Sel<5>::run(a, blocks, st); break;
+        case 6: Sel<6>::run(a, blocks, st); break;
+        case 7: Sel<7>::run(a, blocks, st); break;
+        case 8: Sel<8>::run(a, blocks, st); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+template <int K> struct FwdSel {
+    static void run(const ConvArgs& a, unsigned bl, cudaStream_t st) {
+        conv1d_silu_fwd_kernel<K><<<bl, kConvThreads, 0, st>>>(a);
+    }
+};
+template <int K> struct BwdSel {
+    static void run(const ConvArgs& a, unsigned bl, cudaStream_t st) {
+        conv1d_silu_bwd_kernel<K><<<bl, kConvThreads, 0, st>>>(a);
+    }
+};
+
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, cudaStream_t st) {
+    const long long runs = (a.seqlen + kConvRun - 1) / kConvRun;
+    const long long total = static_cast<long long>(a.dinner / 4) * runs * a.batch;
+    if (total == 0) return cudaSuccess;
+    return dispatch_k<FwdSel>(a.kconv, a, blocks_for(total), st);
+}
+
+cudaError_t launch_conv1d_bwd(const ConvArgs& a, cudaStream_t st) {
+    const long long runs = (a.seqlen + kConvRun - 1) / kConvRun;
+    const long long total = static_cast<long long>(a.dinner / 4) * runs * a.batch;
+    if (total > 0) {
+        cudaError_t e = dispatch_k<BwdSel>(a.kconv, a, blocks_for(total), st);
+        if (e != cudaSuccess) return e;
+    }
+    const int nparts = static_cast<int>(runs * a.batch);
+    const int n = a.dinner * (a.kconv + 1);
+    if (n == 0) return cudaSuccess;
+    conv1d_reduce_kernel<<<std::max(1, std::min(1024, (n + 255) / 256)), 256, 0, st>>>(a, nparts);
+    return cudaGetLastError();
+}
+
+size_t conv1d_bwd_workspace_bytes(int batch, int seqlen, int dinner, int kconv) {
+    const size_t runs = (static_cast<size_t>(seqlen) + kConvRun - 1) / kConvRun;
+    return runs * batch * dinner * (kconv + 1) * sizeof(float);
+}
+
+}  // namespace ssm

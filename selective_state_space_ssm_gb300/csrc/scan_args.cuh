@@ -1,0 +1,95 @@
+// scan_args.cuh -- argument blocks and launch constants shared by the C-ABI
+// layer (abi.cu) and the selective-scan kernels (scan_fwd.cu, scan_bwd.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// Scan-state checkpoint spacing: the forward stores h every kChunk steps and
+// the backward recomputes h inside each chunk of kChunk steps.
+constexpr int kChunk = 8;
+
+// Forward: one thread per channel (all dstate states in registers), one warp
+// per CTA so 32-channel work units spread evenly over the 152 SMs.
+constexpr int kFwdWarps = 1;
+constexpr int kFwdTile = 16;    // steps per TMA-staged tile
+constexpr int kFwdStages = 4;   // tiles in flight
+
+// Backward: one warp per CTA covers 32 channels x all states (each lane owns
+// 4 channels x dstate/4 states); CTAs of a cluster reduce dB/dC through DSMEM.
+constexpr int kBwdWarps = 1;
+constexpr int kBwdStages = 2;
+constexpr int kBwdCluster = 8;
+
+struct ScanFwdArgs {
+    const void* B;
+    const void* C;
+    const float* A_log;
+    const float* D;      // may be null
+    void* out;
+    float* ctx;          // checkpoints [batch][nck][NT][dinner], may be null
+    void* ysave;         // pre-gate y (M, dinner) packed, activation dtype; may be null
+    int batch, seqlen, dinner, dstate;
+    int64_t ld_B, ld_C, ld_out;
+    int nck;             // checkpoints per batch row = ceil(seqlen / kChunk) - 1
+    int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
+};
+
+struct ScanBwdArgs {
+    const void* B;
+    const void* C;
+    const float* A_log;
+    const float* D;      // may be null
+    void* du;
+    void* ddelta;
+    void* dz;            // null when there is no gate
+    float* ws_bc;        // [ncl][batch][seqlen][2][NT] dB | dC partial sums
+    float* ws_dA;        // [batch][dinner][NT] partial d/dA
+    float* ws_dD;        // [batch][dinner] partial dD
+    int batch, seqlen, dinner, dstate;
+    int64_t ld_B, ld_C, ld_du, ld_ddelta, ld_dz;
+    int nck;
+    int ncl;             // number of cluster columns (dB/dC partial planes)
+    int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
+};
+
+struct ScanReduceArgs {
+    const float* ws_bc;
+    const float* ws_dA;
+    const float* ws_dD;
+    const float* A_log;
+    void* dB;
+    void* dC;
+    float* dA_log;
+    float* dD;           // may be null
+    int batch, seqlen, dinner, dstate, nt, ncl;
+    int nb_sum;          // batch planes of ws_dA / ws_dD to add (0 if none were written)
+    int64_t ld_dB, ld_dC;
+    int is_bf16;
+};
+
+// Host launchers (scan_fwd.cu / scan_bwd.cu).  Return cudaSuccess or the launch error.
+// Tensor maps of the forward: u, delta_raw, z (32 channels x kFwdTile steps)
+// and B, C (NT states x kFwdTile steps).
+struct FwdMaps {
+    CUtensorMap u, dr, z, B, C;
+};
+cudaError_t launch_scan_fwd(int dtype, int nt, int disc, bool gate, const FwdMaps& maps,
+                            const ScanFwdArgs& a, cudaStream_t stream);
+// Tensor maps of the backward: u, delta_raw, z, dout, the saved pre-gate y
+// (all 32 channels x kChunk steps boxes) and the checkpoints (32 x NT box).
+struct BwdMaps {
+    CUtensorMap u, dr, z, dout, y, ck, B, C;
+};
+cudaError_t launch_scan_bwd(int dtype, int nt, int disc, bool gate, const BwdMaps& maps,
+                            const ScanBwdArgs& a, int cluster, cudaStream_t stream);
+cudaError_t launch_scan_reduce(const ScanReduceArgs& a, cudaStream_t stream);
+
+// Read and clear the fault word of the forward / backward translation unit.
+cudaError_t read_clear_fault_fwd(unsigned* out);
+cudaError_t read_clear_fault_bwd(unsigned* out);
+
+}  // namespace ssm

@@ -1,0 +1,641 @@
+// scan_bwd.cu -- selective-scan backward for sm_103a.
+//
+// Computes mamba1_cpu.ts mamba1CpuBackward steps 9 (gate) and 8 (scan, walked
+// backwards in time), page "@seanhogg/builderforce-memory-engine 2026.7.12 ->
+// 2026.9.27":
+//   g_t      = C_t dy_t + a_{t+1} g_{t+1}              (dL/dh_t; 0 after the last step)
+//   du_t     = D dy_t + sum_n g_t beta_t/u_t           dz_t = dout_t y_t silu'(z_t)
+//   ddelta_t = sum_n g_t (a_t h_{t-1} A + u_t B_t d(beta/B)/d delta)
+//   dA       = sum_t g_t (a_t h_{t-1} delta_t + u_t B_t d(beta/B)/dA)
+//   dB_t     = sum_d g_t u_t beta_t/B_t     dC_t = sum_d dy_t h_t     dD = sum dy u
+//   dA_log   = dA * A inside (-10, 5), exactly 0 at or beyond the bounds
+//   ddelta_raw = ddelta * sigmoid(delta_raw)
+//
+// Design (GB300): the forward saved h every kChunk (= 8) steps.  A warp-sized
+// CTA owns 32 channels of one batch row and walks the chunks last to first.
+// For each chunk it recomputes h forward from the checkpoint (pass B), keeping
+// a_t h_{t-1} in shared memory, then runs the reverse recurrence for g over
+// the chunk.  Each lane owns 4 channels x dstate/4 states (16 chains), so the
+// sums over states (y, sum g B, sum g A a h) and over channels (dB, dC) are
+// mostly register accumulations and finish with a few warp shuffles.  The 8
+// CTAs of a cluster (256 channels) add their per-chunk dB/dC through
+// distributed shared memory; one partial plane per cluster column is reduced by
+// scan_reduce_kernel, which also finishes dA_log and dD.
+#include <algorithm>
+
+#include "scan_args.cuh"
+#include "ssm_common.cuh"
+
+namespace ssm {
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+    return v;
+}
+
+// Sum of NS values over the 8 lanes that differ in lane bits 4..2.  Returns the
+// sum of value index sel (written through `sel`), and whether this lane is the
+// unique owner of that result among the 8 lanes.
+template <int NS>
+__device__ __forceinline__ float rs_over_cg(float (&v)[NS], int lane, int& sel, bool& owner) {
+    if constexpr (NS == 4) {
+        const bool b4 = lane & 16, b3 = lane & 8;
+        float w0 = (b4 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, b4 ? v[0] : v[2], 16);
+        float w1 = (b4 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, b4 ? v[1] : v[3], 16);
+        float x = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sel = (b4 ? 2 : 0) + (b3 ? 1 : 0);
+        owner = (lane & 4) == 0;
+        return x;
+    } else {  // NS == 2
+        const bool b4 = lane & 16;
+        float x = (b4 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, b4 ? v[0] : v[1], 16);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sel = b4 ? 1 : 0;
+        owner = (lane & 12) == 0;
+        return x;
+    }
+}
+
+template <typename T, int NT, int DISC, bool GATE>
+__global__ void __launch_bounds__(32, 1)
+scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
+    constexpr int TC = kChunk;
+    constexpr int S = kBwdStages;
+    constexpr int NS = NT / 4;                  // states per lane
+    constexpr int NTEN = GATE ? 5 : 3;          // u, delta_raw, dout, [z, y]
+    constexpr int TILE = TC * 32;
+    constexpr int BCT = TC * NT;                // elements per B or C tile
+    constexpr int STAGE = NTEN * TILE + 2 * BCT;
+    constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
+    constexpr uint32_t kBCBytes = 2 * BCT * sizeof(T);
+    constexpr uint32_t kCkBytes = NT * 32 * sizeof(float);
+    constexpr int BCN = 2 * TC * NT;
+    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+    constexpr bool ZOH = DISC == 1;
+    constexpr int NQN = ZOH ? 3 : 2;            // state sums kept per (step, channel)
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* tiles = reinterpret_cast<T*>(smem);                               // [S][STAGE]
+    float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][32]
+    float* bcs = cks + S * NT * 32;                                      // [TC][2NT]
+    float* A2s = bcs + BCN;                                              // [32][NT]
+    float* iAs = A2s + 32 * NT;                                          // [32][NT] (ZOH)
+    float* Pd = iAs + (ZOH ? 32 * NT : 0);                               // [TC][32] delta
+    float* Pbs = Pd + TILE;                                              // [TC][32] delta*u | u
+    float* Pdy = Pbs + TILE;                                             // [TC][32] dy
+    float* part = Pdy + TILE;                                            // [TC][NQN][4][32]
+    float* rBC = part + TC * NQN * 4 * 32;                               // [2][TC][2NT]
+    uint64_t* full = reinterpret_cast<uint64_t*>(rBC + 2 * BCN);         // [S]
+
+    const int lane = threadIdx.x;
+    const int cg = lane >> 2, ng = lane & 3;
+    const int cbase = cg * 4;
+    const int c0 = blockIdx.x * 32;
+    const int b = blockIdx.y;
+    const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
+    const int nchunks = (L + TC - 1) / TC;
+    const size_t row0 = static_cast<size_t>(b) * L;
+    const uint32_t crank = cluster_ctarank();
+    const int dch = c0 + lane;                   // channel of this lane in pro/epilogue
+    const bool lane_ok = dch < Dn;
+    const bool quad_ok = c0 + cbase < Dn;
+
+    // per (channel, state) constants, lane = channel
+    for (int n = 0; n < NT; ++n) {
+        const bool ok = lane_ok && n < N;
+        const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(dch) * N + n]) : -1.0f;
+        A2s[lane * NT + n] = ok ? A * kLog2e : 0.0f;
+        if (ZOH) iAs[lane * NT + n] = 1.0f / A;
+    }
+    const float Dd = (lane_ok && a.D) ? a.D[dch] : 0.0f;
+
+    const T* Bp = static_cast<const T*>(a.B);
+    const T* Cp = static_cast<const T*>(a.C);
+    const bool bc_tma = a.bc_tma != 0;
+    auto issue = [&](int it) {
+        const int kc = nchunks - 1 - it;
+        const int s = it % S;
+        T* dst = tiles + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], kActBytes + (kc > 0 ? kCkBytes : 0u) +
+                                            (bc_tma ? kBCBytes : 0u));
+        if (bc_tma) {
+            tma_load_3d(dst + NTEN * TILE, &maps.B, &full[s], 0, kc * TC, b);
+            tma_load_3d(dst + NTEN * TILE + BCT, &maps.C, &full[s], 0, kc * TC, b);
+        }
+        tma_load_3d(dst, &maps.u, &full[s], c0, kc * TC, b);
+        tma_load_3d(dst + TILE, &maps.dr, &full[s], c0, kc * TC, b);
+        tma_load_3d(dst + 2 * TILE, &maps.dout, &full[s], c0, kc * TC, b);
+        if (GATE) {
+            tma_load_3d(dst + 3 * TILE, &maps.z, &full[s], c0, kc * TC, b);
+            tma_load_3d(dst + 4 * TILE, &maps.y, &full[s], c0, kc * TC, b);
+        }
+        if (kc > 0)
+            tma_load_2d(cks + s * NT * 32, &maps.ck, &full[s], c0,
+                        (b * a.nck + kc - 1) * NT);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int it = 0; it < S && it < nchunks; ++it) issue(it);
+    __syncwarp();
+
+    // The carries of the reverse recurrence (g) and the dA accumulators live in
+    // registers only during the reverse pass and epilogue; between chunks they
+    // are parked in the (then idle) state-sum buffer, so pass B can hold the
+    // chunk's a h_{t-1} values in registers.  stash[(q*NS*4 + k)*32 + lane].
+    float* stash = part;
+    static_assert(2 * 4 * NS <= TC * NQN * 4, "stash fits in the partials buffer");
+    float dA[4][NS], g[4][NS];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jn = 0; jn < NS; ++jn) dA[i][jn] = g[i][jn] = 0.0f;
+    auto park = [&]() {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jn = 0; jn < NS; ++jn) {
+                stash[(i * NS + jn) * 32 + lane] = g[i][jn];
+                stash[((4 + i) * NS + jn) * 32 + lane] = dA[i][jn];
+            }
+    };
+    auto unpark = [&]() {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jn = 0; jn < NS; ++jn) {
+                g[i][jn] = stash[(i * NS + jn) * 32 + lane];
+                dA[i][jn] = stash[((4 + i) * NS + jn) * 32 + lane];
+            }
+    };
+    park();
+    float dl_next[4] = {0.f, 0.f, 0.f, 0.f};    // delta of the step after this chunk
+    float dD_acc = 0.0f;
+
+    T* dup = static_cast<T*>(a.du);
+    T* ddp = static_cast<T*>(a.ddelta);
+    T* dzp = static_cast<T*>(a.dz);
+    bool ok = true;
+    int waited = 0;
+
+    for (int it = 0; it < nchunks; ++it) {
+        const int kc = nchunks - 1 - it;
+        const int t0 = kc * TC;
+        const int jmax = min(TC, L - t0);
+        const int s = it % S;
+        const float* bc = bcs;
+        float* rbc = rBC + (it & 1) * BCN;
+
+        if (ok) ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) waited = it + 1;
+
+        if (ok) {
+            const T* tu = tiles + s * STAGE;
+            // fp32 B|C tile of this chunk: bcs[j][0..NT) = B, bcs[j][NT..2NT) = C
+            {
+                const T* Bs = tu + NTEN * TILE;
+                const T* Cs = Bs + BCT;
+#pragma unroll 4
+                for (int e = lane; e < BCN; e += 32) {
+                    const int j = e / (2 * NT), w = e % (2 * NT);
+                    const int n = w < NT ? w : w - NT;
+                    float v;
+                    if (bc_tma) {
+                        v = Act<T>::to_f(w < NT ? Bs[j * NT + n] : Cs[j * NT + n]);
+                    } else {
+                        const int t = t0 + j;
+                        v = 0.0f;
+                        if (t < L && n < N) {
+                            const size_t r = row0 + t;
+                            v = (w < NT) ? Act<T>::load(Bp + r * a.ld_B + n)
+                                         : Act<T>::load(Cp + r * a.ld_C + n);
+                        }
+                    }
+                    bcs[e] = v;
+                }
+            }
+            const T* tr = tu + TILE;
+            const T* tg = tu + 2 * TILE;
+            const T* tz = tu + 3 * TILE;
+            const T* ty = tu + 4 * TILE;
+            const float* ck = cks + s * NT * 32;
+
+            // ---- prologue (lane = channel): delta, delta*u (or u), dy.  All TC
+            //      steps run: past seqlen the tiles, B and C are zero, so dy = 0
+            //      and the extra steps add exactly nothing to g or any gradient.
+#pragma unroll
+            for (int j = 0; j < TC; ++j) {
+                {
+                    const float uv = Act<T>::to_f(tu[j * 32 + lane]);
+                    const float xr = Act<T>::to_f(tr[j * 32 + lane]);
+                    const float go = Act<T>::to_f(tg[j * 32 + lane]);
+                    float dt, dy = go;
+                    if (GATE) {
+                        const float zv = Act<T>::to_f(tz[j * 32 + lane]);
+                        float sz;
+                        softplus_sigmoid(xr, zv, dt, sz);
+                        dy = go * zv * sz;
+                    } else {
+                        float e;
+                        dt = softplus_e(xr, e);
+                    }
+                    Pd[j * 32 + lane] = dt;
+                    Pbs[j * 32 + lane] = ZOH ? uv : dt * uv;
+                    Pdy[j * 32 + lane] = dy;
+                }
+            }
+            __syncwarp();
+
+            // ---- pass B: h from the checkpoint, a_t h_{t-1} kept in registers;
+            //      dC partials (over this lane's 4 channels) reduced over the 8
+            //      channel groups with shuffles.
+            float2 ah[TC][4][NS / 2];
+            {
+                float2 h[4][NS / 2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p)
+                        h[i][p] = kc > 0 ? make_float2(ck[(ng * NS + 2 * p) * 32 + cbase + i],
+                                                       ck[(ng * NS + 2 * p + 1) * 32 + cbase + i])
+                                         : make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    {
+                        const float4 dl = *reinterpret_cast<const float4*>(Pd + j * 32 + cbase);
+                        const float4 bs = *reinterpret_cast<const float4*>(Pbs + j * 32 + cbase);
+                        const float4 dy = *reinterpret_cast<const float4*>(Pdy + j * 32 + cbase);
+                        const float dlA[4] = {dl.x, dl.y, dl.z, dl.w};
+                        const float bsA[4] = {bs.x, bs.y, bs.z, bs.w};
+                        const float dyA[4] = {dy.x, dy.y, dy.z, dy.w};
+                        float2 Bv[NS / 2];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p)
+                            Bv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + ng * NS + 2 * p);
+                        float2 dC[NS / 2];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                            for (int p = 0; p < NS / 2; ++p) {
+                                const float2 A2p = *reinterpret_cast<const float2*>(
+                                    A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                                const float2 x = mul2(f2(dlA[i]), A2p);
+                                const float2 av = make_float2(ex2(x.x), ex2(x.y));
+                                const float2 ahv = mul2(av, h[i][p]);
+                                float2 bu;
+                                if (!ZOH) {
+                                    bu = mul2(f2(bsA[i]), Bv[p]);
+                                } else {
+                                    const float2 iA = *reinterpret_cast<const float2*>(
+                                        iAs + (cbase + i) * NT + ng * NS + 2 * p);
+                                    const float xn0 = x.x * kLn2, xn1 = x.y * kLn2;
+                                    const float cf0 = fabsf(xn0) < 0.5f ? dlA[i] * phi1_series(xn0)
+                                                                        : (av.x - 1.0f) * iA.x;
+                                    const float cf1 = fabsf(xn1) < 0.5f ? dlA[i] * phi1_series(xn1)
+                                                                        : (av.y - 1.0f) * iA.y;
+                                    bu = mul2(mul2(make_float2(cf0, cf1), f2(bsA[i])), Bv[p]);
+                                }
+                                h[i][p] = add2(ahv, bu);
+                                ah[j][i][p] = ahv;
+                                dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
+                            }
+                        }
+                        float dCv[NS];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) { dCv[2 * p] = dC[p].x; dCv[2 * p + 1] = dC[p].y; }
+                        int sel;
+                        bool own;
+                        const float dCs = rs_over_cg<NS>(dCv, lane, sel, own);
+                        if (own) rbc[j * 2 * NT + NT + ng * NS + sel] = dCs;
+                    }
+                }
+            }
+
+            // ---- reverse pass: g_t = C_t dy_t + a_{t+1} g_{t+1}; state sums to
+            //      shared partials, dB partials reduced with shuffles.
+            unpark();
+            __syncwarp();
+            {
+                float2 an[4][NS / 2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        const float2 A2p = *reinterpret_cast<const float2*>(
+                            A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                        const float2 x = mul2(f2(dl_next[i]), A2p);
+                        an[i][p] = make_float2(ex2(x.x), ex2(x.y));
+                    }
+#pragma unroll
+                for (int j = TC - 1; j >= 0; --j) {
+                    {
+                        const float4 dl = *reinterpret_cast<const float4*>(Pd + j * 32 + cbase);
+                        const float4 bs = *reinterpret_cast<const float4*>(Pbs + j * 32 + cbase);
+                        const float4 dy = *reinterpret_cast<const float4*>(Pdy + j * 32 + cbase);
+                        const float dlA[4] = {dl.x, dl.y, dl.z, dl.w};
+                        const float bsA[4] = {bs.x, bs.y, bs.z, bs.w};
+                        const float dyA[4] = {dy.x, dy.y, dy.z, dy.w};
+                        float2 Bv[NS / 2], Cv[NS / 2];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) {
+                            Bv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + ng * NS + 2 * p);
+                            Cv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + NT + ng * NS + 2 * p);
+                        }
+                        float2 dB[NS / 2];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) dB[p] = make_float2(0.f, 0.f);
+                        float sums[NQN][4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float2 Sg = make_float2(0.f, 0.f), Eg = make_float2(0.f, 0.f);
+                            float2 Sa = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int p = 0; p < NS / 2; ++p) {
+                                const float2 A2p = *reinterpret_cast<const float2*>(
+                                    A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                                // g_t = C_t dy_t + a_{t+1} g_{t+1}
+                                float2 gv = make_float2(g[i][2 * p], g[i][2 * p + 1]);
+                                gv = fma2(an[i][p], gv, mul2(Cv[p], f2(dyA[i])));
+                                g[i][2 * p] = gv.x;
+                                g[i][2 * p + 1] = gv.y;
+                                const float2 q = mul2(gv, ah[j][i][p]);        // g a_t h_{t-1}
+                                Eg = fma2(A2p, q, Eg);
+                                const float2 x = mul2(f2(dlA[i]), A2p);
+                                const float2 av = make_float2(ex2(x.x), ex2(x.y));   // a_t
+                                float2 dAv = make_float2(dA[i][2 * p], dA[i][2 * p + 1]);
+                                if (!ZOH) {
+                                    dAv = fma2(f2(dlA[i]), q, dAv);
+                                    Sg = fma2(gv, Bv[p], Sg);
+                                    dB[p] = fma2(f2(bsA[i]), gv, dB[p]);
+                                } else {
+                                    const float2 iA = *reinterpret_cast<const float2*>(
+                                        iAs + (cbase + i) * NT + ng * NS + 2 * p);
+                                    const float dt = dlA[i], uv = bsA[i];
+                                    float cf[2], dcf[2];
+#pragma unroll
+                                    for (int ee = 0; ee < 2; ++ee) {
+                                        const float xn = (ee ? x.y : x.x) * kLn2;
+                                        const float ae = ee ? av.y : av.x;
+                                        const float ia = ee ? iA.y : iA.x;
+                                        const bool small = fabsf(xn) < 0.5f;
+                                        cf[ee] = small ? dt * phi1_series(xn) : (ae - 1.0f) * ia;
+                                        dcf[ee] = small ? dt * dt * phi2_series(xn)
+                                                        : (xn * ae - (ae - 1.0f)) * ia * ia;
+                                    }
+                                    const float2 gB = mul2(gv, Bv[p]);
+                                    dAv = fma2(f2(dt), q, fma2(mul2(gB, f2(uv)), make_float2(dcf[0], dcf[1]), dAv));
+                                    Sg = fma2(gB, make_float2(cf[0], cf[1]), Sg);
+                                    Sa = fma2(gB, av, Sa);
+                                    dB[p] = fma2(mul2(f2(uv), make_float2(cf[0], cf[1])), gv, dB[p]);
+                                }
+                                dA[i][2 * p] = dAv.x;
+                                dA[i][2 * p + 1] = dAv.y;
+                                an[i][p] = av;
+                            }
+                            sums[0][i] = Sg.x + Sg.y;
+                            sums[1][i] = Eg.x + Eg.y;
+                            if (ZOH) sums[NQN - 1][i] = Sa.x + Sa.y;
+                        }
+#pragma unroll
+                        for (int qn = 0; qn < NQN; ++qn)
+                            *reinterpret_cast<float4*>(part + ((j * NQN + qn) * 4 + ng) * 32 + cbase) =
+                                make_float4(sums[qn][0], sums[qn][1], sums[qn][2], sums[qn][3]);
+                        float dBv[NS];
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) { dBv[2 * p] = dB[p].x; dBv[2 * p + 1] = dB[p].y; }
+                        int sel;
+                        bool own;
+                        const float dBs = rs_over_cg<NS>(dBv, lane, sel, own);
+                        if (own) rbc[j * 2 * NT + ng * NS + sel] = dBs;
+                    }
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
+
+            // ---- epilogue (lane = channel): finish du, ddelta_raw, dz, dD
+            if (lane_ok) {
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    if (j < jmax) {
+                        const size_t r = row0 + t0 + j;
+                        float sm[NQN];
+#pragma unroll
+                        for (int qn = 0; qn < NQN; ++qn) {
+                            const float* pp = part + (j * NQN + qn) * 4 * 32 + lane;
+                            sm[qn] = (pp[0] + pp[32]) + (pp[64] + pp[96]);
+                        }
+                        const float uv = Act<T>::to_f(tu[j * 32 + lane]);
+                        const float xr = Act<T>::to_f(tr[j * 32 + lane]);
+                        const float dt = Pd[j * 32 + lane];
+                        const float dyv = Pdy[j * 32 + lane];
+                        const float Sg = sm[0], Eg = sm[1] * kLn2;
+                        const float du = ZOH ? fmaf(Dd, dyv, Sg) : fmaf(dt, Sg, Dd * dyv);
+                        const float ddl = fmaf(uv, ZOH ? sm[NQN - 1] : Sg, Eg);
+                        dD_acc = fmaf(dyv, uv, dD_acc);
+                        dup[r * a.ld_du + dch] = Act<T>::from_f(du);
+                        ddp[r * a.ld_ddelta + dch] = Act<T>::from_f(ddl * sigmoidf_(xr));
+                        if (GATE) {
+                            const float zv = Act<T>::to_f(tz[j * 32 + lane]);
+                            const float go = Act<T>::to_f(tg[j * 32 + lane]);
+                            const float yv = Act<T>::to_f(ty[j * 32 + lane]);
+                            const float sz = sigmoidf_(zv);
+                            dzp[r * a.ld_dz + dch] =
+                                Act<T>::from_f(go * yv * sz * (1.0f + zv * (1.0f - sz)));
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            park();
+        }
+
+        // ---- dB|dC of this chunk: add the cluster's CTAs through DSMEM
+        cluster_sync();
+        if (ok) {
+            const uint32_t cs = static_cast<uint32_t>(gridDim.x / a.ncl);
+            const int per = BCN / static_cast<int>(cs);
+            const int ncol = blockIdx.x / static_cast<int>(cs);
+            for (int e = lane; e < per; e += 32) {
+                const int idx = static_cast<int>(crank) * per + e;
+                const int j = idx / (2 * NT);
+                if (j < jmax) {
+                    float sum = 0.0f;
+                    for (uint32_t rk = 0; rk < cs; ++rk) sum += ld_dsmem(rbc + idx, rk);
+                    a.ws_bc[((static_cast<size_t>(ncol) * a.batch + b) * L + t0 + j) * 2 * NT +
+                            idx % (2 * NT)] = sum;
+                }
+            }
+        }
+
+        // ---- release this TMA stage
+        __syncwarp();
+        if (lane == 0 && ok && it + S < nchunks) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(it + S);
+        }
+    }
+    cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+
+    if (lane == 0 && !ok) {
+        for (int it = waited; it < nchunks && it < waited + S; ++it)
+            mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
+    }
+    __syncwarp();
+    unpark();
+    if (ok) {
+        if (quad_ok) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jn = 0; jn < NS; ++jn)
+                    a.ws_dA[(static_cast<size_t>(b) * Dn + c0 + cbase + i) * NT + ng * NS + jn] =
+                        dA[i][jn];
+        }
+        if (lane_ok) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc;
+    }
+}
+
+// dB, dC: sum of the per-cluster-column planes; dA_log = A * sum_b dA inside the
+// clamp (exactly 0 at or beyond it); dD = sum_b dD.
+__global__ void scan_reduce_kernel(const ScanReduceArgs a) {
+    const size_t M = static_cast<size_t>(a.batch) * a.seqlen;
+    const size_t nBC = M * a.dstate;
+    const size_t nA = static_cast<size_t>(a.dinner) * a.dstate;
+    const size_t total = nBC + nA + (a.dD ? a.dinner : 0);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        if (i < nBC) {
+            const size_t r = i / a.dstate;
+            const int n = static_cast<int>(i % a.dstate);
+            float sb = 0.0f, sc = 0.0f;
+            for (int p = 0; p < a.ncl; ++p) {
+                const float* src = a.ws_bc + (static_cast<size_t>(p) * M + r) * 2 * a.nt;
+                sb += src[n];
+                sc += src[a.nt + n];
+            }
+            if (a.is_bf16) {
+                static_cast<__nv_bfloat16*>(a.dB)[r * a.ld_dB + n] = __float2bfloat16_rn(sb);
+                static_cast<__nv_bfloat16*>(a.dC)[r * a.ld_dC + n] = __float2bfloat16_rn(sc);
+            } else {
+                static_cast<float*>(a.dB)[r * a.ld_dB + n] = sb;
+                static_cast<float*>(a.dC)[r * a.ld_dC + n] = sc;
+            }
+        } else if (i < nBC + nA) {
+            const size_t k = i - nBC;
+            const int d = static_cast<int>(k / a.dstate), n = static_cast<int>(k % a.dstate);
+            const float al = a.A_log[k];
+            float v = 0.0f;
+            if (al > kALogLo && al < kALogHi) {
+                float s = 0.0f;
+                for (int bb = 0; bb < a.nb_sum; ++bb)
+                    s += a.ws_dA[(static_cast<size_t>(bb) * a.dinner + d) * a.nt + n];
+                v = s * -expf(al);
+            }
+            a.dA_log[k] = v;
+        } else {
+            const int d = static_cast<int>(i - nBC - nA);
+            float s = 0.0f;
+            for (int bb = 0; bb < a.nb_sum; ++bb) s += a.ws_dD[static_cast<size_t>(bb) * a.dinner + d];
+            a.dD[d] = s;
+        }
+    }
+}
+
+template <typename T, int NT, int DISC, bool GATE>
+static size_t bwd_smem_bytes() {
+    constexpr int TC = kChunk;
+    constexpr int NTEN = GATE ? 5 : 3;
+    constexpr int NQN = DISC == 1 ? 3 : 2;
+    return kBwdStages * (NTEN * TC * 32 + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
+           + kBwdStages * NT * 32 * sizeof(float)      // checkpoint tiles
+           + 2 * TC * NT * sizeof(float)               // fp32 B|C
+           + (DISC == 1 ? 2 : 1) * 32 * NT * sizeof(float)   // A2 [, 1/A]
+           + 3 * TC * 32 * sizeof(float)               // delta, delta*u, dy
+           + TC * NQN * 4 * 32 * sizeof(float)         // state-sum partials
+           + 2 * 2 * TC * NT * sizeof(float)           // dB|dC for the cluster exchange
+           + kBwdStages * sizeof(uint64_t);
+}
+
+template <typename T, int NT, int DISC, bool GATE>
+static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, int cluster,
+                                cudaStream_t st) {
+    const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE>();
+    auto kern = scan_bwd_kernel<T, NT, DISC, GATE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.ncl * cluster), static_cast<unsigned>(a.batch));
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, maps, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T, int NT>
+static cudaError_t launch_bwd_nt(int disc, bool gate, const BwdMaps& m, const ScanBwdArgs& a,
+                                 int cl, cudaStream_t st) {
+    if (disc == 0)
+        return gate ? launch_bwd_t<T, NT, 0, true>(m, a, cl, st)
+                    : launch_bwd_t<T, NT, 0, false>(m, a, cl, st);
+    return gate ? launch_bwd_t<T, NT, 1, true>(m, a, cl, st)
+                : launch_bwd_t<T, NT, 1, false>(m, a, cl, st);
+}
+
+cudaError_t launch_scan_bwd(int dtype, int nt, int disc, bool gate, const BwdMaps& maps,
+                            const ScanBwdArgs& a, int cluster, cudaStream_t stream) {
+    if (dtype == 0)
+        return nt == 8 ? launch_bwd_nt<float, 8>(disc, gate, maps, a, cluster, stream)
+                       : launch_bwd_nt<float, 16>(disc, gate, maps, a, cluster, stream);
+    return nt == 8 ? launch_bwd_nt<__nv_bfloat16, 8>(disc, gate, maps, a, cluster, stream)
+                   : launch_bwd_nt<__nv_bfloat16, 16>(disc, gate, maps, a, cluster, stream);
+}
+
+cudaError_t read_clear_fault_bwd(unsigned* out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_ssm_fault, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_ssm_fault, &zero, sizeof(unsigned));
+}
+
+cudaError_t launch_scan_reduce(const ScanReduceArgs& a, cudaStream_t stream) {
+    const size_t M = static_cast<size_t>(a.batch) * a.seqlen;
+    const size_t total = M * a.dstate + static_cast<size_t>(a.dinner) * a.dstate + a.dinner;
+    if (total == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, 152 * 16));
+    scan_reduce_kernel<<<blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm
