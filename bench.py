@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Throughput of the Mamba-1 selective scan forward + backward on GB300.
+
+One step = ssm_scan_fwd + ssm_scan_bwd (through the C ABI) over one batch of
+the Mamba-1.4B-like layer workload: batch 8, seqlen 2048, dinner 4096,
+dstate 16, bf16 activations (u, delta_raw, z, B, C, dout), fp32 A_log / D,
+fp32 state and accumulation, Euler B.  Inputs are seeded synthetic data with
+the distributions of the workload; they are resident in HBM and larger than
+L2 (805 MB of activations per step), so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `value` is whole-job tokens/s in Mtokens/s:
+batch*seqlen tokens per step per rank.  Several GPUs run independent
+replicas (weak scaling): the scan has no cross-rank exchange on this path.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded
+sample of the same workload per step) and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Mamba-1 selective scan fwd+bwd Mtokens/s; achieved % of HBM/SFU roofline"
+WORKLOAD = "mamba1p4b_scan_bf16"
+SM_COUNT = 152
+EX2_PER_CLK_PER_SM = 32          # MUFU ex2 rate of sm_103 (csrc/probe_pipes.cu measures it)
+FP32_LANES_PER_CLK_PER_SM = 128  # FFMA lanes (packed f32x2 does not raise it)
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ----------------------------------------------------------------- algorithmic work
+
+def algorithmic(cfg):
+    """Bytes and exponentials of one forward and one backward pass (the
+    method's own data, not the implementation's checkpoints)."""
+    M, D, N = cfg["batch"] * cfg["seqlen"], cfg["dinner"], cfg["dstate"]
+    s = 2 if cfg["dtype"] == "bf16" else 4
+    small = D * N * 4 + D * 4
+    fwd_bytes = 4 * M * D * s + 2 * M * N * s + small          # u, delta_raw, z in; out; B, C
+    bwd_bytes = 7 * M * D * s + 4 * M * N * s + 2 * small      # u, dr, z, dout in; du, ddr, dz out;
+    #                                                             B, C in; dB, dC out; A_log/D, dA_log/dD
+    exps = M * D * N                                           # exp(delta A) per pass
+    return fwd_bytes, bwd_bytes, exps
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- traffic record
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_ssm_gb300", "csrc")
+    for name in ("scan_bwd.cu", "scan_args.cuh", "ssm_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes (read + write) per backward launch from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "scan_bwd_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_digest") != source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+
+def cpu_oracle_sample(cfg, inp, target_s=12.0):
+    """Time the fp64 oracle (scan fwd + bwd) on a slice of the workload: one
+    batch row, all seqlen steps, the first `dsub` channels.  dB/dC/dA_log/dD
+    over the slice are part of the work.  Returns (Mtokens/s, sample text, s)."""
+    import numpy as np
+    import oracle
+    L, D, N = cfg["seqlen"], cfg["dinner"], cfg["dstate"]
+
+    def run(dsub):
+        sl = slice(0, dsub)
+        u, dr, z, dout = (inp[k][:L, sl].astype(np.float64) for k in ("u", "delta_raw", "z",
+                                                                       "dout"))
+        B, C = inp["B"][:L].astype(np.float64), inp["C"][:L].astype(np.float64)
+        Al, Dv = inp["A_log"][sl].astype(np.float64), inp["D"][sl].astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.scan_fwd(u, dr, Al, B, C, Dv, z, 0, batch=1)
+        oracle.scan_bwd(u, dr, Al, B, C, Dv, z, dout, 0, batch=1)
+        return time.perf_counter() - t0
+
+    oracle.build()
+    probe = 16
+    t = run(probe)
+    dsub = int(min(D, max(probe, probe * target_s / max(t, 1e-3))))
+    dsub = max(8, dsub // 8 * 8)
+    t = run(dsub)
+    tokens = L * dsub / D            # rows of the full-width problem this slice is worth
+    return tokens / t / 1e6, f"batch row 0, {L} steps, channels [0, {dsub}) of {D}", t
+
+
+# ----------------------------------------------------------------- GPU leg
+
+def run_gb300(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group(backend="nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    ssm.load()
+
+    cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
+    inp = workloads.named_scan_inputs(WORKLOAD)
+    bt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    host = {k: torch.from_numpy(inp[k]) for k in ("u", "delta_raw", "z", "B", "C", "dout")}
+    host = {k: v.to(bt) for k, v in host.items()}
+    host["A_log"] = torch.from_numpy(inp["A_log"])
+    host["D"] = torch.from_numpy(inp["D"])
+    t = {k: v.to(dev) for k, v in host.items()}
+    Bn = cfg["batch"]
+    out = torch.empty_like(t["u"])
+    du, ddr, dz = (torch.empty_like(t["u"]) for _ in range(3))
+    dB, dC = torch.empty_like(t["B"]), torch.empty_like(t["C"])
+    dA = torch.empty_like(t["A_log"])
+    dD = torch.empty_like(t["D"])
+    desc = ssm.scan_desc(t["u"], t["delta_raw"], t["A_log"], t["B"], t["C"], t["z"], batch=Bn,
+                         out=out, dout=t["dout"], du=du, ddelta=ddr, dz=dz, dB=dB, dC=dC)
+    ctx = torch.empty(ssm.ssm_scan_ctx_bytes(desc), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ssm.ssm_scan_bwd_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ssm.ssm_scan_fwd(desc, t["u"], t["delta_raw"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+                         out, ctx, None, stream)
+
+    def bwd():
+        ssm.ssm_scan_bwd(desc, t["u"], t["delta_raw"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+                         t["dout"], ctx, du, ddr, dA, dB, dC, dD, dz, wsb, stream)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if ssm.ssm_device_faults():
+        raise RuntimeError("kernel wait timeout during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms_total = start.elapsed_time(end)
+    t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if ssm.ssm_device_faults():
+        raise RuntimeError("kernel wait timeout in the timed region")
+    ms_step = ms_total / K
+    if ws > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    M = cfg["batch"] * cfg["seqlen"]
+    value = ws * M / (ms_step * 1e-3) / 1e6
+
+    # ---- roofline (spec definition: max(bytes / HBM, exps / SFU) per pass)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    sm_mhz = clk["sm_mhz"] or float(peaks.get("sm_max_mhz", 2070.0))
+    sfu_rate = EX2_PER_CLK_PER_SM * SM_COUNT * sm_mhz * 1e6      # ex2 / s
+    fwd_b, bwd_b, exps = algorithmic(cfg)
+    bound_fwd = max(fwd_b / (hbm * 1e9), exps / sfu_rate)
+    bound_bwd = max(bwd_b / (hbm * 1e9), exps / sfu_rate)
+    bwd_hbm_bound = bwd_b / (hbm * 1e9) >= exps / sfu_rate
+    achieved_bwd = (bwd_b / (t_bwd * 1e-3) / 1e9) if bwd_hbm_bound else exps / (t_bwd * 1e-3) / 1e12
+    peak_bwd = hbm if bwd_hbm_bound else sfu_rate / 1e12
+    traffic = recorded_traffic()
+    roofline = {
+        "kernel": "ssm_scan_bwd (scan_bwd_kernel + scan_reduce_kernel)",
+        "bound": "hbm" if bwd_hbm_bound else "sfu",
+        "achieved": round(achieved_bwd, 3),
+        "peak": round(peak_bwd, 3),
+        "unit": "GB/s" if bwd_hbm_bound else "Tex2/s",
+        "frac": round(achieved_bwd / peak_bwd, 4),
+        "traffic": traffic,
+        "peak_source": f"{peak_kind} hbm_gbs" if bwd_hbm_bound else
+                       f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {SM_COUNT} SMs x {sm_mhz:.0f} MHz",
+        "step_frac": round((bound_fwd + bound_bwd) / ((t_fwd + t_bwd) * 1e-3), 4),
+        "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4),
+        "fwd_frac": round(bound_fwd / (t_fwd * 1e-3), 4),
+        "bwd_frac": round(bound_bwd / (t_bwd * 1e-3), 4),
+    }
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        outs = {"out": out, "du": du, "ddelta": ddr, "dz": dz, "dB": dB, "dC": dC, "dA_log": dA,
+                "dD": dD}
+        hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+        K2 = max(1, min(K, 5))
+
+        def e2e_step():
+            for k, v in pin.items():
+                t[k].copy_(v, non_blocking=True)
+            fwd()
+            bwd()
+            for k, v in outs.items():
+                hout[k].copy_(v, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = s0.elapsed_time(s1) / K2
+        if ws > 1:
+            tt = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        e2e = {"value": round(ws * M / (ms_e2e * 1e-3) / 1e6, 4), "unit": "Mtokens/s",
+               "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        v, sample, secs = cpu_oracle_sample(cfg, inp)
+        cpu = {"value": round(v, 6), "unit": "Mtokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample, "seconds": round(secs, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 4), "unit": "Mtokens/s", "n_gpus": ws,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; the workload's distributions)",
+            "config": {"workload": f"{WORKLOAD}: batch 8, seqlen 2048, dinner 4096, dstate 16, "
+                                   "bf16 activations, fp32 A_log/D and state, Euler B, SiLU gate",
+                       "global_batch": cfg["batch"] * ws, "seq_len": cfg["seqlen"],
+                       "dinner": cfg["dinner"], "dstate": cfg["dstate"],
+                       "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (805 MB of activations per step), no flush"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- reference leg
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from selective_state_space_ssm_gb300 import workloads
+    cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
+    inp = workloads.named_scan_inputs(WORKLOAD, batch=1)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals, secs = [], []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        v, sample, s = cpu_oracle_sample(cfg, inp, target_s=per_step)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(s)
+    value = statistics.mean(vals)
+    ms = statistics.mean(secs) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Mtokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; the workload's distributions)",
+        "config": {"workload": f"{WORKLOAD}: batch 8, seqlen 2048, dinner 4096, dstate 16",
+                   "global_batch": cfg["batch"], "seq_len": cfg["seqlen"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "Mtokens/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -64,7 +64,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (M, dinner) activation viewed as [batch][seqlen][dinner] with row stride ld;
 // box = 32 channels x box_rows steps x 1 batch row; out-of-range reads fill 0.
 bool encode_act(CUtensorMap* m, const void* ptr, int dtype, int dinner, int seqlen, int batch,
-                int64_t ld, int box_rows) {
+                int64_t ld, int box_rows, int box_ch = 32) {
     auto fn = encode_fn();
     if (!fn) return false;
     const size_t es = dtype == SSM_BF16 ? 2 : 4;
@@ -72,7 +72,7 @@ bool encode_act(CUtensorMap* m, const void* ptr, int dtype, int dinner, int seql
                           static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es,
                              static_cast<cuuint64_t>(ld) * es * static_cast<cuuint64_t>(seqlen)};
-    cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_ch), static_cast<cuuint32_t>(box_rows), 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = fn(m, dtype == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -242,11 +242,12 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
     ssm::FwdMaps maps;
     const int nt = nt_of(d->dstate);
     const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
-    if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile) ||
+    const int fc = ssm::kFwdChannels;
+    if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile, fc) ||
         !encode_act(&maps.dr, delta_raw, d->dtype, d->dinner, d->seqlen, d->batch, r.delta,
-                    ssm::kFwdTile) ||
+                    ssm::kFwdTile, fc) ||
         !encode_act(&maps.z, z ? z : u, d->dtype, d->dinner, d->seqlen, d->batch, z ? r.z : r.u,
-                    ssm::kFwdTile) ||
+                    ssm::kFwdTile, fc) ||
         !(bct ? encode_bc(&maps.B, B, d->dtype, d->dstate, d->seqlen, d->batch, r.B, nt, ssm::kFwdTile)
               : encode_act(&maps.B, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)) ||
         !(bct ? encode_bc(&maps.C, C, d->dtype, d->dstate, d->seqlen, d->batch, r.C, nt, ssm::kFwdTile)

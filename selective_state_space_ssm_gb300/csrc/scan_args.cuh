@@ -12,9 +12,9 @@ namespace ssm {
 // the backward recomputes h inside each chunk of kChunk steps.
 constexpr int kChunk = 8;
 
-// Forward: one thread per channel (all dstate states in registers), one warp
-// per CTA so 32-channel work units spread evenly over the 152 SMs.
-constexpr int kFwdWarps = 1;
+// Forward: two lanes per channel (half of the states each), one warp of 16
+// channels per CTA, so the work spreads evenly over the 152 SMs.
+constexpr int kFwdChannels = 16;
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
 

@@ -33,9 +33,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
     uint32_t raddr;
@@ -89,12 +91,13 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr int NQN = ZOH ? 3 : 2;            // state sums kept per (step, channel)
 
     extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int AR = NT == 16 ? 20 : 10;      // padded A2 row: conflict-free per-lane reads
     T* tiles = reinterpret_cast<T*>(smem);                               // [S][STAGE]
     float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][32]
-    float* bcs = cks + S * NT * 32;                                      // [TC][2NT]
-    float* A2s = bcs + BCN;                                              // [32][NT]
-    float* iAs = A2s + 32 * NT;                                          // [32][NT] (ZOH)
-    float* Pd = iAs + (ZOH ? 32 * NT : 0);                               // [TC][32] delta
+    float* bcs = cks + S * NT * 32;                                      // [TC][NT] B | [TC][NT] C
+    float* A2s = bcs + BCN;                                              // [32][AR]
+    float* iAs = A2s + 32 * AR;                                          // [32][AR] (ZOH)
+    float* Pd = iAs + (ZOH ? 32 * AR : 0);                               // [TC][32] delta
     float* Pbs = Pd + TILE;                                              // [TC][32] delta*u | u
     float* Pdy = Pbs + TILE;                                             // [TC][32] dy
     float* part = Pdy + TILE;                                            // [TC][NQN][4][32]
@@ -118,8 +121,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     for (int n = 0; n < NT; ++n) {
         const bool ok = lane_ok && n < N;
         const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(dch) * N + n]) : -1.0f;
-        A2s[lane * NT + n] = ok ? A * kLog2e : 0.0f;
-        if (ZOH) iAs[lane * NT + n] = 1.0f / A;
+        A2s[lane * AR + n] = ok ? A * kLog2e : 0.0f;
+        if (ZOH) iAs[lane * AR + n] = 1.0f / A;
     }
     const float Dd = (lane_ok && a.D) ? a.D[dch] : 0.0f;
 
@@ -195,53 +198,91 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     bool ok = true;
     int waited = 0;
 
+    // dB|dC through DSMEM, one chunk behind: at the start of an iteration the
+    // peers have long arrived for the previous chunk, so the wait rarely blocks.
+    const uint32_t cs = static_cast<uint32_t>(gridDim.x / a.ncl);
+    const int ncol = blockIdx.x / static_cast<int>(cs);
+    auto exchange = [&](int kc_prev, int buf) {
+        const int t0p = kc_prev * TC;
+        const int jmp = min(TC, L - t0p);
+        const int per = BCN / static_cast<int>(cs);
+        const float* src = rBC + buf * BCN;
+        for (int e = lane; e < per; e += 32) {
+            const int idx = static_cast<int>(crank) * per + e;
+            const int j = idx / (2 * NT);
+            if (j < jmp) {
+                float sum = 0.0f;
+                for (uint32_t rk = 0; rk < cs; ++rk) sum += ld_dsmem(src + idx, rk);
+                a.ws_bc[((static_cast<size_t>(ncol) * a.batch + b) * L + t0p + j) * 2 * NT +
+                        idx % (2 * NT)] = sum;
+            }
+        }
+    };
+
     for (int it = 0; it < nchunks; ++it) {
         const int kc = nchunks - 1 - it;
         const int t0 = kc * TC;
         const int jmax = min(TC, L - t0);
         const int s = it % S;
-        const float* bc = bcs;
-        float* rbc = rBC + (it & 1) * BCN;
+        float* rbc = rBC + (it & 1) * BCN;   // this chunk's warp-reduced dB|dC
 
+        if (it > 0) {
+            cluster_wait();
+            if (ok) exchange(kc + 1, (it - 1) & 1);
+            __syncwarp();
+        }
         if (ok) ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) waited = it + 1;
 
+        const T* tu = tiles + s * STAGE;
+        const T* tr = tu + TILE;
+        const T* tg = tu + 2 * TILE;
+        const T* tz = tu + 3 * TILE;
+        const T* ty = tu + 4 * TILE;
+        const float* ck = cks + s * NT * 32;
         if (ok) {
-            const T* tu = tiles + s * STAGE;
-            // fp32 B|C tile of this chunk: bcs[j][0..NT) = B, bcs[j][NT..2NT) = C
+            // fp32 B and C of this chunk: [TC][NT] each.  fp32 TMA tiles are used
+            // in place; bf16 tiles are widened into bcs, 8 values per lane.
+            const float* Bf;
+            const float* Cf;
             {
                 const T* Bs = tu + NTEN * TILE;
-                const T* Cs = Bs + BCT;
-#pragma unroll 4
-                for (int e = lane; e < BCN; e += 32) {
-                    const int j = e / (2 * NT), w = e % (2 * NT);
-                    const int n = w < NT ? w : w - NT;
-                    float v;
-                    if (bc_tma) {
-                        v = Act<T>::to_f(w < NT ? Bs[j * NT + n] : Cs[j * NT + n]);
-                    } else {
-                        const int t = t0 + j;
-                        v = 0.0f;
+                if (bc_tma && sizeof(T) == 4) {
+                    Bf = reinterpret_cast<const float*>(Bs);
+                } else if (bc_tma) {
+                    for (int g8 = lane; g8 < BCN / 8; g8 += 32) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        float f[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            f[2 * q] = __uint_as_float(w[q] << 16);
+                            f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+                        }
+                        *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
+                    }
+                    Bf = bcs;
+                } else {
+                    for (int e = lane; e < BCN; e += 32) {
+                        const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = t0 + j;
+                        float v = 0.0f;
                         if (t < L && n < N) {
                             const size_t r = row0 + t;
-                            v = (w < NT) ? Act<T>::load(Bp + r * a.ld_B + n)
-                                         : Act<T>::load(Cp + r * a.ld_C + n);
+                            v = isC ? Act<T>::load(Cp + r * a.ld_C + n) : Act<T>::load(Bp + r * a.ld_B + n);
                         }
+                        bcs[e] = v;
                     }
-                    bcs[e] = v;
+                    Bf = bcs;
                 }
+                Cf = Bf + BCT;
             }
-            const T* tr = tu + TILE;
-            const T* tg = tu + 2 * TILE;
-            const T* tz = tu + 3 * TILE;
-            const T* ty = tu + 4 * TILE;
-            const float* ck = cks + s * NT * 32;
 
             // ---- prologue (lane = channel): delta, delta*u (or u), dy.  All TC
             //      steps run: past seqlen the tiles, B and C are zero, so dy = 0
             //      and the extra steps add exactly nothing to g or any gradient.
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < TC; ++j) {
                 {
                     const float uv = Act<T>::to_f(tu[j * 32 + lane]);
@@ -289,7 +330,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         float2 Bv[NS / 2];
 #pragma unroll
                         for (int p = 0; p < NS / 2; ++p)
-                            Bv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + ng * NS + 2 * p);
+                            Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
                         float2 dC[NS / 2];
 #pragma unroll
                         for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
@@ -298,24 +339,24 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
                             for (int p = 0; p < NS / 2; ++p) {
                                 const float2 A2p = *reinterpret_cast<const float2*>(
-                                    A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                                    A2s + (cbase + i) * AR + ng * NS + 2 * p);
                                 const float2 x = mul2(f2(dlA[i]), A2p);
                                 const float2 av = make_float2(ex2(x.x), ex2(x.y));
                                 const float2 ahv = mul2(av, h[i][p]);
-                                float2 bu;
+                                float2 bu = f2(bsA[i]);
                                 if (!ZOH) {
-                                    bu = mul2(f2(bsA[i]), Bv[p]);
+                                    h[i][p] = fma2(bu, Bv[p], ahv);
                                 } else {
                                     const float2 iA = *reinterpret_cast<const float2*>(
-                                        iAs + (cbase + i) * NT + ng * NS + 2 * p);
+                                        iAs + (cbase + i) * AR + ng * NS + 2 * p);
                                     const float xn0 = x.x * kLn2, xn1 = x.y * kLn2;
                                     const float cf0 = fabsf(xn0) < 0.5f ? dlA[i] * phi1_series(xn0)
                                                                         : (av.x - 1.0f) * iA.x;
                                     const float cf1 = fabsf(xn1) < 0.5f ? dlA[i] * phi1_series(xn1)
                                                                         : (av.y - 1.0f) * iA.y;
                                     bu = mul2(mul2(make_float2(cf0, cf1), f2(bsA[i])), Bv[p]);
+                                    h[i][p] = add2(ahv, bu);
                                 }
-                                h[i][p] = add2(ahv, bu);
                                 ah[j][i][p] = ahv;
                                 dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
                             }
@@ -342,7 +383,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p) {
                         const float2 A2p = *reinterpret_cast<const float2*>(
-                            A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                            A2s + (cbase + i) * AR + ng * NS + 2 * p);
                         const float2 x = mul2(f2(dl_next[i]), A2p);
                         an[i][p] = make_float2(ex2(x.x), ex2(x.y));
                     }
@@ -358,8 +399,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         float2 Bv[NS / 2], Cv[NS / 2];
 #pragma unroll
                         for (int p = 0; p < NS / 2; ++p) {
-                            Bv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + ng * NS + 2 * p);
-                            Cv[p] = *reinterpret_cast<const float2*>(bc + j * 2 * NT + NT + ng * NS + 2 * p);
+                            Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                            Cv[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
                         }
                         float2 dB[NS / 2];
 #pragma unroll
@@ -372,7 +413,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
                             for (int p = 0; p < NS / 2; ++p) {
                                 const float2 A2p = *reinterpret_cast<const float2*>(
-                                    A2s + (cbase + i) * NT + ng * NS + 2 * p);
+                                    A2s + (cbase + i) * AR + ng * NS + 2 * p);
                                 // g_t = C_t dy_t + a_{t+1} g_{t+1}
                                 float2 gv = make_float2(g[i][2 * p], g[i][2 * p + 1]);
                                 gv = fma2(an[i][p], gv, mul2(Cv[p], f2(dyA[i])));
@@ -389,7 +430,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                                     dB[p] = fma2(f2(bsA[i]), gv, dB[p]);
                                 } else {
                                     const float2 iA = *reinterpret_cast<const float2*>(
-                                        iAs + (cbase + i) * NT + ng * NS + 2 * p);
+                                        iAs + (cbase + i) * AR + ng * NS + 2 * p);
                                     const float dt = dlA[i], uv = bsA[i];
                                     float cf[2], dcf[2];
 #pragma unroll
@@ -418,7 +459,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         }
 #pragma unroll
                         for (int qn = 0; qn < NQN; ++qn)
-                            *reinterpret_cast<float4*>(part + ((j * NQN + qn) * 4 + ng) * 32 + cbase) =
+                            *reinterpret_cast<float4*>(part + ((j * NQN + qn) * 4 + ng) * 32 +
+                                                       ((cbase + 8 * ng) & 31)) =
                                 make_float4(sums[qn][0], sums[qn][1], sums[qn][2], sums[qn][3]);
                         float dBv[NS];
 #pragma unroll
@@ -433,18 +475,25 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 4; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
+        }
+        // this chunk's dB|dC rows are in rBC: publish them before the epilogue's
+        // global stores are issued (the release then has little to wait for)
+        __syncwarp();
+        cluster_arrive();
 
+        if (ok) {
             // ---- epilogue (lane = channel): finish du, ddelta_raw, dz, dD
             if (lane_ok) {
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < TC; ++j) {
                     if (j < jmax) {
                         const size_t r = row0 + t0 + j;
                         float sm[NQN];
 #pragma unroll
                         for (int qn = 0; qn < NQN; ++qn) {
-                            const float* pp = part + (j * NQN + qn) * 4 * 32 + lane;
-                            sm[qn] = (pp[0] + pp[32]) + (pp[64] + pp[96]);
+                            const float* pp = part + (j * NQN + qn) * 4 * 32;
+                            sm[qn] = (pp[lane] + pp[32 + ((lane + 8) & 31)]) +
+                                     (pp[64 + ((lane + 16) & 31)] + pp[96 + ((lane + 24) & 31)]);
                         }
                         const float uv = Act<T>::to_f(tu[j * 32 + lane]);
                         const float xr = Act<T>::to_f(tr[j * 32 + lane]);
@@ -471,32 +520,19 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             park();
         }
 
-        // ---- dB|dC of this chunk: add the cluster's CTAs through DSMEM
-        cluster_sync();
-        if (ok) {
-            const uint32_t cs = static_cast<uint32_t>(gridDim.x / a.ncl);
-            const int per = BCN / static_cast<int>(cs);
-            const int ncol = blockIdx.x / static_cast<int>(cs);
-            for (int e = lane; e < per; e += 32) {
-                const int idx = static_cast<int>(crank) * per + e;
-                const int j = idx / (2 * NT);
-                if (j < jmax) {
-                    float sum = 0.0f;
-                    for (uint32_t rk = 0; rk < cs; ++rk) sum += ld_dsmem(rbc + idx, rk);
-                    a.ws_bc[((static_cast<size_t>(ncol) * a.batch + b) * L + t0 + j) * 2 * NT +
-                            idx % (2 * NT)] = sum;
-                }
-            }
-        }
-
         // ---- release this TMA stage
         __syncwarp();
-        if (lane == 0 && ok && it + S < nchunks) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(it + S);
-        }
+        if (lane == 0 && ok && it + S < nchunks) issue(it + S);
     }
-    cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+    if (nchunks > 0) {
+        // the last chunk's rows, then keep every CTA alive until its peers
+        // have finished reading its shared memory
+        cluster_wait();
+        if (ok) exchange(0, (nchunks - 1) & 1);
+        __syncwarp();
+        cluster_arrive();
+        cluster_wait();
+    }
 
     if (lane == 0 && !ok) {
         for (int it = waited; it < nchunks && it < waited + S; ++it)
@@ -570,8 +606,8 @@ static size_t bwd_smem_bytes() {
     constexpr int NQN = DISC == 1 ? 3 : 2;
     return kBwdStages * (NTEN * TC * 32 + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
            + kBwdStages * NT * 32 * sizeof(float)      // checkpoint tiles
-           + 2 * TC * NT * sizeof(float)               // fp32 B|C
-           + (DISC == 1 ? 2 : 1) * 32 * NT * sizeof(float)   // A2 [, 1/A]
+           + 2 * TC * NT * sizeof(float)               // fp32 B|C (bf16 or unaligned B/C)
+           + (DISC == 1 ? 2 : 1) * 32 * (NT == 16 ? 20 : 10) * sizeof(float)   // A2 [, 1/A]
            + 3 * TC * 32 * sizeof(float)               // delta, delta*u, dy
            + TC * NQN * 4 * 32 * sizeof(float)         // state-sum partials
            + 2 * 2 * TC * NT * sizeof(float)           // dB|dC for the cluster exchange

@@ -19,20 +19,19 @@
 
 namespace ssm {
 
-// One step of the recurrence for all NT states of this thread's channel:
-// h = exp(dt A) h + beta u, returns sum_n C_n h_n.  bs = dt*u (Euler) or u (ZOH).
-template <int NT, int DISC>
-__device__ __forceinline__ float fwd_step(float2 (&h)[NT / 2], const float2 (&A2)[NT / 2],
-                                          const float2 (&Anat)[NT / 2], const float2 (&invA)[NT / 2],
-                                          const float* Bt, float dt, float bs) {
-    const float* Ct = Bt + NT;
+// One step of the recurrence for the NL states this lane owns:
+// h = exp(dt A) h + beta u; returns sum_n C_n h_n over those states.
+// Bt/Ct point at the lane's first state in the fp32 B|C tile row.
+// bs = dt*u (Euler) or u (ZOH).
+template <int NL, int DISC>
+__device__ __forceinline__ float fwd_step(float2 (&h)[NL / 2], const float2 (&A2)[NL / 2],
+                                          const float2 (&Anat)[NL / 2], const float2 (&invA)[NL / 2],
+                                          const float* Bt, const float* Ct, float dt, float bs) {
     const float2 dt2 = f2(dt);
     const float2 bs2 = f2(bs);
-    float2 acc[4];
+    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-    for (int m = 0; m < 4; ++m) acc[m] = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int q4 = 0; q4 < NT / 4; ++q4) {
+    for (int q4 = 0; q4 < NL / 4; ++q4) {
         const float4 B4 = *reinterpret_cast<const float4*>(Bt + 4 * q4);
         const float4 C4 = *reinterpret_cast<const float4*>(Ct + 4 * q4);
 #pragma unroll
@@ -53,82 +52,101 @@ __device__ __forceinline__ float fwd_step(float2 (&h)[NT / 2], const float2 (&A2
                 bu = mul2(mul2(make_float2(c0f, c1f), bs2), Bq);
             }
             h[q] = fma2(av, h[q], bu);
-            acc[q % 4] = fma2(Cq, h[q], acc[q % 4]);
+            acc[hq] = fma2(Cq, h[q], acc[hq]);
         }
     }
-    const float2 s = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+    const float2 s = add2(acc[0], acc[1]);
     return s.x + s.y;
 }
 
-// Fill the fp32 B|C tile bcs[TS][2NT] (B in columns [0, NT), C in [NT, 2NT))
-// for steps [k*TS, k*TS + TS), either from the TMA-staged tiles Bs/Cs
-// ([TS][NT] in the activation dtype, zero past seqlen and dstate) or, when B/C
-// are not TMA-aligned, straight from global memory.
+// fp32 B and C of one tile, [TS][NT] each (states past dstate and steps past
+// seqlen read 0).  fp32 TMA tiles are used in place; bf16 TMA tiles are
+// widened into bcs 8 values per lane; B/C that are not TMA-aligned are read
+// straight from global memory into bcs.  Returns the B pointer (C follows
+// TS*NT floats later).
 template <typename T, int NT, int TS>
-__device__ __forceinline__ void fwd_fill_bc(float* bcs, const T* Bs, const T* Cs, bool from_tma,
-                                            const T* Bp, const T* Cp, int64_t ldB, int64_t ldC,
-                                            size_t row0, int k, int L, int N, int lane) {
-    constexpr int BCN = 2 * TS * NT;
-#pragma unroll 4
-    for (int e = lane; e < BCN; e += 32) {
-        const int j = e / (2 * NT), w = e % (2 * NT);
-        const int n = w < NT ? w : w - NT;
-        float v;
-        if (from_tma) {
-            v = Act<T>::to_f(w < NT ? Bs[j * NT + n] : Cs[j * NT + n]);
-        } else {
-            const int t = k * TS + j;
-            v = 0.0f;
-            if (t < L && n < N) {
-                const size_t r = row0 + t;
-                v = (w < NT) ? Act<T>::load(Bp + r * ldB + n) : Act<T>::load(Cp + r * ldC + n);
+__device__ __forceinline__ const float* fwd_stage_bc(float* bcs, const T* Bs, bool from_tma,
+                                                     const T* Bp, const T* Cp, int64_t ldB,
+                                                     int64_t ldC, size_t row0, int k, int L, int N,
+                                                     int lane) {
+    constexpr int BCT = TS * NT;
+    if (from_tma && sizeof(T) == 4) return reinterpret_cast<const float*>(Bs);
+    if (from_tma) {
+        for (int g8 = lane; g8 < 2 * BCT / 8; g8 += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                f[2 * q] = __uint_as_float(w[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
             }
+            *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        return bcs;
+    }
+    for (int e = lane; e < 2 * BCT; e += 32) {
+        const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = k * TS + j;
+        float v = 0.0f;
+        if (t < L && n < N) {
+            const size_t r = row0 + t;
+            v = isC ? Act<T>::load(Cp + r * ldC + n) : Act<T>::load(Bp + r * ldB + n);
         }
         bcs[e] = v;
     }
+    return bcs;
 }
 
+// Lane layout: a warp-sized CTA owns 16 channels; lanes l and l ^ 16 share
+// channel l & 15, lane l < 16 holding states [0, NT/2) and lane l >= 16
+// states [NT/2, NT).  Each lane of a pair works out the per-step scalars
+// (softplus, gate) for half of the tile's steps and the pair swaps them with
+// one shuffle, so nothing per step is computed twice.
 template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(32 * kFwdWarps)
+__global__ void __launch_bounds__(32)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
-    constexpr int CW = 32 * kFwdWarps;
-    static_assert(CW == 32, "one warp per CTA");
+    constexpr int CW = kFwdChannels;                    // channels per CTA (16)
     constexpr int TS = kFwdTile;
+    constexpr int HT = TS / 2;                          // steps whose scalars a lane computes
     constexpr int S = kFwdStages;
     constexpr int NTEN = GATE ? 3 : 2;
+    constexpr int NL = NT / 2;                          // states per lane
+    constexpr int NQ = NL / 2;                          // state pairs per lane
     constexpr int TILE = TS * CW;                       // elements per activation tile
     constexpr int BCT = TS * NT;                        // elements per B or C tile
     constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
     constexpr uint32_t kBCBytes = 2 * BCT * sizeof(T);
     constexpr int STAGE = NTEN * TILE + 2 * BCT;        // elements per stage
-    constexpr int NQ = NT / 2;                          // state pairs
-    static_assert(TS % kChunk == 0, "tiles hold whole checkpoint chunks");
+    static_assert(TS % kChunk == 0 && HT == kChunk, "a lane's half tile is one checkpoint chunk");
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
 
     extern __shared__ __align__(128) unsigned char smem[];
     T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
-    float* bcs = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][2NT]
+    float* bcs = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] B | C
     uint64_t* full = reinterpret_cast<uint64_t*>(bcs + 2 * BCT);             // [S]
 
-    const int tid = threadIdx.x;
+    const int lane = threadIdx.x;
+    const int ch = lane & 15, half = lane >> 4;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
-    const int d = c0 + tid;
+    const int d = c0 + ch;
     const bool active = d < a.dinner;
     const int L = a.seqlen, N = a.dstate;
     const int ntiles = (L + TS - 1) / TS;
     const size_t row0 = static_cast<size_t>(b) * L;
     const bool bc_tma = a.bc_tma != 0;
+    const int nbase = half * NL;                        // first state of this lane
 
-    // Per-channel constants: A*log2(e) as the ex2 argument scale (0 on padding
-    // states and inactive lanes, where B = C = 0 keeps h at 0).
+    // Per-(channel, state) constants: A*log2(e) as the ex2 argument scale (0 on
+    // padding states and inactive lanes, where B = C = 0 keeps h at 0).
     float2 A2[NQ], Anat[NQ], invA[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         float v[2], w[2], r[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = 2 * q + e;
+            const int n = nbase + 2 * q + e;
             const bool ok = active && n < N;
             const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
             v[e] = ok ? A * kLog2e : 0.0f;
@@ -159,12 +177,12 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         }
     };
 
-    if (tid == 0) {
+    if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    if (tid == 0)
+    __syncwarp();
+    if (lane == 0)
         for (int k = 0; k < S && k < ntiles; ++k) issue(k);
 
     T* outp = static_cast<T*>(a.out);
@@ -172,25 +190,28 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     int k = 0;
     for (; k < ntiles; ++k) {
         const int s = k % S;
-        const bool ok = mbar_wait(&full[s], (k / S) & 1, kFaultFwdWait);
-        if (!__syncthreads_and(ok)) break;
+        bool ok = mbar_wait(&full[s], (k / S) & 1, kFaultFwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
 
         const T* tu = tiles + s * STAGE;
         const T* tr = tu + TILE;
         const T* tz = tu + 2 * TILE;
-        fwd_fill_bc<T, NT, TS>(bcs, tu + NTEN * TILE, tu + NTEN * TILE + BCT, bc_tma, Bp, Cp,
-                               a.ld_B, a.ld_C, row0, k, L, N, tid);
+        const float* Bf = fwd_stage_bc<T, NT, TS>(bcs, tu + NTEN * TILE, bc_tma, Bp, Cp, a.ld_B,
+                                                  a.ld_C, row0, k, L, N, lane);
         const int jmax = min(TS, L - k * TS);
 
-        // Phase A: the per-step scalars of the whole tile (independent steps).
-        float dtv[TS], bsc[TS], dterm[TS], gate[TS];
+        // Phase A: this lane's half of the tile's per-step scalars, then swap
+        // delta and delta*u (or u) with the partner lane.
+        float dtv[TS], bsc[TS], dterm[HT], gate[HT];
 #pragma unroll
-        for (int j = 0; j < TS; ++j) {
-            const float uv = Act<T>::to_f(tu[j * CW + tid]);
-            const float xr = Act<T>::to_f(tr[j * CW + tid]);
+        for (int jj = 0; jj < HT; ++jj) {
+            const int j = half * HT + jj;
+            const float uv = Act<T>::to_f(tu[j * CW + ch]);
+            const float xr = Act<T>::to_f(tr[j * CW + ch]);
             float dt, gz = 1.0f;
             if (GATE) {
-                const float zv = Act<T>::to_f(tz[j * CW + tid]);
+                const float zv = Act<T>::to_f(tz[j * CW + ch]);
                 float sz;
                 softplus_sigmoid(xr, zv, dt, sz);
                 gz = zv * sz;                                   // silu(z)
@@ -198,10 +219,15 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
                 float e;
                 dt = softplus_e(xr, e);
             }
-            dtv[j] = dt;
-            bsc[j] = DISC == 0 ? dt * uv : uv;                  // Euler: delta*u; ZOH: u
-            dterm[j] = Dd * uv;
-            gate[j] = gz;
+            const float bs = DISC == 0 ? dt * uv : uv;          // Euler: delta*u; ZOH: u
+            const float dt_o = __shfl_xor_sync(0xffffffffu, dt, 16);
+            const float bs_o = __shfl_xor_sync(0xffffffffu, bs, 16);
+            dtv[jj] = half ? dt_o : dt;
+            dtv[HT + jj] = half ? dt : dt_o;
+            bsc[jj] = half ? bs_o : bs;
+            bsc[HT + jj] = half ? bs : bs_o;
+            dterm[jj] = Dd * uv;
+            gate[jj] = gz;
         }
         __syncwarp();
 
@@ -209,48 +235,50 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         // B|C are zero, so the extra steps only evolve a state never stored.
         float yv[TS];
         float2 hmid[NQ];
+        const float* bl = Bf + nbase;
 #pragma unroll
         for (int j = 0; j < TS; ++j) {
-            yv[j] = fwd_step<NT, DISC>(h, A2, Anat, invA, bcs + j * 2 * NT, dtv[j], bsc[j]) + dterm[j];
+            yv[j] = fwd_step<NL, DISC>(h, A2, Anat, invA, bl + j * NT, bl + BCT + j * NT, dtv[j],
+                                       bsc[j]);
             if (j == kChunk - 1) {
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) hmid[q] = h[q];
             }
         }
-        if (active) {
+        // Each lane finishes the steps of its half: y = own part + partner part.
 #pragma unroll
-            for (int j = 0; j < TS; ++j) {
-                if (j < jmax) {
-                    const size_t r = row0 + k * TS + j;
-                    outp[r * a.ld_out + d] = Act<T>::from_f(GATE ? yv[j] * gate[j] : yv[j]);
-                    if (GATE && ysv) ysv[r * a.dinner + d] = Act<T>::from_f(yv[j]);
-                }
+        for (int jj = 0; jj < HT; ++jj) {
+            const float send = half ? yv[jj] : yv[HT + jj];
+            const float mine = half ? yv[HT + jj] : yv[jj];
+            const float y = mine + __shfl_xor_sync(0xffffffffu, send, 16) + dterm[jj];
+            const int j = half * HT + jj;
+            if (active && j < jmax) {
+                const size_t r = row0 + k * TS + j;
+                outp[r * a.ld_out + d] = Act<T>::from_f(GATE ? y * gate[jj] : y);
+                if (GATE && ysv) ysv[r * a.dinner + d] = Act<T>::from_f(y);
             }
-            if (a.ctx) {
-                // states after steps kChunk-1 and TS-1 of the tile (chunk boundaries)
+        }
+        if (active && a.ctx) {
+            // states after steps kChunk-1 and TS-1 of the tile (chunk boundaries)
 #pragma unroll
-                for (int m = 0; m < TS / kChunk; ++m) {
-                    const int t1 = k * TS + (m + 1) * kChunk;   // first step of the next chunk
-                    if (t1 < L) {
-                        float* cp = a.ctx + ((static_cast<size_t>(b) * a.nck + t1 / kChunk - 1) * NT) *
-                                                a.dinner + d;
+            for (int m = 0; m < TS / kChunk; ++m) {
+                const int t1 = k * TS + (m + 1) * kChunk;       // first step of the next chunk
+                if (t1 < L) {
+                    float* cp = a.ctx + ((static_cast<size_t>(b) * a.nck + t1 / kChunk - 1) * NT + nbase) *
+                                            a.dinner + d;
 #pragma unroll
-                        for (int q = 0; q < NQ; ++q) {
-                            const float2 hv = m == 0 ? hmid[q] : h[q];
-                            cp[static_cast<size_t>(2 * q) * a.dinner] = hv.x;
-                            cp[static_cast<size_t>(2 * q + 1) * a.dinner] = hv.y;
-                        }
+                    for (int q = 0; q < NQ; ++q) {
+                        const float2 hv = m == 0 ? hmid[q] : h[q];
+                        cp[static_cast<size_t>(2 * q) * a.dinner] = hv.x;
+                        cp[static_cast<size_t>(2 * q + 1) * a.dinner] = hv.y;
                     }
                 }
             }
         }
-        __syncthreads();
-        if (tid == 0 && k + S < ntiles) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(k + S);
-        }
+        __syncwarp();
+        if (lane == 0 && k + S < ntiles) issue(k + S);
     }
-    if (k < ntiles && tid == 0) {
+    if (k < ntiles && lane == 0) {
         // A wait gave up: drain the copies still in flight (bounded) before exit.
         for (int kk = k; kk < ntiles && kk < k + S; ++kk)
             mbar_wait(&full[kk % S], (kk / S) & 1, kFaultDrain);
@@ -260,14 +288,14 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
 template <typename T, int NT, int DISC, bool GATE>
 static cudaError_t launch_fwd_t(const FwdMaps& m, const ScanFwdArgs& a, cudaStream_t st) {
     constexpr int NTEN = GATE ? 3 : 2;
-    constexpr int STAGE = NTEN * kFwdTile * 32 + 2 * kFwdTile * NT;
+    constexpr int STAGE = NTEN * kFwdTile * kFwdChannels + 2 * kFwdTile * NT;
     const size_t smem = kFwdStages * STAGE * sizeof(T) + 2 * kFwdTile * NT * sizeof(float) +
                         kFwdStages * sizeof(uint64_t);
     auto kern = scan_fwd_kernel<T, NT, DISC, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid((a.dinner + 31) / 32, a.batch);
+    dim3 grid((a.dinner + kFwdChannels - 1) / kFwdChannels, a.batch);
     kern<<<grid, 32, smem, st>>>(m, a);
     return cudaGetLastError();
 }
