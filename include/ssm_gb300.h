@@ -147,6 +147,32 @@ ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, in
                                float* dx, int64_t ld_dx, float* dw, float* dbias,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ssm_conv1d_silu_bwd without a workspace argument: the same result as
+ * ssm_conv1d_silu_bwd, but the per-run dw/dbias partial sums live in scratch
+ * that the library reserves once, as a fixed 8 MiB array in the device image,
+ * instead of in caller memory.  (The pages have no counterpart; this is an
+ * interface convenience.)  It is meant for callers that cannot give the
+ * library any scratch: a runtime or plugin interface that owns every device
+ * buffer and offers kernels none, or a loop where a cudaMalloc -- which may
+ * synchronise the device -- is not allowed.  The function itself allocates
+ * nothing.
+ *  - Capacity: ceil(seqlen / 64) * batch * dinner * (kconv + 1) floats must not
+ *    exceed 2^21 (8 MiB); larger problems return SSM_ERR_WORKSPACE and launch
+ *    nothing.
+ *  - The first call on a device looks up the scratch's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one scratch array, and it keeps the
+ *    last call's contents; each call writes every partial it reads, so nothing
+ *    has to start at zero.  Calls that overlap on the GPU (for example on two
+ *    streams at once) race on the scratch and must not be issued.
+ * Other arguments, layouts and errors as ssm_conv1d_silu_bwd. */
+ssm_status ssm_conv1d_silu_bwd_noalloc(int32_t batch, int32_t seqlen, int32_t dinner,
+                                       int32_t kconv, const float* x, int64_t ld_x,
+                                       const float* w, const float* bias, const float* dout,
+                                       int64_t ld_dout, float* dx, int64_t ld_dx, float* dw,
+                                       float* dbias, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);
 

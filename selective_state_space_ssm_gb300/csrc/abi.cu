@@ -457,6 +457,50 @@ ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, in
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 
+ssm_status ssm_conv1d_silu_bwd_noalloc(int32_t batch, int32_t seqlen, int32_t dinner,
+                                       int32_t kconv, const float* x, int64_t ld_x,
+                                       const float* w, const float* bias, const float* dout,
+                                       int64_t ld_dout, float* dx, int64_t ld_dx, float* dw,
+                                       float* dbias, cudaStream_t stream) {
+    if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
+    ld_x = ld_x ? ld_x : dinner;
+    ld_dout = ld_dout ? ld_dout : dinner;
+    ld_dx = ld_dx ? ld_dx : dinner;
+    if (ld_x < dinner || ld_dout < dinner || ld_dx < dinner) return SSM_ERR_SHAPE;
+    if (dinner == 0) return SSM_OK;
+    if (!w || !dw) return SSM_ERR_NULL;
+    const bool rows = static_cast<int64_t>(batch) * seqlen > 0;
+    if (rows && (!x || !dout || !dx)) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || ld_dout % 4 || ld_dx % 4 || (x && !aligned16(x)) ||
+        (dout && !aligned16(dout)) || (dx && !aligned16(dx)) || (bias && !aligned16(bias)))
+        return SSM_ERR_ALIGN;
+    const size_t need = ssm::conv1d_bwd_workspace_bytes(batch, seqlen, dinner, kconv);
+    if (need > ssm::kConvNoAllocScratchFloats * sizeof(float)) return SSM_ERR_WORKSPACE;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    float* scratch = nullptr;
+    cudaError_t e = ssm::conv1d_noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return fail_cuda(e, SSM_ERR_DEVICE);
+    ssm::ConvArgs a{};
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.dout = dout;
+    a.dx = dx;
+    a.dw = dw;
+    a.dbias = dbias;
+    a.ws = scratch;
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.dinner = dinner;
+    a.kconv = kconv;
+    a.ld_x = ld_x;
+    a.ld_dout = ld_dout;
+    a.ld_dx = ld_dx;
+    e = ssm::launch_conv1d_bwd(a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
 const char* ssm_status_string(ssm_status s) {
     switch (s) {
         case SSM_OK: return "ok";

@@ -14,6 +14,7 @@
 // last K rows of x (and, backward, of dpre) in registers, so each element is
 // read from HBM once plus a (K-1)/kRun halo.
 #include <algorithm>
+#include <mutex>
 
 #include "conv_args.cuh"
 #include "ssm_common.cuh"
@@ -238,6 +239,33 @@ cudaError_t launch_conv1d_bwd(const ConvArgs& a, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     conv1d_reduce_kernel<<<std::max(1, std::min(1024, (n + 255) / 256)), 256, 0, st>>>(a, nparts);
     return cudaGetLastError();
+}
+
+// Scratch for the allocation-free backward entry point: the per-run dw/dbias
+// partial sums live in this file-scope array instead of a caller workspace.
+// Every GPU that loads the library keeps these kConvNoAllocScratchFloats floats
+// (8 MiB) until the process exits.
+static __device__ __align__(256) float g_conv_bwd_scratch[kConvNoAllocScratchFloats];
+
+// Device address of g_conv_bwd_scratch on the current device, looked up once
+// per device (the name is only a host-side stand-in; the kernel needs this
+// address).  Returns the cudaGetSymbolAddress error, if any.
+cudaError_t conv1d_noalloc_scratch(float** out) {
+    static std::mutex mu;
+    static float* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_conv_bwd_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float*>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 size_t conv1d_bwd_workspace_bytes(int batch, int seqlen, int dinner, int kconv) {

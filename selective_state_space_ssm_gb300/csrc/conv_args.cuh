@@ -24,7 +24,12 @@ struct ConvArgs {
     int64_t ld_x, ld_out, ld_dout, ld_dx;
 };
 
+// Capacity, in floats, of the file-scope scratch used by the allocation-free
+// backward entry point (8 MiB).
+constexpr size_t kConvNoAllocScratchFloats = size_t(1) << 21;
+
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, cudaStream_t st);
+cudaError_t conv1d_noalloc_scratch(float** out);
 cudaError_t launch_conv1d_bwd(const ConvArgs& a, cudaStream_t st);
 size_t conv1d_bwd_workspace_bytes(int batch, int seqlen, int dinner, int kconv);
 
