@@ -147,6 +147,73 @@ ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, in
                                float* dx, int64_t ld_dx, float* dw, float* dbias,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Linear layer (cpu_ops.ts linearForward): Y (M, N) = X (M, K) W^T + bias
+ * (+ R), fp32, on the tensor cores as three TF32 products of hi/lo splits
+ * with the partial sums drained to fp32 every 128 K (about fp32 accuracy).
+ * W is (N, K) as torch.nn.Linear stores it; row strides ldx, ldw, ldr, ldy in
+ * elements (0 = packed); bias (N) and R (M, N) may be NULL; R may alias Y.
+ * workspace (16-byte aligned) must hold ssm_linear_workspace_bytes(M, N, K)
+ * bytes.  K = 0 is rejected (SSM_ERR_SHAPE). */
+size_t ssm_linear_workspace_bytes(int32_t M, int32_t N, int32_t K);
+ssm_status ssm_linear_fwd(int32_t M, int32_t N, int32_t K, const float* X, int64_t ldx,
+                          const float* W, int64_t ldw, const float* bias, const float* R,
+                          int64_t ldr, float* Y, int64_t ldy,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---- The whole Mamba-1 block (mamba1_cpu.ts mamba1CpuForward /
+ * mamba1CpuBackward, with the linear and RMSNorm primitives of cpu_ops.ts):
+ *   xn   = rmsnorm(x) * norm_w            inv = 1/sqrt(mean(x^2) + 1e-6)
+ *   xz   = xn in_proj_w^T + in_proj_b      (M, 2 dinner) -> x_in | z
+ *   u    = silu(conv1d(x_in))              causal depthwise, kconv taps
+ *   xd   = u x_proj_w^T + x_proj_b         (M, dtrank + 2 dstate) -> dt | B | C
+ *   draw = dt dt_proj_w^T + dt_proj_b      (M, dinner): the scan's delta_raw
+ *   g    = scan(u, draw, A_log, B, C, D) * silu(z)
+ *   out  = g out_proj_w^T + out_proj_b + x
+ * Every tensor is fp32, row-major and packed; weights are (out, in) as
+ * torch.nn.Linear stores them, conv_w is (dinner, kconv) with tap 0 on the
+ * current step.  The projections run on the tensor cores as three TF32
+ * products of hi/lo splits (about fp32 accuracy); the scan is ssm_scan_fwd /
+ * ssm_scan_bwd.  dmodel, dinner, dtrank and dstate must be multiples of 4
+ * (else SSM_ERR_ALIGN); 1 <= dstate <= 16; 1 <= kconv <= 8; dtrank >= 1. */
+typedef struct ssm_block_desc {
+    int32_t batch, seqlen, dmodel, dinner, dstate, dtrank, dconv;
+    int32_t disc;  /* ssm_disc */
+} ssm_block_desc;
+
+/* The 13 block parameters, in the pages' order (Mamba1CpuWeights). */
+typedef struct ssm_block_weights {
+    const float *in_proj_w, *in_proj_b, *conv_w, *conv_b, *x_proj_w, *x_proj_b,
+                *dt_proj_w, *dt_proj_b, *A_log, *D, *out_proj_w, *out_proj_b, *norm_w;
+} ssm_block_weights;
+/* Their gradients (same shapes), written by ssm_block_bwd. */
+typedef struct ssm_block_grads {
+    float *in_proj_w, *in_proj_b, *conv_w, *conv_b, *x_proj_w, *x_proj_b,
+          *dt_proj_w, *dt_proj_b, *A_log, *D, *out_proj_w, *out_proj_b, *norm_w;
+} ssm_block_grads;
+
+/* Bytes of the activations ssm_block_fwd saves for ssm_block_bwd (xn, inv,
+ * xz, u, xd, draw, g and the scan context), and of the device scratch either
+ * call needs.  0 for an invalid descriptor. */
+size_t ssm_block_ctx_bytes(const ssm_block_desc* desc);
+size_t ssm_block_workspace_bytes(const ssm_block_desc* desc);
+
+/* Block forward: x, out (M, dmodel).  ctx (required, 16-byte aligned) must
+ * hold ssm_block_ctx_bytes and workspace ssm_block_workspace_bytes bytes;
+ * out may not alias x.  Every weight pointer is required. */
+ssm_status ssm_block_fwd(const ssm_block_desc* desc, const float* x,
+                         const ssm_block_weights* weights, float* out,
+                         void* ctx, size_t ctx_bytes,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Block backward, given dout = dL/d(out) (M, dmodel) and the ctx written by
+ * ssm_block_fwd for the same x and weights: writes dx (M, dmodel) and every
+ * gradient in *grads (all required). */
+ssm_status ssm_block_bwd(const ssm_block_desc* desc, const float* x,
+                         const ssm_block_weights* weights, const float* dout,
+                         const void* ctx, size_t ctx_bytes, float* dx,
+                         const ssm_block_grads* grads,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ssm_conv1d_silu_bwd without a workspace argument: the same result as
  * ssm_conv1d_silu_bwd, but the per-run dw/dbias partial sums live in scratch
  * that the library reserves once, as a fixed 8 MiB array in the device image,
@@ -186,7 +253,8 @@ int ssm_abi_version(void);
 /* Fault bits recorded by the kernels since the last call, then cleared:
  * every wait of a kernel on an asynchronous copy is bounded, and a wait that
  * gives up sets a bit here (1: forward copy wait, 2: backward copy wait,
- * 4: drain after a failed wait) instead of hanging; that call's outputs are
+ * 4: drain after a failed wait, 8: block GEMM pipeline wait) instead of
+ * hanging; that call's outputs are
  * then invalid.  Synchronous: call it after the work has completed.  Returns
  * 0 when no sm_103 device is current. */
 unsigned ssm_device_faults(void);

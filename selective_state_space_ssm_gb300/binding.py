@@ -8,8 +8,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
 missing library raises instead of degrading.
 
 The helpers at the bottom (``scan_fwd``, ``scan_bwd``, ``conv1d_silu``,
-``conv1d_silu_bwd``) allocate the output, context and workspace tensors with
-torch and then call the entry points.
+``conv1d_silu_bwd``, ``block_fwd``, ``block_bwd``) allocate the output,
+context and workspace tensors with torch and then call the entry points.
 """
 from __future__ import annotations
 
@@ -23,8 +23,11 @@ __all__ = [
     "ssm_scan_ctx_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv1d_silu", "ssm_conv1d_silu_bwd",
     "ssm_conv1d_silu_bwd_workspace_bytes", "ssm_status_string", "ssm_abi_version",
-    "ssm_device_faults",
-    "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "EXPORTED_SYMBOLS",
+    "ssm_device_faults", "BlockDesc", "BlockWeights", "BlockGrads", "BLOCK_PARAM_NAMES",
+    "block_desc", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
+    "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "linear",
+    "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "block_fwd", "block_bwd",
+    "EXPORTED_SYMBOLS",
 ]
 
 SSM_F32, SSM_BF16 = 0, 1
@@ -39,8 +42,17 @@ EXPORTED_SYMBOLS = (
     "ssm_scan_ctx_bytes", "ssm_scan_fwd_workspace_bytes", "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv1d_silu", "ssm_conv1d_silu_bwd_workspace_bytes",
     "ssm_conv1d_silu_bwd", "ssm_status_string", "ssm_last_cuda_error", "ssm_abi_version",
-    "ssm_device_faults",
+    "ssm_device_faults", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
+    "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd",
 )
+
+# The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
+# and the matching ssm_block_weights / ssm_block_grads fields.
+BLOCK_PARAM_NAMES = ("wInProj", "bInProj", "wConv", "bConv", "wXProj", "bXProj",
+                     "wDtProj", "bDtProj", "A_log", "D_vec", "wOutProj", "bOutProj",
+                     "normWeight")
+_BLOCK_FIELDS = ("in_proj_w", "in_proj_b", "conv_w", "conv_b", "x_proj_w", "x_proj_b",
+                 "dt_proj_w", "dt_proj_b", "A_log", "D", "out_proj_w", "out_proj_b", "norm_w")
 
 
 class SsmError(RuntimeError):
@@ -55,6 +67,19 @@ class ScanDesc(ctypes.Structure):
                 [(n, ctypes.c_int64) for n in
                  ("ld_u", "ld_delta", "ld_z", "ld_B", "ld_C", "ld_out", "ld_dout", "ld_du",
                   "ld_ddelta", "ld_dz", "ld_dB", "ld_dC")])
+
+
+class BlockDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("batch", "seqlen", "dmodel", "dinner", "dstate", "dtrank", "dconv", "disc")]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _BLOCK_FIELDS]
+
+
+class BlockGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _BLOCK_FIELDS]
 
 
 def library_path() -> str:
@@ -92,6 +117,20 @@ def load():
             "ssm_last_cuda_error": (ctypes.c_int, []),
             "ssm_abi_version": (ctypes.c_int, []),
             "ssm_device_faults": (ctypes.c_uint, []),
+            "ssm_linear_workspace_bytes": (sz, [i32, i32, i32]),
+            # M, N, K, X, ldx, W, ldw, bias, R, ldr, Y, ldy, ws, ws_bytes, stream
+            "ssm_linear_fwd": (ctypes.c_int, [i32, i32, i32, vp, i64, vp, i64, vp, vp, i64, vp,
+                                              i64, vp, sz, vp]),
+            "ssm_block_ctx_bytes": (sz, [ctypes.POINTER(BlockDesc)]),
+            "ssm_block_workspace_bytes": (sz, [ctypes.POINTER(BlockDesc)]),
+            # desc, x, weights, out, ctx, ctx_bytes, ws, ws_bytes, stream
+            "ssm_block_fwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
+                                             ctypes.POINTER(BlockWeights), vp, vp, sz, vp, sz,
+                                             vp]),
+            # desc, x, weights, dout, ctx, ctx_bytes, dx, grads, ws, ws_bytes, stream
+            "ssm_block_bwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
+                                             ctypes.POINTER(BlockWeights), vp, vp, sz, vp,
+                                             ctypes.POINTER(BlockGrads), vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -215,6 +254,55 @@ def ssm_device_faults() -> int:
     return load().ssm_device_faults()
 
 
+def ssm_linear_workspace_bytes(M, N, K) -> int:
+    return load().ssm_linear_workspace_bytes(M, N, K)
+
+
+def ssm_linear_fwd(X, W, bias, R, Y, workspace, stream=None):
+    M, K = X.shape
+    N = W.shape[0]
+    st = load().ssm_linear_fwd(M, N, K, _ptr(X), _ld(X), _ptr(W), _ld(W), _ptr(bias), _ptr(R),
+                               _ld(R), _ptr(Y), _ld(Y), _ptr(workspace), _nbytes(workspace),
+                               _stream(stream))
+    _check("ssm_linear_fwd", st)
+
+
+def block_desc(dims, disc=SSM_DISC_EULER) -> BlockDesc:
+    """dims: batch, seqlen, dmodel, dinner, dstate, dtrank, dconv."""
+    return BlockDesc(dims["batch"], dims["seqlen"], dims["dmodel"], dims["dinner"],
+                     dims["dstate"], dims["dtrank"], dims["dconv"], disc)
+
+
+def _block_ptrs(cls, tensors):
+    return cls(**{f: tensors[n].data_ptr() for n, f in zip(BLOCK_PARAM_NAMES, _BLOCK_FIELDS)})
+
+
+def ssm_block_ctx_bytes(desc: BlockDesc) -> int:
+    return load().ssm_block_ctx_bytes(ctypes.byref(desc))
+
+
+def ssm_block_workspace_bytes(desc: BlockDesc) -> int:
+    return load().ssm_block_workspace_bytes(ctypes.byref(desc))
+
+
+def ssm_block_fwd(desc, x, weights, out, ctx, workspace, stream=None):
+    """weights: dict keyed by BLOCK_PARAM_NAMES (fp32 device tensors)."""
+    w = _block_ptrs(BlockWeights, weights)
+    st = load().ssm_block_fwd(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(out), _ptr(ctx),
+                              _nbytes(ctx), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check("ssm_block_fwd", st)
+
+
+def ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, workspace, stream=None):
+    """grads: dict keyed by BLOCK_PARAM_NAMES (written)."""
+    w = _block_ptrs(BlockWeights, weights)
+    g = _block_ptrs(BlockGrads, grads)
+    st = load().ssm_block_bwd(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(dout), _ptr(ctx),
+                              _nbytes(ctx), _ptr(dx), ctypes.byref(g), _ptr(workspace),
+                              _nbytes(workspace), _stream(stream))
+    _check("ssm_block_bwd", st)
+
+
 # ----------------------------------------------------------------- allocating helpers
 
 def _bytes_tensor(nbytes, like):
@@ -273,3 +361,39 @@ def conv1d_silu_bwd(x, w, bias, dout, *, batch, stream=None):
                                                            w.shape[1]), x)
     ssm_conv1d_silu_bwd(batch, x, w, bias, dout, dx, dw, db, ws, stream)
     return dx, dw, db
+
+
+def linear(X, W, bias=None, R=None, *, stream=None):
+    """Y = X W^T + bias (+ R) through ssm_linear_fwd (allocates Y and the workspace)."""
+    import torch
+    M, K = X.shape
+    N = W.shape[0]
+    Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    ws = _bytes_tensor(ssm_linear_workspace_bytes(M, N, K), X)
+    ssm_linear_fwd(X, W, bias, R, Y, ws, stream)
+    return Y
+
+
+def block_fwd(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
+    """Allocate out, the saved activations and the workspace and run
+    ssm_block_fwd.  Returns (out, ctx, workspace); pass ctx (and, to avoid a
+    second allocation, workspace) to block_bwd."""
+    import torch
+    desc = block_desc(dims, disc)
+    out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ctx = _bytes_tensor(ssm_block_ctx_bytes(desc), x)
+    ws = _bytes_tensor(ssm_block_workspace_bytes(desc), x)
+    ssm_block_fwd(desc, x, weights, out, ctx, ws, stream)
+    return out, ctx, ws
+
+
+def block_bwd(x, weights, dims, dout, ctx, *, disc=SSM_DISC_EULER, workspace=None, stream=None):
+    """Allocate dx and the 13 gradients and run ssm_block_bwd.  Returns
+    (dx, grads) with grads keyed by BLOCK_PARAM_NAMES."""
+    import torch
+    desc = block_desc(dims, disc)
+    dx = torch.empty_like(x, memory_format=torch.contiguous_format)
+    grads = {n: torch.empty_like(weights[n]) for n in BLOCK_PARAM_NAMES}
+    ws = workspace if workspace is not None else _bytes_tensor(ssm_block_workspace_bytes(desc), x)
+    ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, ws, stream)
+    return dx, grads

@@ -11,20 +11,19 @@
 #include <mutex>
 
 #include "conv_args.cuh"
+#include "gemm_args.cuh"
+#include "host_util.h"
 #include "scan_args.cuh"
 #include "ssm_gb300.h"
 
-namespace {
+namespace ssm_host {
 
 thread_local int g_last_cuda_error = 0;
 
-ssm_status fail_cuda(cudaError_t e, ssm_status s = SSM_ERR_LAUNCH) {
+ssm_status fail_cuda(cudaError_t e, ssm_status s) {
     g_last_cuda_error = static_cast<int>(e);
     return s;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 // ---- device check: the kernels are built for sm_103a only
 ssm_status check_device() {
@@ -60,6 +59,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+}  // namespace ssm_host
+
+namespace {
+
+using ssm_host::aligned16;
+using ssm_host::align256;
+using ssm_host::check_device;
+using ssm_host::encode_fn;
+using ssm_host::fail_cuda;
+using ssm_host::g_last_cuda_error;
 
 // (M, dinner) activation viewed as [batch][seqlen][dinner] with row stride ld;
 // box = 32 channels x box_rows steps x 1 batch row; out-of-range reads fill 0.
@@ -520,11 +530,12 @@ int ssm_last_cuda_error(void) { return g_last_cuda_error; }
 int ssm_abi_version(void) { return SSM_GB300_ABI_VERSION; }
 
 unsigned ssm_device_faults(void) {
-    unsigned f1 = 0, f2 = 0;
+    unsigned f1 = 0, f2 = 0, f3 = 0;
     if (check_device() != SSM_OK) return 0;
     ssm::read_clear_fault_fwd(&f1);
     ssm::read_clear_fault_bwd(&f2);
-    return f1 | f2;
+    ssm::read_clear_fault_gemm(&f3);
+    return f1 | f2 | f3;
 }
 
 }  // extern "C"

@@ -1,0 +1,450 @@
+// block.cu -- extern "C" entry points of the whole Mamba-1 block
+// (mamba1_cpu.ts mamba1CpuForward steps 1-11 and mamba1CpuBackward steps
+// 11-1; linear and RMSNorm as cpu_ops.ts defines them).  Host-side
+// orchestration only: every step runs in this library's kernels (RMSNorm,
+// TF32 split, tcgen05 GEMM, conv1d+SiLU, selective scan, column sums), in
+// stream order on the caller's stream, in caller-owned memory.
+#include <algorithm>
+#include <cstring>
+
+#include "gemm_args.cuh"
+#include "host_util.h"
+#include "ssm_gb300.h"
+
+namespace {
+
+using ssm_host::align256;
+using ssm_host::aligned16;
+using ssm_host::check_device;
+using ssm_host::encode_fn;
+using ssm_host::fail_cuda;
+
+constexpr float kRmsEps = 1e-6f;   // cpu_ops.ts RMSNORM_EPS
+
+int64_t round4(int64_t n) { return (n + 3) & ~static_cast<int64_t>(3); }
+
+// Byte offsets of one buffer layout (each region 256-byte aligned).
+struct Carve {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    }
+};
+
+struct Dims {
+    int64_t M;
+    int B, L, Dm, D, N, R, K, P, disc;
+};
+
+ssm_status check_desc(const ssm_block_desc* d, Dims& s) {
+    if (!d) return SSM_ERR_NULL;
+    if (d->disc != SSM_DISC_EULER && d->disc != SSM_DISC_ZOH) return SSM_ERR_DTYPE;
+    if (d->batch < 0 || d->seqlen < 0 || d->dmodel <= 0 || d->dinner <= 0 || d->dstate <= 0 ||
+        d->dstate > SSM_MAX_DSTATE || d->dtrank <= 0 || d->dconv < 1 || d->dconv > 8)
+        return SSM_ERR_SHAPE;
+    if (d->dmodel % 4 || d->dinner % 4 || d->dstate % 4 || d->dtrank % 4) return SSM_ERR_ALIGN;
+    s.B = d->batch;
+    s.L = d->seqlen;
+    s.M = static_cast<int64_t>(d->batch) * d->seqlen;
+    if (s.M > (int64_t(1) << 30)) return SSM_ERR_SHAPE;
+    s.Dm = d->dmodel;
+    s.D = d->dinner;
+    s.N = d->dstate;
+    s.R = d->dtrank;
+    s.K = d->dconv;
+    s.P = d->dtrank + 2 * d->dstate;
+    s.disc = d->disc;
+    return SSM_OK;
+}
+
+ssm_scan_desc scan_desc_of(const Dims& s) {
+    ssm_scan_desc sd;
+    std::memset(&sd, 0, sizeof(sd));
+    sd.batch = s.B;
+    sd.seqlen = s.L;
+    sd.dinner = s.D;
+    sd.dstate = s.N;
+    sd.dtype = SSM_F32;
+    sd.disc = s.disc;
+    sd.ld_u = s.D;
+    sd.ld_delta = s.D;
+    sd.ld_z = 2 * s.D;
+    sd.ld_B = s.P;
+    sd.ld_C = s.P;
+    sd.ld_out = s.D;
+    sd.ld_dout = s.D;
+    sd.ld_du = s.D;
+    sd.ld_ddelta = s.D;
+    sd.ld_dz = 2 * s.D;
+    sd.ld_dB = s.P;
+    sd.ld_dC = s.P;
+    return sd;
+}
+
+// Saved activations of the forward.
+struct Ctx {
+    size_t xn, inv, xz, u, xd, draw, g, scan, total;
+};
+Ctx ctx_layout(const Dims& s) {
+    const size_t f = sizeof(float), M = static_cast<size_t>(s.M);
+    Carve c;
+    Ctx x;
+    x.xn = c.take(M * s.Dm * f);
+    x.inv = c.take(M * f);
+    x.xz = c.take(M * 2 * s.D * f);
+    x.u = c.take(M * s.D * f);
+    x.xd = c.take(M * s.P * f);
+    x.draw = c.take(M * s.D * f);
+    x.g = c.take(M * s.D * f);
+    ssm_scan_desc sd = scan_desc_of(s);
+    x.scan = c.take(ssm_scan_ctx_bytes(&sd));
+    x.total = c.off;
+    return x;
+}
+
+// Scratch shared by forward and backward (regions reused in stream order).
+struct Ws {
+    size_t a_hi, a_lo, b_hi, b_lo, w_hi, w_lo;            // TF32 splits
+    size_t dg, du, ddelta, dxd, dxz, dxn;                 // backward activations
+    size_t scan, conv, red, total;
+};
+Ws ws_layout(const Dims& s) {
+    const size_t f = sizeof(float);
+    const int64_t ldM = round4(s.M);
+    const int64_t wide = round4(std::max({int64_t(2) * s.D, int64_t(s.Dm), int64_t(s.P), int64_t(s.R)}));
+    const int64_t deep = round4(std::max({int64_t(s.D), int64_t(s.R), int64_t(s.Dm)}));
+    auto wsz = [](int64_t rows, int64_t cols) {
+        return static_cast<size_t>(std::max(rows * round4(cols), cols * round4(rows)));
+    };
+    const size_t wmax = std::max({wsz(2 * s.D, s.Dm), wsz(s.P, s.D), wsz(s.D, s.R), wsz(s.Dm, s.D)});
+    const size_t M = static_cast<size_t>(s.M);
+    Carve c;
+    Ws w;
+    w.a_hi = c.take(static_cast<size_t>(ldM * wide) * f);
+    w.a_lo = c.take(static_cast<size_t>(ldM * wide) * f);
+    w.b_hi = c.take(static_cast<size_t>(ldM * deep) * f);
+    w.b_lo = c.take(static_cast<size_t>(ldM * deep) * f);
+    w.w_hi = c.take(wmax * f);
+    w.w_lo = c.take(wmax * f);
+    w.dg = c.take(M * s.D * f);
+    w.du = c.take(M * s.D * f);
+    w.ddelta = c.take(M * s.D * f);
+    w.dxd = c.take(M * s.P * f);
+    w.dxz = c.take(M * 2 * s.D * f);
+    w.dxn = c.take(M * s.Dm * f);
+    ssm_scan_desc sd = scan_desc_of(s);
+    w.scan = c.take(ssm_scan_bwd_workspace_bytes(&sd));
+    w.conv = c.take(ssm_conv1d_silu_bwd_workspace_bytes(s.B, s.L, s.D, s.K));
+    const int rows = static_cast<int>(s.M);
+    const size_t red = std::max({ssm::colsum_ws_floats(rows, 2 * s.D), ssm::colsum_ws_floats(rows, s.Dm),
+                                 ssm::colsum_ws_floats(rows, s.P), ssm::rmsnorm_ws_floats(rows, s.Dm)});
+    w.red = c.take(std::max<size_t>(red, 1) * f);
+    w.total = c.off;
+    return w;
+}
+
+// One GEMM operand: hi/lo TF32 halves of a (rows, cols) matrix, row stride ld.
+struct Op {
+    const float* hi;
+    const float* lo;
+    int rows, cols;
+    int64_t ld;
+};
+
+bool encode_op(CUtensorMap* m, const float* p, const Op& o) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ld) * sizeof(float)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(ssm::kGemmBK), static_cast<cuuint32_t>(ssm::kGemmBM)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Stream-ordered step list of one call; the first failure sticks.
+struct Run {
+    cudaStream_t st;
+    ssm_status status = SSM_OK;
+
+    bool ok() const { return status == SSM_OK; }
+    void cuda(cudaError_t e) {
+        if (ok() && e != cudaSuccess) status = fail_cuda(e);
+    }
+    void check(ssm_status s) {
+        if (ok() && s != SSM_OK) status = s;
+    }
+
+    // Split x (rows, cols; stride ldx) into hi/lo, transposed or not.
+    Op split(const float* x, int64_t ldx, int rows, int cols, bool transpose, float* hi, float* lo) {
+        Op o{hi, lo, transpose ? cols : rows, transpose ? rows : cols, 0};
+        o.ld = round4(o.cols);
+        if (ok()) cuda(ssm::launch_split_tf32(x, ldx, rows, cols, transpose ? 1 : 0, hi, lo, o.ld, st));
+        return o;
+    }
+
+    // C (A.rows, B.rows) = A B^T (+ bias) (+ R); A.cols == B.cols.
+    void gemm(const Op& A, const Op& B, float* C, int64_t ldc, const float* bias, const float* R,
+              int64_t ldr) {
+        if (!ok()) return;
+        ssm::GemmMaps maps;
+        if (!encode_op(&maps.a_hi, A.hi, A) || !encode_op(&maps.a_lo, A.lo, A) ||
+            !encode_op(&maps.b_hi, B.hi, B) || !encode_op(&maps.b_lo, B.lo, B)) {
+            status = SSM_ERR_DEVICE;
+            return;
+        }
+        ssm::GemmArgs a{};
+        a.C = C;
+        a.bias = bias;
+        a.R = R;
+        a.M = A.rows;
+        a.N = B.rows;
+        a.K = A.cols;
+        a.ldc = ldc;
+        a.ldr = ldr;
+        cuda(ssm::launch_gemm_tf32x3(maps, a, st));
+    }
+};
+
+template <class T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <class T>
+const T* at(const void* base, size_t off) {
+    return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+bool all_weights(const ssm_block_weights* w) {
+    return w && w->in_proj_w && w->in_proj_b && w->conv_w && w->conv_b && w->x_proj_w && w->x_proj_b &&
+           w->dt_proj_w && w->dt_proj_b && w->A_log && w->D && w->out_proj_w && w->out_proj_b && w->norm_w;
+}
+bool all_grads(const ssm_block_grads* g) {
+    return g && g->in_proj_w && g->in_proj_b && g->conv_w && g->conv_b && g->x_proj_w && g->x_proj_b &&
+           g->dt_proj_w && g->dt_proj_b && g->A_log && g->D && g->out_proj_w && g->out_proj_b && g->norm_w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_linear_workspace_bytes(int32_t M, int32_t N, int32_t K) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    const size_t f = sizeof(float);
+    return 2 * align256(static_cast<size_t>(M) * round4(K) * f) +
+           2 * align256(static_cast<size_t>(N) * round4(K) * f);
+}
+
+ssm_status ssm_linear_fwd(int32_t M, int32_t N, int32_t K, const float* X, int64_t ldx,
+                          const float* W, int64_t ldw, const float* bias, const float* R,
+                          int64_t ldr, float* Y, int64_t ldy, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return SSM_ERR_SHAPE;
+    ldx = ldx ? ldx : K;
+    ldw = ldw ? ldw : K;
+    ldy = ldy ? ldy : N;
+    ldr = ldr ? ldr : N;
+    if (ldx < K || ldw < K || ldy < N || (R && ldr < N)) return SSM_ERR_SHAPE;
+    if (M == 0 || N == 0) return SSM_OK;
+    if (!Y || (K > 0 && (!X || !W))) return SSM_ERR_NULL;
+    if (!workspace) return SSM_ERR_NULL;
+    if (!aligned16(workspace)) return SSM_ERR_ALIGN;
+    if (workspace_bytes < ssm_linear_workspace_bytes(M, N, K)) return SSM_ERR_WORKSPACE;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    if (K == 0) return SSM_ERR_SHAPE;
+    const size_t f = sizeof(float);
+    const size_t xa = align256(static_cast<size_t>(M) * round4(K) * f);
+    float* xhi = static_cast<float*>(workspace);
+    float* xlo = at<float>(workspace, xa);
+    float* whi = at<float>(workspace, 2 * xa);
+    float* wlo = at<float>(workspace, 2 * xa + align256(static_cast<size_t>(N) * round4(K) * f));
+    Run run{stream};
+    Op A = run.split(X, ldx, M, K, false, xhi, xlo);
+    Op B = run.split(W, ldw, N, K, false, whi, wlo);
+    run.gemm(A, B, Y, ldy, bias, R, ldr);
+    return run.status;
+}
+
+size_t ssm_block_ctx_bytes(const ssm_block_desc* d) {
+    Dims s;
+    if (check_desc(d, s) != SSM_OK) return 0;
+    return ctx_layout(s).total;
+}
+
+size_t ssm_block_workspace_bytes(const ssm_block_desc* d) {
+    Dims s;
+    if (check_desc(d, s) != SSM_OK) return 0;
+    return ws_layout(s).total;
+}
+
+ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
+                         float* out, void* ctx, size_t ctx_bytes, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (s.M == 0) return SSM_OK;
+    if (!x || !out || !ctx || !workspace || !all_weights(w)) return SSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ctx) || !aligned16(workspace))
+        return SSM_ERR_ALIGN;
+    const Ctx c = ctx_layout(s);
+    const Ws ws = ws_layout(s);
+    if (ctx_bytes < c.total || workspace_bytes < ws.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+
+    const int M = static_cast<int>(s.M), Dm = s.Dm, D = s.D, N = s.N, R = s.R, P = s.P;
+    float* xn = at<float>(ctx, c.xn);
+    float* inv = at<float>(ctx, c.inv);
+    float* xz = at<float>(ctx, c.xz);
+    float* u = at<float>(ctx, c.u);
+    float* xd = at<float>(ctx, c.xd);
+    float* draw = at<float>(ctx, c.draw);
+    float* g = at<float>(ctx, c.g);
+    float* ahi = at<float>(workspace, ws.a_hi);
+    float* alo = at<float>(workspace, ws.a_lo);
+    float* whi = at<float>(workspace, ws.w_hi);
+    float* wlo = at<float>(workspace, ws.w_lo);
+
+    Run run{stream};
+    // 1. RMSNorm
+    run.cuda(ssm::launch_rmsnorm_fwd(x, w->norm_w, M, Dm, kRmsEps, xn, inv, stream));
+    // 2. in_proj (x_in | z)
+    {
+        Op A = run.split(xn, Dm, M, Dm, false, ahi, alo);
+        Op W = run.split(w->in_proj_w, Dm, 2 * D, Dm, false, whi, wlo);
+        run.gemm(A, W, xz, 2 * D, w->in_proj_b, nullptr, 0);
+    }
+    // 4-5. causal conv1d + SiLU on the x_in columns
+    if (run.ok()) run.check(ssm_conv1d_silu(s.B, s.L, D, s.K, xz, 2 * D, w->conv_w, w->conv_b, u, D, stream));
+    // 6. x_proj -> (dt | B | C)
+    {
+        Op A = run.split(u, D, M, D, false, ahi, alo);
+        Op W = run.split(w->x_proj_w, D, P, D, false, whi, wlo);
+        run.gemm(A, W, xd, P, w->x_proj_b, nullptr, 0);
+    }
+    // 7. dt_proj -> delta_raw
+    {
+        Op A = run.split(xd, P, M, R, false, ahi, alo);
+        Op W = run.split(w->dt_proj_w, R, D, R, false, whi, wlo);
+        run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
+    }
+    // 8-9. selective scan with the SiLU(z) gate
+    if (run.ok()) {
+        ssm_scan_desc sd = scan_desc_of(s);
+        run.check(ssm_scan_fwd(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, g,
+                               at<char>(ctx, c.scan), c.total - c.scan, nullptr, 0, stream));
+    }
+    // 10-11. out_proj + residual
+    {
+        Op A = run.split(g, D, M, D, false, ahi, alo);
+        Op W = run.split(w->out_proj_w, D, Dm, D, false, whi, wlo);
+        run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
+    }
+    return run.status;
+}
+
+ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
+                         const float* dout, const void* ctx, size_t ctx_bytes, float* dx,
+                         const ssm_block_grads* gr, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (!all_grads(gr)) return SSM_ERR_NULL;
+    if (s.M == 0) {
+        // No rows: every gradient is zero.
+        if ((st = check_device()) != SSM_OK) return st;
+        const size_t f = sizeof(float);
+        const int64_t D = s.D, Dm = s.Dm, P = s.P, R = s.R, N = s.N, K = s.K;
+        const std::pair<float*, size_t> zs[] = {
+            {gr->in_proj_w, 2 * D * Dm}, {gr->in_proj_b, 2 * D}, {gr->conv_w, D * K}, {gr->conv_b, D},
+            {gr->x_proj_w, P * D},       {gr->x_proj_b, P},      {gr->dt_proj_w, D * R}, {gr->dt_proj_b, D},
+            {gr->A_log, D * N},          {gr->D, D},             {gr->out_proj_w, Dm * D}, {gr->out_proj_b, Dm},
+            {gr->norm_w, Dm}};
+        for (const auto& z : zs) {
+            cudaError_t e = cudaMemsetAsync(z.first, 0, z.second * f, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+        return SSM_OK;
+    }
+    if (!x || !dout || !ctx || !dx || !workspace || !all_weights(w)) return SSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(dout) || !aligned16(ctx) || !aligned16(dx) || !aligned16(workspace))
+        return SSM_ERR_ALIGN;
+    const Ctx c = ctx_layout(s);
+    const Ws ws = ws_layout(s);
+    if (ctx_bytes < c.total || workspace_bytes < ws.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+
+    const int M = static_cast<int>(s.M), Dm = s.Dm, D = s.D, N = s.N, R = s.R, P = s.P;
+    const float* xn = at<float>(ctx, c.xn);
+    const float* inv = at<float>(ctx, c.inv);
+    const float* xz = at<float>(ctx, c.xz);
+    const float* u = at<float>(ctx, c.u);
+    const float* xd = at<float>(ctx, c.xd);
+    const float* draw = at<float>(ctx, c.draw);
+    const float* g = at<float>(ctx, c.g);
+    float* ahi = at<float>(workspace, ws.a_hi);
+    float* alo = at<float>(workspace, ws.a_lo);
+    float* bhi = at<float>(workspace, ws.b_hi);
+    float* blo = at<float>(workspace, ws.b_lo);
+    float* whi = at<float>(workspace, ws.w_hi);
+    float* wlo = at<float>(workspace, ws.w_lo);
+    float* dg = at<float>(workspace, ws.dg);
+    float* du = at<float>(workspace, ws.du);
+    float* ddelta = at<float>(workspace, ws.ddelta);
+    float* dxd = at<float>(workspace, ws.dxd);
+    float* dxz = at<float>(workspace, ws.dxz);
+    float* dxn = at<float>(workspace, ws.dxn);
+    float* red = at<float>(workspace, ws.red);
+
+    Run run{stream};
+    // Linear backward of Y = X W^T + b (cpu_ops.ts linearBackward), with
+    // dY (rows, nout; stride lddy), X (rows, k; stride ldx), W (nout, k):
+    //   dX = dY W  -> dX (stride lddx, + R when accumulate)
+    //   dW = dY^T X, db = column sums of dY.
+    auto linear_bwd = [&](const float* dY, int64_t lddy, int nout, const float* X, int64_t ldx, int k,
+                          const float* W, float* dX, int64_t lddx, bool accumulate, float* dW, float* db) {
+        if (dX) {
+            Op A = run.split(dY, lddy, M, nout, false, ahi, alo);
+            Op Wt = run.split(W, k, nout, k, true, whi, wlo);   // (k, nout)
+            run.gemm(A, Wt, dX, lddx, nullptr, accumulate ? dX : nullptr, lddx);
+        }
+        Op At = run.split(dY, lddy, M, nout, true, ahi, alo);   // (nout, M)
+        Op Xt = run.split(X, ldx, M, k, true, bhi, blo);        // (k, M)
+        run.gemm(At, Xt, dW, k, nullptr, nullptr, 0);
+        if (run.ok()) run.cuda(ssm::launch_colsum(dY, lddy, M, nout, db, red, stream));
+    };
+
+    // 10. out_proj (the residual's share of dx is added at step 1)
+    linear_bwd(dout, Dm, Dm, g, D, D, w->out_proj_w, dg, D, false, gr->out_proj_w, gr->out_proj_b);
+    // 9-8. gate and selective scan: du, ddelta, dB | dC into dxd, dz into dxz
+    if (run.ok()) {
+        ssm_scan_desc sd = scan_desc_of(s);
+        run.check(ssm_scan_bwd(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, dg,
+                               at<char>(ctx, c.scan), c.total - c.scan, du, ddelta, gr->A_log, dxd + R,
+                               dxd + R + N, gr->D, dxz + D, at<char>(workspace, ws.scan),
+                               ws.conv - ws.scan, stream));
+    }
+    // 7. dt_proj: d(dt) into the first R columns of dxd
+    linear_bwd(ddelta, D, D, xd, P, R, w->dt_proj_w, dxd, P, false, gr->dt_proj_w, gr->dt_proj_b);
+    // 6. x_proj: du += dxd W_x
+    linear_bwd(dxd, P, P, u, D, D, w->x_proj_w, du, D, true, gr->x_proj_w, gr->x_proj_b);
+    // 5-4. SiLU and the causal conv: d(x_in) into the first D columns of dxz
+    if (run.ok())
+        run.check(ssm_conv1d_silu_bwd(s.B, s.L, D, s.K, xz, 2 * D, w->conv_w, w->conv_b, du, D, dxz, 2 * D,
+                                      gr->conv_w, gr->conv_b, at<char>(workspace, ws.conv),
+                                      ws.red - ws.conv, stream));
+    // 2. in_proj
+    linear_bwd(dxz, 2 * D, 2 * D, xn, Dm, Dm, w->in_proj_w, dxn, Dm, false, gr->in_proj_w, gr->in_proj_b);
+    // 1. RMSNorm, plus the residual path: dx = dout + d(rmsnorm)
+    if (run.ok())
+        run.cuda(ssm::launch_rmsnorm_bwd(dxn, x, w->norm_w, inv, dout, M, Dm, dx, gr->norm_w, red, stream));
+    (void)N;
+    return run.status;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// gemm_args.cuh -- argument blocks of the fp32 linear-algebra kernels
+// (gemm.cu, rmsnorm.cu) shared with the C-ABI layer (abi.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// TN GEMM tile: 128 x 128 output, K in blocks of 32 fp32 (one 128-byte
+// swizzle row), three-stage TMA pipeline.
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 128;
+constexpr int kGemmBK = 32;
+constexpr int kGemmStages = 3;
+// K-blocks accumulated by the tensor core before the partial sum is added into
+// fp32 registers (bounds the tensor core's accumulation drift at 128 products).
+constexpr int kGemmGroup = 4;
+
+// C[m, n] = sum_k A[m, k] B[n, k] (+ bias[n]) (+ R[m, n]), fp32 in and out,
+// computed as three TF32 tensor-core products of hi/lo splits
+// (A_hi B_hi + A_hi B_lo + A_lo B_hi) accumulated in fp32 in tensor memory.
+// A_hi/A_lo are (M, K) and B_hi/B_lo are (N, K), row-major, K-contiguous.
+struct GemmArgs {
+    float* C;
+    const float* bias;   // may be null
+    const float* R;      // may be null; may alias C (accumulate)
+    int M, N, K;
+    int64_t ldc, ldr;
+};
+struct GemmMaps {
+    CUtensorMap a_hi, a_lo, b_hi, b_lo;
+};
+
+cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st);
+
+// hi = x rounded to TF32 (10 mantissa bits), lo = x - hi, for a (rows, cols)
+// fp32 matrix with row stride ldx.  transpose = 0 writes (rows, cols) with
+// row stride ldo; transpose = 1 writes the transpose (cols, rows).
+cudaError_t launch_split_tf32(const float* x, int64_t ldx, int rows, int cols, int transpose,
+                              float* hi, float* lo, int64_t ldo, cudaStream_t st);
+
+// out[n] = sum_m x[m, n] (fixed-order partial sums, no atomics); ws must hold
+// colsum_ws_floats(rows, cols) floats.
+size_t colsum_ws_floats(int rows, int cols);
+cudaError_t launch_colsum(const float* x, int64_t ldx, int rows, int cols, float* out, float* ws,
+                          cudaStream_t st);
+
+// RMSNorm of cpu_ops.ts: inv[r] = 1/sqrt(mean_i x[r,i]^2 + eps); y = x inv w.
+cudaError_t launch_rmsnorm_fwd(const float* x, const float* w, int rows, int dm, float eps,
+                               float* y, float* inv, cudaStream_t st);
+// Backward: dx[r,i] = res[r,i] + g_i inv - inv^3/dm * (sum_j g_j x_j) x_i with
+// g = dy w (res may be null); dw = sum_r dy x inv (written; ws must hold
+// rmsnorm_ws_floats(rows, dm) floats).
+size_t rmsnorm_ws_floats(int rows, int dm);
+cudaError_t launch_rmsnorm_bwd(const float* dy, const float* x, const float* w, const float* inv,
+                               const float* res, int rows, int dm, float* dx, float* dw, float* ws,
+                               cudaStream_t st);
+
+// Reads and clears the bounded-wait fault word of the GEMM kernel.
+cudaError_t read_clear_fault_gemm(unsigned* out);
+
+}  // namespace ssm

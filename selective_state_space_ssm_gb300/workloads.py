@@ -107,9 +107,11 @@ def conv_inputs(batch, seqlen, dinner, kconv, seed=0):
                 kconv=kconv)
 
 
-def block_inputs(dmodel, dinner, dtrank, dstate, dconv, batch, seqlen, seed=4):
+def block_inputs(dmodel, dinner, dtrank, dstate, dconv, batch, seqlen, seed=4, perturb=False):
     """Block input x, upstream gradient dout and the 13 block weights (names as in
-    the pages' Mamba1CpuWeights)."""
+    the pages' Mamba1CpuWeights).  perturb=True replaces the initial zero biases,
+    unit D / norm weights and the A_log ramp by seeded random values near them,
+    so that every parameter enters the result."""
     rng = np.random.Generator(np.random.PCG64(seed))
     M = batch * seqlen
     P = dtrank + 2 * dstate
@@ -130,6 +132,13 @@ def block_inputs(dmodel, dinner, dtrank, dstate, dconv, batch, seqlen, seed=4):
         wOutProj=w(dmodel, dinner), bOutProj=np.zeros(dmodel, np.float32),
         normWeight=np.ones(dmodel, np.float32),
     )
+    if perturb:
+        for k in ("bInProj", "bConv", "bXProj", "bDtProj", "bOutProj"):
+            weights[k] = (0.1 * _normal(rng, weights[k].shape)).astype(np.float32)
+        for k in ("D_vec", "normWeight"):
+            weights[k] = (1.0 + 0.1 * _normal(rng, weights[k].shape)).astype(np.float32)
+        weights["A_log"] = (weights["A_log"] + 0.1 * _normal(rng, weights["A_log"].shape)
+                            ).astype(np.float32)
     dims = dict(dmodel=dmodel, dinner=dinner, dtrank=dtrank, dstate=dstate, dconv=dconv,
                 batch=batch, seqlen=seqlen)
     return dict(x=x, dout=dout, weights=weights, dims=dims)

@@ -112,3 +112,68 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         binding.load()
+
+
+def _bdesc(**kw):
+    base = dict(batch=2, seqlen=64, dmodel=64, dinner=128, dstate=16, dtrank=8, dconv=4, disc=0)
+    base.update(kw)
+    return binding.BlockDesc(**base)
+
+
+def _a256(n):
+    return (n + 255) // 256 * 256
+
+
+def test_block_size_queries(lib):
+    d = _bdesc(batch=8, seqlen=2048, dmodel=768, dinner=1536, dstate=16, dtrank=48)
+    M, dm, D, P = 8 * 2048, 768, 1536, 48 + 32
+    sd = binding.ScanDesc(batch=8, seqlen=2048, dinner=D, dstate=16, dtype=0, disc=0,
+                          ld_u=D, ld_delta=D, ld_z=2 * D, ld_B=P, ld_C=P, ld_out=D)
+    # xn, inv, xz, u, xd, delta_raw, gated (fp32) and the scan's context
+    acts = [M * dm, M, 2 * M * D, M * D, M * P, M * D, M * D]
+    expect = sum(_a256(4 * n) for n in acts) + _a256(binding.ssm_scan_ctx_bytes(sd))
+    assert lib.ssm_block_ctx_bytes(ctypes.byref(d)) == expect
+    assert lib.ssm_block_workspace_bytes(ctypes.byref(d)) > 0
+    for bad in (dict(dmodel=30), dict(dinner=6), dict(dstate=17), dict(dtrank=0), dict(dconv=9),
+                dict(disc=3), dict(batch=-1)):
+        assert lib.ssm_block_ctx_bytes(ctypes.byref(_bdesc(**bad))) == 0, bad
+
+
+def _weights(p):
+    return binding.BlockWeights(*([p] * 13))
+
+
+def test_block_validation(lib):
+    p = ctypes.c_void_p(256)
+    w = _weights(256)
+    g = binding.BlockGrads(*([256] * 13))
+    big = 1 << 40
+
+    def fwd(d, x=p, wts=w, ctx_bytes=big, ctx=p):
+        return lib.ssm_block_fwd(ctypes.byref(d), x, ctypes.byref(wts), p, ctx, ctx_bytes, p, big,
+                                 None)
+
+    def bwd(d, x=p, grads=g):
+        return lib.ssm_block_bwd(ctypes.byref(d), x, ctypes.byref(w), p, p, big, p,
+                                 ctypes.byref(grads), p, big, None)
+
+    assert fwd(_bdesc(dstate=17)) == 2
+    assert fwd(_bdesc(dconv=0)) == 2
+    assert fwd(_bdesc(dmodel=30)) == 3
+    assert fwd(_bdesc(disc=2)) == 4
+    assert fwd(_bdesc(), x=None) == 1
+    assert fwd(_bdesc(), ctx=None) == 1
+    missing = _weights(256)
+    missing.conv_b = None
+    assert fwd(_bdesc(), wts=missing) == 1
+    assert fwd(_bdesc(), x=ctypes.c_void_p(264)) == 3
+    assert fwd(_bdesc(), ctx_bytes=16) == 5
+    assert fwd(_bdesc(batch=0)) == 0
+    no_grad = binding.BlockGrads(*([256] * 13))
+    no_grad.norm_w = None
+    assert bwd(_bdesc(), grads=no_grad) == 1
+    assert bwd(_bdesc(), x=None) == 1
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert fwd(_bdesc()) == 7
+        assert bwd(_bdesc()) == 7
