@@ -189,15 +189,14 @@ bool bc_tma_ok(const ssm_scan_desc* d, const void* B, const void* C, int64_t ldB
 }
 
 struct BwdLayout {
-    int cluster, ncl;
+    int ncl;
     size_t off_bc, off_dA, off_dD, total;
 };
 
 BwdLayout bwd_layout(const ssm_scan_desc* d) {
     BwdLayout l{};
     const int64_t tiles = (static_cast<int64_t>(d->dinner) + 31) / 32;
-    l.cluster = tiles >= ssm::kBwdCluster ? ssm::kBwdCluster : 1;
-    l.ncl = static_cast<int>((tiles + l.cluster - 1) / l.cluster);
+    l.ncl = static_cast<int>(tiles);
     const size_t M = static_cast<size_t>(d->batch) * d->seqlen;
     const size_t NT = nt_of(d->dstate);
     l.off_bc = 0;
@@ -250,6 +249,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
     if ((st = check_device()) != SSM_OK) return st;
 
     ssm::FwdMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
     const int nt = nt_of(d->dstate);
     const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
     const int fc = ssm::kFwdChannels;
@@ -261,8 +261,17 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
         !(bct ? encode_bc(&maps.B, B, d->dtype, d->dstate, d->seqlen, d->batch, r.B, nt, ssm::kFwdTile)
               : encode_act(&maps.B, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)) ||
         !(bct ? encode_bc(&maps.C, C, d->dtype, d->dstate, d->seqlen, d->batch, r.C, nt, ssm::kFwdTile)
-              : encode_act(&maps.C, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)))
+              : encode_act(&maps.C, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kFwdTile)) ||
+        !encode_act(&maps.out, out, d->dtype, d->dinner, d->seqlen, d->batch, r.out, ssm::kFwdTile, fc))
         return SSM_ERR_DEVICE;
+    if (ctx) {
+        // saved pre-gate y (packed) and the chunk-boundary states
+        if (!encode_act(&maps.y, static_cast<char*>(ctx) + ctx_y_offset(d), d->dtype, d->dinner, d->seqlen,
+                        d->batch, d->dinner, ssm::kFwdTile, fc))
+            return SSM_ERR_DEVICE;
+        const int64_t ck_rows = static_cast<int64_t>(d->batch) * nck_of(d->seqlen) * nt;
+        if (ck_rows > 0 && !encode_ck(&maps.ck, ctx, d->dinner, ck_rows, nt)) return SSM_ERR_DEVICE;
+    }
     ssm::ScanFwdArgs a{};
     a.B = B;
     a.C = C;
@@ -364,8 +373,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         a.nck = static_cast<int>(nck_of(d->seqlen));
         a.ncl = lay.ncl;
         a.bc_tma = bct ? 1 : 0;
-        cudaError_t e = ssm::launch_scan_bwd(d->dtype, nt, d->disc, z != nullptr, maps, a,
-                                             lay.cluster, stream);
+        cudaError_t e = ssm::launch_scan_bwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
         if (e != cudaSuccess) return fail_cuda(e);
     }
     ssm::ScanReduceArgs ra{};

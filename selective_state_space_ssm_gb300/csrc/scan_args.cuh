@@ -12,17 +12,16 @@ namespace ssm {
 // the backward recomputes h inside each chunk of kChunk steps.
 constexpr int kChunk = 8;
 
-// Forward: two lanes per channel (half of the states each), one warp of 16
-// channels per CTA, so the work spreads evenly over the 152 SMs.
-constexpr int kFwdChannels = 16;
+// Forward: one lane per channel (all states of it), one warp of 32 channels
+// per CTA.
+constexpr int kFwdChannels = 32;
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
 
 // Backward: one warp per CTA covers 32 channels x all states (each lane owns
-// 4 channels x dstate/4 states); CTAs of a cluster reduce dB/dC through DSMEM.
+// 4 channels x dstate/4 states); every CTA writes its own dB/dC partial plane.
 constexpr int kBwdWarps = 1;
 constexpr int kBwdStages = 2;
-constexpr int kBwdCluster = 8;
 
 struct ScanFwdArgs {
     const void* B;
@@ -46,13 +45,13 @@ struct ScanBwdArgs {
     void* du;
     void* ddelta;
     void* dz;            // null when there is no gate
-    float* ws_bc;        // [ncl][batch][seqlen][2][NT] dB | dC partial sums
+    float* ws_bc;        // [ncl][batch][seqlen][2][NT] dB | dC partial sums, one plane per CTA column
     float* ws_dA;        // [batch][dinner][NT] partial d/dA
     float* ws_dD;        // [batch][dinner] partial dD
     int batch, seqlen, dinner, dstate;
     int64_t ld_B, ld_C, ld_du, ld_ddelta, ld_dz;
     int nck;
-    int ncl;             // number of cluster columns (dB/dC partial planes)
+    int ncl;             // CTA columns = ceil(dinner / 32) = dB/dC partial planes
     int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
 };
 
@@ -72,10 +71,12 @@ struct ScanReduceArgs {
 };
 
 // Host launchers (scan_fwd.cu / scan_bwd.cu).  Return cudaSuccess or the launch error.
-// Tensor maps of the forward: u, delta_raw, z (32 channels x kFwdTile steps)
-// and B, C (NT states x kFwdTile steps).
+// Tensor maps of the forward: loads of u, delta_raw, z (32 channels x kFwdTile
+// steps) and B, C (NT states x kFwdTile steps).
+// Stores: out and the saved pre-gate y (32 channels x kFwdTile steps) and the
+// checkpoints (32 channels x NT states of one chunk boundary).
 struct FwdMaps {
-    CUtensorMap u, dr, z, B, C;
+    CUtensorMap u, dr, z, B, C, out, y, ck;
 };
 cudaError_t launch_scan_fwd(int dtype, int nt, int disc, bool gate, const FwdMaps& maps,
                             const ScanFwdArgs& a, cudaStream_t stream);
@@ -85,7 +86,7 @@ struct BwdMaps {
     CUtensorMap u, dr, z, dout, y, ck, B, C;
 };
 cudaError_t launch_scan_bwd(int dtype, int nt, int disc, bool gate, const BwdMaps& maps,
-                            const ScanBwdArgs& a, int cluster, cudaStream_t stream);
+                            const ScanBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_scan_reduce(const ScanReduceArgs& a, cudaStream_t stream);
 
 // Read and clear the fault word of the forward / backward translation unit.

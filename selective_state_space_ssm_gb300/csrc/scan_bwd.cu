@@ -17,35 +17,18 @@
 // a_t h_{t-1} in shared memory, then runs the reverse recurrence for g over
 // the chunk.  Each lane owns 4 channels x dstate/4 states (16 chains), so the
 // sums over states (y, sum g B, sum g A a h) and over channels (dB, dC) are
-// mostly register accumulations and finish with a few warp shuffles.  The 8
-// CTAs of a cluster (256 channels) add their per-chunk dB/dC through
-// distributed shared memory; one partial plane per cluster column is reduced by
-// scan_reduce_kernel, which also finishes dA_log and dD.
+// mostly register accumulations and finish with a few warp shuffles.  Each
+// CTA writes its warp-reduced dB/dC rows of every chunk to its own partial
+// plane with plain vector stores (no inter-CTA synchronisation: an earlier
+// cluster/DSMEM exchange cost a cluster-scope release fence per chunk, about
+// 16% of the kernel); scan_reduce_kernel adds the planes and also finishes
+// dA_log and dD.
 #include <algorithm>
 
 #include "scan_args.cuh"
 #include "ssm_common.cuh"
 
 namespace ssm {
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-    uint32_t raddr;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-    return v;
-}
 
 // Sum of NS values over the 8 lanes that differ in lane bits 4..2.  Returns the
 // sum of value index sel (written through `sel`), and whether this lane is the
@@ -101,8 +84,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     float* Pbs = Pd + TILE;                                              // [TC][32] delta*u | u
     float* Pdy = Pbs + TILE;                                             // [TC][32] dy
     float* part = Pdy + TILE;                                            // [TC][NQN][4][32]
-    float* rBC = part + TC * NQN * 4 * 32;                               // [2][TC][2NT]
-    uint64_t* full = reinterpret_cast<uint64_t*>(rBC + 2 * BCN);         // [S]
+    float* rbc = part + TC * NQN * 4 * 32;                               // [TC][2NT]
+    uint64_t* full = reinterpret_cast<uint64_t*>(rbc + BCN);             // [S]
 
     const int lane = threadIdx.x;
     const int cg = lane >> 2, ng = lane & 3;
@@ -112,7 +95,6 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
     const int nchunks = (L + TC - 1) / TC;
     const size_t row0 = static_cast<size_t>(b) * L;
-    const uint32_t crank = cluster_ctarank();
     const int dch = c0 + lane;                   // channel of this lane in pro/epilogue
     const bool lane_ok = dch < Dn;
     const bool quad_ok = c0 + cbase < Dn;
@@ -198,39 +180,14 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     bool ok = true;
     int waited = 0;
 
-    // dB|dC through DSMEM, one chunk behind: at the start of an iteration the
-    // peers have long arrived for the previous chunk, so the wait rarely blocks.
-    const uint32_t cs = static_cast<uint32_t>(gridDim.x / a.ncl);
-    const int ncol = blockIdx.x / static_cast<int>(cs);
-    auto exchange = [&](int kc_prev, int buf) {
-        const int t0p = kc_prev * TC;
-        const int jmp = min(TC, L - t0p);
-        const int per = BCN / static_cast<int>(cs);
-        const float* src = rBC + buf * BCN;
-        for (int e = lane; e < per; e += 32) {
-            const int idx = static_cast<int>(crank) * per + e;
-            const int j = idx / (2 * NT);
-            if (j < jmp) {
-                float sum = 0.0f;
-                for (uint32_t rk = 0; rk < cs; ++rk) sum += ld_dsmem(src + idx, rk);
-                a.ws_bc[((static_cast<size_t>(ncol) * a.batch + b) * L + t0p + j) * 2 * NT +
-                        idx % (2 * NT)] = sum;
-            }
-        }
-    };
+    // this CTA's partial plane of dB|dC: [batch][seqlen][2][NT]
+    float* plane = a.ws_bc + static_cast<size_t>(blockIdx.x) * a.batch * L * 2 * NT;
 
     for (int it = 0; it < nchunks; ++it) {
         const int kc = nchunks - 1 - it;
         const int t0 = kc * TC;
         const int jmax = min(TC, L - t0);
         const int s = it % S;
-        float* rbc = rBC + (it & 1) * BCN;   // this chunk's warp-reduced dB|dC
-
-        if (it > 0) {
-            cluster_wait();
-            if (ok) exchange(kc + 1, (it - 1) & 1);
-            __syncwarp();
-        }
         if (ok) ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) waited = it + 1;
@@ -476,10 +433,14 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
         }
-        // this chunk's dB|dC rows are in rBC: publish them before the epilogue's
-        // global stores are issued (the release then has little to wait for)
+        // this chunk's warp-reduced dB|dC rows (rbc) go to the CTA's plane
         __syncwarp();
-        cluster_arrive();
+        if (ok) {
+            float4* dst = reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + t0) * 2 * NT);
+            const float4* src = reinterpret_cast<const float4*>(rbc);
+            for (int e = lane; e < jmax * 2 * NT / 4; e += 32) dst[e] = src[e];
+        }
+        __syncwarp();
 
         if (ok) {
             // ---- epilogue (lane = channel): finish du, ddelta_raw, dz, dD
@@ -524,16 +485,6 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         __syncwarp();
         if (lane == 0 && ok && it + S < nchunks) issue(it + S);
     }
-    if (nchunks > 0) {
-        // the last chunk's rows, then keep every CTA alive until its peers
-        // have finished reading its shared memory
-        cluster_wait();
-        if (ok) exchange(0, (nchunks - 1) & 1);
-        __syncwarp();
-        cluster_arrive();
-        cluster_wait();
-    }
-
     if (lane == 0 && !ok) {
         for (int it = waited; it < nchunks && it < waited + S; ++it)
             mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
@@ -553,7 +504,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     }
 }
 
-// dB, dC: sum of the per-cluster-column planes; dA_log = A * sum_b dA inside the
+// dB, dC: sum of the per-CTA-column planes; dA_log = A * sum_b dA inside the
 // clamp (exactly 0 at or beyond it); dD = sum_b dD.
 __global__ void scan_reduce_kernel(const ScanReduceArgs a) {
     const size_t M = static_cast<size_t>(a.batch) * a.seqlen;
@@ -610,52 +561,36 @@ static size_t bwd_smem_bytes() {
            + (DISC == 1 ? 2 : 1) * 32 * (NT == 16 ? 20 : 10) * sizeof(float)   // A2 [, 1/A]
            + 3 * TC * 32 * sizeof(float)               // delta, delta*u, dy
            + TC * NQN * 4 * 32 * sizeof(float)         // state-sum partials
-           + 2 * 2 * TC * NT * sizeof(float)           // dB|dC for the cluster exchange
+           + 2 * TC * NT * sizeof(float)               // warp-reduced dB|dC of a chunk
            + kBwdStages * sizeof(uint64_t);
 }
 
 template <typename T, int NT, int DISC, bool GATE>
-static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, int cluster,
-                                cudaStream_t st) {
+static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
     const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE>();
     auto kern = scan_bwd_kernel<T, NT, DISC, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.ncl * cluster), static_cast<unsigned>(a.batch));
-    cfg.blockDim = dim3(32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, maps, a);
-    if (e != cudaSuccess) return e;
+    kern<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch)), 32, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
 template <typename T, int NT>
 static cudaError_t launch_bwd_nt(int disc, bool gate, const BwdMaps& m, const ScanBwdArgs& a,
-                                 int cl, cudaStream_t st) {
+                                 cudaStream_t st) {
     if (disc == 0)
-        return gate ? launch_bwd_t<T, NT, 0, true>(m, a, cl, st)
-                    : launch_bwd_t<T, NT, 0, false>(m, a, cl, st);
-    return gate ? launch_bwd_t<T, NT, 1, true>(m, a, cl, st)
-                : launch_bwd_t<T, NT, 1, false>(m, a, cl, st);
+        return gate ? launch_bwd_t<T, NT, 0, true>(m, a, st) : launch_bwd_t<T, NT, 0, false>(m, a, st);
+    return gate ? launch_bwd_t<T, NT, 1, true>(m, a, st) : launch_bwd_t<T, NT, 1, false>(m, a, st);
 }
 
 cudaError_t launch_scan_bwd(int dtype, int nt, int disc, bool gate, const BwdMaps& maps,
-                            const ScanBwdArgs& a, int cluster, cudaStream_t stream) {
+                            const ScanBwdArgs& a, cudaStream_t stream) {
     if (dtype == 0)
-        return nt == 8 ? launch_bwd_nt<float, 8>(disc, gate, maps, a, cluster, stream)
-                       : launch_bwd_nt<float, 16>(disc, gate, maps, a, cluster, stream);
-    return nt == 8 ? launch_bwd_nt<__nv_bfloat16, 8>(disc, gate, maps, a, cluster, stream)
-                   : launch_bwd_nt<__nv_bfloat16, 16>(disc, gate, maps, a, cluster, stream);
+        return nt == 8 ? launch_bwd_nt<float, 8>(disc, gate, maps, a, stream)
+                       : launch_bwd_nt<float, 16>(disc, gate, maps, a, stream);
+    return nt == 8 ? launch_bwd_nt<__nv_bfloat16, 8>(disc, gate, maps, a, stream)
+                   : launch_bwd_nt<__nv_bfloat16, 16>(disc, gate, maps, a, stream);
 }
 
 cudaError_t read_clear_fault_bwd(unsigned* out) {

@@ -11,8 +11,8 @@
 // dstate states of it in registers for the whole sequence, so every element
 // costs one ex2 and four fp32 ops (two packed f32x2 instructions per state
 // pair) and nothing crosses threads.  A warp-sized CTA streams u / delta_raw /
-// z tiles of kFwdTile steps x 32 channels with TMA (4 tiles in flight) and
-// B/C tiles with plain loads, both shared by the 32 channels.  Every kChunk
+// z tiles of kFwdTile steps x 32 channels and the B/C tiles of the same steps
+// (shared by the 32 channels) with TMA, 4 tiles in flight.  Every kChunk
 // steps the state is written to the context buffer for the backward.
 #include "scan_args.cuh"
 #include "ssm_common.cuh"
@@ -98,55 +98,52 @@ __device__ __forceinline__ const float* fwd_stage_bc(float* bcs, const T* Bs, bo
     return bcs;
 }
 
-// Lane layout: a warp-sized CTA owns 16 channels; lanes l and l ^ 16 share
-// channel l & 15, lane l < 16 holding states [0, NT/2) and lane l >= 16
-// states [NT/2, NT).  Each lane of a pair works out the per-step scalars
-// (softplus, gate) for half of the tile's steps and the pair swaps them with
-// one shuffle, so nothing per step is computed twice.
+// Lane layout: a warp-sized CTA owns 32 channels of one batch row, one
+// channel per lane with all NT states of it in registers, so nothing per step
+// is computed twice and no value crosses lanes.
 template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32, 1)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
-    constexpr int CW = kFwdChannels;                    // channels per CTA (16)
+    constexpr int CW = kFwdChannels;                    // channels per CTA (32)
     constexpr int TS = kFwdTile;
-    constexpr int HT = TS / 2;                          // steps whose scalars a lane computes
     constexpr int S = kFwdStages;
     constexpr int NTEN = GATE ? 3 : 2;
-    constexpr int NL = NT / 2;                          // states per lane
-    constexpr int NQ = NL / 2;                          // state pairs per lane
+    constexpr int NQ = NT / 2;                          // state pairs per lane
     constexpr int TILE = TS * CW;                       // elements per activation tile
     constexpr int BCT = TS * NT;                        // elements per B or C tile
     constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
     constexpr uint32_t kBCBytes = 2 * BCT * sizeof(T);
     constexpr int STAGE = NTEN * TILE + 2 * BCT;        // elements per stage
-    static_assert(TS % kChunk == 0 && HT == kChunk, "a lane's half tile is one checkpoint chunk");
+    static_assert(TS % kChunk == 0, "tiles hold whole checkpoint chunks");
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
 
+    constexpr int NCK = TS / kChunk;                    // chunk boundaries per tile
     extern __shared__ __align__(128) unsigned char smem[];
     T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
     float* bcs = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] B | C
-    uint64_t* full = reinterpret_cast<uint64_t*>(bcs + 2 * BCT);             // [S]
+    float* ckst = bcs + 2 * BCT;                                             // [2][NCK][NT][CW]
+    T* ost = reinterpret_cast<T*>(ckst + 2 * NCK * NT * CW);                // [2][2][TS][CW] out | y
+    uint64_t* full = reinterpret_cast<uint64_t*>(ost + 2 * 2 * TILE);        // [S]
 
     const int lane = threadIdx.x;
-    const int ch = lane & 15, half = lane >> 4;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
-    const int d = c0 + ch;
+    const int d = c0 + lane;
     const bool active = d < a.dinner;
     const int L = a.seqlen, N = a.dstate;
     const int ntiles = (L + TS - 1) / TS;
     const size_t row0 = static_cast<size_t>(b) * L;
     const bool bc_tma = a.bc_tma != 0;
-    const int nbase = half * NL;                        // first state of this lane
 
     // Per-(channel, state) constants: A*log2(e) as the ex2 argument scale (0 on
-    // padding states and inactive lanes, where B = C = 0 keeps h at 0).
+    // padding states and inactive lanes, where B = C = 0 or u = 0 keeps h at 0).
     float2 A2[NQ], Anat[NQ], invA[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         float v[2], w[2], r[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = nbase + 2 * q + e;
+            const int n = 2 * q + e;
             const bool ok = active && n < N;
             const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
             v[e] = ok ? A * kLog2e : 0.0f;
@@ -185,8 +182,8 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     if (lane == 0)
         for (int k = 0; k < S && k < ntiles; ++k) issue(k);
 
-    T* outp = static_cast<T*>(a.out);
-    T* ysv = static_cast<T*>(a.ysave);
+    const bool save_y = GATE && a.ysave != nullptr;
+    const bool save_ck = a.ctx != nullptr && a.nck > 0;
     int k = 0;
     for (; k < ntiles; ++k) {
         const int s = k % S;
@@ -199,19 +196,19 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         const T* tz = tu + 2 * TILE;
         const float* Bf = fwd_stage_bc<T, NT, TS>(bcs, tu + NTEN * TILE, bc_tma, Bp, Cp, a.ld_B,
                                                   a.ld_C, row0, k, L, N, lane);
+        __syncwarp();
         const int jmax = min(TS, L - k * TS);
 
-        // Phase A: this lane's half of the tile's per-step scalars, then swap
-        // delta and delta*u (or u) with the partner lane.
-        float dtv[TS], bsc[TS], dterm[HT], gate[HT];
+        // Phase A: the per-step scalars of the whole tile (independent across
+        // steps, so their dependency chains overlap).
+        float dtv[TS], bsv[TS], gzv[TS], duv[TS];
 #pragma unroll
-        for (int jj = 0; jj < HT; ++jj) {
-            const int j = half * HT + jj;
-            const float uv = Act<T>::to_f(tu[j * CW + ch]);
-            const float xr = Act<T>::to_f(tr[j * CW + ch]);
+        for (int j = 0; j < TS; ++j) {
+            const float uv = Act<T>::to_f(tu[j * CW + lane]);
+            const float xr = Act<T>::to_f(tr[j * CW + lane]);
             float dt, gz = 1.0f;
             if (GATE) {
-                const float zv = Act<T>::to_f(tz[j * CW + ch]);
+                const float zv = Act<T>::to_f(tz[j * CW + lane]);
                 float sz;
                 softplus_sigmoid(xr, zv, dt, sz);
                 gz = zv * sz;                                   // silu(z)
@@ -219,78 +216,69 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
                 float e;
                 dt = softplus_e(xr, e);
             }
-            const float bs = DISC == 0 ? dt * uv : uv;          // Euler: delta*u; ZOH: u
-            const float dt_o = __shfl_xor_sync(0xffffffffu, dt, 16);
-            const float bs_o = __shfl_xor_sync(0xffffffffu, bs, 16);
-            dtv[jj] = half ? dt_o : dt;
-            dtv[HT + jj] = half ? dt : dt_o;
-            bsc[jj] = half ? bs_o : bs;
-            bsc[HT + jj] = half ? bs : bs_o;
-            dterm[jj] = Dd * uv;
-            gate[jj] = gz;
+            dtv[j] = dt;
+            bsv[j] = DISC == 0 ? dt * uv : uv;                  // Euler: delta*u; ZOH: u
+            gzv[j] = gz;
+            duv[j] = Dd * uv;
         }
-        __syncwarp();
 
-        // Phase B: every tile runs all TS steps: past seqlen the TMA tiles and
-        // B|C are zero, so the extra steps only evolve a state never stored.
-        float yv[TS];
-        float2 hmid[NQ];
-        const float* bl = Bf + nbase;
+        // Phase B: the recurrence.  Every tile runs all TS steps: past seqlen
+        // the TMA tiles and B|C are zero, so the extra steps only evolve a
+        // state that is never stored.  Outputs go to a staging tile in shared
+        // memory (double-buffered) and leave by TMA store; the store of tile
+        // k-2 must have finished reading its buffer first.
+        if (lane == 0 && k >= 2) bulk_wait_read_1();
+        __syncwarp();
+        T* so = ost + (k & 1) * 2 * TILE;
+        float* sc = ckst + (k & 1) * NCK * NT * CW;
 #pragma unroll
         for (int j = 0; j < TS; ++j) {
-            yv[j] = fwd_step<NL, DISC>(h, A2, Anat, invA, bl + j * NT, bl + BCT + j * NT, dtv[j],
-                                       bsc[j]);
-            if (j == kChunk - 1) {
+            const float y = fwd_step<NT, DISC>(h, A2, Anat, invA, Bf + j * NT, Bf + BCT + j * NT, dtv[j],
+                                               bsv[j]) + duv[j];
+            so[j * CW + lane] = Act<T>::from_f(GATE ? y * gzv[j] : y);
+            if (save_y) so[TILE + j * CW + lane] = Act<T>::from_f(y);
+            if ((j + 1) % kChunk == 0 && save_ck) {
+                // state after the last step of a chunk = checkpoint of the next one
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) hmid[q] = h[q];
-            }
-        }
-        // Each lane finishes the steps of its half: y = own part + partner part.
-#pragma unroll
-        for (int jj = 0; jj < HT; ++jj) {
-            const float send = half ? yv[jj] : yv[HT + jj];
-            const float mine = half ? yv[HT + jj] : yv[jj];
-            const float y = mine + __shfl_xor_sync(0xffffffffu, send, 16) + dterm[jj];
-            const int j = half * HT + jj;
-            if (active && j < jmax) {
-                const size_t r = row0 + k * TS + j;
-                outp[r * a.ld_out + d] = Act<T>::from_f(GATE ? y * gate[jj] : y);
-                if (GATE && ysv) ysv[r * a.dinner + d] = Act<T>::from_f(y);
-            }
-        }
-        if (active && a.ctx) {
-            // states after steps kChunk-1 and TS-1 of the tile (chunk boundaries)
-#pragma unroll
-            for (int m = 0; m < TS / kChunk; ++m) {
-                const int t1 = k * TS + (m + 1) * kChunk;       // first step of the next chunk
-                if (t1 < L) {
-                    float* cp = a.ctx + ((static_cast<size_t>(b) * a.nck + t1 / kChunk - 1) * NT + nbase) *
-                                            a.dinner + d;
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) {
-                        const float2 hv = m == 0 ? hmid[q] : h[q];
-                        cp[static_cast<size_t>(2 * q) * a.dinner] = hv.x;
-                        cp[static_cast<size_t>(2 * q + 1) * a.dinner] = hv.y;
-                    }
+                for (int q = 0; q < NQ; ++q) {
+                    sc[((j / kChunk) * NT + 2 * q) * CW + lane] = h[q].x;
+                    sc[((j / kChunk) * NT + 2 * q + 1) * CW + lane] = h[q].y;
                 }
             }
         }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && k + S < ntiles) issue(k + S);
+        if (lane == 0) {
+            tma_store_3d(&maps.out, so, c0, k * TS, b);
+            if (save_y) tma_store_3d(&maps.y, so + TILE, c0, k * TS, b);
+            if (save_ck) {
+#pragma unroll
+                for (int m = 0; m < NCK; ++m) {
+                    const int t1 = k * TS + (m + 1) * kChunk;   // first step of the next chunk
+                    if (t1 < L)
+                        tma_store_2d(&maps.ck, sc + m * NT * CW, c0, (b * a.nck + t1 / kChunk - 1) * NT);
+                }
+            }
+            bulk_commit();
+            if (k + S < ntiles) issue(k + S);
+        }
     }
     if (k < ntiles && lane == 0) {
         // A wait gave up: drain the copies still in flight (bounded) before exit.
         for (int kk = k; kk < ntiles && kk < k + S; ++kk)
             mbar_wait(&full[kk % S], (kk / S) & 1, kFaultDrain);
     }
+    if (lane == 0) bulk_wait_all();   // the staged stores have left shared memory
 }
 
 template <typename T, int NT, int DISC, bool GATE>
 static cudaError_t launch_fwd_t(const FwdMaps& m, const ScanFwdArgs& a, cudaStream_t st) {
     constexpr int NTEN = GATE ? 3 : 2;
-    constexpr int STAGE = NTEN * kFwdTile * kFwdChannels + 2 * kFwdTile * NT;
+    constexpr int TILE = kFwdTile * kFwdChannels;
+    constexpr int STAGE = NTEN * TILE + 2 * kFwdTile * NT;
     const size_t smem = kFwdStages * STAGE * sizeof(T) + 2 * kFwdTile * NT * sizeof(float) +
-                        kFwdStages * sizeof(uint64_t);
+                        2 * (kFwdTile / kChunk) * NT * kFwdChannels * sizeof(float) +
+                        2 * 2 * TILE * sizeof(T) + kFwdStages * sizeof(uint64_t);
     auto kern = scan_fwd_kernel<T, NT, DISC, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
