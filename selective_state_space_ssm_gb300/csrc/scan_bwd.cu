@@ -14,11 +14,12 @@
 // Design (GB300): the forward saved h every kChunk (= 8) steps.  A warp-sized
 // CTA owns 32 channels of one batch row and walks the chunks last to first.
 // For each chunk it recomputes h forward from the checkpoint (pass B), keeping
-// a_t h_{t-1} in shared memory, then runs the reverse recurrence for g over
+// a_t h_{t-1} in registers, then runs the reverse recurrence for g over
 // the chunk.  Each lane owns 4 channels x dstate/4 states (16 chains), so the
 // sums over states (y, sum g B, sum g A a h) and over channels (dB, dC) are
-// mostly register accumulations and finish with a few warp shuffles.  Each
-// CTA writes its warp-reduced dB/dC rows of every chunk to its own partial
+// mostly register accumulations.  Per step, a lane's dB/dC partials (its 4
+// channels) go to shared memory by channel group; once per chunk the warp
+// adds the 8 groups with float4 loads and writes the rows of its own partial
 // plane with plain vector stores (no inter-CTA synchronisation: an earlier
 // cluster/DSMEM exchange cost a cluster-scope release fence per chunk, about
 // 16% of the kernel); scan_reduce_kernel adds the planes and also finishes
@@ -29,31 +30,6 @@
 #include "ssm_common.cuh"
 
 namespace ssm {
-
-// Sum of NS values over the 8 lanes that differ in lane bits 4..2.  Returns the
-// sum of value index sel (written through `sel`), and whether this lane is the
-// unique owner of that result among the 8 lanes.
-template <int NS>
-__device__ __forceinline__ float rs_over_cg(float (&v)[NS], int lane, int& sel, bool& owner) {
-    if constexpr (NS == 4) {
-        const bool b4 = lane & 16, b3 = lane & 8;
-        float w0 = (b4 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, b4 ? v[0] : v[2], 16);
-        float w1 = (b4 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, b4 ? v[1] : v[3], 16);
-        float x = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        sel = (b4 ? 2 : 0) + (b3 ? 1 : 0);
-        owner = (lane & 4) == 0;
-        return x;
-    } else {  // NS == 2
-        const bool b4 = lane & 16;
-        float x = (b4 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, b4 ? v[0] : v[1], 16);
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        sel = b4 ? 1 : 0;
-        owner = (lane & 12) == 0;
-        return x;
-    }
-}
 
 template <typename T, int NT, int DISC, bool GATE>
 __global__ void __launch_bounds__(32, 1)
@@ -84,8 +60,9 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     float* Pbs = Pd + TILE;                                              // [TC][32] delta*u | u
     float* Pdy = Pbs + TILE;                                             // [TC][32] dy
     float* part = Pdy + TILE;                                            // [TC][NQN][4][32]
-    float* rbc = part + TC * NQN * 4 * 32;                               // [TC][2NT]
-    uint64_t* full = reinterpret_cast<uint64_t*>(rbc + BCN);             // [S]
+    constexpr int PJ = 9 * NT;                  // padded row: conflict-free float4 sums
+    float* pbuf = part + TC * NQN * 4 * 32;                              // [TC][PJ] dB or dC by channel group
+    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + TC * PJ);        // [S]
 
     const int lane = threadIdx.x;
     const int cg = lane >> 2, ng = lane & 3;
@@ -182,6 +159,35 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 
     // this CTA's partial plane of dB|dC: [batch][seqlen][2][NT]
     float* plane = a.ws_bc + static_cast<size_t>(blockIdx.x) * a.batch * L * 2 * NT;
+    // dB or dC partials of one step, summed over this lane's 4 channels, go to
+    // pbuf by channel group; flush() adds the 8 groups (the warp's 32 channels)
+    // and writes the chunk's rows to the plane, float4 per lane.
+    auto store_partial = [&](int j, const float2 (&v)[NS / 2]) {
+        float* pp = pbuf + j * PJ + cg * NT + ng * NS;
+        if constexpr (NS == 4)
+            *reinterpret_cast<float4*>(pp) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        else
+            *reinterpret_cast<float2*>(pp) = v[0];
+    };
+    auto flush = [&](int coff, int t0f, int jmaxf) {
+        constexpr int NM = NT / 4;
+        if (lane < TC * NM) {
+            const int j = lane / NM, m = lane % NM;
+            float4 acc = *reinterpret_cast<const float4*>(pbuf + j * PJ + 4 * m);
+#pragma unroll
+            for (int c = 1; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(pbuf + j * PJ + c * NT + 4 * m);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            if (j < jmaxf)
+                *reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + t0f + j) * 2 * NT + coff +
+                                           4 * m) = acc;
+        }
+        __syncwarp();
+    };
 
     for (int it = 0; it < nchunks; ++it) {
         const int kc = nchunks - 1 - it;
@@ -318,16 +324,12 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                                 dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
                             }
                         }
-                        float dCv[NS];
-#pragma unroll
-                        for (int p = 0; p < NS / 2; ++p) { dCv[2 * p] = dC[p].x; dCv[2 * p + 1] = dC[p].y; }
-                        int sel;
-                        bool own;
-                        const float dCs = rs_over_cg<NS>(dCv, lane, sel, own);
-                        if (own) rbc[j * 2 * NT + NT + ng * NS + sel] = dCs;
+                        store_partial(j, dC);
                     }
                 }
             }
+            __syncwarp();
+            flush(NT, t0, jmax);   // dC rows of this chunk
 
             // ---- reverse pass: g_t = C_t dy_t + a_{t+1} g_{t+1}; state sums to
             //      shared partials, dB partials reduced with shuffles.
@@ -419,26 +421,14 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                             *reinterpret_cast<float4*>(part + ((j * NQN + qn) * 4 + ng) * 32 +
                                                        ((cbase + 8 * ng) & 31)) =
                                 make_float4(sums[qn][0], sums[qn][1], sums[qn][2], sums[qn][3]);
-                        float dBv[NS];
-#pragma unroll
-                        for (int p = 0; p < NS / 2; ++p) { dBv[2 * p] = dB[p].x; dBv[2 * p + 1] = dB[p].y; }
-                        int sel;
-                        bool own;
-                        const float dBs = rs_over_cg<NS>(dBv, lane, sel, own);
-                        if (own) rbc[j * 2 * NT + ng * NS + sel] = dBs;
+                        store_partial(j, dB);
                     }
                 }
             }
             __syncwarp();
+            flush(0, t0, jmax);    // dB rows of this chunk
 #pragma unroll
             for (int i = 0; i < 4; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
-        }
-        // this chunk's warp-reduced dB|dC rows (rbc) go to the CTA's plane
-        __syncwarp();
-        if (ok) {
-            float4* dst = reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + t0) * 2 * NT);
-            const float4* src = reinterpret_cast<const float4*>(rbc);
-            for (int e = lane; e < jmax * 2 * NT / 4; e += 32) dst[e] = src[e];
         }
         __syncwarp();
 
@@ -561,7 +551,7 @@ static size_t bwd_smem_bytes() {
            + (DISC == 1 ? 2 : 1) * 32 * (NT == 16 ? 20 : 10) * sizeof(float)   // A2 [, 1/A]
            + 3 * TC * 32 * sizeof(float)               // delta, delta*u, dy
            + TC * NQN * 4 * 32 * sizeof(float)         // state-sum partials
-           + 2 * TC * NT * sizeof(float)               // warp-reduced dB|dC of a chunk
+           + TC * 9 * NT * sizeof(float)               // dB or dC partials by channel group
            + kBwdStages * sizeof(uint64_t);
 }
 
