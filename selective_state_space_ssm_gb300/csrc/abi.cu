@@ -72,7 +72,7 @@ using ssm_host::fail_cuda;
 using ssm_host::g_last_cuda_error;
 
 // (M, dinner) activation viewed as [batch][seqlen][dinner] with row stride ld;
-// box = 32 channels x box_rows steps x 1 batch row; out-of-range reads fill 0.
+// box = box_ch channels x box_rows steps x 1 batch row; out-of-range reads fill 0.
 bool encode_act(CUtensorMap* m, const void* ptr, int dtype, int dinner, int seqlen, int batch,
                 int64_t ld, int box_rows, int box_ch = 32) {
     auto fn = encode_fn();
@@ -149,12 +149,12 @@ size_t ctx_total_bytes(const ssm_scan_desc* d) {
     return ctx_y_offset(d) + static_cast<size_t>(d->batch) * d->seqlen * d->dinner * es;
 }
 
-bool encode_ck(CUtensorMap* m, const void* ptr, int dinner, int64_t rows, int nt) {
+bool encode_ck(CUtensorMap* m, const void* ptr, int dinner, int64_t rows, int nt, int box_ch) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(dinner), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(dinner) * 4};
-    cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(nt)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_ch), static_cast<cuuint32_t>(nt)};
     cuuint32_t estr[2] = {1u, 1u};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -189,14 +189,14 @@ bool bc_tma_ok(const ssm_scan_desc* d, const void* B, const void* C, int64_t ldB
 }
 
 struct BwdLayout {
-    int ncl;
+    int cw, ncl;
     size_t off_bc, off_dA, off_dD, total;
 };
 
 BwdLayout bwd_layout(const ssm_scan_desc* d) {
     BwdLayout l{};
-    const int64_t tiles = (static_cast<int64_t>(d->dinner) + 31) / 32;
-    l.ncl = static_cast<int>(tiles);
+    l.cw = ssm::bwd_channels(d->batch, d->dinner);
+    l.ncl = static_cast<int>((static_cast<int64_t>(d->dinner) + l.cw - 1) / l.cw);
     const size_t M = static_cast<size_t>(d->batch) * d->seqlen;
     const size_t NT = nt_of(d->dstate);
     l.off_bc = 0;
@@ -270,7 +270,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
                         d->batch, d->dinner, ssm::kFwdTile, fc))
             return SSM_ERR_DEVICE;
         const int64_t ck_rows = static_cast<int64_t>(d->batch) * nck_of(d->seqlen) * nt;
-        if (ck_rows > 0 && !encode_ck(&maps.ck, ctx, d->dinner, ck_rows, nt)) return SSM_ERR_DEVICE;
+        if (ck_rows > 0 && !encode_ck(&maps.ck, ctx, d->dinner, ck_rows, nt, fc)) return SSM_ERR_DEVICE;
     }
     ssm::ScanFwdArgs a{};
     a.B = B;
@@ -333,18 +333,19 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
         const bool ysaved = z != nullptr && ctx != nullptr;
         const void* ybuf = ysaved ? static_cast<const char*>(ctx) + ctx_y_offset(d) : u;
-        if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk) ||
+        const int bc = lay.cw;
+        if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk, bc) ||
             !encode_act(&maps.dr, delta_raw, d->dtype, d->dinner, d->seqlen, d->batch, r.delta,
-                        ssm::kChunk) ||
+                        ssm::kChunk, bc) ||
             !encode_act(&maps.dout, dout, d->dtype, d->dinner, d->seqlen, d->batch, r.dout,
-                        ssm::kChunk) ||
+                        ssm::kChunk, bc) ||
             !encode_act(&maps.z, z ? z : u, d->dtype, d->dinner, d->seqlen, d->batch, z ? r.z : r.u,
-                        ssm::kChunk) ||
+                        ssm::kChunk, bc) ||
             !encode_act(&maps.y, ybuf, d->dtype, d->dinner, d->seqlen, d->batch,
-                        ysaved ? d->dinner : r.u, ssm::kChunk) ||
-            !(nck > 0 ? encode_ck(&maps.ck, ctx, d->dinner, static_cast<int64_t>(d->batch) * nck * nt, nt)
+                        ysaved ? d->dinner : r.u, ssm::kChunk, bc) ||
+            !(nck > 0 ? encode_ck(&maps.ck, ctx, d->dinner, static_cast<int64_t>(d->batch) * nck * nt, nt, bc)
                       : encode_act(&maps.ck, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u,
-                                   ssm::kChunk)) ||
+                                   ssm::kChunk, bc)) ||
             !(bct ? encode_bc(&maps.B, B, d->dtype, d->dstate, d->seqlen, d->batch, r.B, nt, ssm::kChunk)
                   : encode_act(&maps.B, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk)) ||
             !(bct ? encode_bc(&maps.C, C, d->dtype, d->dstate, d->seqlen, d->batch, r.C, nt, ssm::kChunk)
@@ -372,6 +373,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         a.ld_dz = r.dz;
         a.nck = static_cast<int>(nck_of(d->seqlen));
         a.ncl = lay.ncl;
+        a.cw = lay.cw;
         a.bc_tma = bct ? 1 : 0;
         cudaError_t e = ssm::launch_scan_bwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
         if (e != cudaSuccess) return fail_cuda(e);

@@ -18,10 +18,18 @@ constexpr int kFwdChannels = 32;
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
 
-// Backward: one warp per CTA covers 32 channels x all states (each lane owns
-// 4 channels x dstate/4 states); every CTA writes its own dB/dC partial plane.
-constexpr int kBwdWarps = 1;
+// Backward: one warp per CTA covers 32 or 16 channels x all states (each lane
+// owns 4 or 2 channels x dstate/4 states); every CTA writes its own dB/dC
+// partial plane.  The 16-channel kernel is held to 128 registers so that 14
+// CTAs fit an SM.
 constexpr int kBwdStages = 2;
+constexpr int kBwdMinBlocks16 = 14;
+// Channels per backward CTA: 32 when 32-channel CTAs already give at least 6
+// warps per SM on the 152 SMs of a GB300, else 16 (twice the warps).
+inline int bwd_channels(int batch, int dinner) {
+    const long long ctas32 = static_cast<long long>(batch) * ((dinner + 31) / 32);
+    return ctas32 >= 152LL * 6 ? 32 : 16;
+}
 
 struct ScanFwdArgs {
     const void* B;
@@ -51,7 +59,8 @@ struct ScanBwdArgs {
     int batch, seqlen, dinner, dstate;
     int64_t ld_B, ld_C, ld_du, ld_ddelta, ld_dz;
     int nck;
-    int ncl;             // CTA columns = ceil(dinner / 32) = dB/dC partial planes
+    int ncl;             // CTA columns = ceil(dinner / cw) = dB/dC partial planes
+    int cw;              // channels per CTA (bwd_channels)
     int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
 };
 
@@ -81,7 +90,7 @@ struct FwdMaps {
 cudaError_t launch_scan_fwd(int dtype, int nt, int disc, bool gate, const FwdMaps& maps,
                             const ScanFwdArgs& a, cudaStream_t stream);
 // Tensor maps of the backward: u, delta_raw, z, dout, the saved pre-gate y
-// (all 32 channels x kChunk steps boxes) and the checkpoints (32 x NT box).
+// (all cw channels x kChunk steps boxes) and the checkpoints (cw x NT box).
 struct BwdMaps {
     CUtensorMap u, dr, z, dout, y, ck, B, C;
 };

@@ -31,58 +31,100 @@
 
 namespace ssm {
 
-template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(32, 1)
+// Loads CPL consecutive floats (CPL = 2 or 4) from shared memory.
+template <int CPL>
+__device__ __forceinline__ void ld_cpl(const float* p, float (&v)[CPL]) {
+    if constexpr (CPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        v[0] = t.x; v[1] = t.y;
+    }
+}
+template <int CPL>
+__device__ __forceinline__ void st_cpl(float* p, const float (&v)[CPL]) {
+    if constexpr (CPL == 4)
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    else
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+}
+
+// CW = channels per CTA (one warp): 32 (each lane 4 channels) or 16 (each lane
+// 2 channels: half the work per warp and fewer registers, so twice the warps
+// when the problem has few channels).
+template <typename T, int NT, int DISC, bool GATE, int CW>
+__global__ void __launch_bounds__(32, CW == 16 ? kBwdMinBlocks16 : 1)
 scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr int TC = kChunk;
     constexpr int S = kBwdStages;
+    constexpr int CPL = CW / 8;                 // channels per lane
     constexpr int NS = NT / 4;                  // states per lane
     constexpr int NTEN = GATE ? 5 : 3;          // u, delta_raw, dout, [z, y]
-    constexpr int TILE = TC * 32;
+    constexpr int TILE = TC * CW;
     constexpr int BCT = TC * NT;                // elements per B or C tile
     constexpr int STAGE = NTEN * TILE + 2 * BCT;
     constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
     constexpr uint32_t kBCBytes = 2 * BCT * sizeof(T);
-    constexpr uint32_t kCkBytes = NT * 32 * sizeof(float);
+    constexpr uint32_t kCkBytes = NT * CW * sizeof(float);
     constexpr int BCN = 2 * TC * NT;
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+    static_assert((CPL == 2 || CPL == 4) && TC == 8, "lane layout below");
+    constexpr int SPL = 32 / CW;                // steps per lane-iteration of pro/epilogue
     constexpr bool ZOH = DISC == 1;
     constexpr int NQN = ZOH ? 3 : 2;            // state sums kept per (step, channel)
+    constexpr int PR = CW == 32 ? TC : 4;       // steps per dB/dC flush
+    constexpr int PJ = 9 * NT;                  // padded partial row: conflict-free float4 sums
 
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int AR = NT == 16 ? 20 : 10;      // padded A2 row: conflict-free per-lane reads
     T* tiles = reinterpret_cast<T*>(smem);                               // [S][STAGE]
-    float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][32]
-    float* bcs = cks + S * NT * 32;                                      // [TC][NT] B | [TC][NT] C
-    float* A2s = bcs + BCN;                                              // [32][AR]
-    float* iAs = A2s + 32 * AR;                                          // [32][AR] (ZOH)
-    float* Pd = iAs + (ZOH ? 32 * AR : 0);                               // [TC][32] delta
-    float* Pbs = Pd + TILE;                                              // [TC][32] delta*u | u
-    float* Pdy = Pbs + TILE;                                             // [TC][32] dy
-    float* part = Pdy + TILE;                                            // [TC][NQN][4][32]
-    constexpr int PJ = 9 * NT;                  // padded row: conflict-free float4 sums
-    float* pbuf = part + TC * NQN * 4 * 32;                              // [TC][PJ] dB or dC by channel group
-    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + TC * PJ);        // [S]
+    float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][CW]
+    float* bcs = cks + S * NT * CW;                                      // [TC][NT] B | [TC][NT] C
+    float* Pd = bcs + BCN;                                               // [TC][CW] delta
+    float* Pbs = Pd + TILE;                                              // [TC][CW] delta*u | u
+    float* Pdy = Pbs + TILE;                                             // [TC][CW] dy
+    float* part = Pdy + TILE;                                            // [TC][NQN][4][CW]
+    float* pbuf = part + TC * NQN * 4 * CW;                              // [PR][PJ] dB or dC by channel group
+    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + PR * PJ);        // [S]
 
     const int lane = threadIdx.x;
-    const int cg = lane >> 2, ng = lane & 3;
-    const int cbase = cg * 4;
-    const int c0 = blockIdx.x * 32;
+    const int cg = lane >> 2, ng = lane & 3;     // channel group (CPL channels), state group (NS states)
+    const int cbase = cg * CPL;
+    const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
     const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
     const int nchunks = (L + TC - 1) / TC;
     const size_t row0 = static_cast<size_t>(b) * L;
-    const int dch = c0 + lane;                   // channel of this lane in pro/epilogue
+    // prologue / epilogue layout: lane = (channel pc, step phase pj)
+    const int pc = lane % CW, pj = lane / CW;
+    const int dch = c0 + pc;
     const bool lane_ok = dch < Dn;
-    const bool quad_ok = c0 + cbase < Dn;
+    // column of channel c in state-group row k of `part`: rotated (CW = 32) or
+    // xor-swizzled (CW = 16) so that the per-step writes and the epilogue's
+    // reads hit distinct banks
+    auto part_col = [](int c, int k) {
+        return CW == 32 ? ((c + 8 * k) & 31) : (c ^ (8 * (k >> 1)));
+    };
 
-    // per (channel, state) constants, lane = channel
-    for (int n = 0; n < NT; ++n) {
-        const bool ok = lane_ok && n < N;
-        const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(dch) * N + n]) : -1.0f;
-        A2s[lane * AR + n] = ok ? A * kLog2e : 0.0f;
-        if (ZOH) iAs[lane * AR + n] = 1.0f / A;
-    }
+    // per (channel, state) constants of this lane's chains: A log2(e) (0 on
+    // padding states and channels) [and 1/A for ZOH]
+    float2 A2r[CPL][NS / 2], iAr[CPL][NS / 2];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+#pragma unroll
+        for (int p = 0; p < NS / 2; ++p) {
+            float v[2], w[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int d = c0 + cbase + i, n = ng * NS + 2 * p + e;
+                const bool ok = d < Dn && n < N;
+                const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
+                v[e] = ok ? A * kLog2e : 0.0f;
+                w[e] = 1.0f / A;
+            }
+            A2r[i][p] = make_float2(v[0], v[1]);
+            iAr[i][p] = make_float2(w[0], w[1]);
+        }
     const float Dd = (lane_ok && a.D) ? a.D[dch] : 0.0f;
 
     const T* Bp = static_cast<const T*>(a.B);
@@ -106,8 +148,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             tma_load_3d(dst + 4 * TILE, &maps.y, &full[s], c0, kc * TC, b);
         }
         if (kc > 0)
-            tma_load_2d(cks + s * NT * 32, &maps.ck, &full[s], c0,
-                        (b * a.nck + kc - 1) * NT);
+            tma_load_2d(cks + s * NT * CW, &maps.ck, &full[s], c0, (b * a.nck + kc - 1) * NT);
     };
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
@@ -121,34 +162,36 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     // The carries of the reverse recurrence (g) and the dA accumulators live in
     // registers only during the reverse pass and epilogue; between chunks they
     // are parked in the (then idle) state-sum buffer, so pass B can hold the
-    // chunk's a h_{t-1} values in registers.  stash[(q*NS*4 + k)*32 + lane].
+    // chunk's a h_{t-1} values in registers.
     float* stash = part;
-    static_assert(2 * 4 * NS <= TC * NQN * 4, "stash fits in the partials buffer");
-    float dA[4][NS], g[4][NS];
+    static_assert(2 * CPL * NS * 32 <= TC * NQN * 4 * CW, "stash fits in the partials buffer");
+    float2 dA[CPL][NS / 2], g[CPL][NS / 2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < CPL; ++i)
 #pragma unroll
-        for (int jn = 0; jn < NS; ++jn) dA[i][jn] = g[i][jn] = 0.0f;
+        for (int p = 0; p < NS / 2; ++p) dA[i][p] = g[i][p] = make_float2(0.f, 0.f);
     auto park = [&]() {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < CPL; ++i)
 #pragma unroll
-            for (int jn = 0; jn < NS; ++jn) {
-                stash[(i * NS + jn) * 32 + lane] = g[i][jn];
-                stash[((4 + i) * NS + jn) * 32 + lane] = dA[i][jn];
+            for (int p = 0; p < NS / 2; ++p) {
+                reinterpret_cast<float2*>(stash)[(i * NS / 2 + p) * 32 + lane] = g[i][p];
+                reinterpret_cast<float2*>(stash)[((CPL + i) * NS / 2 + p) * 32 + lane] = dA[i][p];
             }
     };
     auto unpark = [&]() {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < CPL; ++i)
 #pragma unroll
-            for (int jn = 0; jn < NS; ++jn) {
-                g[i][jn] = stash[(i * NS + jn) * 32 + lane];
-                dA[i][jn] = stash[((4 + i) * NS + jn) * 32 + lane];
+            for (int p = 0; p < NS / 2; ++p) {
+                g[i][p] = reinterpret_cast<const float2*>(stash)[(i * NS / 2 + p) * 32 + lane];
+                dA[i][p] = reinterpret_cast<const float2*>(stash)[((CPL + i) * NS / 2 + p) * 32 + lane];
             }
     };
     park();
-    float dl_next[4] = {0.f, 0.f, 0.f, 0.f};    // delta of the step after this chunk
+    float dl_next[CPL];                         // delta of the step after this chunk
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) dl_next[i] = 0.0f;
     float dD_acc = 0.0f;
 
     T* dup = static_cast<T*>(a.du);
@@ -159,19 +202,20 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 
     // this CTA's partial plane of dB|dC: [batch][seqlen][2][NT]
     float* plane = a.ws_bc + static_cast<size_t>(blockIdx.x) * a.batch * L * 2 * NT;
-    // dB or dC partials of one step, summed over this lane's 4 channels, go to
-    // pbuf by channel group; flush() adds the 8 groups (the warp's 32 channels)
-    // and writes the chunk's rows to the plane, float4 per lane.
+    // dB or dC partials of one step, summed over this lane's CPL channels, go
+    // to pbuf by channel group; flush() adds the 8 groups (the CTA's channels)
+    // for PR steps and writes those rows of the plane, float4 per lane.
     auto store_partial = [&](int j, const float2 (&v)[NS / 2]) {
-        float* pp = pbuf + j * PJ + cg * NT + ng * NS;
+        float* pp = pbuf + (j % PR) * PJ + cg * NT + ng * NS;
         if constexpr (NS == 4)
             *reinterpret_cast<float4*>(pp) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
         else
             *reinterpret_cast<float2*>(pp) = v[0];
     };
-    auto flush = [&](int coff, int t0f, int jmaxf) {
+    auto flush = [&](int coff, int tf, int nrows) {
         constexpr int NM = NT / 4;
-        if (lane < TC * NM) {
+        __syncwarp();
+        if (lane < PR * NM) {
             const int j = lane / NM, m = lane % NM;
             float4 acc = *reinterpret_cast<const float4*>(pbuf + j * PJ + 4 * m);
 #pragma unroll
@@ -182,8 +226,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 acc.z += v.z;
                 acc.w += v.w;
             }
-            if (j < jmaxf)
-                *reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + t0f + j) * 2 * NT + coff +
+            if (j < nrows)
+                *reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + tf + j) * 2 * NT + coff +
                                            4 * m) = acc;
         }
         __syncwarp();
@@ -194,6 +238,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         const int t0 = kc * TC;
         const int jmax = min(TC, L - t0);
         const int s = it % S;
+
         if (ok) ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) waited = it + 1;
@@ -203,7 +248,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         const T* tg = tu + 2 * TILE;
         const T* tz = tu + 3 * TILE;
         const T* ty = tu + 4 * TILE;
-        const float* ck = cks + s * NT * 32;
+        const float* ck = cks + s * NT * CW;
         if (ok) {
             // fp32 B and C of this chunk: [TC][NT] each.  fp32 TMA tiles are used
             // in place; bf16 tiles are widened into bcs, 8 values per lane.
@@ -242,214 +287,198 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 Cf = Bf + BCT;
             }
 
-            // ---- prologue (lane = channel): delta, delta*u (or u), dy.  All TC
-            //      steps run: past seqlen the tiles, B and C are zero, so dy = 0
-            //      and the extra steps add exactly nothing to g or any gradient.
-#pragma unroll 1
-            for (int j = 0; j < TC; ++j) {
-                {
-                    const float uv = Act<T>::to_f(tu[j * 32 + lane]);
-                    const float xr = Act<T>::to_f(tr[j * 32 + lane]);
-                    const float go = Act<T>::to_f(tg[j * 32 + lane]);
-                    float dt, dy = go;
-                    if (GATE) {
-                        const float zv = Act<T>::to_f(tz[j * 32 + lane]);
-                        float sz;
-                        softplus_sigmoid(xr, zv, dt, sz);
-                        dy = go * zv * sz;
-                    } else {
-                        float e;
-                        dt = softplus_e(xr, e);
-                    }
-                    Pd[j * 32 + lane] = dt;
-                    Pbs[j * 32 + lane] = ZOH ? uv : dt * uv;
-                    Pdy[j * 32 + lane] = dy;
+            // ---- prologue (lane = channel, step parity): delta, delta*u (or u),
+            //      dy.  All TC steps run: past seqlen the tiles, B and C are
+            //      zero, so dy = 0 and the extra steps add nothing.
+#pragma unroll
+            for (int jj = 0; jj < TC / SPL; ++jj) {
+                const int j = SPL * jj + pj;
+                const float uv = Act<T>::to_f(tu[j * CW + pc]);
+                const float xr = Act<T>::to_f(tr[j * CW + pc]);
+                const float go = Act<T>::to_f(tg[j * CW + pc]);
+                float dt, dy = go;
+                if (GATE) {
+                    const float zv = Act<T>::to_f(tz[j * CW + pc]);
+                    float sz;
+                    softplus_sigmoid(xr, zv, dt, sz);
+                    dy = go * zv * sz;
+                } else {
+                    float e;
+                    dt = softplus_e(xr, e);
                 }
+                Pd[j * CW + pc] = dt;
+                Pbs[j * CW + pc] = ZOH ? uv : dt * uv;
+                Pdy[j * CW + pc] = dy;
             }
             __syncwarp();
 
             // ---- pass B: h from the checkpoint, a_t h_{t-1} kept in registers;
-            //      dC partials (over this lane's 4 channels) reduced over the 8
-            //      channel groups with shuffles.
-            float2 ah[TC][4][NS / 2];
+            //      dC partials (over this lane's channels) to pbuf.
+            float2 ah[TC][CPL][NS / 2];
             {
-                float2 h[4][NS / 2];
+                float2 h[CPL][NS / 2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < CPL; ++i)
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p)
-                        h[i][p] = kc > 0 ? make_float2(ck[(ng * NS + 2 * p) * 32 + cbase + i],
-                                                       ck[(ng * NS + 2 * p + 1) * 32 + cbase + i])
+                        h[i][p] = kc > 0 ? make_float2(ck[(ng * NS + 2 * p) * CW + cbase + i],
+                                                       ck[(ng * NS + 2 * p + 1) * CW + cbase + i])
                                          : make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < TC; ++j) {
-                    {
-                        const float4 dl = *reinterpret_cast<const float4*>(Pd + j * 32 + cbase);
-                        const float4 bs = *reinterpret_cast<const float4*>(Pbs + j * 32 + cbase);
-                        const float4 dy = *reinterpret_cast<const float4*>(Pdy + j * 32 + cbase);
-                        const float dlA[4] = {dl.x, dl.y, dl.z, dl.w};
-                        const float bsA[4] = {bs.x, bs.y, bs.z, bs.w};
-                        const float dyA[4] = {dy.x, dy.y, dy.z, dy.w};
-                        float2 Bv[NS / 2];
+                    float dlA[CPL], bsA[CPL], dyA[CPL];
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlA);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsA);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyA);
+                    float2 Bv[NS / 2];
 #pragma unroll
-                        for (int p = 0; p < NS / 2; ++p)
-                            Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
-                        float2 dC[NS / 2];
+                    for (int p = 0; p < NS / 2; ++p)
+                        Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                    float2 dC[NS / 2];
 #pragma unroll
-                        for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
+                    for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < CPL; ++i) {
 #pragma unroll
-                            for (int p = 0; p < NS / 2; ++p) {
-                                const float2 A2p = *reinterpret_cast<const float2*>(
-                                    A2s + (cbase + i) * AR + ng * NS + 2 * p);
-                                const float2 x = mul2(f2(dlA[i]), A2p);
-                                const float2 av = make_float2(ex2(x.x), ex2(x.y));
-                                const float2 ahv = mul2(av, h[i][p]);
-                                float2 bu = f2(bsA[i]);
-                                if (!ZOH) {
-                                    h[i][p] = fma2(bu, Bv[p], ahv);
-                                } else {
-                                    const float2 iA = *reinterpret_cast<const float2*>(
-                                        iAs + (cbase + i) * AR + ng * NS + 2 * p);
-                                    const float xn0 = x.x * kLn2, xn1 = x.y * kLn2;
-                                    const float cf0 = fabsf(xn0) < 0.5f ? dlA[i] * phi1_series(xn0)
-                                                                        : (av.x - 1.0f) * iA.x;
-                                    const float cf1 = fabsf(xn1) < 0.5f ? dlA[i] * phi1_series(xn1)
-                                                                        : (av.y - 1.0f) * iA.y;
-                                    bu = mul2(mul2(make_float2(cf0, cf1), f2(bsA[i])), Bv[p]);
-                                    h[i][p] = add2(ahv, bu);
-                                }
-                                ah[j][i][p] = ahv;
-                                dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
+                        for (int p = 0; p < NS / 2; ++p) {
+                            const float2 x = mul2(f2(dlA[i]), A2r[i][p]);
+                            const float2 av = make_float2(ex2(x.x), ex2(x.y));
+                            const float2 ahv = mul2(av, h[i][p]);
+                            float2 bu = f2(bsA[i]);
+                            if (!ZOH) {
+                                h[i][p] = fma2(bu, Bv[p], ahv);
+                            } else {
+                                const float xn0 = x.x * kLn2, xn1 = x.y * kLn2;
+                                const float cf0 = fabsf(xn0) < 0.5f ? dlA[i] * phi1_series(xn0)
+                                                                    : (av.x - 1.0f) * iAr[i][p].x;
+                                const float cf1 = fabsf(xn1) < 0.5f ? dlA[i] * phi1_series(xn1)
+                                                                    : (av.y - 1.0f) * iAr[i][p].y;
+                                bu = mul2(mul2(make_float2(cf0, cf1), f2(bsA[i])), Bv[p]);
+                                h[i][p] = add2(ahv, bu);
                             }
+                            ah[j][i][p] = ahv;
+                            dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
                         }
-                        store_partial(j, dC);
                     }
+                    store_partial(j, dC);
+                    if (j % PR == PR - 1) flush(NT, t0 + j + 1 - PR, jmax - (j + 1 - PR));
                 }
             }
-            __syncwarp();
-            flush(NT, t0, jmax);   // dC rows of this chunk
 
             // ---- reverse pass: g_t = C_t dy_t + a_{t+1} g_{t+1}; state sums to
-            //      shared partials, dB partials reduced with shuffles.
+            //      shared partials, dB partials to pbuf.
             unpark();
             __syncwarp();
             {
-                float2 an[4][NS / 2];
+                float2 an[CPL][NS / 2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < CPL; ++i)
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p) {
-                        const float2 A2p = *reinterpret_cast<const float2*>(
-                            A2s + (cbase + i) * AR + ng * NS + 2 * p);
-                        const float2 x = mul2(f2(dl_next[i]), A2p);
+                        const float2 x = mul2(f2(dl_next[i]), A2r[i][p]);
                         an[i][p] = make_float2(ex2(x.x), ex2(x.y));
                     }
 #pragma unroll
                 for (int j = TC - 1; j >= 0; --j) {
-                    {
-                        const float4 dl = *reinterpret_cast<const float4*>(Pd + j * 32 + cbase);
-                        const float4 bs = *reinterpret_cast<const float4*>(Pbs + j * 32 + cbase);
-                        const float4 dy = *reinterpret_cast<const float4*>(Pdy + j * 32 + cbase);
-                        const float dlA[4] = {dl.x, dl.y, dl.z, dl.w};
-                        const float bsA[4] = {bs.x, bs.y, bs.z, bs.w};
-                        const float dyA[4] = {dy.x, dy.y, dy.z, dy.w};
-                        float2 Bv[NS / 2], Cv[NS / 2];
+                    float dlA[CPL], bsA[CPL], dyA[CPL];
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlA);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsA);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyA);
+                    float2 Bv[NS / 2], Cv[NS / 2];
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                        Cv[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
+                    }
+                    float2 dB[NS / 2];
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) dB[p] = make_float2(0.f, 0.f);
+                    float sums[NQN][CPL];
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+                        float2 Sg = make_float2(0.f, 0.f), Eg = make_float2(0.f, 0.f);
+                        float2 Sa = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int p = 0; p < NS / 2; ++p) {
-                            Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
-                            Cv[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
-                        }
-                        float2 dB[NS / 2];
+                            const float2 A2p = A2r[i][p];
+                            // g_t = C_t dy_t + a_{t+1} g_{t+1}
+                            const float2 gv = fma2(an[i][p], g[i][p], mul2(Cv[p], f2(dyA[i])));
+                            g[i][p] = gv;
+                            const float2 q = mul2(gv, ah[j][i][p]);        // g a_t h_{t-1}
+                            Eg = fma2(A2p, q, Eg);
+                            const float2 x = mul2(f2(dlA[i]), A2p);
+                            const float2 av = make_float2(ex2(x.x), ex2(x.y));   // a_t
+                            float2 dAv = dA[i][p];
+                            if (!ZOH) {
+                                dAv = fma2(f2(dlA[i]), q, dAv);
+                                Sg = fma2(gv, Bv[p], Sg);
+                                dB[p] = fma2(f2(bsA[i]), gv, dB[p]);
+                            } else {
+                                const float dt = dlA[i], uv = bsA[i];
+                                float cf[2], dcf[2];
 #pragma unroll
-                        for (int p = 0; p < NS / 2; ++p) dB[p] = make_float2(0.f, 0.f);
-                        float sums[NQN][4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float2 Sg = make_float2(0.f, 0.f), Eg = make_float2(0.f, 0.f);
-                            float2 Sa = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int p = 0; p < NS / 2; ++p) {
-                                const float2 A2p = *reinterpret_cast<const float2*>(
-                                    A2s + (cbase + i) * AR + ng * NS + 2 * p);
-                                // g_t = C_t dy_t + a_{t+1} g_{t+1}
-                                float2 gv = make_float2(g[i][2 * p], g[i][2 * p + 1]);
-                                gv = fma2(an[i][p], gv, mul2(Cv[p], f2(dyA[i])));
-                                g[i][2 * p] = gv.x;
-                                g[i][2 * p + 1] = gv.y;
-                                const float2 q = mul2(gv, ah[j][i][p]);        // g a_t h_{t-1}
-                                Eg = fma2(A2p, q, Eg);
-                                const float2 x = mul2(f2(dlA[i]), A2p);
-                                const float2 av = make_float2(ex2(x.x), ex2(x.y));   // a_t
-                                float2 dAv = make_float2(dA[i][2 * p], dA[i][2 * p + 1]);
-                                if (!ZOH) {
-                                    dAv = fma2(f2(dlA[i]), q, dAv);
-                                    Sg = fma2(gv, Bv[p], Sg);
-                                    dB[p] = fma2(f2(bsA[i]), gv, dB[p]);
-                                } else {
-                                    const float2 iA = *reinterpret_cast<const float2*>(
-                                        iAs + (cbase + i) * AR + ng * NS + 2 * p);
-                                    const float dt = dlA[i], uv = bsA[i];
-                                    float cf[2], dcf[2];
-#pragma unroll
-                                    for (int ee = 0; ee < 2; ++ee) {
-                                        const float xn = (ee ? x.y : x.x) * kLn2;
-                                        const float ae = ee ? av.y : av.x;
-                                        const float ia = ee ? iA.y : iA.x;
-                                        const bool small = fabsf(xn) < 0.5f;
-                                        cf[ee] = small ? dt * phi1_series(xn) : (ae - 1.0f) * ia;
-                                        dcf[ee] = small ? dt * dt * phi2_series(xn)
-                                                        : (xn * ae - (ae - 1.0f)) * ia * ia;
-                                    }
-                                    const float2 gB = mul2(gv, Bv[p]);
-                                    dAv = fma2(f2(dt), q, fma2(mul2(gB, f2(uv)), make_float2(dcf[0], dcf[1]), dAv));
-                                    Sg = fma2(gB, make_float2(cf[0], cf[1]), Sg);
-                                    Sa = fma2(gB, av, Sa);
-                                    dB[p] = fma2(mul2(f2(uv), make_float2(cf[0], cf[1])), gv, dB[p]);
+                                for (int ee = 0; ee < 2; ++ee) {
+                                    const float xn = (ee ? x.y : x.x) * kLn2;
+                                    const float ae = ee ? av.y : av.x;
+                                    const float ia = ee ? iAr[i][p].y : iAr[i][p].x;
+                                    const bool small = fabsf(xn) < 0.5f;
+                                    cf[ee] = small ? dt * phi1_series(xn) : (ae - 1.0f) * ia;
+                                    dcf[ee] = small ? dt * dt * phi2_series(xn)
+                                                    : (xn * ae - (ae - 1.0f)) * ia * ia;
                                 }
-                                dA[i][2 * p] = dAv.x;
-                                dA[i][2 * p + 1] = dAv.y;
-                                an[i][p] = av;
+                                const float2 gB = mul2(gv, Bv[p]);
+                                dAv = fma2(f2(dt), q, fma2(mul2(gB, f2(uv)), make_float2(dcf[0], dcf[1]), dAv));
+                                Sg = fma2(gB, make_float2(cf[0], cf[1]), Sg);
+                                Sa = fma2(gB, av, Sa);
+                                dB[p] = fma2(mul2(f2(uv), make_float2(cf[0], cf[1])), gv, dB[p]);
                             }
-                            sums[0][i] = Sg.x + Sg.y;
-                            sums[1][i] = Eg.x + Eg.y;
-                            if (ZOH) sums[NQN - 1][i] = Sa.x + Sa.y;
+                            dA[i][p] = dAv;
+                            an[i][p] = av;
                         }
-#pragma unroll
-                        for (int qn = 0; qn < NQN; ++qn)
-                            *reinterpret_cast<float4*>(part + ((j * NQN + qn) * 4 + ng) * 32 +
-                                                       ((cbase + 8 * ng) & 31)) =
-                                make_float4(sums[qn][0], sums[qn][1], sums[qn][2], sums[qn][3]);
-                        store_partial(j, dB);
+                        sums[0][i] = Sg.x + Sg.y;
+                        sums[1][i] = Eg.x + Eg.y;
+                        if (ZOH) sums[NQN - 1][i] = Sa.x + Sa.y;
                     }
+#pragma unroll
+                    for (int qn = 0; qn < NQN; ++qn)
+                        st_cpl<CPL>(part + ((j * NQN + qn) * 4 + ng) * CW + part_col(cbase, ng), sums[qn]);
+                    store_partial(j, dB);
+                    if (j % PR == 0) flush(0, t0 + j, jmax - j);
                 }
             }
             __syncwarp();
-            flush(0, t0, jmax);    // dB rows of this chunk
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
+            for (int i = 0; i < CPL; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
         }
         __syncwarp();
 
         if (ok) {
-            // ---- epilogue (lane = channel): finish du, ddelta_raw, dz, dD
+            // ---- epilogue (lane = channel, step parity): finish du,
+            //      ddelta_raw, dz, dD
             if (lane_ok) {
 #pragma unroll 1
-                for (int j = 0; j < TC; ++j) {
+                for (int jj = 0; jj < TC / SPL; ++jj) {
+                    const int j = SPL * jj + pj;
                     if (j < jmax) {
                         const size_t r = row0 + t0 + j;
                         float sm[NQN];
 #pragma unroll
                         for (int qn = 0; qn < NQN; ++qn) {
-                            const float* pp = part + (j * NQN + qn) * 4 * 32;
-                            sm[qn] = (pp[lane] + pp[32 + ((lane + 8) & 31)]) +
-                                     (pp[64 + ((lane + 16) & 31)] + pp[96 + ((lane + 24) & 31)]);
+                            // the 4 state groups' sums; a step-phase-1 lane reads
+                            // them in the order 1,0,3,2 (other banks, same sum)
+                            const float* pp = part + (j * NQN + qn) * 4 * CW;
+                            float v[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int kk = k ^ pj;
+                                v[k] = pp[kk * CW + part_col(pc, kk)];
+                            }
+                            sm[qn] = (v[0] + v[1]) + (v[2] + v[3]);
                         }
-                        const float uv = Act<T>::to_f(tu[j * 32 + lane]);
-                        const float xr = Act<T>::to_f(tr[j * 32 + lane]);
-                        const float dt = Pd[j * 32 + lane];
-                        const float dyv = Pdy[j * 32 + lane];
+                        const float uv = Act<T>::to_f(tu[j * CW + pc]);
+                        const float xr = Act<T>::to_f(tr[j * CW + pc]);
+                        const float dt = Pd[j * CW + pc];
+                        const float dyv = Pdy[j * CW + pc];
                         const float Sg = sm[0], Eg = sm[1] * kLn2;
                         const float du = ZOH ? fmaf(Dd, dyv, Sg) : fmaf(dt, Sg, Dd * dyv);
                         const float ddl = fmaf(uv, ZOH ? sm[NQN - 1] : Sg, Eg);
@@ -457,9 +486,9 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         dup[r * a.ld_du + dch] = Act<T>::from_f(du);
                         ddp[r * a.ld_ddelta + dch] = Act<T>::from_f(ddl * sigmoidf_(xr));
                         if (GATE) {
-                            const float zv = Act<T>::to_f(tz[j * 32 + lane]);
-                            const float go = Act<T>::to_f(tg[j * 32 + lane]);
-                            const float yv = Act<T>::to_f(ty[j * 32 + lane]);
+                            const float zv = Act<T>::to_f(tz[j * CW + pc]);
+                            const float go = Act<T>::to_f(tg[j * CW + pc]);
+                            const float yv = Act<T>::to_f(ty[j * CW + pc]);
                             const float sz = sigmoidf_(zv);
                             dzp[r * a.ld_dz + dch] =
                                 Act<T>::from_f(go * yv * sz * (1.0f + zv * (1.0f - sz)));
@@ -475,6 +504,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         __syncwarp();
         if (lane == 0 && ok && it + S < nchunks) issue(it + S);
     }
+
     if (lane == 0 && !ok) {
         for (int it = waited; it < nchunks && it < waited + S; ++it)
             mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
@@ -482,15 +512,25 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     __syncwarp();
     unpark();
     if (ok) {
-        if (quad_ok) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < CPL; ++i) {
+            const int d = c0 + cbase + i;
+            if (d < Dn) {
 #pragma unroll
-                for (int jn = 0; jn < NS; ++jn)
-                    a.ws_dA[(static_cast<size_t>(b) * Dn + c0 + cbase + i) * NT + ng * NS + jn] =
-                        dA[i][jn];
+                for (int p = 0; p < NS / 2; ++p) {
+                    float* dst = a.ws_dA + (static_cast<size_t>(b) * Dn + d) * NT + ng * NS + 2 * p;
+                    dst[0] = dA[i][p].x;
+                    dst[1] = dA[i][p].y;
+                }
+            }
         }
-        if (lane_ok) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc;
+        if constexpr (SPL == 2) {
+            // the two step-phase lanes of a channel each hold half of its dD sum
+            const float dD_other = __shfl_xor_sync(0xffffffffu, dD_acc, 16);
+            if (lane_ok && pj == 0) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc + dD_other;
+        } else {
+            if (lane_ok) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc;
+        }
     }
 }
 
@@ -540,30 +580,35 @@ __global__ void scan_reduce_kernel(const ScanReduceArgs a) {
     }
 }
 
-template <typename T, int NT, int DISC, bool GATE>
+template <typename T, int NT, int DISC, bool GATE, int CW>
 static size_t bwd_smem_bytes() {
     constexpr int TC = kChunk;
     constexpr int NTEN = GATE ? 5 : 3;
     constexpr int NQN = DISC == 1 ? 3 : 2;
-    return kBwdStages * (NTEN * TC * 32 + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
-           + kBwdStages * NT * 32 * sizeof(float)      // checkpoint tiles
+    return kBwdStages * (NTEN * TC * CW + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
+           + kBwdStages * NT * CW * sizeof(float)      // checkpoint tiles
            + 2 * TC * NT * sizeof(float)               // fp32 B|C (bf16 or unaligned B/C)
-           + (DISC == 1 ? 2 : 1) * 32 * (NT == 16 ? 20 : 10) * sizeof(float)   // A2 [, 1/A]
-           + 3 * TC * 32 * sizeof(float)               // delta, delta*u, dy
-           + TC * NQN * 4 * 32 * sizeof(float)         // state-sum partials
-           + TC * 9 * NT * sizeof(float)               // dB or dC partials by channel group
+           + 3 * TC * CW * sizeof(float)               // delta, delta*u, dy
+           + TC * NQN * 4 * CW * sizeof(float)         // state-sum partials
+           + (CW == 32 ? TC : 4) * 9 * NT * sizeof(float)   // dB or dC partials by channel group
            + kBwdStages * sizeof(uint64_t);
 }
 
-template <typename T, int NT, int DISC, bool GATE>
-static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
-    const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE>();
-    auto kern = scan_bwd_kernel<T, NT, DISC, GATE>;
+template <typename T, int NT, int DISC, bool GATE, int CW>
+static cudaError_t launch_bwd_cw(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
+    const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE, CW>();
+    auto kern = scan_bwd_kernel<T, NT, DISC, GATE, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch)), 32, smem, st>>>(maps, a);
     return cudaGetLastError();
+}
+
+template <typename T, int NT, int DISC, bool GATE>
+static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
+    return a.cw == 32 ? launch_bwd_cw<T, NT, DISC, GATE, 32>(maps, a, st)
+                      : launch_bwd_cw<T, NT, DISC, GATE, 16>(maps, a, st);
 }
 
 template <typename T, int NT>

@@ -1,5 +1,8 @@
 """GPU parity of ssm_scan_fwd / ssm_scan_bwd against the fp64 oracle on small
-shapes that span several tiles, chunks and clusters with ragged tails."""
+shapes that span several tiles and chunks with ragged tails.  The backward
+uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
+otherwise; the wide cases below (short sequences, many channels) run the
+32-channel kernel, the rest the 16-channel one."""
 import numpy as np
 import pytest
 
@@ -16,11 +19,15 @@ CASES = [
     (2, 37, 40, 5, "f32", 0, True, 0.3, 0.0),       # ragged L, D, N
     (3, 1, 64, 16, "bf16", 0, True, 0.0, 0.0),      # L = 1
     (1, 100, 96, 16, "f32", 1, False, 0.5, 0.05),   # ZOH, no gate, clamp entries
-    (2, 256, 320, 12, "bf16", 0, True, 0.5, 0.05),  # 10 channel tiles -> cluster of 8 + padding
+    (2, 256, 320, 12, "bf16", 0, True, 0.5, 0.05),  # 20 channel tiles + padding
     (1, 9, 8, 1, "f32", 0, True, 0.0, 0.0),
     (2, 1000, 64, 16, "f32", 0, True, 0.5, 0.02),
-    (1, 130, 512, 16, "f32", 1, True, 0.5, 0.02),   # 16 tiles: two full clusters
+    (1, 130, 512, 16, "f32", 1, True, 0.5, 0.02),   # 32 channel tiles
     (2, 24, 16, 0, "f32", 0, True, 0.0, 0.0),       # dstate = 0: y = D u
+    # 32-channel backward CTAs (4 * 256 = 1024 CTAs of 32 channels)
+    (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
+    (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
+    (8, 17, 3680, 6, "f32", 0, False, 0.3, 0.0),    # ragged dinner (not a multiple of 32), NT = 8
 ]
 
 
