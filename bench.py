@@ -37,18 +37,21 @@ if ROOT not in sys.path:
 METRIC = "Mamba-1 selective scan fwd+bwd Mtokens/s; achieved % of HBM/SFU roofline"
 WORKLOAD = "mamba1p4b_scan_bf16"
 SM_COUNT = 152
-EX2_PER_CLK_PER_SM = 32          # MUFU ex2 rate of sm_103 (csrc/probe_pipes.cu measures it)
+EX2_PER_CLK_PER_SM = 32          # MUFU ex2 rate of sm_103, measured with a dependency-free ex2 loop
 FP32_LANES_PER_CLK_PER_SM = 128  # FFMA lanes (packed f32x2 does not raise it)
 
 
 def parse():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    p.add_argument("--seqlen", type=int, default=None,
+                   help="run the workload's generator at this sequence length instead "
+                        "(smaller cases for profiler captures; not the benchmark line)")
     return p.parse_args()
 
 
@@ -101,7 +104,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -110,7 +113,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def window(self, t0, t1):
+        """Keep only the samples read between host times t0 and t1."""
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
         if self.proc is None:
@@ -122,7 +129,10 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t0", -math.inf), getattr(self, "t1", math.inf)
+        for ts, ln in self.lines:
+            if not t0 <= ts <= t1:
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -167,32 +177,39 @@ def recorded_traffic():
 # ----------------------------------------------------------------- CPU oracle leg
 
 def cpu_oracle_sample(cfg, inp, target_s=12.0):
-    """Time the fp64 oracle (scan fwd + bwd) on a slice of the workload: one
-    batch row, all seqlen steps, the first `dsub` channels.  dB/dC/dA_log/dD
-    over the slice are part of the work.  Returns (Mtokens/s, sample text, s)."""
+    """Time the fp64 oracle (scan fwd + bwd) on a slice of the workload: the
+    first `nb` batch rows, all seqlen steps, the first `dsub` channels, grown
+    until it takes about target_s.  dB/dC/dA_log/dD over the slice are part of
+    the work.  Returns (Mtokens/s, sample text, seconds)."""
     import numpy as np
     import oracle
-    L, D, N = cfg["seqlen"], cfg["dinner"], cfg["dstate"]
+    L, D, Bn = cfg["seqlen"], cfg["dinner"], cfg["batch"]
 
-    def run(dsub):
-        sl = slice(0, dsub)
-        u, dr, z, dout = (inp[k][:L, sl].astype(np.float64) for k in ("u", "delta_raw", "z",
-                                                                       "dout"))
-        B, C = inp["B"][:L].astype(np.float64), inp["C"][:L].astype(np.float64)
+    def run(nb, dsub):
+        sl, rows = slice(0, dsub), slice(0, nb * L)
+        u, dr, z, dout = (inp[k][rows, sl].astype(np.float64) for k in ("u", "delta_raw", "z",
+                                                                         "dout"))
+        B, C = inp["B"][rows].astype(np.float64), inp["C"][rows].astype(np.float64)
         Al, Dv = inp["A_log"][sl].astype(np.float64), inp["D"][sl].astype(np.float64)
         t0 = time.perf_counter()
-        oracle.scan_fwd(u, dr, Al, B, C, Dv, z, 0, batch=1)
-        oracle.scan_bwd(u, dr, Al, B, C, Dv, z, dout, 0, batch=1)
+        oracle.scan_fwd(u, dr, Al, B, C, Dv, z, 0, batch=nb)
+        oracle.scan_bwd(u, dr, Al, B, C, Dv, z, dout, 0, batch=nb)
         return time.perf_counter() - t0
 
     oracle.build()
-    probe = 16
-    t = run(probe)
-    dsub = int(min(D, max(probe, probe * target_s / max(t, 1e-3))))
-    dsub = max(8, dsub // 8 * 8)
-    t = run(dsub)
-    tokens = L * dsub / D            # rows of the full-width problem this slice is worth
-    return tokens / t / 1e6, f"batch row 0, {L} steps, channels [0, {dsub}) of {D}", t
+    nb, dsub = 1, 16
+    t = run(nb, dsub)
+    for _ in range(3):                 # grow the slice until it takes about target_s
+        if t >= 0.7 * target_s or (dsub >= D and nb >= Bn):
+            break
+        scale = target_s / max(t, 1e-3)
+        if dsub < D:
+            dsub = max(8, int(min(D, max(dsub + 8, dsub * scale))) // 8 * 8)
+        else:
+            nb = int(min(Bn, max(nb + 1, math.floor(nb * scale))))
+        t = run(nb, dsub)
+    tokens = nb * L * dsub / D       # rows of the full-width problem this slice is worth
+    return tokens / t / 1e6, f"batch rows [0, {nb}), {L} steps, channels [0, {dsub}) of {D}", t
 
 
 # ----------------------------------------------------------------- GPU leg
@@ -213,7 +230,11 @@ def run_gb300(args):
     ssm.load()
 
     cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
-    inp = workloads.named_scan_inputs(WORKLOAD)
+    if args.seqlen:
+        cfg["seqlen"] = args.seqlen
+        inp = workloads.scan_inputs(**cfg)
+    else:
+        inp = workloads.named_scan_inputs(WORKLOAD)
     bt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
     host = {k: torch.from_numpy(inp[k]) for k in ("u", "delta_raw", "z", "B", "C", "dout")}
     host = {k: v.to(bt) for k, v in host.items()}
@@ -259,6 +280,7 @@ def run_gb300(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    h0 = time.perf_counter()
     start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
@@ -268,6 +290,7 @@ def run_gb300(args):
         ev[i][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    clocks.window(h0 + 0.05, time.perf_counter())
     clk = clocks.stop()
     barrier()
     ms_total = start.elapsed_time(end)
@@ -360,7 +383,8 @@ def run_gb300(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; the workload's distributions)",
-            "config": {"workload": f"{WORKLOAD}: batch 8, seqlen 2048, dinner 4096, dstate 16, "
+            "config": {"workload": f"{WORKLOAD}: batch {cfg['batch']}, seqlen {cfg['seqlen']}, "
+                                   f"dinner {cfg['dinner']}, dstate {cfg['dstate']}, "
                                    "bf16 activations, fp32 A_log/D and state, Euler B, SiLU gate",
                        "global_batch": cfg["batch"] * ws, "seq_len": cfg["seqlen"],
                        "dinner": cfg["dinner"], "dstate": cfg["dstate"],
