@@ -189,9 +189,35 @@ bool bc_tma_ok(const ssm_scan_desc* d, const void* B, const void* C, int64_t ldB
 }
 
 struct BwdLayout {
-    int cw, ncl;
+    int cw, ncl, nseg, seg_chunks;
+    size_t off_cg, off_cdl, off_sg, off_sds, off_sd0;
     size_t off_bc, off_dA, off_dD, total;
 };
+
+// Forward workspace: the time-segment buffers (none with one segment).
+struct FwdLayout {
+    int nseg, seg_tiles;
+    size_t off_h0, off_segh, off_segds, total;
+};
+FwdLayout fwd_layout(const ssm_scan_desc* d) {
+    FwdLayout l{};
+    const int g = ssm::fwd_segments(d->batch, d->dinner, d->seqlen);
+    l.seg_tiles = ssm::fwd_seg_tiles(d->seqlen, g);
+    const int ntiles = (d->seqlen + ssm::kFwdTile - 1) / ssm::kFwdTile;
+    l.nseg = l.seg_tiles > 0 ? (ntiles + l.seg_tiles - 1) / l.seg_tiles : 1;
+    if (l.nseg <= 1) {
+        l.nseg = 1;
+        l.seg_tiles = ntiles > 0 ? ntiles : 1;
+        return l;
+    }
+    const size_t NT = nt_of(d->dstate);
+    const size_t hb = static_cast<size_t>(d->batch) * l.nseg * NT * d->dinner * sizeof(float);
+    l.off_h0 = 0;
+    l.off_segh = align256(hb);
+    l.off_segds = l.off_segh + align256(hb);
+    l.total = l.off_segds + align256(static_cast<size_t>(d->batch) * l.nseg * d->dinner * sizeof(float));
+    return l;
+}
 
 BwdLayout bwd_layout(const ssm_scan_desc* d) {
     BwdLayout l{};
@@ -199,10 +225,26 @@ BwdLayout bwd_layout(const ssm_scan_desc* d) {
     l.ncl = static_cast<int>((static_cast<int64_t>(d->dinner) + l.cw - 1) / l.cw);
     const size_t M = static_cast<size_t>(d->batch) * d->seqlen;
     const size_t NT = nt_of(d->dstate);
+    const int nchunks = static_cast<int>(nchunks_of(d->seqlen));
+    const int g = ssm::bwd_segments(d->batch, d->dinner, d->seqlen, l.cw);
+    l.seg_chunks = nchunks > 0 ? (nchunks + g - 1) / g : 1;
+    l.nseg = nchunks > 0 ? (nchunks + l.seg_chunks - 1) / l.seg_chunks : 1;
+    const size_t planes = static_cast<size_t>(d->batch) * l.nseg;   // dA / dD partial planes
     l.off_bc = 0;
     l.off_dA = align256(static_cast<size_t>(l.ncl) * M * 2 * NT * sizeof(float));
-    l.off_dD = l.off_dA + align256(static_cast<size_t>(d->batch) * d->dinner * NT * sizeof(float));
-    l.total = l.off_dD + align256(static_cast<size_t>(d->batch) * d->dinner * sizeof(float));
+    l.off_dD = l.off_dA + align256(planes * d->dinner * NT * sizeof(float));
+    size_t end = l.off_dD + align256(planes * d->dinner * sizeof(float));
+    if (l.nseg > 1) {
+        const size_t gs = align256(planes * NT * d->dinner * sizeof(float));
+        const size_t ds = align256(planes * d->dinner * sizeof(float));
+        l.off_cg = end;
+        l.off_sg = l.off_cg + gs;
+        l.off_cdl = l.off_sg + gs;
+        l.off_sds = l.off_cdl + ds;
+        l.off_sd0 = l.off_sds + ds;
+        end = l.off_sd0 + ds;
+    }
+    l.total = end;
     return l;
 }
 
@@ -217,8 +259,9 @@ size_t ssm_scan_ctx_bytes(const ssm_scan_desc* d) {
 }
 
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* d) {
-    (void)d;
-    return 0;
+    Lds r;
+    if (validate(d, r) != SSM_OK) return 0;
+    return fwd_layout(d).total;
 }
 
 size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
@@ -231,8 +274,6 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
                         const float* A_log, const void* B, const void* C, const float* D,
                         const void* z, void* out, void* ctx, size_t ctx_bytes, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     Lds r;
     ssm_status st = validate(d, r);
     if (st != SSM_OK) return st;
@@ -245,6 +286,11 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
     if (ctx) {
         if (ctx_bytes < ssm_scan_ctx_bytes(d)) return SSM_ERR_WORKSPACE;
         if (!aligned16(ctx)) return SSM_ERR_ALIGN;
+    }
+    const FwdLayout fl = fwd_layout(d);
+    if (fl.total > 0) {
+        if (!workspace || workspace_bytes < fl.total) return SSM_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SSM_ERR_ALIGN;
     }
     if ((st = check_device()) != SSM_OK) return st;
 
@@ -289,6 +335,14 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
     a.ld_out = r.out;
     a.nck = static_cast<int>(nck_of(d->seqlen));
     a.bc_tma = bct ? 1 : 0;
+    a.nseg = fl.nseg;
+    a.seg_tiles = fl.seg_tiles;
+    if (fl.nseg > 1) {
+        char* w = static_cast<char*>(workspace);
+        a.h0 = reinterpret_cast<float*>(w + fl.off_h0);
+        a.seg_h = reinterpret_cast<float*>(w + fl.off_segh);
+        a.seg_ds = reinterpret_cast<float*>(w + fl.off_segds);
+    }
     cudaError_t e = ssm::launch_scan_fwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
@@ -362,6 +416,15 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         a.ws_bc = reinterpret_cast<float*>(ws + lay.off_bc);
         a.ws_dA = reinterpret_cast<float*>(ws + lay.off_dA);
         a.ws_dD = reinterpret_cast<float*>(ws + lay.off_dD);
+        a.nseg = lay.nseg;
+        a.seg_chunks = lay.seg_chunks;
+        if (lay.nseg > 1) {
+            a.carry_g = reinterpret_cast<float*>(ws + lay.off_cg);
+            a.seg_g = reinterpret_cast<float*>(ws + lay.off_sg);
+            a.carry_dl = reinterpret_cast<float*>(ws + lay.off_cdl);
+            a.seg_ds = reinterpret_cast<float*>(ws + lay.off_sds);
+            a.seg_d0 = reinterpret_cast<float*>(ws + lay.off_sd0);
+        }
         a.batch = d->batch;
         a.seqlen = d->seqlen;
         a.dinner = d->dinner;
@@ -393,7 +456,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
     ra.dstate = d->dstate;
     ra.nt = nt;
     ra.ncl = any_work ? lay.ncl : 0;
-    ra.nb_sum = any_work ? d->batch : 0;
+    ra.nb_sum = any_work ? d->batch * lay.nseg : 0;
     ra.ld_dB = r.dB;
     ra.ld_dC = r.dC;
     ra.is_bf16 = d->dtype == SSM_BF16;

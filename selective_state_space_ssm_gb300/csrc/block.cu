@@ -108,7 +108,7 @@ Ctx ctx_layout(const Dims& s) {
 struct Ws {
     size_t a_hi, a_lo, b_hi, b_lo, w_hi, w_lo;            // TF32 splits
     size_t dg, du, ddelta, dxd, dxz, dxn;                 // backward activations
-    size_t scan, conv, red, total;
+    size_t scan, conv, red, scanf, total;
 };
 Ws ws_layout(const Dims& s) {
     const size_t f = sizeof(float);
@@ -141,6 +141,7 @@ Ws ws_layout(const Dims& s) {
     const size_t red = std::max({ssm::colsum_ws_floats(rows, 2 * s.D), ssm::colsum_ws_floats(rows, s.Dm),
                                  ssm::colsum_ws_floats(rows, s.P), ssm::rmsnorm_ws_floats(rows, s.Dm)});
     w.red = c.take(std::max<size_t>(red, 1) * f);
+    w.scanf = c.take(ssm_scan_fwd_workspace_bytes(&sd));
     w.total = c.off;
     return w;
 }
@@ -336,7 +337,8 @@ ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_bloc
     if (run.ok()) {
         ssm_scan_desc sd = scan_desc_of(s);
         run.check(ssm_scan_fwd(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, g,
-                               at<char>(ctx, c.scan), c.total - c.scan, nullptr, 0, stream));
+                               at<char>(ctx, c.scan), c.total - c.scan, at<char>(workspace, ws.scanf),
+                               ws.total - ws.scanf, stream));
     }
     // 10-11. out_proj + residual
     {

@@ -17,6 +17,23 @@ constexpr int kChunk = 8;
 constexpr int kFwdChannels = 32;
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
+// Time segments of the forward: one per batch row unless batch x ceil(dinner/32)
+// warps leave the 152 SMs with fewer than 2 warps each (measured: at 2.5 warps
+// per SM the segment pass costs more than it gains); then enough segments (of
+// at least 256 steps) for about 6 warps per SM.
+inline int fwd_segments(int batch, int dinner, int seqlen) {
+    const long long warps = static_cast<long long>(batch) * ((dinner + 31) / 32);
+    if (warps <= 0 || warps >= 152LL * 2) return 1;
+    long long g = (152LL * 6 + warps - 1) / warps;
+    const long long gmax = seqlen / 256;
+    if (g > gmax) g = gmax;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+// Tiles per segment for g segments, and the resulting segment count.
+inline int fwd_seg_tiles(int seqlen, int g) {
+    const int ntiles = (seqlen + kFwdTile - 1) / kFwdTile;
+    return (ntiles + g - 1) / g;
+}
 
 // Backward: one warp per CTA covers 32 or 16 channels x all states (each lane
 // owns 4 or 2 channels x dstate/4 states); every CTA writes its own dB/dC
@@ -29,6 +46,17 @@ constexpr int kBwdMinBlocks16 = 14;
 inline int bwd_channels(int batch, int dinner) {
     const long long ctas32 = static_cast<long long>(batch) * ((dinner + 31) / 32);
     return ctas32 >= 152LL * 6 ? 32 : 16;
+}
+// Time segments of the backward: one unless the CTAs of cw channels leave the
+// SMs with fewer than 2 warps each; then enough segments (of at least 32
+// chunks) for about 6 warps per SM.
+inline int bwd_segments(int batch, int dinner, int seqlen, int cw) {
+    const long long warps = static_cast<long long>(batch) * ((dinner + cw - 1) / cw);
+    if (warps <= 0 || warps >= 152LL * 2) return 1;
+    long long g = (152LL * 6 + warps - 1) / warps;
+    const long long gmax = ((seqlen + kChunk - 1) / kChunk) / 32;
+    if (g > gmax) g = gmax;
+    return g < 1 ? 1 : static_cast<int>(g);
 }
 
 struct ScanFwdArgs {
@@ -43,6 +71,14 @@ struct ScanFwdArgs {
     int64_t ld_B, ld_C, ld_out;
     int nck;             // checkpoints per batch row = ceil(seqlen / kChunk) - 1
     int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
+    // Time segments (scanned in parallel when the channels alone give too few
+    // warps): nseg segments of seg_tiles tiles; segment g > 0 starts from
+    // h0[b][g][NT][dinner].  seg_h / seg_ds: end state from a zero start and
+    // sum of delta of each segment (segment pass output, combine input).
+    int nseg, seg_tiles;
+    float* h0;
+    float* seg_h;
+    float* seg_ds;
 };
 
 struct ScanBwdArgs {
@@ -61,6 +97,19 @@ struct ScanBwdArgs {
     int nck;
     int ncl;             // CTA columns = ceil(dinner / cw) = dB/dC partial planes
     int cw;              // channels per CTA (bwd_channels)
+    // Time segments (walked in parallel when the channels alone give too few
+    // warps): nseg segments of seg_chunks chunks.  Segment sg < nseg-1 starts
+    // its reverse walk from carry_g[b][sg][NT][dinner] (dL/dh at the first step
+    // of segment sg+1) and carry_dl[b][sg][dinner] (delta there).  seg_g,
+    // seg_ds, seg_d0: the segment pass's dL/dh at each segment's first step
+    // from a zero carry, sum of delta over its steps after the first, and
+    // delta at its first step.  ws_dA / ws_dD then hold batch*nseg planes.
+    int nseg, seg_chunks;
+    float* carry_g;
+    float* carry_dl;
+    float* seg_g;
+    float* seg_ds;
+    float* seg_d0;
     int bc_tma;          // 1: B and C arrive by TMA with the activation tiles
 };
 
@@ -87,6 +136,8 @@ struct ScanReduceArgs {
 struct FwdMaps {
     CUtensorMap u, dr, z, B, C, out, y, ck;
 };
+// With a.nseg > 1 this runs the segment pass, the combine and the segmented
+// forward, in stream order.
 cudaError_t launch_scan_fwd(int dtype, int nt, int disc, bool gate, const FwdMaps& maps,
                             const ScanFwdArgs& a, cudaStream_t stream);
 // Tensor maps of the backward: u, delta_raw, z, dout, the saved pre-gate y

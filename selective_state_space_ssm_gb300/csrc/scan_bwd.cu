@@ -94,6 +94,12 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     const int b = blockIdx.y;
     const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
     const int nchunks = (L + TC - 1) / TC;
+    // this CTA's time segment: chunks [kcb, kce), walked last to first
+    const int sg = blockIdx.z;
+    const int kcb = sg * a.seg_chunks;
+    const int kce = min(nchunks, kcb + a.seg_chunks);
+    const int nit = kce - kcb;
+    const size_t plane_b = static_cast<size_t>(b) * a.nseg + sg;   // dA / dD plane
     const size_t row0 = static_cast<size_t>(b) * L;
     // prologue / epilogue layout: lane = (channel pc, step phase pj)
     const int pc = lane % CW, pj = lane / CW;
@@ -131,7 +137,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     const T* Cp = static_cast<const T*>(a.C);
     const bool bc_tma = a.bc_tma != 0;
     auto issue = [&](int it) {
-        const int kc = nchunks - 1 - it;
+        const int kc = kce - 1 - it;
         const int s = it % S;
         T* dst = tiles + s * STAGE;
         mbar_arrive_expect_tx(&full[s], kActBytes + (kc > 0 ? kCkBytes : 0u) +
@@ -156,7 +162,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     }
     __syncwarp();
     if (lane == 0)
-        for (int it = 0; it < S && it < nchunks; ++it) issue(it);
+        for (int it = 0; it < S && it < nit; ++it) issue(it);
     __syncwarp();
 
     // The carries of the reverse recurrence (g) and the dA accumulators live in
@@ -188,10 +194,25 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 dA[i][p] = reinterpret_cast<const float2*>(stash)[((CPL + i) * NS / 2 + p) * 32 + lane];
             }
     };
-    park();
     float dl_next[CPL];                         // delta of the step after this chunk
 #pragma unroll
     for (int i = 0; i < CPL; ++i) dl_next[i] = 0.0f;
+    if (sg + 1 < a.nseg) {
+        // dL/dh and delta at the first step of the next segment
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int d = c0 + cbase + i;
+            if (d < Dn) {
+                dl_next[i] = a.carry_dl[plane_b * Dn + d];
+#pragma unroll
+                for (int p = 0; p < NS / 2; ++p) {
+                    const float* cp = a.carry_g + (plane_b * NT + ng * NS + 2 * p) * Dn + d;
+                    g[i][p] = make_float2(cp[0], cp[Dn]);
+                }
+            }
+        }
+    }
+    park();
     float dD_acc = 0.0f;
 
     T* dup = static_cast<T*>(a.du);
@@ -233,8 +254,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         __syncwarp();
     };
 
-    for (int it = 0; it < nchunks; ++it) {
-        const int kc = nchunks - 1 - it;
+    for (int it = 0; it < nit; ++it) {
+        const int kc = kce - 1 - it;
         const int t0 = kc * TC;
         const int jmax = min(TC, L - t0);
         const int s = it % S;
@@ -502,11 +523,11 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 
         // ---- release this TMA stage
         __syncwarp();
-        if (lane == 0 && ok && it + S < nchunks) issue(it + S);
+        if (lane == 0 && ok && it + S < nit) issue(it + S);
     }
 
     if (lane == 0 && !ok) {
-        for (int it = waited; it < nchunks && it < waited + S; ++it)
+        for (int it = waited; it < nit && it < waited + S; ++it)
             mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
     }
     __syncwarp();
@@ -518,7 +539,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             if (d < Dn) {
 #pragma unroll
                 for (int p = 0; p < NS / 2; ++p) {
-                    float* dst = a.ws_dA + (static_cast<size_t>(b) * Dn + d) * NT + ng * NS + 2 * p;
+                    float* dst = a.ws_dA + (plane_b * Dn + d) * NT + ng * NS + 2 * p;
                     dst[0] = dA[i][p].x;
                     dst[1] = dA[i][p].y;
                 }
@@ -527,10 +548,198 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         if constexpr (SPL == 2) {
             // the two step-phase lanes of a channel each hold half of its dD sum
             const float dD_other = __shfl_xor_sync(0xffffffffu, dD_acc, 16);
-            if (lane_ok && pj == 0) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc + dD_other;
+            if (lane_ok && pj == 0) a.ws_dD[plane_b * Dn + dch] = dD_acc + dD_other;
         } else {
-            if (lane_ok) a.ws_dD[static_cast<size_t>(b) * Dn + dch] = dD_acc;
+            if (lane_ok) a.ws_dD[plane_b * Dn + dch] = dD_acc;
         }
+    }
+}
+
+// Segment pass of the time-parallel backward: for segment sg >= 1 of batch
+// row b, walk its steps last to first with g = 0 after its last step,
+//   g_t = C_t dy_t + a_{t+1} g_{t+1},
+// and keep g at its first step, the sum of delta over its steps after the
+// first, and delta at its first step.  Because the product of a_s over steps
+// t0+1 .. t1+1 is exp(A (that sum + delta at t1+1)), the true g at the first
+// step of a segment is its zero-carry value plus that product times the true
+// g at the first step of the next segment (scan_bwd_combine_kernel).  A lane
+// owns NT * CW / 32 states of one channel.
+template <typename T, int NT, bool GATE, int CW>
+__global__ void __launch_bounds__(32, 1)
+scan_bwd_segsum_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
+    constexpr int TC = kChunk;
+    constexpr int S = kBwdStages;
+    constexpr int SPL = 32 / CW;                 // lanes per channel
+    constexpr int NL = NT / SPL;                 // states per lane
+    constexpr int NQ = NL / 2;
+    constexpr int TILE = TC * CW;
+    constexpr int BCT = TC * NT;
+    constexpr int NTEN = GATE ? 3 : 2;           // delta_raw, dout, [z]
+    constexpr int STAGE = NTEN * TILE + BCT;     // + C
+    constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
+    constexpr uint32_t kCBytes = BCT * sizeof(T);
+    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
+    float* csm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TC][NT] fp32 C
+    uint64_t* full = reinterpret_cast<uint64_t*>(csm + BCT);                 // [S]
+
+    const int lane = threadIdx.x;
+    const int c = lane % CW, half = lane / CW;
+    const int nbase = half * NL;
+    const int c0 = blockIdx.x * CW;
+    const int b = blockIdx.y;
+    const int sg = blockIdx.z + 1;               // segments 1 .. nseg-1
+    const int d = c0 + c;
+    const bool active = d < a.dinner;
+    const int L = a.seqlen, N = a.dstate;
+    const int nchunks = (L + TC - 1) / TC;
+    const int kcb = sg * a.seg_chunks;
+    const int kce = min(nchunks, kcb + a.seg_chunks);
+    const int nit = kce - kcb;
+    const size_t row0 = static_cast<size_t>(b) * L;
+    const bool bc_tma = a.bc_tma != 0;
+
+    float2 A2[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = nbase + 2 * q + e;
+            const bool ok = active && n < N;
+            v[e] = ok ? a2_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : 0.0f;
+        }
+        A2[q] = make_float2(v[0], v[1]);
+    }
+    float2 gl[NQ], an[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) gl[q] = an[q] = make_float2(0.0f, 0.0f);
+    float dsum = 0.0f, dfirst = 0.0f;
+
+    const T* Cp = static_cast<const T*>(a.C);
+    auto issue = [&](int it) {
+        const int kc = kce - 1 - it;
+        const int s = it % S;
+        T* dst = tiles + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kCBytes : 0u));
+        tma_load_3d(dst, &maps.dr, &full[s], c0, kc * TC, b);
+        tma_load_3d(dst + TILE, &maps.dout, &full[s], c0, kc * TC, b);
+        if (GATE) tma_load_3d(dst + 2 * TILE, &maps.z, &full[s], c0, kc * TC, b);
+        if (bc_tma) tma_load_3d(dst + NTEN * TILE, &maps.C, &full[s], 0, kc * TC, b);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int it = 0; it < S && it < nit; ++it) issue(it);
+
+    int it = 0;
+    for (; it < nit; ++it) {
+        const int kc = kce - 1 - it;
+        const int s = it % S;
+        bool ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const T* tr = tiles + s * STAGE;
+        const T* tg = tr + TILE;
+        const T* tz = tr + 2 * TILE;
+        const T* tc = tr + NTEN * TILE;
+        const float* Cf;
+        if (bc_tma && sizeof(T) == 4) {
+            Cf = reinterpret_cast<const float*>(tc);
+        } else {
+            for (int e = lane; e < BCT; e += 32) {
+                float v;
+                if (bc_tma) {
+                    v = Act<T>::to_f(tc[e]);
+                } else {
+                    const int j = e / NT, n = e % NT, t = kc * TC + j;
+                    v = (n < N && t < L) ? Act<T>::load(Cp + (row0 + t) * a.ld_C + n) : 0.0f;
+                }
+                csm[e] = v;
+            }
+            Cf = csm;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = TC - 1; j >= 0; --j) {
+            const int t = kc * TC + j;
+            const float xr = Act<T>::to_f(tr[j * CW + c]);
+            const float go = Act<T>::to_f(tg[j * CW + c]);
+            float dt, dy = go;
+            if (GATE) {
+                const float zv = Act<T>::to_f(tz[j * CW + c]);
+                float sz;
+                softplus_sigmoid(xr, zv, dt, sz);
+                dy = go * zv * sz;
+            } else {
+                float e;
+                dt = softplus_e(xr, e);
+            }
+            // past seqlen the tiles are zero: dy = 0 keeps g at 0 there
+            const float2 dy2 = f2(dy), dt2 = f2(dt);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float2 Cq = *reinterpret_cast<const float2*>(Cf + j * NT + nbase + 2 * q);
+                gl[q] = fma2(an[q], gl[q], mul2(Cq, dy2));
+                const float2 x = mul2(dt2, A2[q]);
+                an[q] = make_float2(ex2(x.x), ex2(x.y));
+            }
+            if (t < L) {
+                if (t == kcb * TC) dfirst = dt;
+                else dsum += dt;
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && it + S < nit) issue(it + S);
+    }
+    if (it < nit && lane == 0) {
+        for (int k2 = it; k2 < nit && k2 < it + S; ++k2)
+            mbar_wait(&full[k2 % S], (k2 / S) & 1, kFaultDrain);
+    }
+    if (active && it == nit) {
+        const size_t pb = static_cast<size_t>(b) * a.nseg + sg;
+        float* gp = a.seg_g + (pb * NT + nbase) * a.dinner + d;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            gp[static_cast<size_t>(2 * q) * a.dinner] = gl[q].x;
+            gp[static_cast<size_t>(2 * q + 1) * a.dinner] = gl[q].y;
+        }
+        if (half == 0) {
+            a.seg_ds[pb * a.dinner + d] = dsum;
+            a.seg_d0[pb * a.dinner + d] = dfirst;
+        }
+    }
+}
+
+// Combine of the backward's time segments: one thread per (batch row, state,
+// channel) walks the segments last to first and writes the carry (true dL/dh
+// and delta at the first step of the next segment) of every segment but the
+// last.
+template <int NT>
+__global__ void scan_bwd_combine_kernel(const ScanBwdArgs a) {
+    const size_t total = static_cast<size_t>(a.batch) * NT * a.dinner;
+    const size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    if (i >= total) return;
+    const int d = static_cast<int>(i % a.dinner);
+    const int n = static_cast<int>((i / a.dinner) % NT);
+    const int b = static_cast<int>(i / (static_cast<size_t>(a.dinner) * NT));
+    const float A2 = n < a.dstate ? a2_from_alog(a.A_log[static_cast<size_t>(d) * a.dstate + n]) : 0.0f;
+    float carry = 0.0f;
+    for (int s = a.nseg - 1; s >= 1; --s) {
+        const size_t pb = static_cast<size_t>(b) * a.nseg + s;
+        float gstart = a.seg_g[(pb * NT + n) * a.dinner + d];
+        if (s + 1 < a.nseg) {
+            const float P = ex2(A2 * (a.seg_ds[pb * a.dinner + d] + a.seg_d0[(pb + 1) * a.dinner + d]));
+            gstart = fmaf(P, carry, gstart);
+        }
+        a.carry_g[((pb - 1) * NT + n) * a.dinner + d] = gstart;
+        if (n == 0) a.carry_dl[(pb - 1) * a.dinner + d] = a.seg_d0[pb * a.dinner + d];
+        carry = gstart;
     }
 }
 
@@ -601,7 +810,25 @@ static cudaError_t launch_bwd_cw(const BwdMaps& maps, const ScanBwdArgs& a, cuda
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch)), 32, smem, st>>>(maps, a);
+    if (a.nseg > 1) {
+        // segment pass (segments 1 .. nseg-1), then the combine of the carries
+        constexpr int NTEN1 = GATE ? 3 : 2;
+        const size_t sm1 = kBwdStages * (NTEN1 * kChunk * CW + kChunk * NT) * sizeof(T) +
+                           kChunk * NT * sizeof(float) + kBwdStages * sizeof(uint64_t);
+        auto k1 = scan_bwd_segsum_kernel<T, NT, GATE, CW>;
+        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm1));
+        if (e != cudaSuccess) return e;
+        k1<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch),
+                  static_cast<unsigned>(a.nseg - 1)), 32, sm1, st>>>(maps, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const size_t total = static_cast<size_t>(a.batch) * NT * a.dinner;
+        scan_bwd_combine_kernel<NT><<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch), static_cast<unsigned>(a.nseg)),
+           32, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 

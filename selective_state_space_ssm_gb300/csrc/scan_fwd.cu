@@ -155,14 +155,25 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         invA[q] = make_float2(r[0], r[1]);
     }
     const float Dd = (active && a.D) ? a.D[d] : 0.0f;
+    // This CTA's time segment: tiles [kb, ke).  A segment after the first starts
+    // from the state the segment pass left in h0 (exact: see the combine).
+    const int g = blockIdx.z;
+    const int kb = g * a.seg_tiles;
+    const int ke = min(ntiles, kb + a.seg_tiles);
     float2 h[NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) h[q] = make_float2(0.0f, 0.0f);
+    for (int q = 0; q < NQ; ++q) {
+        h[q] = make_float2(0.0f, 0.0f);
+        if (g > 0 && active) {
+            const float* hp = a.h0 + ((static_cast<size_t>(b) * a.nseg + g) * NT + 2 * q) * a.dinner + d;
+            h[q] = make_float2(hp[0], hp[a.dinner]);
+        }
+    }
 
     const T* Bp = static_cast<const T*>(a.B);
     const T* Cp = static_cast<const T*>(a.C);
     auto issue = [&](int k) {
-        const int s = k % S;
+        const int s = (k - kb) % S;
         T* dst = tiles + s * STAGE;
         mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kBCBytes : 0u));
         tma_load_3d(dst, &maps.u, &full[s], c0, k * TS, b);
@@ -180,14 +191,14 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     }
     __syncwarp();
     if (lane == 0)
-        for (int k = 0; k < S && k < ntiles; ++k) issue(k);
+        for (int k = kb; k < kb + S && k < ke; ++k) issue(k);
 
     const bool save_y = GATE && a.ysave != nullptr;
     const bool save_ck = a.ctx != nullptr && a.nck > 0;
-    int k = 0;
-    for (; k < ntiles; ++k) {
-        const int s = k % S;
-        bool ok = mbar_wait(&full[s], (k / S) & 1, kFaultFwdWait);
+    int k = kb;
+    for (; k < ke; ++k) {
+        const int s = (k - kb) % S;
+        bool ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
 
@@ -227,10 +238,10 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         // state that is never stored.  Outputs go to a staging tile in shared
         // memory (double-buffered) and leave by TMA store; the store of tile
         // k-2 must have finished reading its buffer first.
-        if (lane == 0 && k >= 2) bulk_wait_read_1();
+        if (lane == 0 && k - kb >= 2) bulk_wait_read_1();
         __syncwarp();
-        T* so = ost + (k & 1) * 2 * TILE;
-        float* sc = ckst + (k & 1) * NCK * NT * CW;
+        T* so = ost + ((k - kb) & 1) * 2 * TILE;
+        float* sc = ckst + ((k - kb) & 1) * NCK * NT * CW;
 #pragma unroll
         for (int j = 0; j < TS; ++j) {
             const float y = fwd_step<NT, DISC>(h, A2, Anat, invA, Bf + j * NT, Bf + BCT + j * NT, dtv[j],
@@ -260,15 +271,187 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
                 }
             }
             bulk_commit();
-            if (k + S < ntiles) issue(k + S);
+            if (k + S < ke) issue(k + S);
         }
     }
-    if (k < ntiles && lane == 0) {
+    if (k < ke && lane == 0) {
         // A wait gave up: drain the copies still in flight (bounded) before exit.
-        for (int kk = k; kk < ntiles && kk < k + S; ++kk)
-            mbar_wait(&full[kk % S], (kk / S) & 1, kFaultDrain);
+        for (int kk = k; kk < ke && kk < k + S; ++kk)
+            mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
     }
     if (lane == 0) bulk_wait_all();   // the staged stores have left shared memory
+}
+
+// Segment pass of the time-parallel forward: for segment g of batch row b,
+// run the recurrence from h = 0 and keep only the end state and the sum of
+// delta over the segment.  Since exp(delta_t A) multiplies across steps into
+// exp(A sum_t delta_t), the true state entering segment g+1 is
+//   h_start(g+1) = exp(A sum_g delta) h_start(g) + h_end_from_zero(g),
+// which scan_fwd_combine_kernel evaluates segment by segment.
+template <typename T, int NT, int DISC>
+__global__ void __launch_bounds__(32, 1)
+scan_fwd_segsum_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
+    constexpr int CW = kFwdChannels;
+    constexpr int TS = kFwdTile;
+    constexpr int S = kFwdStages;
+    constexpr int NQ = NT / 2;
+    constexpr int TILE = TS * CW;
+    constexpr int BCT = TS * NT;
+    constexpr int STAGE = 2 * TILE + BCT;               // u, delta_raw, B
+    constexpr uint32_t kActBytes = 2 * TILE * sizeof(T);
+    constexpr uint32_t kBBytes = BCT * sizeof(T);
+    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
+    float* bsm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] fp32 B
+    uint64_t* full = reinterpret_cast<uint64_t*>(bsm + BCT);                 // [S]
+
+    const int lane = threadIdx.x;
+    const int c0 = blockIdx.x * CW;
+    const int b = blockIdx.y;
+    const int g = blockIdx.z;
+    const int d = c0 + lane;
+    const bool active = d < a.dinner;
+    const int L = a.seqlen, N = a.dstate;
+    const size_t row0 = static_cast<size_t>(b) * L;
+    const bool bc_tma = a.bc_tma != 0;
+    const int kb = g * a.seg_tiles, ke = kb + a.seg_tiles;   // a full segment (never the last)
+
+    float2 A2[NQ], Anat[NQ], invA[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        float v[2], w[2], r[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = 2 * q + e;
+            const bool ok = active && n < N;
+            const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
+            v[e] = ok ? A * kLog2e : 0.0f;
+            w[e] = A;
+            r[e] = 1.0f / A;
+        }
+        A2[q] = make_float2(v[0], v[1]);
+        Anat[q] = make_float2(w[0], w[1]);
+        invA[q] = make_float2(r[0], r[1]);
+    }
+    float2 h[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) h[q] = make_float2(0.0f, 0.0f);
+    float dsum = 0.0f;
+
+    const T* Bp = static_cast<const T*>(a.B);
+    auto issue = [&](int k) {
+        const int s = (k - kb) % S;
+        T* dst = tiles + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kBBytes : 0u));
+        tma_load_3d(dst, &maps.u, &full[s], c0, k * TS, b);
+        tma_load_3d(dst + TILE, &maps.dr, &full[s], c0, k * TS, b);
+        if (bc_tma) tma_load_3d(dst + 2 * TILE, &maps.B, &full[s], 0, k * TS, b);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int k = kb; k < kb + S && k < ke; ++k) issue(k);
+
+    int k = kb;
+    for (; k < ke; ++k) {
+        const int s = (k - kb) % S;
+        bool ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const T* tu = tiles + s * STAGE;
+        const T* tr = tu + TILE;
+        const T* tb = tu + 2 * TILE;
+        // fp32 B of this tile ([TS][NT]; past dstate 0)
+        const float* Bf;
+        if (bc_tma && sizeof(T) == 4) {
+            Bf = reinterpret_cast<const float*>(tb);
+        } else {
+            for (int e = lane; e < BCT; e += 32) {
+                float v;
+                if (bc_tma) {
+                    v = Act<T>::to_f(tb[e]);
+                } else {
+                    const int j = e / NT, n = e % NT;
+                    v = n < N ? Act<T>::load(Bp + (row0 + static_cast<size_t>(k) * TS + j) * a.ld_B + n)
+                              : 0.0f;
+                }
+                bsm[e] = v;
+            }
+            Bf = bsm;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < TS; ++j) {
+            const float uv = Act<T>::to_f(tu[j * CW + lane]);
+            const float xr = Act<T>::to_f(tr[j * CW + lane]);
+            float e;
+            const float dt = softplus_e(xr, e);
+            dsum += dt;
+            const float bs = DISC == 0 ? dt * uv : uv;
+            const float2 dt2 = f2(dt), bs2 = f2(bs);
+#pragma unroll
+            for (int q4 = 0; q4 < NT / 4; ++q4) {
+                const float4 B4 = *reinterpret_cast<const float4*>(Bf + j * NT + 4 * q4);
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    const int q = 2 * q4 + hq;
+                    const float2 Bq = hq ? make_float2(B4.z, B4.w) : make_float2(B4.x, B4.y);
+                    const float2 x = mul2(dt2, A2[q]);
+                    const float2 av = make_float2(ex2(x.x), ex2(x.y));
+                    float2 bu;
+                    if (DISC == 0) {
+                        bu = mul2(bs2, Bq);
+                    } else {
+                        const float2 xn = mul2(dt2, Anat[q]);
+                        const float c0f = fabsf(xn.x) < 0.5f ? dt * phi1_series(xn.x) : (av.x - 1.0f) * invA[q].x;
+                        const float c1f = fabsf(xn.y) < 0.5f ? dt * phi1_series(xn.y) : (av.y - 1.0f) * invA[q].y;
+                        bu = mul2(mul2(make_float2(c0f, c1f), bs2), Bq);
+                    }
+                    h[q] = fma2(av, h[q], bu);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && k + S < ke) issue(k + S);
+    }
+    if (k < ke && lane == 0) {
+        for (int kk = k; kk < ke && kk < k + S; ++kk)
+            mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
+    }
+    if (active && k == ke) {
+        float* hp = a.seg_h + (static_cast<size_t>(b) * a.nseg + g) * NT * a.dinner + d;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            hp[static_cast<size_t>(2 * q) * a.dinner] = h[q].x;
+            hp[static_cast<size_t>(2 * q + 1) * a.dinner] = h[q].y;
+        }
+        a.seg_ds[(static_cast<size_t>(b) * a.nseg + g) * a.dinner + d] = dsum;
+    }
+}
+
+// Combine of the time segments: one thread per (batch row, state, channel)
+// walks the segments in order and writes the state entering each segment.
+template <int NT>
+__global__ void scan_fwd_combine_kernel(const ScanFwdArgs a) {
+    const size_t total = static_cast<size_t>(a.batch) * NT * a.dinner;
+    const size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    if (i >= total) return;
+    const int d = static_cast<int>(i % a.dinner);
+    const int n = static_cast<int>((i / a.dinner) % NT);
+    const int b = static_cast<int>(i / (static_cast<size_t>(a.dinner) * NT));
+    const float A2 = n < a.dstate ? a2_from_alog(a.A_log[static_cast<size_t>(d) * a.dstate + n]) : 0.0f;
+    float h = 0.0f;
+    for (int g = 0; g + 1 < a.nseg; ++g) {
+        const size_t sg = static_cast<size_t>(b) * a.nseg + g;
+        const float P = ex2(A2 * a.seg_ds[sg * a.dinner + d]);   // product of a_t over segment g
+        h = fmaf(P, h, a.seg_h[(sg * NT + n) * a.dinner + d]);
+        a.h0[((sg + 1) * NT + n) * a.dinner + d] = h;
+    }
 }
 
 template <typename T, int NT, int DISC, bool GATE>
@@ -283,8 +466,24 @@ static cudaError_t launch_fwd_t(const FwdMaps& m, const ScanFwdArgs& a, cudaStre
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid((a.dinner + kFwdChannels - 1) / kFwdChannels, a.batch);
-    kern<<<grid, 32, smem, st>>>(m, a);
+    const unsigned gx = (a.dinner + kFwdChannels - 1) / kFwdChannels;
+    if (a.nseg > 1) {
+        // segment pass (every segment but the last), then the combine
+        constexpr int STG = 2 * kFwdTile * kFwdChannels + kFwdTile * NT;
+        const size_t sm1 = kFwdStages * STG * sizeof(T) + kFwdTile * NT * sizeof(float) +
+                           kFwdStages * sizeof(uint64_t);
+        auto k1 = scan_fwd_segsum_kernel<T, NT, DISC>;
+        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm1));
+        if (e != cudaSuccess) return e;
+        k1<<<dim3(gx, a.batch, a.nseg - 1), 32, sm1, st>>>(m, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const size_t total = static_cast<size_t>(a.batch) * NT * a.dinner;
+        scan_fwd_combine_kernel<NT><<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<dim3(gx, a.batch, a.nseg), 32, smem, st>>>(m, a);
     return cudaGetLastError();
 }
 

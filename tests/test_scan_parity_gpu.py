@@ -2,7 +2,9 @@
 shapes that span several tiles and chunks with ragged tails.  The backward
 uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
 otherwise; the wide cases below (short sequences, many channels) run the
-32-channel kernel, the rest the 16-channel one."""
+32-channel kernel, the rest the 16-channel one.  The forward scans time
+segments in parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512
+(the B2 L1000 case and the two marked below)."""
 import numpy as np
 import pytest
 
@@ -24,6 +26,9 @@ CASES = [
     (2, 1000, 64, 16, "f32", 0, True, 0.5, 0.02),
     (1, 130, 512, 16, "f32", 1, True, 0.5, 0.02),   # 32 channel tiles
     (2, 24, 16, 0, "f32", 0, True, 0.0, 0.0),       # dstate = 0: y = D u
+    # time-segmented forward (few channels, seqlen >= 512): ragged last segment
+    (1, 777, 96, 16, "bf16", 1, False, 0.5, 0.02),
+    (3, 1030, 40, 5, "f32", 0, True, 0.3, 0.0),
     # 32-channel backward CTAs (4 * 256 = 1024 CTAs of 32 channels)
     (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
     (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
