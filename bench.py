@@ -52,6 +52,11 @@ def parse():
     p.add_argument("--seqlen", type=int, default=None,
                    help="run the workload's generator at this sequence length instead "
                         "(smaller cases for profiler captures; not the benchmark line)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="batch override, like --seqlen (profiler captures only)")
+    p.add_argument("--block", action="store_true",
+                   help="time the whole Mamba-1 block (ssm_block_fwd + ssm_block_bwd) on the "
+                        "block workload instead of the scan step")
     return p.parse_args()
 
 
@@ -212,6 +217,16 @@ def cpu_oracle_sample(cfg, inp, target_s=12.0):
     return tokens / t / 1e6, f"batch rows [0, {nb}), {L} steps, channels [0, {dsub}) of {D}", t
 
 
+def config_dict(cfg, ws):
+    return {"workload": f"{WORKLOAD}: batch {cfg['batch']}, seqlen {cfg['seqlen']}, "
+                        f"dinner {cfg['dinner']}, dstate {cfg['dstate']}, "
+                        "bf16 activations, fp32 A_log/D and state, Euler B, SiLU gate",
+            "global_batch": cfg["batch"] * ws, "seq_len": cfg["seqlen"],
+            "dinner": cfg["dinner"], "dstate": cfg["dstate"],
+            "parallelism": f"replicas x{ws}",
+            "l2": "inputs larger than L2 (805 MB of activations per step), no flush"}
+
+
 # ----------------------------------------------------------------- GPU leg
 
 def run_gb300(args):
@@ -230,8 +245,9 @@ def run_gb300(args):
     ssm.load()
 
     cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
-    if args.seqlen:
-        cfg["seqlen"] = args.seqlen
+    if args.seqlen or args.batch:
+        cfg["seqlen"] = args.seqlen or cfg["seqlen"]
+        cfg["batch"] = args.batch or cfg["batch"]
         inp = workloads.scan_inputs(**cfg)
     else:
         inp = workloads.named_scan_inputs(WORKLOAD)
@@ -251,11 +267,13 @@ def run_gb300(args):
                          out=out, dout=t["dout"], du=du, ddelta=ddr, dz=dz, dB=dB, dC=dC)
     ctx = torch.empty(ssm.ssm_scan_ctx_bytes(desc), dtype=torch.uint8, device=dev)
     wsb = torch.empty(ssm.ssm_scan_bwd_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    nfw = ssm.ssm_scan_fwd_workspace_bytes(desc)
+    wsf = torch.empty(nfw, dtype=torch.uint8, device=dev) if nfw else None
     stream = torch.cuda.current_stream()
 
     def fwd():
         ssm.ssm_scan_fwd(desc, t["u"], t["delta_raw"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
-                         out, ctx, None, stream)
+                         out, ctx, wsf, stream)
 
     def bwd():
         ssm.ssm_scan_bwd(desc, t["u"], t["delta_raw"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
@@ -383,19 +401,121 @@ def run_gb300(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; the workload's distributions)",
-            "config": {"workload": f"{WORKLOAD}: batch {cfg['batch']}, seqlen {cfg['seqlen']}, "
-                                   f"dinner {cfg['dinner']}, dstate {cfg['dstate']}, "
-                                   "bf16 activations, fp32 A_log/D and state, Euler B, SiLU gate",
-                       "global_batch": cfg["batch"] * ws, "seq_len": cfg["seqlen"],
-                       "dinner": cfg["dinner"], "dstate": cfg["dstate"],
-                       "parallelism": f"replicas x{ws}",
-                       "l2": "inputs larger than L2 (805 MB of activations per step), no flush"},
+            "config": config_dict(cfg, ws),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- block leg
+
+BLOCK_METRIC = "Mamba-1 block fwd+bwd Mtokens/s; achieved % of the TF32 tensor roofline"
+
+
+def block_flops(dims):
+    """fp32 multiply-add flops of the block's four projections, forward and
+    backward (dX and dW each repeat the forward product)."""
+    M = dims["batch"] * dims["seqlen"]
+    dm, D, R, N = dims["dmodel"], dims["dinner"], dims["dtrank"], dims["dstate"]
+    P = R + 2 * N
+    fwd = 2 * M * (dm * 2 * D + D * P + R * D + D * dm)
+    return fwd, 2 * fwd
+
+
+def run_block(args):
+    import numpy as np
+    import torch
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        raise SystemExit("--block runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    ssm.load()
+    cfg = dict(workloads.BLOCK_WORKLOADS["mamba_block_fp32"])
+    seed = cfg.pop("seed")
+    if args.seqlen:
+        cfg["seqlen"] = args.seqlen
+    if args.batch:
+        cfg["batch"] = args.batch
+    inp = workloads.block_inputs(**cfg, seed=seed)
+    dims = inp["dims"]
+    x = torch.from_numpy(inp["x"]).to(dev)
+    dout = torch.from_numpy(inp["dout"]).to(dev)
+    w = {k: torch.from_numpy(v).to(dev) for k, v in inp["weights"].items()}
+    desc = ssm.block_desc(dims)
+    out = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    grads = {k: torch.empty_like(v) for k, v in w.items()}
+    ctx = torch.empty(ssm.ssm_block_ctx_bytes(desc), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ssm.ssm_block_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ssm.ssm_block_fwd(desc, x, w, out, ctx, wsb, stream)
+
+    def bwd():
+        ssm.ssm_block_bwd(desc, x, w, dout, ctx, dx, grads, wsb, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if ssm.ssm_device_faults():
+        raise RuntimeError("kernel wait timeout during warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    h0 = time.perf_counter()
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks.window(h0 + 0.05, time.perf_counter())
+    clk = clocks.stop()
+    if ssm.ssm_device_faults():
+        raise RuntimeError("kernel wait timeout in the timed region")
+    t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_step = t_fwd + t_bwd
+    M = dims["batch"] * dims["seqlen"]
+    f_fwd, f_bwd = block_flops(dims)
+    peaks, peak_kind = measured_peaks()
+    # TF32 dense peak: the measured bf16 rate x the nominal tf32 / bf16 ratio (1.1 / 2.25)
+    tf32_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * 1.1 / 2.25
+    achieved = (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": BLOCK_METRIC, "value": round(M / (ms_step * 1e-3) / 1e6, 4), "unit": "Mtokens/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; the workload's distributions)",
+        "config": {"workload": "mamba_block_fp32: dmodel {dmodel}, dinner {dinner}, dtrank {dtrank}, "
+                               "dstate {dstate}, dconv {dconv}, batch {batch}, seqlen {seqlen}, "
+                               "fp32".format(**dims),
+                   "global_batch": dims["batch"], "seq_len": dims["seqlen"]},
+        "roofline": {"kernel": "whole block step (projection GEMMs dominate the flops)",
+                     "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / tf32_peak, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained x 1.1/2.25 (tf32/bf16)",
+                     "flops_per_step": f_fwd + f_bwd,
+                     "note": "fp32 products as three TF32 passes: the tensor cores run 3x these "
+                             "flops, so 1/3 is this figure's ceiling",
+                     "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4)},
+        "gpu_launches": None, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------- reference leg
@@ -422,8 +542,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; the workload's distributions)",
-        "config": {"workload": f"{WORKLOAD}: batch 8, seqlen 2048, dinner 4096, dstate 16",
-                   "global_batch": cfg["batch"], "seq_len": cfg["seqlen"]},
+        "config": config_dict(cfg, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "Mtokens/s", "cores": 1,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
@@ -436,6 +555,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.block:
+        run_block(args)
     else:
         run_gb300(args)
 

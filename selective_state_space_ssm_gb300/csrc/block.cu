@@ -108,7 +108,7 @@ Ctx ctx_layout(const Dims& s) {
 struct Ws {
     size_t a_hi, a_lo, b_hi, b_lo, w_hi, w_lo;            // TF32 splits
     size_t dg, du, ddelta, dxd, dxz, dxn;                 // backward activations
-    size_t scan, conv, red, scanf, total;
+    size_t scan, conv, red, scanf, part, part_floats, total;
 };
 Ws ws_layout(const Dims& s) {
     const size_t f = sizeof(float);
@@ -142,6 +142,12 @@ Ws ws_layout(const Dims& s) {
                                  ssm::colsum_ws_floats(rows, s.P), ssm::rmsnorm_ws_floats(rows, s.Dm)});
     w.red = c.take(std::max<size_t>(red, 1) * f);
     w.scanf = c.take(ssm_scan_fwd_workspace_bytes(&sd));
+    // split-K partial sums of the GEMMs with few output tiles
+    const size_t biggest = std::max({M * 2 * s.D, M * static_cast<size_t>(s.Dm), M * static_cast<size_t>(s.P),
+                                     static_cast<size_t>(2) * s.D * s.Dm, static_cast<size_t>(s.P) * s.D,
+                                     static_cast<size_t>(s.D) * s.R});
+    w.part_floats = std::min<size_t>(size_t(8) << 20, 4 * biggest);
+    w.part = c.take(w.part_floats * f);
     w.total = c.off;
     return w;
 }
@@ -169,6 +175,8 @@ bool encode_op(CUtensorMap* m, const float* p, const Op& o) {
 // Stream-ordered step list of one call; the first failure sticks.
 struct Run {
     cudaStream_t st;
+    float* part = nullptr;        // split-K partial sums (null: no split)
+    size_t part_floats = 0;
     ssm_status status = SSM_OK;
 
     bool ok() const { return status == SSM_OK; }
@@ -206,6 +214,8 @@ struct Run {
         a.K = A.cols;
         a.ldc = ldc;
         a.ldr = ldr;
+        a.ksplit = part ? ssm::gemm_ksplit(a.M, a.N, a.K, part_floats) : 1;
+        a.part = part;
         cuda(ssm::launch_gemm_tf32x3(maps, a, st));
     }
 };
@@ -310,7 +320,7 @@ ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_bloc
     float* whi = at<float>(workspace, ws.w_hi);
     float* wlo = at<float>(workspace, ws.w_lo);
 
-    Run run{stream};
+    Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
     // 1. RMSNorm
     run.cuda(ssm::launch_rmsnorm_fwd(x, w->norm_w, M, Dm, kRmsEps, xn, inv, stream));
     // 2. in_proj (x_in | z)
@@ -403,7 +413,7 @@ ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_bloc
     float* dxn = at<float>(workspace, ws.dxn);
     float* red = at<float>(workspace, ws.red);
 
-    Run run{stream};
+    Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
     // Linear backward of Y = X W^T + b (cpu_ops.ts linearBackward), with
     // dY (rows, nout; stride lddy), X (rows, k; stride ldx), W (nout, k):
     //   dX = dY W  -> dX (stride lddx, + R when accumulate)

@@ -107,7 +107,12 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kGemmBN, m0 = blockIdx.y * kGemmBM;
-    const int nk = (a.K + kGemmBK - 1) / kGemmBK;
+    // this CTA's K range (split-K: blockIdx.z of ksplit slices, partial sums to
+    // a.part, added up by gemm_splitk_reduce_kernel)
+    const int nk_all = (a.K + kGemmBK - 1) / kGemmBK;
+    const int per = (nk_all + a.ksplit - 1) / a.ksplit;
+    const int kb0 = blockIdx.z * per;
+    const int nk = max(0, min(per, nk_all - kb0));
     const int ngroups = (nk + G - 1) / G;
 
     if (threadIdx.x == 0) {
@@ -138,10 +143,11 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, kFaultGemm)) break;
                 unsigned char* st = smem + s * 4 * kOpTileBytes;
                 mbar_arrive_expect_tx(&full[s], 4 * kOpTileBytes);
-                tma_load_2d(st, &maps.a_hi, &full[s], kb * kGemmBK, m0);
-                tma_load_2d(st + kOpTileBytes, &maps.a_lo, &full[s], kb * kGemmBK, m0);
-                tma_load_2d(st + 2 * kOpTileBytes, &maps.b_hi, &full[s], kb * kGemmBK, n0);
-                tma_load_2d(st + 3 * kOpTileBytes, &maps.b_lo, &full[s], kb * kGemmBK, n0);
+                const int kx = (kb0 + kb) * kGemmBK;
+                tma_load_2d(st, &maps.a_hi, &full[s], kx, m0);
+                tma_load_2d(st + kOpTileBytes, &maps.a_lo, &full[s], kx, m0);
+                tma_load_2d(st + 2 * kOpTileBytes, &maps.b_hi, &full[s], kx, n0);
+                tma_load_2d(st + 3 * kOpTileBytes, &maps.b_lo, &full[s], kx, n0);
             }
             // copies still in flight land before the CTA may exit (bounded)
             for (int j = std::max(0, kb - S); j < kb; ++j)
@@ -219,15 +225,30 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             for (int j = 0; j < 32; ++j) tile[lane * 33 + j] = acc[c0 + j];
             __syncwarp();
             const int col = n0 + c0 + lane;
-            if (got && col < a.N) {
-                const float bv = a.bias ? a.bias[col] : 0.0f;
-#pragma unroll 4
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int row = m0 + 32 * q + rr;
-                    if (row >= a.M) break;
-                    float o = tile[rr * 33 + lane] + bv;
-                    if (a.R) o += a.R[static_cast<size_t>(row) * a.ldr + col];
-                    a.C[static_cast<size_t>(row) * a.ldc + col] = o;
+            const int rbase = m0 + 32 * q;
+            const int rows = min(32, a.M - rbase);
+            if (got && col < a.N && rows > 0) {
+                if (a.ksplit > 1) {
+                    float* P = a.part + static_cast<size_t>(blockIdx.z) * a.M * a.N;
+#pragma unroll 8
+                    for (int rr = 0; rr < 32; ++rr)
+                        if (rr < rows) P[static_cast<size_t>(rbase + rr) * a.N + col] = tile[rr * 33 + lane];
+                } else {
+                    const float bv = a.bias ? a.bias[col] : 0.0f;
+                    // residual rows fetched 8 at a time so their loads overlap
+#pragma unroll
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        float res[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            res[u] = (a.R && r0 + u < rows)
+                                         ? a.R[static_cast<size_t>(rbase + r0 + u) * a.ldr + col] : 0.0f;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (r0 + u < rows)
+                                a.C[static_cast<size_t>(rbase + r0 + u) * a.ldc + col] =
+                                    tile[(r0 + u) * 33 + lane] + bv + res[u];
+                    }
                 }
             }
             __syncwarp();
@@ -249,14 +270,35 @@ cudaError_t read_clear_fault_gemm(unsigned* out) {
     return cudaMemcpyToSymbol(g_ssm_fault, &zero, sizeof(unsigned));
 }
 
+// C = sum_z part[z] (+ bias) (+ R): the split-K finish, fixed order.
+__global__ void gemm_splitk_reduce_kernel(const GemmArgs a) {
+    const size_t total = static_cast<size_t>(a.M) * a.N;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t m = i / a.N;
+        const int n = static_cast<int>(i % a.N);
+        float o = 0.0f;
+        for (int z = 0; z < a.ksplit; ++z) o += a.part[static_cast<size_t>(z) * total + i];
+        if (a.bias) o += a.bias[n];
+        if (a.R) o += a.R[m * a.ldr + n];
+        a.C[m * a.ldc + n] = o;
+    }
+}
+
 cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
+    if (a.ksplit < 1 || (a.ksplit > 1 && !a.part)) return cudaErrorInvalidValue;
     const size_t smem = kGemmStages * 4 * kOpTileBytes + (2 * kGemmStages + 4) * 8 + 16 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kGemmBN - 1) / kGemmBN, (a.M + kGemmBM - 1) / kGemmBM);
+    dim3 grid((a.N + kGemmBN - 1) / kGemmBN, (a.M + kGemmBM - 1) / kGemmBM, a.ksplit);
     gemm_tf32x3_kernel<<<grid, 192, smem, st>>>(maps, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.ksplit == 1) return e;
+    const size_t total = static_cast<size_t>(a.M) * a.N;
+    const unsigned blocks = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, 152 * 8));
+    gemm_splitk_reduce_kernel<<<blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

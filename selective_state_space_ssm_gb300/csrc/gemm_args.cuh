@@ -29,7 +29,20 @@ struct GemmArgs {
     const float* R;      // may be null; may alias C (accumulate)
     int M, N, K;
     int64_t ldc, ldr;
+    int ksplit;          // K slices computed by separate CTAs (1: none)
+    float* part;         // ksplit > 1: [ksplit][M][N] partial sums (workspace)
 };
+// Split-K for GEMMs whose output tiles leave SMs idle: returns the number of
+// K slices (1 = none) given the partial-sum space available (floats).
+inline int gemm_ksplit(int M, int N, int K, size_t part_floats) {
+    const long long tiles = static_cast<long long>((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
+    const int nk = (K + kGemmBK - 1) / kGemmBK;
+    if (tiles >= 152 || nk < 16) return 1;
+    long long ks = (2 * 152 + tiles - 1) / tiles;
+    if (ks > nk / 8) ks = nk / 8;
+    while (ks > 1 && static_cast<size_t>(ks) * M * N > part_floats) --ks;
+    return ks < 1 ? 1 : static_cast<int>(ks);
+}
 struct GemmMaps {
     CUtensorMap a_hi, a_lo, b_hi, b_lo;
 };

@@ -24,11 +24,14 @@ NAMES = ("wInProj", "bInProj", "wConv", "bConv", "wXProj", "bXProj", "wDtProj", 
 
 # (dmodel, dinner, dtrank, dstate, dconv, batch, seqlen): several 128-row GEMM
 # tiles with ragged tails, x_proj / dt_proj widths below one tile, dt_proj K
-# below one 32-wide K block, odd sequence lengths and kconv != 4.
+# below one 32-wide K block, odd sequence lengths, kconv != 4, and (last)
+# weight-gradient GEMMs with a single output tile and 25 K blocks, which the
+# GEMM splits over K.
 SMALL = [
     (64, 128, 8, 16, 4, 2, 200),
     (36, 20, 4, 4, 3, 3, 37),
     (128, 256, 16, 8, 2, 1, 129),
+    (36, 20, 4, 4, 3, 2, 400),     # weight-gradient GEMMs over 800 rows: split-K
 ]
 
 
