@@ -67,6 +67,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms, ws, device):
+    """Slowest rank's time: every rank's work counts only once all are done."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(tokens_per_rank, ws, ms):
+    """Mtokens/s of the whole job: all ranks' tokens over the slowest rank's time."""
+    return ws * tokens_per_rank / (ms * 1e-3) / 1e6
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -316,13 +332,9 @@ def run_gb300(args):
     t_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     if ssm.ssm_device_faults():
         raise RuntimeError("kernel wait timeout in the timed region")
-    ms_step = ms_total / K
-    if ws > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(ms_total / K, ws, dev)
     M = cfg["batch"] * cfg["seqlen"]
-    value = ws * M / (ms_step * 1e-3) / 1e6
+    value = whole_job_rate(M, ws, ms_step)
 
     # ---- roofline (spec definition: max(bytes / HBM, exps / SFU) per pass)
     peaks, peak_kind = measured_peaks()
@@ -380,12 +392,8 @@ def run_gb300(args):
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = s0.elapsed_time(s1) / K2
-        if ws > 1:
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        e2e = {"value": round(ws * M / (ms_e2e * 1e-3) / 1e6, 4), "unit": "Mtokens/s",
+        ms_e2e = max_over_ranks(s0.elapsed_time(s1) / K2, ws, dev)
+        e2e = {"value": round(whole_job_rate(M, ws, ms_e2e), 4), "unit": "Mtokens/s",
                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 

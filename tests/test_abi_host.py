@@ -177,3 +177,21 @@ def test_block_validation(lib):
     if not torch.cuda.is_available():
         assert fwd(_bdesc()) == 7
         assert bwd(_bdesc()) == 7
+
+
+def test_scan_workspace_reflects_time_segments(lib):
+    def d(**kw):
+        base = dict(dtype=0, disc=0)
+        base.update(kw)
+        return binding.ScanDesc(**base)
+    # plenty of channels: one segment, no forward scratch
+    assert binding.ssm_scan_fwd_workspace_bytes(d(batch=8, seqlen=2048, dinner=4096, dstate=16)) == 0
+    # one batch row of 2048 channels over 65536 steps: segments, so scratch
+    long_fwd = binding.ssm_scan_fwd_workspace_bytes(d(batch=1, seqlen=65536, dinner=2048, dstate=16))
+    assert long_fwd > 0
+    # the backward's per-segment dA / dD planes and carries make it grow too
+    short_bwd = binding.ssm_scan_bwd_workspace_bytes(d(batch=1, seqlen=256, dinner=2048, dstate=16))
+    long_bwd = binding.ssm_scan_bwd_workspace_bytes(d(batch=1, seqlen=65536, dinner=2048, dstate=16))
+    assert long_bwd > 256 * short_bwd // 2
+    # too short to split (segments need at least 256 steps)
+    assert binding.ssm_scan_fwd_workspace_bytes(d(batch=1, seqlen=300, dinner=32, dstate=16)) == 0
