@@ -311,25 +311,41 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             // ---- prologue (lane = channel, step parity): delta, delta*u (or u),
             //      dy.  All TC steps run: past seqlen the tiles, B and C are
             //      zero, so dy = 0 and the extra steps add nothing.
+            {
+                // loads, math and stores in separate passes, so that the steps'
+                // independent chains overlap (stores could alias later loads)
+                constexpr int NJ = TC / SPL;
+                float uvA[NJ], xrA[NJ], goA[NJ], zvA[NJ];
 #pragma unroll
-            for (int jj = 0; jj < TC / SPL; ++jj) {
-                const int j = SPL * jj + pj;
-                const float uv = Act<T>::to_f(tu[j * CW + pc]);
-                const float xr = Act<T>::to_f(tr[j * CW + pc]);
-                const float go = Act<T>::to_f(tg[j * CW + pc]);
-                float dt, dy = go;
-                if (GATE) {
-                    const float zv = Act<T>::to_f(tz[j * CW + pc]);
-                    float sz;
-                    softplus_sigmoid(xr, zv, dt, sz);
-                    dy = go * zv * sz;
-                } else {
-                    float e;
-                    dt = softplus_e(xr, e);
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * jj + pj;
+                    uvA[jj] = Act<T>::to_f(tu[j * CW + pc]);
+                    xrA[jj] = Act<T>::to_f(tr[j * CW + pc]);
+                    goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
+                    zvA[jj] = GATE ? Act<T>::to_f(tz[j * CW + pc]) : 0.0f;
                 }
-                Pd[j * CW + pc] = dt;
-                Pbs[j * CW + pc] = ZOH ? uv : dt * uv;
-                Pdy[j * CW + pc] = dy;
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    float dt, dy = goA[jj];
+                    if (GATE) {
+                        float sz;
+                        softplus_sigmoid(xrA[jj], zvA[jj], dt, sz);
+                        dy = goA[jj] * zvA[jj] * sz;
+                    } else {
+                        float e;
+                        dt = softplus_e(xrA[jj], e);
+                    }
+                    xrA[jj] = dt;                               // reuse: delta
+                    goA[jj] = dy;                               // reuse: dy
+                    uvA[jj] = ZOH ? uvA[jj] : dt * uvA[jj];     // reuse: delta*u | u
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * jj + pj;
+                    Pd[j * CW + pc] = xrA[jj];
+                    Pbs[j * CW + pc] = uvA[jj];
+                    Pdy[j * CW + pc] = goA[jj];
+                }
             }
             __syncwarp();
 
