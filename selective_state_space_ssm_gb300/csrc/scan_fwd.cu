@@ -242,20 +242,33 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         __syncwarp();
         T* so = ost + ((k - kb) & 1) * 2 * TILE;
         float* sc = ckst + ((k - kb) & 1) * NCK * NT * CW;
+        // The recurrence first, the staging stores after it: a store could
+        // alias the next step's B|C loads, which would then have to wait.
+        float yv[TS];
+        float2 hck[NCK][NQ];                            // states at the chunk ends
 #pragma unroll
         for (int j = 0; j < TS; ++j) {
-            const float y = fwd_step<NT, DISC>(h, A2, Anat, invA, Bf + j * NT, Bf + BCT + j * NT, dtv[j],
-                                               bsv[j]) + duv[j];
-            so[j * CW + lane] = Act<T>::from_f(GATE ? y * gzv[j] : y);
-            if (save_y) so[TILE + j * CW + lane] = Act<T>::from_f(y);
-            if ((j + 1) % kChunk == 0 && save_ck) {
-                // state after the last step of a chunk = checkpoint of the next one
+            yv[j] = fwd_step<NT, DISC>(h, A2, Anat, invA, Bf + j * NT, Bf + BCT + j * NT, dtv[j], bsv[j]) +
+                    duv[j];
+            if ((j + 1) % kChunk == 0) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) hck[j / kChunk][q] = h[q];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < TS; ++j) {
+            so[j * CW + lane] = Act<T>::from_f(GATE ? yv[j] * gzv[j] : yv[j]);
+            if (save_y) so[TILE + j * CW + lane] = Act<T>::from_f(yv[j]);
+        }
+        if (save_ck) {
+            // state after the last step of a chunk = checkpoint of the next one
+#pragma unroll
+            for (int m = 0; m < NCK; ++m)
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
-                    sc[((j / kChunk) * NT + 2 * q) * CW + lane] = h[q].x;
-                    sc[((j / kChunk) * NT + 2 * q + 1) * CW + lane] = h[q].y;
+                    sc[(m * NT + 2 * q) * CW + lane] = hck[m][q].x;
+                    sc[(m * NT + 2 * q + 1) * CW + lane] = hck[m][q].y;
                 }
-            }
         }
         fence_proxy_async_smem();
         __syncwarp();
