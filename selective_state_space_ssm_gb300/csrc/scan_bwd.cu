@@ -361,16 +361,32 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         h[i][p] = kc > 0 ? make_float2(ck[(ng * NS + 2 * p) * CW + cbase + i],
                                                        ck[(ng * NS + 2 * p + 1) * CW + cbase + i])
                                          : make_float2(0.f, 0.f);
+                // a step's inputs are loaded one step ahead: a partial-sum store
+                // could alias them, so they could not move above it otherwise
+                float dlN[CPL], bsN[CPL], dyN[CPL];
+                float2 BN[NS / 2];
+                auto load_b = [&](int j) {
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlN);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsN);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyN);
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p)
+                        BN[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                };
+                load_b(0);
 #pragma unroll
                 for (int j = 0; j < TC; ++j) {
                     float dlA[CPL], bsA[CPL], dyA[CPL];
-                    ld_cpl<CPL>(Pd + j * CW + cbase, dlA);
-                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsA);
-                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyA);
                     float2 Bv[NS / 2];
 #pragma unroll
-                    for (int p = 0; p < NS / 2; ++p)
-                        Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                    for (int i = 0; i < CPL; ++i) {
+                        dlA[i] = dlN[i];
+                        bsA[i] = bsN[i];
+                        dyA[i] = dyN[i];
+                    }
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) Bv[p] = BN[p];
+                    if (j + 1 < TC) load_b(j + 1);
                     float2 dC[NS / 2];
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
@@ -415,18 +431,36 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                         const float2 x = mul2(f2(dl_next[i]), A2r[i][p]);
                         an[i][p] = make_float2(ex2(x.x), ex2(x.y));
                     }
+                // inputs one step ahead (see pass B)
+                float dlN[CPL], bsN[CPL], dyN[CPL];
+                float2 BN[NS / 2], CN[NS / 2];
+                auto load_r = [&](int j) {
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlN);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsN);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyN);
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        BN[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                        CN[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
+                    }
+                };
+                load_r(TC - 1);
 #pragma unroll
                 for (int j = TC - 1; j >= 0; --j) {
                     float dlA[CPL], bsA[CPL], dyA[CPL];
-                    ld_cpl<CPL>(Pd + j * CW + cbase, dlA);
-                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsA);
-                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyA);
                     float2 Bv[NS / 2], Cv[NS / 2];
 #pragma unroll
-                    for (int p = 0; p < NS / 2; ++p) {
-                        Bv[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
-                        Cv[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
+                    for (int i = 0; i < CPL; ++i) {
+                        dlA[i] = dlN[i];
+                        bsA[i] = bsN[i];
+                        dyA[i] = dyN[i];
                     }
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        Bv[p] = BN[p];
+                        Cv[p] = CN[p];
+                    }
+                    if (j > 0) load_r(j - 1);
                     float2 dB[NS / 2];
 #pragma unroll
                     for (int p = 0; p < NS / 2; ++p) dB[p] = make_float2(0.f, 0.f);
