@@ -527,45 +527,66 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             // ---- epilogue (lane = channel, step parity): finish du,
             //      ddelta_raw, dz, dD
             if (lane_ok) {
+                // loads, math and stores in separate passes (see the prologue),
+                // two steps at a time for 32-channel CTAs (register pressure)
+                constexpr int NJALL = TC / SPL;
+                constexpr int NJ = (CW == 32) ? 2 : NJALL;   // steps per load/compute/store block
 #pragma unroll 1
-                for (int jj = 0; jj < TC / SPL; ++jj) {
-                    const int j = SPL * jj + pj;
-                    if (j < jmax) {
-                        const size_t r = row0 + t0 + j;
-                        float sm[NQN];
+                for (int jb = 0; jb < NJALL; jb += NJ) {
+                float Sg[NJ], Eg[NJ], Sa[NJ], uvA[NJ], xrA[NJ], dtA[NJ], dyA2[NJ], zvA[NJ], goA[NJ], yvA[NJ];
 #pragma unroll
-                        for (int qn = 0; qn < NQN; ++qn) {
-                            // the 4 state groups' sums; a step-phase-1 lane reads
-                            // them in the order 1,0,3,2 (other banks, same sum)
-                            const float* pp = part + (j * NQN + qn) * 4 * CW;
-                            float v[4];
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    float sm[NQN];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int kk = k ^ pj;
-                                v[k] = pp[kk * CW + part_col(pc, kk)];
-                            }
-                            sm[qn] = (v[0] + v[1]) + (v[2] + v[3]);
+                    for (int qn = 0; qn < NQN; ++qn) {
+                        // the 4 state groups' sums; a step-phase-1 lane reads
+                        // them in the order 1,0,3,2 (other banks, same sum)
+                        const float* pp = part + (j * NQN + qn) * 4 * CW;
+                        float v[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int kk = k ^ pj;
+                            v[k] = pp[kk * CW + part_col(pc, kk)];
                         }
-                        const float uv = Act<T>::to_f(tu[j * CW + pc]);
-                        const float xr = Act<T>::to_f(tr[j * CW + pc]);
-                        const float dt = Pd[j * CW + pc];
-                        const float dyv = Pdy[j * CW + pc];
-                        const float Sg = sm[0], Eg = sm[1] * kLn2;
-                        const float du = ZOH ? fmaf(Dd, dyv, Sg) : fmaf(dt, Sg, Dd * dyv);
-                        const float ddl = fmaf(uv, ZOH ? sm[NQN - 1] : Sg, Eg);
-                        dD_acc = fmaf(dyv, uv, dD_acc);
-                        dup[r * a.ld_du + dch] = Act<T>::from_f(du);
-                        ddp[r * a.ld_ddelta + dch] = Act<T>::from_f(ddl * sigmoidf_(xr));
-                        if (GATE) {
-                            const float zv = Act<T>::to_f(tz[j * CW + pc]);
-                            const float go = Act<T>::to_f(tg[j * CW + pc]);
-                            const float yv = Act<T>::to_f(ty[j * CW + pc]);
-                            const float sz = sigmoidf_(zv);
-                            dzp[r * a.ld_dz + dch] =
-                                Act<T>::from_f(go * yv * sz * (1.0f + zv * (1.0f - sz)));
-                        }
+                        sm[qn] = (v[0] + v[1]) + (v[2] + v[3]);
+                    }
+                    Sg[jj] = sm[0];
+                    Eg[jj] = sm[1] * kLn2;
+                    Sa[jj] = sm[NQN - 1];
+                    uvA[jj] = Act<T>::to_f(tu[j * CW + pc]);
+                    xrA[jj] = Act<T>::to_f(tr[j * CW + pc]);
+                    dtA[jj] = Pd[j * CW + pc];
+                    dyA2[jj] = Pdy[j * CW + pc];
+                    if (GATE) {
+                        zvA[jj] = Act<T>::to_f(tz[j * CW + pc]);
+                        goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
+                        yvA[jj] = Act<T>::to_f(ty[j * CW + pc]);
                     }
                 }
+                float duO[NJ], ddO[NJ], dzO[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    duO[jj] = ZOH ? fmaf(Dd, dyA2[jj], Sg[jj]) : fmaf(dtA[jj], Sg[jj], Dd * dyA2[jj]);
+                    ddO[jj] = fmaf(uvA[jj], ZOH ? Sa[jj] : Sg[jj], Eg[jj]) * sigmoidf_(xrA[jj]);
+                    if (j < jmax) dD_acc = fmaf(dyA2[jj], uvA[jj], dD_acc);
+                    if (GATE) {
+                        const float sz = sigmoidf_(zvA[jj]);
+                        dzO[jj] = goA[jj] * yvA[jj] * sz * (1.0f + zvA[jj] * (1.0f - sz));
+                    }
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    if (j < jmax) {
+                        const size_t r = row0 + t0 + j;
+                        dup[r * a.ld_du + dch] = Act<T>::from_f(duO[jj]);
+                        ddp[r * a.ld_ddelta + dch] = Act<T>::from_f(ddO[jj]);
+                        if (GATE) dzp[r * a.ld_dz + dch] = Act<T>::from_f(dzO[jj]);
+                    }
+                }
+            }
             }
             __syncwarp();
             park();
