@@ -84,9 +84,15 @@ def _load():
             lib.ssm_oracle_block_bwd.argtypes = [ctypes.POINTER(_BlockDims), i, _dp,
                                                  ctypes.POINTER(_BlockPtrs), _dp, _dp,
                                                  ctypes.POINTER(_BlockPtrs)]
+            lib.ssm_oracle_scan_step.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                                 _dp, _dp]
+            lib.ssm_oracle_scan_fwd_state.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp,
+                                                      _dp, _dp, _dp]
+            lib.ssm_oracle_conv1d_silu_step.argtypes = [i, i, i, l, _dp, _dp, _dp, _dp, _dp]
             for fn in ("ssm_oracle_scan_chain", "ssm_oracle_scan_fwd", "ssm_oracle_scan_bwd",
                        "ssm_oracle_conv1d_silu_fwd", "ssm_oracle_conv1d_silu_bwd",
-                       "ssm_oracle_block_fwd", "ssm_oracle_block_bwd"):
+                       "ssm_oracle_block_fwd", "ssm_oracle_block_bwd", "ssm_oracle_scan_step",
+                       "ssm_oracle_scan_fwd_state", "ssm_oracle_conv1d_silu_step"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -207,6 +213,62 @@ def conv1d_silu_bwd(x, w, bias, dout, batch=1):
                                         _p(x), _p(w), _p(b), _p(g), _p(dx), _p(dw), _p(db))
     _check(rc, "conv1d_silu_bwd")
     return dx, dw, db
+
+
+def scan_step(h, u, delta_raw, A_log, B, C, D=None, z=None, disc=EULER):
+    """One decode step of the scan for every batch row.  h: (batch, dstate,
+    dinner) state; u, delta_raw, z: (batch, dinner); B, C: (batch, dstate).
+    Returns (out, h_next); h is not modified."""
+    lib = _load()
+    u, dr, Al, Bm, Cm = map(_f64, (u, delta_raw, A_log, B, C))
+    Dv = None if D is None else _f64(D)
+    zz = None if z is None else _f64(z)
+    hn = _f64(h).copy()
+    batch, dinner = u.shape
+    dstate = Al.shape[1]
+    assert hn.shape == (batch, dstate, dinner)
+    out = np.empty((batch, dinner))
+    rc = lib.ssm_oracle_scan_step(batch, dinner, dstate, int(disc), _p(u), _p(dr), _p(Al), _p(Bm),
+                                  _p(Cm), _p(Dv), _p(zz), _p(hn), _p(out))
+    _check(rc, "scan_step")
+    return out, hn
+
+
+def scan_fwd_state(u, delta_raw, A_log, B, C, D=None, z=None, disc=EULER, batch=1, h_init=None):
+    """Scan forward from the state h_init ((batch, dstate, dinner); None = 0),
+    walked as single steps.  Returns (out, h_last)."""
+    lib = _load()
+    u, dr, Al, Bm, Cm = map(_f64, (u, delta_raw, A_log, B, C))
+    Dv = None if D is None else _f64(D)
+    zz = None if z is None else _f64(z)
+    M, dinner = u.shape
+    dstate = Al.shape[1]
+    batch = int(batch)
+    h = (np.zeros((batch, dstate, dinner)) if h_init is None else _f64(h_init).copy())
+    assert h.shape == (batch, dstate, dinner)
+    out = np.empty((M, dinner))
+    rc = lib.ssm_oracle_scan_fwd_state(batch, M // batch, dinner, dstate, int(disc), _p(u), _p(dr),
+                                       _p(Al), _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(h), _p(out))
+    _check(rc, "scan_fwd_state")
+    return out, h
+
+
+def conv1d_silu_step(ring, x, w, bias, pos):
+    """One decode step of the causal conv1d + SiLU at position ``pos``.  ring:
+    (batch, kconv-1, dinner), input at position p in slot p mod (kconv-1); x:
+    (batch, dinner).  Returns (out, ring_next); ring is not modified."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = None if bias is None else _f64(bias)
+    batch, dinner = x.shape
+    kconv = w.shape[1]
+    rn = _f64(ring).copy()
+    assert rn.shape == (batch, kconv - 1, dinner)
+    out = np.empty((batch, dinner))
+    rc = lib.ssm_oracle_conv1d_silu_step(batch, dinner, kconv, int(pos), _p(x), _p(w), _p(b),
+                                         _p(rn), _p(out))
+    _check(rc, "conv1d_silu_step")
+    return out, rn
 
 
 def _block_args(dims, weights):

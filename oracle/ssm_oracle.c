@@ -280,6 +280,122 @@ int ssm_oracle_conv1d_silu_bwd(int batch, int seqlen, int dinner, int kconv, lon
     return 0;
 }
 
+/* ---------------- single-token decode (inference) ---------------- */
+
+/*
+ * One step of the recurrence of mamba1_cpu.ts step 8 (and the gate of step 9)
+ * for every (batch row, channel), with the state carried in from the caller
+ * instead of h_{-1} = 0:
+ *   h[n] <- exp(dt A_n) h[n] + beta_n u ;  y = sum_n C_n h[n] + D u ;
+ *   out = y * silu(z)   (or y when z == NULL).
+ * u, dt_raw, z, out are (batch, dinner); B, C are (batch, dstate); A_log is
+ * (dinner, dstate); Dv (dinner) may be NULL; h is (batch, dstate, dinner),
+ * element (b, n, d) at [(b*dstate + n)*dinner + d], read and overwritten.
+ */
+int ssm_oracle_scan_step(int batch, int dinner, int dstate, int disc,
+                         const double* u, const double* dt_raw, const double* A_log,
+                         const double* B, const double* C, const double* Dv,
+                         const double* z, double* h, double* out) {
+    const int zoh = (disc == 1);
+    for (int b = 0; b < batch; ++b)
+        for (int d = 0; d < dinner; ++d) {
+            size_t o = (size_t)b * dinner + d;
+            double dv = softplus_(dt_raw[o]);
+            double uv = u[o];
+            double acc = Dv ? Dv[d] * uv : 0.0;
+            for (int n = 0; n < dstate; ++n) {
+                disc_t q = discretise_(dv, a_cont_(A_log[(size_t)d * dstate + n]), zoh);
+                double* hp = h + ((size_t)b * dstate + n) * dinner + d;
+                *hp = q.a * *hp + q.bcoef * B[(size_t)b * dstate + n] * uv;
+                acc += C[(size_t)b * dstate + n] * *hp;
+            }
+            out[o] = z ? acc * silu_(z[o]) : acc;
+        }
+    return 0;
+}
+
+/*
+ * The scan forward from a given initial state, walked as seqlen single steps
+ * (ssm_oracle_scan_step on row t of every batch row).  u, dt_raw, z, out are
+ * (M, dinner) with M = batch*seqlen; B, C (M, dstate).  h is (batch, dstate,
+ * dinner): the initial state on entry (all zero gives the scan of the pages),
+ * the state after the last step on return.
+ */
+int ssm_oracle_scan_fwd_state(int batch, int seqlen, int dinner, int dstate, int disc,
+                              const double* u, const double* dt_raw, const double* A_log,
+                              const double* B, const double* C, const double* Dv,
+                              const double* z, double* h, double* out) {
+    double* row[5];
+    for (int i = 0; i < 5; ++i) {
+        row[i] = (double*)malloc((size_t)batch * (i < 3 ? dinner : dstate) * sizeof(double));
+        if (!row[i]) {
+            for (int j = 0; j < i; ++j) free(row[j]);
+            return -1;
+        }
+    }
+    double* ob = (double*)malloc((size_t)batch * dinner * sizeof(double));
+    if (!ob) {
+        for (int j = 0; j < 5; ++j) free(row[j]);
+        return -1;
+    }
+    for (int t = 0; t < seqlen; ++t) {
+        /* gather row t of every batch row: u, dt_raw, z | B, C */
+        for (int b = 0; b < batch; ++b) {
+            size_t r = (size_t)b * seqlen + t;
+            for (int d = 0; d < dinner; ++d) {
+                row[0][(size_t)b * dinner + d] = u[r * dinner + d];
+                row[1][(size_t)b * dinner + d] = dt_raw[r * dinner + d];
+                row[2][(size_t)b * dinner + d] = z ? z[r * dinner + d] : 0.0;
+            }
+            for (int n = 0; n < dstate; ++n) {
+                row[3][(size_t)b * dstate + n] = B[r * dstate + n];
+                row[4][(size_t)b * dstate + n] = C[r * dstate + n];
+            }
+        }
+        ssm_oracle_scan_step(batch, dinner, dstate, disc, row[0], row[1], A_log, row[3], row[4],
+                             Dv, z ? row[2] : NULL, h, ob);
+        for (int b = 0; b < batch; ++b)
+            for (int d = 0; d < dinner; ++d)
+                out[((size_t)b * seqlen + t) * dinner + d] = ob[(size_t)b * dinner + d];
+    }
+    for (int j = 0; j < 5; ++j) free(row[j]);
+    free(ob);
+    return 0;
+}
+
+/*
+ * One step of the causal depthwise conv1d + SiLU of mamba1_cpu.ts steps 4-5 at
+ * sequence position pos, with the kconv-1 previous inputs kept by the caller
+ * in a ring: input x at position p of batch row b sits in slot p mod (kconv-1),
+ * element (b, slot, d) at [(b*(kconv-1) + slot)*dinner + d].
+ *   out[b, d] = silu(bias[d] + w[d, 0] x[b, d] + sum_{1 <= k < kconv, pos >= k}
+ *                    w[d, k] * (input at position pos-k))
+ * after which x is stored in slot pos mod (kconv-1).  Positions before 0 add
+ * nothing (the pages' t >= k condition), whatever those slots hold.
+ * x, out are (batch, dinner); w (dinner, kconv); bias (dinner) may be NULL.
+ */
+int ssm_oracle_conv1d_silu_step(int batch, int dinner, int kconv, long pos,
+                                const double* x, const double* w, const double* bias,
+                                double* ring, double* out) {
+    const int R = kconv - 1;
+    for (int b = 0; b < batch; ++b)
+        for (int d = 0; d < dinner; ++d) {
+            double acc = bias ? bias[d] : 0.0;
+            acc += w[(size_t)d * kconv] * x[(size_t)b * dinner + d];
+            for (int k = 1; k < kconv; ++k) {
+                long p = pos - k;
+                if (p < 0) continue;
+                acc += w[(size_t)d * kconv + k] * ring[((size_t)b * R + (size_t)(p % R)) * dinner + d];
+            }
+            out[(size_t)b * dinner + d] = silu_(acc);
+        }
+    if (R > 0)
+        for (int b = 0; b < batch; ++b)
+            for (int d = 0; d < dinner; ++d)
+                ring[((size_t)b * R + (size_t)(pos % R)) * dinner + d] = x[(size_t)b * dinner + d];
+    return 0;
+}
+
 /* ---------------- the whole Mamba-1 block ---------------- */
 
 /* cpu_ops.ts linearForward: Y (M,Nout) = X (M,K) W^T + b, W (Nout,K). */
