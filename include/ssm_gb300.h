@@ -244,6 +244,61 @@ ssm_status ssm_conv1d_silu_bwd_noalloc(int32_t batch, int32_t seqlen, int32_t di
                                        int64_t ld_dout, float* dx, int64_t ld_dx, float* dw,
                                        float* dbias, cudaStream_t stream);
 
+/* ---- Single-token decode (inference) ----------------------------------
+ * The same recurrence one position at a time, for serving: the scan state of
+ * a batch of sequences is kept by the caller between calls.
+ *   h    : (batch, dstate, dinner) fp32, element (b, n, d) at
+ *          h[(b*dstate + n)*dinner + d]; 16-byte aligned.
+ *   ring : (batch, kconv-1, dinner) fp32, the conv1d's previous inputs: the
+ *          input at sequence position p of batch row b sits in slot
+ *          p mod (kconv-1), element at ring[(b*(kconv-1) + slot)*dinner + d];
+ *          16-byte aligned.  Slots of positions before 0 are never read, so
+ *          a new sequence needs no zeroing. */
+
+/* Scan forward from a carried state and/or returning the final state (prefill):
+ * ssm_scan_fwd without a saved context, plus
+ *   h_init : state before the first step of every batch row (NULL = zero);
+ *   h_last : receives the state after the last step (may be NULL).
+ * Both (batch, dstate, dinner) as above, 4-byte aligned, and they must not
+ * overlap (SSM_ERR_SHAPE).  seqlen = 0 copies h_init (or zero) to h_last.
+ * There is no backward for a non-zero h_init.  workspace as ssm_scan_fwd. */
+ssm_status ssm_scan_fwd_state(const ssm_scan_desc* desc,
+                              const void* u, const void* delta_raw, const float* A_log,
+                              const void* B, const void* C, const float* D, const void* z,
+                              void* out, const float* h_init, float* h_last,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* One decode step of the scan (mamba1_cpu.ts mamba1CpuForward steps 8-9 at a
+ * single position): desc->seqlen must be 1 and row b of every activation
+ * belongs to batch row b.  For every (b, d):
+ *   delta = softplus(delta_raw);  h[b,n,d] <- exp(delta A[d,n]) h[b,n,d] + beta u
+ *   out = (sum_n C[b,n] h[b,n,d] + D[d] u) * silu(z)     (no gate when z == NULL)
+ * h is read and overwritten in place.  D may be NULL.  Activation types,
+ * strides and alignment as ssm_scan_fwd. */
+ssm_status ssm_scan_step(const ssm_scan_desc* desc,
+                         const void* u, const void* delta_raw, const float* A_log,
+                         const void* B, const void* C, const float* D, const void* z,
+                         float* h, void* out, cudaStream_t stream);
+
+/* One decode step of the causal depthwise conv1d + SiLU (mamba1_cpu.ts
+ * forward steps 4-5 at sequence position pos >= 0):
+ *   out[b,d] = silu(bias[d] + w[d,0] x[b,d] + sum_{1<=k<kconv, pos>=k} w[d,k] x_{pos-k}[b,d])
+ * with x_p read from the ring, then x stored in slot pos mod (kconv-1).
+ * x, out: (batch, dinner) fp32 with row strides ld_x, ld_out (0 = packed);
+ * w (dinner, kconv), tap 0 on the current input; bias may be NULL.
+ * dinner, ld_x, ld_out multiples of 4 and x, out, ring, bias 16-byte aligned
+ * (else SSM_ERR_ALIGN); 1 <= kconv <= 8. */
+ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, int64_t pos,
+                                const float* x, int64_t ld_x, const float* w, const float* bias,
+                                float* ring, float* out, int64_t ld_out, cudaStream_t stream);
+
+/* Fill the ring from a prompt x (batch*seqlen, dinner) fp32 (row stride ld_x)
+ * so that decoding continues at position seqlen: slot p mod (kconv-1) gets
+ * the input at position p for the last kconv-1 positions p >= 0.  Alignment
+ * as ssm_conv1d_silu_step. */
+ssm_status ssm_conv1d_ring_fill(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                                const float* x, int64_t ld_x, float* ring, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);
 

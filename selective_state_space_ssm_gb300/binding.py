@@ -27,6 +27,8 @@ __all__ = [
     "block_desc", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "linear",
     "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "block_fwd", "block_bwd",
+    "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_ring_fill",
+    "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_ring_fill",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -43,7 +45,8 @@ EXPORTED_SYMBOLS = (
     "ssm_scan_fwd", "ssm_scan_bwd", "ssm_conv1d_silu", "ssm_conv1d_silu_bwd_workspace_bytes",
     "ssm_conv1d_silu_bwd", "ssm_status_string", "ssm_last_cuda_error", "ssm_abi_version",
     "ssm_device_faults", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
-    "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd",
+    "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
+    "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_ring_fill",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -131,6 +134,15 @@ def load():
             "ssm_block_bwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
                                              ctypes.POINTER(BlockWeights), vp, vp, sz, vp,
                                              ctypes.POINTER(BlockGrads), vp, sz, vp]),
+            # desc, u, delta_raw, A_log, B, C, D, z, out, h_init, h_last, ws, ws_bytes, stream
+            "ssm_scan_fwd_state": (ctypes.c_int, [dp] + [vp] * 11 + [sz, vp]),
+            # desc, u, delta_raw, A_log, B, C, D, z, h, out, stream
+            "ssm_scan_step": (ctypes.c_int, [dp] + [vp] * 10),
+            # batch, dinner, kconv, pos, x, ld_x, w, bias, ring, out, ld_out, stream
+            "ssm_conv1d_silu_step": (ctypes.c_int, [i32, i32, i32, i64, vp, i64, vp, vp, vp, vp,
+                                                    i64, vp]),
+            # batch, seqlen, dinner, kconv, x, ld_x, ring, stream
+            "ssm_conv1d_ring_fill": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -242,6 +254,35 @@ def ssm_conv1d_silu_bwd(batch, x, w, bias, dout, dx, dw, dbias, workspace=None, 
     _check("ssm_conv1d_silu_bwd", st)
 
 
+def ssm_scan_fwd_state(desc, u, delta_raw, A_log, B, C, D, z, out, h_init=None, h_last=None,
+                       workspace=None, stream=None):
+    st = load().ssm_scan_fwd_state(ctypes.byref(desc), _ptr(u), _ptr(delta_raw), _ptr(A_log),
+                                   _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(out), _ptr(h_init),
+                                   _ptr(h_last), _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream))
+    _check("ssm_scan_fwd_state", st)
+
+
+def ssm_scan_step(desc, u, delta_raw, A_log, B, C, D, z, h, out, stream=None):
+    st = load().ssm_scan_step(ctypes.byref(desc), _ptr(u), _ptr(delta_raw), _ptr(A_log), _ptr(B),
+                              _ptr(C), _ptr(D), _ptr(z), _ptr(h), _ptr(out), _stream(stream))
+    _check("ssm_scan_step", st)
+
+
+def ssm_conv1d_silu_step(x, w, bias, ring, out, pos, stream=None):
+    batch, dinner = x.shape
+    st = load().ssm_conv1d_silu_step(batch, dinner, w.shape[1], int(pos), _ptr(x), _ld(x), _ptr(w),
+                                     _ptr(bias), _ptr(ring), _ptr(out), _ld(out), _stream(stream))
+    _check("ssm_conv1d_silu_step", st)
+
+
+def ssm_conv1d_ring_fill(batch, x, kconv, ring, stream=None):
+    M, dinner = x.shape
+    st = load().ssm_conv1d_ring_fill(batch, M // batch, dinner, int(kconv), _ptr(x), _ld(x),
+                                     _ptr(ring), _stream(stream))
+    _check("ssm_conv1d_ring_fill", st)
+
+
 def ssm_status_string(status: int) -> str:
     return load().ssm_status_string(status).decode()
 
@@ -342,6 +383,49 @@ def scan_bwd(u, delta_raw, A_log, B, C, D, z, dout, ctx, *, batch, disc=SSM_DISC
     ssm_scan_bwd(desc, u, delta_raw, A_log, B, C, D, z, dout, ctx, du, ddelta, dA_log, dB, dC, dD,
                  dz, ws, stream)
     return dict(du=du, ddelta_raw=ddelta, dA_log=dA_log, dB=dB, dC=dC, dD=dD, dz=dz)
+
+
+def scan_fwd_state(u, delta_raw, A_log, B, C, D=None, z=None, *, batch, h_init=None,
+                   disc=SSM_DISC_EULER, stream=None):
+    """Prefill: run the scan from h_init (None = 0) and return (out, h_last),
+    h_last of shape (batch, dstate, dinner) fp32."""
+    import torch
+    out = torch.empty_like(u, memory_format=torch.contiguous_format)
+    desc = scan_desc(u, delta_raw, A_log, B, C, z, batch=batch, disc=disc, out=out)
+    h_last = torch.empty((batch, A_log.shape[1], u.shape[1]), dtype=torch.float32, device=u.device)
+    ws = _bytes_tensor(ssm_scan_fwd_workspace_bytes(desc), u)
+    ssm_scan_fwd_state(desc, u, delta_raw, A_log, B, C, D, z, out, h_init, h_last, ws, stream)
+    return out, h_last
+
+
+def scan_step(h, u, delta_raw, A_log, B, C, D=None, z=None, *, disc=SSM_DISC_EULER, out=None,
+              stream=None):
+    """One decode step: u, delta_raw, z (batch, dinner); B, C (batch, dstate);
+    h (batch, dstate, dinner) fp32 is updated in place.  Returns out."""
+    import torch
+    if out is None:
+        out = torch.empty_like(u, memory_format=torch.contiguous_format)
+    desc = scan_desc(u, delta_raw, A_log, B, C, z, batch=u.shape[0], disc=disc, out=out)
+    ssm_scan_step(desc, u, delta_raw, A_log, B, C, D, z, h, out, stream)
+    return out
+
+
+def conv1d_silu_step(x, w, bias, ring, pos, *, out=None, stream=None):
+    """One decode step of the conv at position pos: x (batch, dinner); ring
+    (batch, kconv-1, dinner) fp32 is updated in place.  Returns out."""
+    import torch
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ssm_conv1d_silu_step(x, w, bias, ring, out, pos, stream)
+    return out
+
+
+def conv1d_ring_fill(x, kconv, *, batch, stream=None):
+    """The ring (batch, kconv-1, dinner) that continues a prompt x (batch*seqlen, dinner)."""
+    import torch
+    ring = torch.zeros((batch, kconv - 1, x.shape[1]), dtype=torch.float32, device=x.device)
+    ssm_conv1d_ring_fill(batch, x, kconv, ring, stream)
+    return ring
 
 
 def conv1d_silu(x, w, bias=None, *, batch, stream=None):

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libssm_gb300.so")
-SOURCES = ["abi.cu", "scan_fwd.cu", "scan_bwd.cu", "conv1d.cu", "gemm.cu", "rmsnorm.cu", "block.cu"]
+SOURCES = ["abi.cu", "scan_fwd.cu", "scan_bwd.cu", "conv1d.cu", "gemm.cu", "rmsnorm.cu", "block.cu",
+           "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

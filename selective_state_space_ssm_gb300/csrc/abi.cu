@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "conv_args.cuh"
+#include "decode_args.cuh"
 #include "gemm_args.cuh"
 #include "host_util.h"
 #include "scan_args.cuh"
@@ -270,14 +271,35 @@ size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
     return bwd_layout(d).total;
 }
 
-ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta_raw,
-                        const float* A_log, const void* B, const void* C, const float* D,
-                        const void* z, void* out, void* ctx, size_t ctx_bytes, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward behind ssm_scan_fwd (h_init = h_last = null) and
+// ssm_scan_fwd_state (ctx = null).
+ssm_status scan_fwd_impl(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                         const float* A_log, const void* B, const void* C, const float* D,
+                         const void* z, void* out, void* ctx, size_t ctx_bytes, const float* h_init,
+                         float* h_last, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Lds r;
     ssm_status st = validate(d, r);
     if (st != SSM_OK) return st;
     const int64_t M = static_cast<int64_t>(d->batch) * d->seqlen;
+    const size_t hbytes = static_cast<size_t>(d->batch) * d->dstate * d->dinner * sizeof(float);
+    if (h_init && h_last && hbytes > 0) {
+        const char *i0 = reinterpret_cast<const char*>(h_init), *l0 = reinterpret_cast<const char*>(h_last);
+        if (i0 < l0 + hbytes && l0 < i0 + hbytes) return SSM_ERR_SHAPE;   // the two states overlap
+    }
+    if ((h_init && (reinterpret_cast<uintptr_t>(h_init) & 3u)) ||
+        (h_last && (reinterpret_cast<uintptr_t>(h_last) & 3u)))
+        return SSM_ERR_ALIGN;
+    if (M == 0 && h_last && hbytes > 0) {
+        // no step: the final state is the initial one
+        if ((st = check_device()) != SSM_OK) return st;
+        cudaError_t e = h_init ? cudaMemcpyAsync(h_last, h_init, hbytes, cudaMemcpyDeviceToDevice, stream)
+                               : cudaMemsetAsync(h_last, 0, hbytes, stream);
+        return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+    }
     if (M == 0 || d->dinner == 0) return SSM_OK;
     if (!u || !delta_raw || !out) return SSM_ERR_NULL;
     if (d->dstate > 0 && (!B || !C || !A_log)) return SSM_ERR_NULL;
@@ -343,8 +365,30 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
         a.seg_h = reinterpret_cast<float*>(w + fl.off_segh);
         a.seg_ds = reinterpret_cast<float*>(w + fl.off_segds);
     }
+    a.h_init = h_init;
+    a.h_last = h_last;
     cudaError_t e = ssm::launch_scan_fwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                        const float* A_log, const void* B, const void* C, const float* D,
+                        const void* z, void* out, void* ctx, size_t ctx_bytes, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    return scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, ctx, ctx_bytes, nullptr, nullptr,
+                         workspace, workspace_bytes, stream);
+}
+
+ssm_status ssm_scan_fwd_state(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                              const float* A_log, const void* B, const void* C, const float* D,
+                              const void* z, void* out, const float* h_init, float* h_last,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, nullptr, 0, h_init, h_last,
+                         workspace, workspace_bytes, stream);
 }
 
 ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta_raw,
@@ -461,6 +505,95 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
     ra.ld_dC = r.dC;
     ra.is_bf16 = d->dtype == SSM_BF16;
     cudaError_t e = ssm::launch_scan_reduce(ra, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+ssm_status ssm_scan_step(const ssm_scan_desc* d, const void* u, const void* delta_raw,
+                         const float* A_log, const void* B, const void* C, const float* D,
+                         const void* z, float* h, void* out, cudaStream_t stream) {
+    Lds r;
+    ssm_status st = validate(d, r);
+    if (st != SSM_OK) return st;
+    if (d->seqlen != 1) return SSM_ERR_SHAPE;
+    if (d->batch == 0 || d->dinner == 0) return SSM_OK;
+    if (!u || !delta_raw || !out) return SSM_ERR_NULL;
+    if (d->dstate > 0 && (!B || !C || !A_log || !h)) return SSM_ERR_NULL;
+    if (!aligned16(u) || !aligned16(delta_raw) || !aligned16(out) || (z && !aligned16(z)) ||
+        (d->dstate > 0 && !aligned16(h)))
+        return SSM_ERR_ALIGN;
+    if ((st = check_device()) != SSM_OK) return st;
+    ssm::ScanStepArgs a{};
+    a.u = u;
+    a.dr = delta_raw;
+    a.z = z;
+    a.B = B;
+    a.C = C;
+    a.A_log = A_log;
+    a.D = D;
+    a.h = h;
+    a.out = out;
+    a.batch = d->batch;
+    a.dinner = d->dinner;
+    a.dstate = d->dstate;
+    a.ld_u = r.u;
+    a.ld_dr = r.delta;
+    a.ld_z = r.z;
+    a.ld_B = r.B;
+    a.ld_C = r.C;
+    a.ld_out = r.out;
+    cudaError_t e = ssm::launch_scan_step(d->dtype, nt_of(d->dstate), d->disc, z != nullptr, a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, int64_t pos,
+                                const float* x, int64_t ld_x, const float* w, const float* bias,
+                                float* ring, float* out, int64_t ld_out, cudaStream_t stream) {
+    if (batch < 0 || dinner < 0 || kconv < 1 || kconv > 8 || pos < 0) return SSM_ERR_SHAPE;
+    ld_x = ld_x ? ld_x : dinner;
+    ld_out = ld_out ? ld_out : dinner;
+    if (ld_x < dinner || ld_out < dinner) return SSM_ERR_SHAPE;
+    if (batch == 0 || dinner == 0) return SSM_OK;
+    if (!x || !w || !out || (kconv > 1 && !ring)) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || ld_out % 4 || !aligned16(x) || !aligned16(out) ||
+        (ring && !aligned16(ring)) || (bias && !aligned16(bias)))
+        return SSM_ERR_ALIGN;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    ssm::ConvStepArgs a{};
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.ring = ring;
+    a.out = out;
+    a.batch = batch;
+    a.dinner = dinner;
+    a.kconv = kconv;
+    a.pos = pos;
+    a.ld_x = ld_x;
+    a.ld_out = ld_out;
+    cudaError_t e = ssm::launch_conv_step(a, stream);
+    return e == cudaSuccess ? SSM_OK : fail_cuda(e);
+}
+
+ssm_status ssm_conv1d_ring_fill(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
+                                const float* x, int64_t ld_x, float* ring, cudaStream_t stream) {
+    if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
+    ld_x = ld_x ? ld_x : dinner;
+    if (ld_x < dinner) return SSM_ERR_SHAPE;
+    if (batch == 0 || seqlen == 0 || dinner == 0 || kconv == 1) return SSM_OK;
+    if (!x || !ring) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || !aligned16(x) || !aligned16(ring)) return SSM_ERR_ALIGN;
+    ssm_status st = check_device();
+    if (st != SSM_OK) return st;
+    ssm::RingFillArgs a{};
+    a.x = x;
+    a.ring = ring;
+    a.batch = batch;
+    a.seqlen = seqlen;
+    a.dinner = dinner;
+    a.kconv = kconv;
+    a.ld_x = ld_x;
+    cudaError_t e = ssm::launch_ring_fill(a, stream);
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 

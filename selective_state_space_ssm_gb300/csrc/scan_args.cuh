@@ -79,6 +79,11 @@ struct ScanFwdArgs {
     float* h0;
     float* seg_h;
     float* seg_ds;
+    // Carried state (inference): h_init is the state before the first step
+    // (null = 0), h_last receives the state after the last step (may be null);
+    // both [batch][dstate][dinner].
+    const float* h_init;
+    float* h_last;
 };
 
 struct ScanBwdArgs {

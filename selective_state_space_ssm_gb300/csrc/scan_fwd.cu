@@ -167,6 +167,11 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         if (g > 0 && active) {
             const float* hp = a.h0 + ((static_cast<size_t>(b) * a.nseg + g) * NT + 2 * q) * a.dinner + d;
             h[q] = make_float2(hp[0], hp[a.dinner]);
+        } else if (g == 0 && active && a.h_init) {
+            // caller's initial state [batch][dstate][dinner]
+            const float* hp = a.h_init + (static_cast<size_t>(b) * N + 2 * q) * a.dinner + d;
+            if (2 * q < N) h[q].x = hp[0];
+            if (2 * q + 1 < N) h[q].y = hp[a.dinner];
         }
     }
 
@@ -232,10 +237,18 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             gzv[j] = gz;
             duv[j] = Dd * uv;
         }
+        if (a.h_last && jmax < TS) {
+            // steps past seqlen: delta = 0 keeps the state exactly (a = 1,
+            // beta u = 0), so it is the state after the last step at the end
+#pragma unroll
+            for (int j = 0; j < TS; ++j)
+                if (j >= jmax) dtv[j] = bsv[j] = 0.0f;
+        }
 
         // Phase B: the recurrence.  Every tile runs all TS steps: past seqlen
         // the TMA tiles and B|C are zero, so the extra steps only evolve a
-        // state that is never stored.  Outputs go to a staging tile in shared
+        // state that is never stored (or, when the final state is asked for,
+        // leave it unchanged: see above).  Outputs go to a staging tile in shared
         // memory (double-buffered) and leave by TMA store; the store of tile
         // k-2 must have finished reading its buffer first.
         if (lane == 0 && k - kb >= 2) bulk_wait_read_1();
@@ -293,6 +306,14 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
     }
     if (lane == 0) bulk_wait_all();   // the staged stores have left shared memory
+    if (a.h_last && k == ke && ke == ntiles && active) {
+        float* hp = a.h_last + static_cast<size_t>(b) * N * a.dinner + d;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            if (2 * q < N) hp[static_cast<size_t>(2 * q) * a.dinner] = h[q].x;
+            if (2 * q + 1 < N) hp[static_cast<size_t>(2 * q + 1) * a.dinner] = h[q].y;
+        }
+    }
 }
 
 // Segment pass of the time-parallel forward: for segment g of batch row b,
@@ -448,7 +469,8 @@ scan_fwd_segsum_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a
 }
 
 // Combine of the time segments: one thread per (batch row, state, channel)
-// walks the segments in order and writes the state entering each segment.
+// walks the segments in order, from the caller's initial state (or 0), and
+// writes the state entering each segment.
 template <int NT>
 __global__ void scan_fwd_combine_kernel(const ScanFwdArgs a) {
     const size_t total = static_cast<size_t>(a.batch) * NT * a.dinner;
@@ -458,7 +480,8 @@ __global__ void scan_fwd_combine_kernel(const ScanFwdArgs a) {
     const int n = static_cast<int>((i / a.dinner) % NT);
     const int b = static_cast<int>(i / (static_cast<size_t>(a.dinner) * NT));
     const float A2 = n < a.dstate ? a2_from_alog(a.A_log[static_cast<size_t>(d) * a.dstate + n]) : 0.0f;
-    float h = 0.0f;
+    float h = (a.h_init && n < a.dstate)
+                  ? a.h_init[(static_cast<size_t>(b) * a.dstate + n) * a.dinner + d] : 0.0f;
     for (int g = 0; g + 1 < a.nseg; ++g) {
         const size_t sg = static_cast<size_t>(b) * a.nseg + g;
         const float P = ex2(A2 * a.seg_ds[sg * a.dinner + d]);   // product of a_t over segment g

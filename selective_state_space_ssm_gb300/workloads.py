@@ -87,6 +87,12 @@ def scan_inputs(batch, seqlen, dinner, dstate, seed=0, dtype="f32", A_log_noise=
                 dtype=dtype)
 
 
+def state_inputs(batch, dstate, dinner, seed=0, scale=1.0):
+    """A carried scan state (batch, dstate, dinner) fp32 ~ N(0, scale^2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return (scale * _normal(rng, (batch, dstate, dinner))).astype(np.float32)
+
+
 def named_scan_inputs(name, **overrides):
     """Inputs of a named scan workload; keyword overrides replace its fields."""
     cfg = dict(SCAN_WORKLOADS[name])

@@ -195,3 +195,49 @@ def test_scan_workspace_reflects_time_segments(lib):
     assert long_bwd > 256 * short_bwd // 2
     # too short to split (segments need at least 256 steps)
     assert binding.ssm_scan_fwd_workspace_bytes(d(batch=1, seqlen=300, dinner=32, dstate=16)) == 0
+
+
+def _step(lib, d, ptr=16, h=16):
+    p = ctypes.c_void_p(ptr) if ptr is not None else None
+    hp = ctypes.c_void_p(h) if h is not None else None
+    return lib.ssm_scan_step(ctypes.byref(d), p, p, p, p, p, None, None, hp, p, None)
+
+
+def test_decode_step_validation(lib):
+    assert _step(lib, _desc(seqlen=2)) == 2                 # one position per batch row
+    assert _step(lib, _desc(seqlen=1, dstate=17)) == 2
+    assert _step(lib, _desc(seqlen=1), h=None) == 1
+    assert _step(lib, _desc(seqlen=1), h=8) == 3            # state not 16-byte aligned
+    assert _step(lib, _desc(seqlen=1, dinner=6)) == 3
+    assert _step(lib, _desc(seqlen=1, batch=0), ptr=None, h=None) == 0
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert _step(lib, _desc(seqlen=1)) == 7
+
+
+def test_fwd_state_validation(lib):
+    p = ctypes.c_void_p(16)
+    f = lambda d, hi, hl: lib.ssm_scan_fwd_state(ctypes.byref(d), p, p, p, p, p, None, None, p,
+                                                 hi, hl, None, 0, None)
+    d = _desc()
+    nbytes = 2 * 16 * 64 * 4
+    # overlapping initial and final states are rejected
+    assert f(d, ctypes.c_void_p(4096), ctypes.c_void_p(4096 + nbytes - 4)) == 2
+    assert f(d, ctypes.c_void_p(4098), None) == 3
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert f(d, ctypes.c_void_p(4096), ctypes.c_void_p(4096 + nbytes)) == 7
+
+
+def test_conv_step_validation(lib):
+    f = lib.ssm_conv1d_silu_step
+    p = ctypes.c_void_p(16)
+    assert f(1, 8, 0, 0, p, 0, p, None, p, p, 0, None) == 2       # kconv 0
+    assert f(1, 8, 4, -1, p, 0, p, None, p, p, 0, None) == 2      # negative position
+    assert f(1, 6, 4, 0, p, 0, p, None, p, p, 0, None) == 3       # dinner not a multiple of 4
+    assert f(1, 8, 4, 0, p, 0, p, None, None, p, 0, None) == 1    # no ring with kconv > 1
+    assert f(0, 8, 4, 0, None, 0, None, None, None, None, 0, None) == 0
+    g = lib.ssm_conv1d_ring_fill
+    assert g(1, 5, 8, 9, p, 0, p, None) == 2
+    assert g(1, 5, 8, 1, None, 0, None, None) == 0                # no ring for kconv 1
+    assert g(1, 5, 8, 4, p, 0, ctypes.c_void_p(8), None) == 3
