@@ -88,7 +88,7 @@ def _load():
                                                  _dp, _dp]
             lib.ssm_oracle_scan_fwd_state.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp,
                                                       _dp, _dp, _dp]
-            lib.ssm_oracle_conv1d_silu_step.argtypes = [i, i, i, l, _dp, _dp, _dp, _dp, _dp]
+            lib.ssm_oracle_conv1d_silu_step.argtypes = [i, i, i, _dp, _dp, _dp, _dp, _dp]
             for fn in ("ssm_oracle_scan_chain", "ssm_oracle_scan_fwd", "ssm_oracle_scan_bwd",
                        "ssm_oracle_conv1d_silu_fwd", "ssm_oracle_conv1d_silu_bwd",
                        "ssm_oracle_block_fwd", "ssm_oracle_block_bwd", "ssm_oracle_scan_step",
@@ -253,22 +253,23 @@ def scan_fwd_state(u, delta_raw, A_log, B, C, D=None, z=None, disc=EULER, batch=
     return out, h
 
 
-def conv1d_silu_step(ring, x, w, bias, pos):
-    """One decode step of the causal conv1d + SiLU at position ``pos``.  ring:
-    (batch, kconv-1, dinner), input at position p in slot p mod (kconv-1); x:
-    (batch, dinner).  Returns (out, ring_next); ring is not modified."""
+def conv1d_silu_step(state, x, w, bias):
+    """One decode step of the causal conv1d + SiLU.  state: (batch, kconv-1,
+    dinner), slot j = the input kconv-1-j steps back (zeros before the
+    sequence); x: (batch, dinner).  Returns (out, state_next); state is not
+    modified."""
     lib = _load()
     x, w = _f64(x), _f64(w)
     b = None if bias is None else _f64(bias)
     batch, dinner = x.shape
     kconv = w.shape[1]
-    rn = _f64(ring).copy()
-    assert rn.shape == (batch, kconv - 1, dinner)
+    sn = _f64(state).copy()
+    assert sn.shape == (batch, kconv - 1, dinner)
     out = np.empty((batch, dinner))
-    rc = lib.ssm_oracle_conv1d_silu_step(batch, dinner, kconv, int(pos), _p(x), _p(w), _p(b),
-                                         _p(rn), _p(out))
+    rc = lib.ssm_oracle_conv1d_silu_step(batch, dinner, kconv, _p(x), _p(w), _p(b), _p(sn),
+                                         _p(out))
     _check(rc, "conv1d_silu_step")
-    return out, rn
+    return out, sn
 
 
 def _block_args(dims, weights):

@@ -364,35 +364,34 @@ int ssm_oracle_scan_fwd_state(int batch, int seqlen, int dinner, int dstate, int
 }
 
 /*
- * One step of the causal depthwise conv1d + SiLU of mamba1_cpu.ts steps 4-5 at
- * sequence position pos, with the kconv-1 previous inputs kept by the caller
- * in a ring: input x at position p of batch row b sits in slot p mod (kconv-1),
- * element (b, slot, d) at [(b*(kconv-1) + slot)*dinner + d].
- *   out[b, d] = silu(bias[d] + w[d, 0] x[b, d] + sum_{1 <= k < kconv, pos >= k}
- *                    w[d, k] * (input at position pos-k))
- * after which x is stored in slot pos mod (kconv-1).  Positions before 0 add
- * nothing (the pages' t >= k condition), whatever those slots hold.
+ * One step of the causal depthwise conv1d + SiLU of mamba1_cpu.ts steps 4-5,
+ * with the kconv-1 previous inputs of every batch row kept by the caller in
+ * a shift register: slot j (0 <= j < kconv-1) holds the input k = kconv-1-j
+ * steps back, element (b, j, d) at [(b*(kconv-1) + j)*dinner + d].  A new
+ * sequence starts from all zeros, which is the pages' t >= k condition (no
+ * input before position 0).
+ *   out[b, d] = silu(bias[d] + w[d, 0] x[b, d] + sum_{1 <= k < kconv} w[d, k] * state[b, kconv-1-k, d])
+ * after which every slot moves one step back and x enters the last slot.
  * x, out are (batch, dinner); w (dinner, kconv); bias (dinner) may be NULL.
  */
-int ssm_oracle_conv1d_silu_step(int batch, int dinner, int kconv, long pos,
+int ssm_oracle_conv1d_silu_step(int batch, int dinner, int kconv,
                                 const double* x, const double* w, const double* bias,
-                                double* ring, double* out) {
+                                double* state, double* out) {
     const int R = kconv - 1;
     for (int b = 0; b < batch; ++b)
         for (int d = 0; d < dinner; ++d) {
             double acc = bias ? bias[d] : 0.0;
             acc += w[(size_t)d * kconv] * x[(size_t)b * dinner + d];
-            for (int k = 1; k < kconv; ++k) {
-                long p = pos - k;
-                if (p < 0) continue;
-                acc += w[(size_t)d * kconv + k] * ring[((size_t)b * R + (size_t)(p % R)) * dinner + d];
-            }
+            for (int k = 1; k < kconv; ++k)
+                acc += w[(size_t)d * kconv + k] * state[((size_t)b * R + (size_t)(R - k)) * dinner + d];
             out[(size_t)b * dinner + d] = silu_(acc);
         }
-    if (R > 0)
-        for (int b = 0; b < batch; ++b)
-            for (int d = 0; d < dinner; ++d)
-                ring[((size_t)b * R + (size_t)(pos % R)) * dinner + d] = x[(size_t)b * dinner + d];
+    for (int b = 0; b < batch; ++b)
+        for (int d = 0; d < dinner; ++d) {
+            for (int j = 0; j + 1 < R; ++j)
+                state[((size_t)b * R + j) * dinner + d] = state[((size_t)b * R + j + 1) * dinner + d];
+            if (R > 0) state[((size_t)b * R + R - 1) * dinner + d] = x[(size_t)b * dinner + d];
+        }
     return 0;
 }
 

@@ -2,7 +2,8 @@
 
 The decode step is the scan recurrence of mamba1_cpu.ts step 8 taken one
 position at a time with the state carried by the caller, and the conv step is
-mamba1_cpu.ts steps 4-5 at one position with the previous inputs in a ring.
+mamba1_cpu.ts steps 4-5 at one position with the previous inputs in a shift
+register.
 Each is pinned to something outside its own code:
 
 * the scan walked as steps from h = 0 equals the whole-sequence scan (itself
@@ -11,9 +12,10 @@ Each is pinned to something outside its own code:
   explicit product form for the final state, exact halving when
   exp(delta A) = 1/2 and B = 0, the memoryless limit, and the split
   invariance scan(x1 ++ x2) = scan(x2 from the final state of x1);
-* the conv step walked over a sequence equals the whole-sequence conv (pinned
-  by its impulse response and finite differences), whatever the ring held
-  before position 0, and also when the ring is filled from a prompt.
+* the conv step walked over a sequence from a zero state equals the
+  whole-sequence conv (pinned by its impulse response and finite
+  differences), also when the state is filled from a prompt; an impulse in a
+  state slot meets the tap of its age, and the slots shift by one.
 """
 import numpy as np
 import pytest
@@ -168,16 +170,34 @@ def test_conv_steps_equal_the_conv(kconv):
     ref, _ = oracle.conv1d_silu_fwd(x, w, bias, batch=batch)
     ref = ref.reshape(batch, L, D)
     xs = x.reshape(batch, L, D)
-    # garbage in the ring before position 0 must not leak in
-    ring = 1e6 * rng.standard_normal((batch, kconv - 1, D))
+    state = np.zeros((batch, kconv - 1, D))              # a new sequence
     for t in range(L):
-        o, ring = oracle.conv1d_silu_step(ring, xs[:, t], w, bias, t)
+        o, state = oracle.conv1d_silu_step(state, xs[:, t], w, bias)
         np.testing.assert_allclose(o, ref[:, t], rtol=1e-13, atol=1e-13)
-    # continuing after a prompt: ring filled from positions P-kconv+1 .. P-1
+    # continuing after a prompt of P positions: slot j holds position P-(kconv-1)+j (0 before 0)
     P = 6
-    ring = np.zeros((batch, kconv - 1, D))
-    for p in range(max(0, P - kconv + 1), P):
-        ring[:, p % (kconv - 1)] = xs[:, p]
+    state = np.zeros((batch, kconv - 1, D))
+    for j in range(kconv - 1):
+        p = P - (kconv - 1) + j
+        if p >= 0:
+            state[:, j] = xs[:, p]
     for t in range(P, L):
-        o, ring = oracle.conv1d_silu_step(ring, xs[:, t], w, bias, t)
+        o, state = oracle.conv1d_silu_step(state, xs[:, t], w, bias)
         np.testing.assert_allclose(o, ref[:, t], rtol=1e-13, atol=1e-13)
+
+
+def test_conv_step_tap_order():
+    # an impulse in slot j is the input kconv-1-j steps back: it meets tap kconv-1-j
+    D, K = 2, 4
+    w = np.arange(1.0, 1.0 + D * K).reshape(D, K) / 10.0
+    for j in range(K - 1):
+        state = np.zeros((1, K - 1, D))
+        state[0, j] = 1.0
+        o, s2 = oracle.conv1d_silu_step(state, np.zeros((1, D)), w, None)
+        pre = w[:, K - 1 - j]
+        np.testing.assert_allclose(o[0], silu(pre), rtol=1e-14)
+        # the slots moved one step back and the (zero) input entered last
+        want = np.zeros((1, K - 1, D))
+        if j > 0:
+            want[0, j - 1] = 1.0
+        np.testing.assert_array_equal(s2, want)
