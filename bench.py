@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--block", action="store_true",
                    help="time the whole Mamba-1 block (ssm_block_fwd + ssm_block_bwd) on the "
                         "block workload instead of the scan step")
+    p.add_argument("--decode", action="store_true",
+                   help="time single-token decode (conv1d+SiLU step + scan step per layer) on "
+                        "the decode workload instead of the scan step")
     return p.parse_args()
 
 
@@ -526,6 +529,173 @@ def run_block(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- decode leg
+
+DECODE_WORKLOAD = "mamba1p4b_decode_fp32"
+DECODE_METRIC = ("Mamba-1 decode (conv1d+SiLU step + scan step per layer) tokens/s; "
+                 "achieved % of the HBM roofline")
+
+
+def decode_bytes(cfg):
+    """Algorithmic HBM bytes of one scan step and one conv step of one layer
+    (fp32): the states are read and written, each activation read or written once."""
+    Bn, D, N, K = cfg["batch"], cfg["dinner"], cfg["dstate"], cfg["dconv"]
+    scan = 2 * Bn * N * D * 4 + 4 * Bn * D * 4 + 2 * Bn * N * 4 + D * N * 4 + D * 4
+    conv = Bn * D * 4 * (1 + 2 * (K - 1) + 1) + D * K * 4 + D * 4   # x, state in + out, out
+    return scan, conv
+
+
+def decode_cpu_sample(layer_inp, cfg, target_s=10.0):
+    """The fp64 oracle's conv step + scan step on the workload's layers, one
+    after another until about target_s; scaled to tokens/s of the full step."""
+    import oracle
+    oracle.build()
+    Bn, NL = cfg["batch"], cfg["layers"]
+    t0 = time.perf_counter()
+    done = 0
+    while done < NL and time.perf_counter() - t0 < target_s:
+        li = layer_inp[done % len(layer_inp)]
+        u, _ = oracle.conv1d_silu_step(li["conv_state"], li["x"], li["w"], li["bias"])
+        oracle.scan_step(li["h"], u, li["delta_raw"], li["A_log"], li["B"], li["C"], li["D"],
+                         li["z"], 0)
+        done += 1
+    secs = time.perf_counter() - t0
+    per_layer = secs / done
+    return Bn / (per_layer * NL), f"{done} of {NL} layers of one step, batch {Bn}", secs
+
+
+def run_decode(args):
+    import ctypes
+    import numpy as np
+    import torch
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        raise SystemExit("--decode runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    lib = ssm.load()
+    cfg = dict(workloads.DECODE_WORKLOADS[DECODE_WORKLOAD])
+    if args.batch:
+        cfg["batch"] = args.batch
+    Bn, D, N, K, NL, seed = (cfg[k] for k in ("batch", "dinner", "dstate", "dconv", "layers", "seed"))
+
+    # per layer: parameters (A_log, D, conv w/bias), the token's inputs, the carried states
+    layers, host_sample = [], []
+    for l in range(NL):
+        si = workloads.scan_inputs(Bn, 1, D, N, seed=seed * 1000 + l, A_log_noise=0.5,
+                                   clamp_frac=0.02)
+        ci = workloads.conv_inputs(Bn, 1, D, K, seed=seed * 1000 + 500 + l)
+        li = dict(x=ci["x"], w=ci["w"], bias=ci["bias"], delta_raw=si["delta_raw"], B=si["B"],
+                  C=si["C"], z=si["z"], A_log=si["A_log"], D=si["D"],
+                  h=workloads.state_inputs(Bn, N, D, seed=seed * 1000 + 800 + l, scale=0.1),
+                  conv_state=workloads.state_inputs(Bn, K - 1, D, seed=seed * 1000 + 900 + l))
+        if l < 2:
+            host_sample.append(li)
+        t = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in li.items()}
+        t["u"] = torch.empty((Bn, D), dtype=torch.float32, device=dev)
+        t["out"] = torch.empty((Bn, D), dtype=torch.float32, device=dev)
+        layers.append(t)
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda x: ctypes.c_void_p(x.data_ptr())
+    descs = [ssm.ScanDesc(batch=Bn, seqlen=1, dinner=D, dstate=N, dtype=ssm.SSM_F32,
+                          disc=ssm.SSM_DISC_EULER) for _ in range(NL)]
+    conv_args = [(Bn, D, K, P(t["x"]), D, P(t["w"]), P(t["bias"]), P(t["conv_state"]), P(t["u"]),
+                  D, sp) for t in layers]
+    scan_args = [(ctypes.byref(descs[l]), P(t["u"]), P(t["delta_raw"]), P(t["A_log"]), P(t["B"]),
+                  P(t["C"]), P(t["D"]), P(t["z"]), P(t["h"]), P(t["out"]), sp)
+                 for l, t in enumerate(layers)]
+    conv_fn, scan_fn = lib.ssm_conv1d_silu_step, lib.ssm_scan_step
+
+    def step():
+        bad = 0
+        for l in range(NL):
+            bad |= conv_fn(*conv_args[l])
+            bad |= scan_fn(*scan_args[l])
+        if bad:
+            raise RuntimeError(f"decode step failed with status {bad}")
+
+    def scans_only():
+        for l in range(NL):
+            scan_fn(*scan_args[l])
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    Kst = args.steps
+    # the ABI calls captured once into CUDA graphs (no position argument: the
+    # captured step is the step at every position), then replayed
+    g_step, g_scan = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        step()
+    with torch.cuda.graph(g_scan, stream=stream):
+        scans_only()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            g_step.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    h0 = time.perf_counter()
+    ms_step = timed(g_step.replay, Kst)
+    ms_scans = timed(g_scan.replay, Kst)
+    ms_eager = timed(step, max(1, Kst // 5))
+    clocks.window(h0 + 0.05, time.perf_counter())
+    clk = clocks.stop()
+    ms_scan_launch = ms_scans / NL
+    value = Bn / (ms_step * 1e-3)
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    scan_b, conv_b = decode_bytes(cfg)
+    achieved = scan_b / (ms_scan_launch * 1e-3) / 1e9
+    step_bytes = NL * (scan_b + conv_b)
+    cpu = None
+    if not args.no_cpu:
+        v, sample, secs = decode_cpu_sample(host_sample, cfg)
+        cpu = {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample, "seconds": round(secs, 2)}
+    line = {
+        "metric": DECODE_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": Kst, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; the workload's distributions)",
+        "config": {"workload": f"{DECODE_WORKLOAD}: batch {Bn}, dinner {D}, dstate {N}, dconv {K}, "
+                               f"{NL} layers (one token per sequence through every layer's "
+                               "conv1d+SiLU step and scan step), fp32",
+                   "global_batch": Bn, "seq_len": 1,
+                   "launch": "the step's 2 x layers ABI calls captured in one CUDA graph, replayed",
+                   "l2": f"{NL} layers' states ({NL * Bn * N * D * 4 / 1e6:.0f} MB) exceed L2, no flush"},
+        "roofline": {"kernel": "scan_step_kernel (ssm_scan_step)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": round(hbm, 1), "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": scan_b, "us_per_launch": round(ms_scan_launch * 1e3, 3),
+                     "step_frac": round(step_bytes / (hbm * 1e9) / (ms_step * 1e-3), 4)},
+        "eager_ms_per_step": round(ms_eager, 4),
+        "cpu_baseline": cpu, "e2e": None,
+        "e2e_note": "decode inputs come from the previous layer on the device; no host copies",
+        "gpu_launches": 2 * NL * Kst, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------- reference leg
 
 def run_reference(args):
@@ -565,6 +735,8 @@ def main():
         run_reference(args)
     elif args.block:
         run_block(args)
+    elif args.decode:
+        run_decode(args)
     else:
         run_gb300(args)
 

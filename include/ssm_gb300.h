@@ -249,11 +249,12 @@ ssm_status ssm_conv1d_silu_bwd_noalloc(int32_t batch, int32_t seqlen, int32_t di
  * a batch of sequences is kept by the caller between calls.
  *   h    : (batch, dstate, dinner) fp32, element (b, n, d) at
  *          h[(b*dstate + n)*dinner + d]; 16-byte aligned.
- *   ring : (batch, kconv-1, dinner) fp32, the conv1d's previous inputs: the
- *          input at sequence position p of batch row b sits in slot
- *          p mod (kconv-1), element at ring[(b*(kconv-1) + slot)*dinner + d];
- *          16-byte aligned.  Slots of positions before 0 are never read, so
- *          a new sequence needs no zeroing. */
+ *   conv_state : (batch, kconv-1, dinner) fp32, the conv1d's previous inputs:
+ *          slot j holds the input kconv-1-j steps back, element (b, j, d) at
+ *          conv_state[(b*(kconv-1) + j)*dinner + d]; 16-byte aligned.  A new
+ *          sequence starts from zeros (no input before position 0); each step
+ *          shifts the slots by one, so a decode step takes no position and the
+ *          same call can be replayed (e.g. from a CUDA graph) at every position. */
 
 /* Scan forward from a carried state and/or returning the final state (prefill):
  * ssm_scan_fwd without a saved context, plus
@@ -281,23 +282,25 @@ ssm_status ssm_scan_step(const ssm_scan_desc* desc,
                          float* h, void* out, cudaStream_t stream);
 
 /* One decode step of the causal depthwise conv1d + SiLU (mamba1_cpu.ts
- * forward steps 4-5 at sequence position pos >= 0):
- *   out[b,d] = silu(bias[d] + w[d,0] x[b,d] + sum_{1<=k<kconv, pos>=k} w[d,k] x_{pos-k}[b,d])
- * with x_p read from the ring, then x stored in slot pos mod (kconv-1).
+ * forward steps 4-5 at one position):
+ *   out[b,d] = silu(bias[d] + w[d,0] x[b,d] + sum_{1<=k<kconv} w[d,k] conv_state[b, kconv-1-k, d])
+ * then conv_state[b, j] <- conv_state[b, j+1] and conv_state[b, kconv-2] <- x.
  * x, out: (batch, dinner) fp32 with row strides ld_x, ld_out (0 = packed);
  * w (dinner, kconv), tap 0 on the current input; bias may be NULL.
- * dinner, ld_x, ld_out multiples of 4 and x, out, ring, bias 16-byte aligned
- * (else SSM_ERR_ALIGN); 1 <= kconv <= 8. */
-ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, int64_t pos,
+ * dinner, ld_x, ld_out multiples of 4 and x, out, conv_state, bias 16-byte
+ * aligned (else SSM_ERR_ALIGN); 1 <= kconv <= 8 (kconv = 1: no state, may be
+ * NULL). */
+ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv,
                                 const float* x, int64_t ld_x, const float* w, const float* bias,
-                                float* ring, float* out, int64_t ld_out, cudaStream_t stream);
+                                float* conv_state, float* out, int64_t ld_out, cudaStream_t stream);
 
-/* Fill the ring from a prompt x (batch*seqlen, dinner) fp32 (row stride ld_x)
- * so that decoding continues at position seqlen: slot p mod (kconv-1) gets
- * the input at position p for the last kconv-1 positions p >= 0.  Alignment
- * as ssm_conv1d_silu_step. */
-ssm_status ssm_conv1d_ring_fill(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
-                                const float* x, int64_t ld_x, float* ring, cudaStream_t stream);
+/* The conv_state that continues a prompt x (batch*seqlen, dinner) fp32 (row
+ * stride ld_x) at position seqlen: slot j <- the input at position
+ * seqlen-(kconv-1)+j, or zero where that is before 0.  Alignment as
+ * ssm_conv1d_silu_step. */
+ssm_status ssm_conv1d_state_from_prompt(int32_t batch, int32_t seqlen, int32_t dinner,
+                                        int32_t kconv, const float* x, int64_t ld_x,
+                                        float* conv_state, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);

@@ -27,8 +27,8 @@ __all__ = [
     "block_desc", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "linear",
     "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "block_fwd", "block_bwd",
-    "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_ring_fill",
-    "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_ring_fill",
+    "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
+    "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_state_from_prompt",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -46,7 +46,7 @@ EXPORTED_SYMBOLS = (
     "ssm_conv1d_silu_bwd", "ssm_status_string", "ssm_last_cuda_error", "ssm_abi_version",
     "ssm_device_faults", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
-    "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_ring_fill",
+    "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -138,11 +138,11 @@ def load():
             "ssm_scan_fwd_state": (ctypes.c_int, [dp] + [vp] * 11 + [sz, vp]),
             # desc, u, delta_raw, A_log, B, C, D, z, h, out, stream
             "ssm_scan_step": (ctypes.c_int, [dp] + [vp] * 10),
-            # batch, dinner, kconv, pos, x, ld_x, w, bias, ring, out, ld_out, stream
-            "ssm_conv1d_silu_step": (ctypes.c_int, [i32, i32, i32, i64, vp, i64, vp, vp, vp, vp,
-                                                    i64, vp]),
-            # batch, seqlen, dinner, kconv, x, ld_x, ring, stream
-            "ssm_conv1d_ring_fill": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp]),
+            # batch, dinner, kconv, x, ld_x, w, bias, conv_state, out, ld_out, stream
+            "ssm_conv1d_silu_step": (ctypes.c_int, [i32, i32, i32, vp, i64, vp, vp, vp, vp, i64,
+                                                    vp]),
+            # batch, seqlen, dinner, kconv, x, ld_x, conv_state, stream
+            "ssm_conv1d_state_from_prompt": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -269,18 +269,19 @@ def ssm_scan_step(desc, u, delta_raw, A_log, B, C, D, z, h, out, stream=None):
     _check("ssm_scan_step", st)
 
 
-def ssm_conv1d_silu_step(x, w, bias, ring, out, pos, stream=None):
+def ssm_conv1d_silu_step(x, w, bias, conv_state, out, stream=None):
     batch, dinner = x.shape
-    st = load().ssm_conv1d_silu_step(batch, dinner, w.shape[1], int(pos), _ptr(x), _ld(x), _ptr(w),
-                                     _ptr(bias), _ptr(ring), _ptr(out), _ld(out), _stream(stream))
+    st = load().ssm_conv1d_silu_step(batch, dinner, w.shape[1], _ptr(x), _ld(x), _ptr(w),
+                                     _ptr(bias), _ptr(conv_state), _ptr(out), _ld(out),
+                                     _stream(stream))
     _check("ssm_conv1d_silu_step", st)
 
 
-def ssm_conv1d_ring_fill(batch, x, kconv, ring, stream=None):
+def ssm_conv1d_state_from_prompt(batch, x, kconv, conv_state, stream=None):
     M, dinner = x.shape
-    st = load().ssm_conv1d_ring_fill(batch, M // batch, dinner, int(kconv), _ptr(x), _ld(x),
-                                     _ptr(ring), _stream(stream))
-    _check("ssm_conv1d_ring_fill", st)
+    st = load().ssm_conv1d_state_from_prompt(batch, M // batch, dinner, int(kconv), _ptr(x), _ld(x),
+                                             _ptr(conv_state), _stream(stream))
+    _check("ssm_conv1d_state_from_prompt", st)
 
 
 def ssm_status_string(status: int) -> str:
@@ -410,22 +411,24 @@ def scan_step(h, u, delta_raw, A_log, B, C, D=None, z=None, *, disc=SSM_DISC_EUL
     return out
 
 
-def conv1d_silu_step(x, w, bias, ring, pos, *, out=None, stream=None):
-    """One decode step of the conv at position pos: x (batch, dinner); ring
-    (batch, kconv-1, dinner) fp32 is updated in place.  Returns out."""
+def conv1d_silu_step(x, w, bias, conv_state, *, out=None, stream=None):
+    """One decode step of the conv: x (batch, dinner); conv_state (batch,
+    kconv-1, dinner) fp32 (zeros for a new sequence) is updated in place.
+    Returns out."""
     import torch
     if out is None:
         out = torch.empty_like(x, memory_format=torch.contiguous_format)
-    ssm_conv1d_silu_step(x, w, bias, ring, out, pos, stream)
+    ssm_conv1d_silu_step(x, w, bias, conv_state, out, stream)
     return out
 
 
-def conv1d_ring_fill(x, kconv, *, batch, stream=None):
-    """The ring (batch, kconv-1, dinner) that continues a prompt x (batch*seqlen, dinner)."""
+def conv1d_state_from_prompt(x, kconv, *, batch, stream=None):
+    """The conv_state (batch, kconv-1, dinner) that continues a prompt x
+    (batch*seqlen, dinner)."""
     import torch
-    ring = torch.zeros((batch, kconv - 1, x.shape[1]), dtype=torch.float32, device=x.device)
-    ssm_conv1d_ring_fill(batch, x, kconv, ring, stream)
-    return ring
+    st = torch.empty((batch, kconv - 1, x.shape[1]), dtype=torch.float32, device=x.device)
+    ssm_conv1d_state_from_prompt(batch, x, kconv, st, stream)
+    return st
 
 
 def conv1d_silu(x, w, bias=None, *, batch, stream=None):

@@ -545,17 +545,17 @@ ssm_status ssm_scan_step(const ssm_scan_desc* d, const void* u, const void* delt
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 
-ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, int64_t pos,
-                                const float* x, int64_t ld_x, const float* w, const float* bias,
-                                float* ring, float* out, int64_t ld_out, cudaStream_t stream) {
-    if (batch < 0 || dinner < 0 || kconv < 1 || kconv > 8 || pos < 0) return SSM_ERR_SHAPE;
+ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, const float* x,
+                                int64_t ld_x, const float* w, const float* bias, float* conv_state,
+                                float* out, int64_t ld_out, cudaStream_t stream) {
+    if (batch < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
     ld_x = ld_x ? ld_x : dinner;
     ld_out = ld_out ? ld_out : dinner;
     if (ld_x < dinner || ld_out < dinner) return SSM_ERR_SHAPE;
     if (batch == 0 || dinner == 0) return SSM_OK;
-    if (!x || !w || !out || (kconv > 1 && !ring)) return SSM_ERR_NULL;
+    if (!x || !w || !out || (kconv > 1 && !conv_state)) return SSM_ERR_NULL;
     if (dinner % 4 || ld_x % 4 || ld_out % 4 || !aligned16(x) || !aligned16(out) ||
-        (ring && !aligned16(ring)) || (bias && !aligned16(bias)))
+        (kconv > 1 && !aligned16(conv_state)) || (bias && !aligned16(bias)))
         return SSM_ERR_ALIGN;
     ssm_status st = check_device();
     if (st != SSM_OK) return st;
@@ -563,37 +563,37 @@ ssm_status ssm_conv1d_silu_step(int32_t batch, int32_t dinner, int32_t kconv, in
     a.x = x;
     a.w = w;
     a.bias = bias;
-    a.ring = ring;
+    a.state = conv_state;
     a.out = out;
     a.batch = batch;
     a.dinner = dinner;
     a.kconv = kconv;
-    a.pos = pos;
     a.ld_x = ld_x;
     a.ld_out = ld_out;
     cudaError_t e = ssm::launch_conv_step(a, stream);
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 
-ssm_status ssm_conv1d_ring_fill(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
-                                const float* x, int64_t ld_x, float* ring, cudaStream_t stream) {
+ssm_status ssm_conv1d_state_from_prompt(int32_t batch, int32_t seqlen, int32_t dinner,
+                                        int32_t kconv, const float* x, int64_t ld_x,
+                                        float* conv_state, cudaStream_t stream) {
     if (batch < 0 || seqlen < 0 || dinner < 0 || kconv < 1 || kconv > 8) return SSM_ERR_SHAPE;
     ld_x = ld_x ? ld_x : dinner;
     if (ld_x < dinner) return SSM_ERR_SHAPE;
-    if (batch == 0 || seqlen == 0 || dinner == 0 || kconv == 1) return SSM_OK;
-    if (!x || !ring) return SSM_ERR_NULL;
-    if (dinner % 4 || ld_x % 4 || !aligned16(x) || !aligned16(ring)) return SSM_ERR_ALIGN;
+    if (batch == 0 || dinner == 0 || kconv == 1) return SSM_OK;
+    if (!conv_state || (seqlen > 0 && !x)) return SSM_ERR_NULL;
+    if (dinner % 4 || ld_x % 4 || (x && !aligned16(x)) || !aligned16(conv_state)) return SSM_ERR_ALIGN;
     ssm_status st = check_device();
     if (st != SSM_OK) return st;
-    ssm::RingFillArgs a{};
+    ssm::ConvStateFillArgs a{};
     a.x = x;
-    a.ring = ring;
+    a.state = conv_state;
     a.batch = batch;
     a.seqlen = seqlen;
     a.dinner = dinner;
     a.kconv = kconv;
     a.ld_x = ld_x;
-    cudaError_t e = ssm::launch_ring_fill(a, stream);
+    cudaError_t e = ssm::launch_conv_state_fill(a, stream);
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 

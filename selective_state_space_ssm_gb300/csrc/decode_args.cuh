@@ -25,24 +25,25 @@ struct ScanStepArgs {
     int64_t ld_u, ld_dr, ld_z, ld_B, ld_C, ld_out;
 };
 
-// One step of the causal conv1d + SiLU at sequence position pos; the kconv-1
-// previous inputs of batch row b sit in ring [batch][kconv-1][dinner], the
-// input at position p in slot p mod (kconv-1).
+// One step of the causal conv1d + SiLU; the kconv-1 previous inputs of batch
+// row b sit in state [batch][kconv-1][dinner], slot j = the input kconv-1-j
+// steps back (zeros before the sequence); the step shifts them by one.
 struct ConvStepArgs {
     const float* x;
     const float* w;        // (dinner, kconv), tap 0 = current step
     const float* bias;     // may be null
-    float* ring;
+    float* state;
     float* out;
     int batch, dinner, kconv;
-    int64_t pos, ld_x, ld_out;
+    int64_t ld_x, ld_out;
 };
 
-// Fill the ring from the last kconv-1 rows of a prompt of seqlen rows per
-// batch row (x is (batch*seqlen, dinner) with row stride ld_x).
-struct RingFillArgs {
+// The conv state that continues a prompt of seqlen rows per batch row (x is
+// (batch*seqlen, dinner) with row stride ld_x): slot j = the input at position
+// seqlen-(kconv-1)+j, zero where that is before 0.
+struct ConvStateFillArgs {
     const float* x;
-    float* ring;
+    float* state;
     int batch, seqlen, dinner, kconv;
     int64_t ld_x;
 };
@@ -50,6 +51,6 @@ struct RingFillArgs {
 cudaError_t launch_scan_step(int dtype, int nt, int disc, bool gate, const ScanStepArgs& a,
                              cudaStream_t st);
 cudaError_t launch_conv_step(const ConvStepArgs& a, cudaStream_t st);
-cudaError_t launch_ring_fill(const RingFillArgs& a, cudaStream_t st);
+cudaError_t launch_conv_state_fill(const ConvStateFillArgs& a, cudaStream_t st);
 
 }  // namespace ssm

@@ -33,6 +33,11 @@ SCAN_WORKLOADS = {
                                 seed=2, A_log_noise=0.5, clamp_frac=0.02),
     "long_scan_fp32": dict(batch=1, seqlen=65536, dinner=2048, dstate=16, dtype="f32", seed=3),
 }
+# Decode: one token per sequence through `layers` layers of the 1.4B shape
+# (conv1d+SiLU step, then scan step), fp32 activations and state.
+DECODE_WORKLOADS = {
+    "mamba1p4b_decode_fp32": dict(batch=64, dinner=4096, dstate=16, dconv=4, layers=48, seed=5),
+}
 BLOCK_WORKLOADS = {
     "mamba_block_fp32": dict(dmodel=768, dinner=1536, dtrank=48, dstate=16, dconv=4,
                              batch=8, seqlen=2048, seed=4),

@@ -232,12 +232,14 @@ def test_fwd_state_validation(lib):
 def test_conv_step_validation(lib):
     f = lib.ssm_conv1d_silu_step
     p = ctypes.c_void_p(16)
-    assert f(1, 8, 0, 0, p, 0, p, None, p, p, 0, None) == 2       # kconv 0
-    assert f(1, 8, 4, -1, p, 0, p, None, p, p, 0, None) == 2      # negative position
-    assert f(1, 6, 4, 0, p, 0, p, None, p, p, 0, None) == 3       # dinner not a multiple of 4
-    assert f(1, 8, 4, 0, p, 0, p, None, None, p, 0, None) == 1    # no ring with kconv > 1
-    assert f(0, 8, 4, 0, None, 0, None, None, None, None, 0, None) == 0
-    g = lib.ssm_conv1d_ring_fill
+    assert f(1, 8, 0, p, 0, p, None, p, p, 0, None) == 2          # kconv 0
+    assert f(1, 8, 9, p, 0, p, None, p, p, 0, None) == 2          # kconv 9
+    assert f(1, 6, 4, p, 0, p, None, p, p, 0, None) == 3          # dinner not a multiple of 4
+    assert f(1, 8, 4, p, 0, p, None, None, p, 0, None) == 1       # no state with kconv > 1
+    assert f(1, 8, 4, p, 0, p, None, ctypes.c_void_p(8), p, 0, None) == 3
+    assert f(0, 8, 4, None, 0, None, None, None, None, 0, None) == 0
+    g = lib.ssm_conv1d_state_from_prompt
     assert g(1, 5, 8, 9, p, 0, p, None) == 2
-    assert g(1, 5, 8, 1, None, 0, None, None) == 0                # no ring for kconv 1
+    assert g(1, 5, 8, 1, None, 0, None, None) == 0                # no state for kconv 1
     assert g(1, 5, 8, 4, p, 0, ctypes.c_void_p(8), None) == 3
+    assert g(1, 5, 8, 4, p, 0, None, None) == 1

@@ -1,7 +1,7 @@
 """GPU parity of the single-token decode path against the fp64 oracle:
 ssm_scan_step (one position, carried state), ssm_scan_fwd_state (prefill from
 an initial state, returning the final state), ssm_conv1d_silu_step and
-ssm_conv1d_ring_fill, alone and chained (prefill then decode)."""
+ssm_conv1d_state_from_prompt, alone and chained (prefill then decode)."""
 import numpy as np
 import pytest
 
@@ -121,7 +121,7 @@ def test_scan_fwd_state(lib, case):
 
 
 def test_prefill_then_decode(lib):
-    """Prefill a prompt (forward with final state, ring filled from the conv
+    """Prefill a prompt (forward with final state, conv state from the conv
     input), then decode the rest token by token: equals the whole sequence."""
     import torch
     Bt, P, L, D, N, K = 2, 70, 83, 64, 16, 4
@@ -140,10 +140,10 @@ def test_prefill_then_decode(lib):
     out_p, h = lib.scan_fwd_state(up, _gpu(part(inp["delta_raw"], 0, P)), A,
                                   _gpu(part(inp["B"], 0, P)), _gpu(part(inp["C"], 0, P)), Dv,
                                   _gpu(part(inp["z"], 0, P)), batch=Bt)
-    ring = lib.conv1d_ring_fill(xp, K, batch=Bt)
+    cst = lib.conv1d_state_from_prompt(xp, K, batch=Bt)
     outs = [_f64(out_p).reshape(Bt, P, D)]
     for t in range(P, L):
-        u_t = lib.conv1d_silu_step(_gpu(part(cin["x"], t, t + 1)), w, bias, ring, t)
+        u_t = lib.conv1d_silu_step(_gpu(part(cin["x"], t, t + 1)), w, bias, cst)
         o = lib.scan_step(h, u_t, _gpu(part(inp["delta_raw"], t, t + 1)), A,
                           _gpu(part(inp["B"], t, t + 1)), _gpu(part(inp["C"], t, t + 1)), Dv,
                           _gpu(part(inp["z"], t, t + 1)))
@@ -161,16 +161,20 @@ def test_conv_step(lib, K):
     ref, _ = oracle.conv1d_silu_fwd(cin["x"], cin["w"], cin["bias"], batch=Bt)
     ref = ref.reshape(Bt, L, D)
     xs = cin["x"].reshape(Bt, L, D)
-    # garbage in the ring before position 0 must not leak in
-    ring = _gpu(1e6 * np.random.default_rng(K).standard_normal((Bt, K - 1, D)))
     w, bias = _gpu(cin["w"]), _gpu(cin["bias"])
+    # a new sequence: zero state
+    cst = torch.zeros((Bt, K - 1, D), dtype=torch.float32, device="cuda")
+    ost = np.zeros((Bt, K - 1, D))
     for t in range(L):
-        o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, ring, t)
+        o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, cst)
+        _, ost = oracle.conv1d_silu_step(ost, xs[:, t], cin["w"], cin["bias"])
         torch.cuda.synchronize()
         assert parity.rel_l2(_f64(o), ref[:, t]) <= parity.TOL_FWD_F32, t
-    # the ring after a prompt of P positions continues the sequence
-    P = 11
-    ring = lib.conv1d_ring_fill(_gpu(np.ascontiguousarray(xs[:, :P].reshape(-1, D))), K, batch=Bt)
-    for t in range(P, L):
-        o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, ring, t)
-        assert parity.rel_l2(_f64(o), ref[:, t]) <= parity.TOL_FWD_F32, t
+        np.testing.assert_array_equal(_f64(cst), ost)   # the shift moves values exactly
+    # the state after a prompt of P positions continues the sequence
+    for P in (2, 11):
+        cst = lib.conv1d_state_from_prompt(_gpu(np.ascontiguousarray(xs[:, :P].reshape(-1, D))), K,
+                                           batch=Bt)
+        for t in range(P, L):
+            o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, cst)
+            assert parity.rel_l2(_f64(o), ref[:, t]) <= parity.TOL_FWD_F32, (P, t)
