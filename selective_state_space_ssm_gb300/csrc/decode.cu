@@ -57,8 +57,9 @@ __device__ __forceinline__ float silu_f(float x) { return x * rcp(1.0f + ex2(-x 
 // kStepRows batch rows of its CTA.  A log2(e) of its channels is computed once
 // (vector loads of their A_log rows) and kept in shared memory for the rows;
 // the states of the next row are loaded while the current one is computed and
-// stored, so reads and writes of the state overlap within a CTA.
-template <typename T, int NT, int DISC, bool GATE>
+// stored, so reads and writes of the state overlap within a CTA.  FULL:
+// dstate == NT, so the per-state guards and strides are compile-time.
+template <typename T, int NT, int DISC, bool GATE, bool FULL>
 __global__ void __launch_bounds__(kStepThreads, 4)
 scan_step_kernel(const ScanStepArgs a) {
     constexpr int CH = 2 * kStepThreads;          // channels per CTA
@@ -69,7 +70,7 @@ scan_step_kernel(const ScanStepArgs a) {
     const int b0 = blockIdx.y * RB;
     const int nrow = min(RB, a.batch - b0);
     const int cbase = blockIdx.x * CH;
-    const int N = a.dstate, Dn = a.dinner;
+    const int N = FULL ? NT : a.dstate, Dn = a.dinner;
     const int d0 = cbase + 2 * threadIdx.x;
     const bool active = d0 < Dn;
 
@@ -103,7 +104,7 @@ scan_step_kernel(const ScanStepArgs a) {
     if (active) {
         const float* al = a.A_log + static_cast<size_t>(d0) * N;
         auto a2 = [](float v) { return -ex2(fminf(fmaxf(v, kALogLo), kALogHi) * kLog2e) * kLog2e; };
-        if (NT == 16 && N == 16 && (reinterpret_cast<uintptr_t>(al) & 15u) == 0) {
+        if (NT == 16 && N == 16 && (reinterpret_cast<uintptr_t>(al) & 15u) == 0) {   // 8 x 16-byte loads
             float4 q[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) q[k] = reinterpret_cast<const float4*>(al)[k];
@@ -265,12 +266,20 @@ conv_state_fill_kernel(const ConvStateFillArgs a) {
 template <typename T, int NT>
 static cudaError_t launch_step_nt(int disc, bool gate, const ScanStepArgs& a, cudaStream_t st) {
     const dim3 grid((a.dinner / 2 + kStepThreads - 1) / kStepThreads, (a.batch + kStepRows - 1) / kStepRows);
+    // compile-time dstate for Euler B when the states fill NT (the ZOH path
+    // would spill with it)
+    const bool full = a.dstate == NT;
     if (disc == 0) {
-        if (gate) scan_step_kernel<T, NT, 0, true><<<grid, kStepThreads, 0, st>>>(a);
-        else scan_step_kernel<T, NT, 0, false><<<grid, kStepThreads, 0, st>>>(a);
+        if (gate) {
+            if (full) scan_step_kernel<T, NT, 0, true, true><<<grid, kStepThreads, 0, st>>>(a);
+            else scan_step_kernel<T, NT, 0, true, false><<<grid, kStepThreads, 0, st>>>(a);
+        } else {
+            if (full) scan_step_kernel<T, NT, 0, false, true><<<grid, kStepThreads, 0, st>>>(a);
+            else scan_step_kernel<T, NT, 0, false, false><<<grid, kStepThreads, 0, st>>>(a);
+        }
     } else {
-        if (gate) scan_step_kernel<T, NT, 1, true><<<grid, kStepThreads, 0, st>>>(a);
-        else scan_step_kernel<T, NT, 1, false><<<grid, kStepThreads, 0, st>>>(a);
+        if (gate) scan_step_kernel<T, NT, 1, true, false><<<grid, kStepThreads, 0, st>>>(a);
+        else scan_step_kernel<T, NT, 1, false, false><<<grid, kStepThreads, 0, st>>>(a);
     }
     return cudaGetLastError();
 }
