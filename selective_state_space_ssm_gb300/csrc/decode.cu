@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kStepThreads = 128;
 constexpr int kStepRows = 2;     // batch rows per decode-step CTA
-constexpr int kConvRows = 2;     // batch rows per conv-step thread
+constexpr int kConvRows = 4;     // batch rows per conv-step thread
 
 __device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4f(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
