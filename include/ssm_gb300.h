@@ -302,6 +302,21 @@ ssm_status ssm_conv1d_state_from_prompt(int32_t batch, int32_t seqlen, int32_t d
                                         int32_t kconv, const float* x, int64_t ld_x,
                                         float* conv_state, cudaStream_t stream);
 
+/* One decode step of the whole block (mamba1_cpu.ts mamba1CpuForward steps
+ * 1-11 at a single position): desc->seqlen must be 1 (SSM_ERR_SHAPE) and x,
+ * out are (batch, dmodel) fp32, row b = the next token of sequence b.  The
+ * conv1d and the scan continue from conv_state (batch, dconv-1, dinner) and
+ * h (batch, dstate, dinner), laid out as for ssm_conv1d_silu_step and
+ * ssm_scan_step and updated in place (zeros for new sequences).  The
+ * projections run as in ssm_block_fwd (with batch rows); workspace (16-byte
+ * aligned) must hold ssm_block_step_workspace_bytes(desc) bytes (0 for an
+ * invalid descriptor).  Other rules as ssm_block_fwd. */
+size_t ssm_block_step_workspace_bytes(const ssm_block_desc* desc);
+ssm_status ssm_block_step(const ssm_block_desc* desc, const float* x,
+                          const ssm_block_weights* weights, float* conv_state, float* h,
+                          float* out, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);
 

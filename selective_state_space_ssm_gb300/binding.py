@@ -29,6 +29,7 @@ __all__ = [
     "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "block_fwd", "block_bwd",
     "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_state_from_prompt",
+    "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -47,6 +48,7 @@ EXPORTED_SYMBOLS = (
     "ssm_device_faults", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
     "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
+    "ssm_block_step_workspace_bytes", "ssm_block_step",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -143,6 +145,10 @@ def load():
                                                     vp]),
             # batch, seqlen, dinner, kconv, x, ld_x, conv_state, stream
             "ssm_conv1d_state_from_prompt": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp]),
+            "ssm_block_step_workspace_bytes": (sz, [ctypes.POINTER(BlockDesc)]),
+            # desc, x, weights, conv_state, h, out, ws, ws_bytes, stream
+            "ssm_block_step": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
+                                              ctypes.POINTER(BlockWeights), vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -335,6 +341,18 @@ def ssm_block_fwd(desc, x, weights, out, ctx, workspace, stream=None):
     _check("ssm_block_fwd", st)
 
 
+def ssm_block_step_workspace_bytes(desc: BlockDesc) -> int:
+    return load().ssm_block_step_workspace_bytes(ctypes.byref(desc))
+
+
+def ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream=None):
+    w = _block_ptrs(BlockWeights, weights)
+    st = load().ssm_block_step(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(conv_state),
+                               _ptr(h), _ptr(out), _ptr(workspace), _nbytes(workspace),
+                               _stream(stream))
+    _check("ssm_block_step", st)
+
+
 def ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, workspace, stream=None):
     """grads: dict keyed by BLOCK_PARAM_NAMES (written)."""
     w = _block_ptrs(BlockWeights, weights)
@@ -472,6 +490,20 @@ def block_fwd(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
     ws = _bytes_tensor(ssm_block_workspace_bytes(desc), x)
     ssm_block_fwd(desc, x, weights, out, ctx, ws, stream)
     return out, ctx, ws
+
+
+def block_step(x, weights, dims, conv_state, h, *, disc=SSM_DISC_EULER, workspace=None,
+               stream=None):
+    """One decode step of the block: x (batch, dmodel); conv_state (batch,
+    dconv-1, dinner) and h (batch, dstate, dinner) fp32 are updated in place.
+    Returns out (batch, dmodel)."""
+    import torch
+    desc = block_desc(dict(dims, batch=x.shape[0], seqlen=1), disc)
+    out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if workspace is None:
+        workspace = _bytes_tensor(ssm_block_step_workspace_bytes(desc), x)
+    ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream)
+    return out
 
 
 def block_bwd(x, weights, dims, dout, ctx, *, disc=SSM_DISC_EULER, workspace=None, stream=None):

@@ -229,6 +229,36 @@ const T* at(const void* base, size_t off) {
     return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
 }
 
+// Scratch of one decode step of the block (M = batch rows of one position).
+struct StepWs {
+    size_t xn, inv, xz, u, xd, draw, g, a_hi, a_lo, w_hi, w_lo, part, part_floats, total;
+};
+StepWs step_layout(const Dims& s) {
+    const size_t f = sizeof(float), M = static_cast<size_t>(s.M);
+    const size_t deep = static_cast<size_t>(round4(std::max({int64_t(s.Dm), int64_t(s.D), int64_t(s.R)})));
+    auto wsz = [](int64_t rows, int64_t cols) { return static_cast<size_t>(rows * round4(cols)); };
+    const size_t wmax = std::max({wsz(2 * s.D, s.Dm), wsz(s.P, s.D), wsz(s.D, s.R), wsz(s.Dm, s.D)});
+    Carve c;
+    StepWs w;
+    w.xn = c.take(M * s.Dm * f);
+    w.inv = c.take(M * f);
+    w.xz = c.take(M * 2 * s.D * f);
+    w.u = c.take(M * s.D * f);
+    w.xd = c.take(M * s.P * f);
+    w.draw = c.take(M * s.D * f);
+    w.g = c.take(M * s.D * f);
+    w.a_hi = c.take(M * deep * f);
+    w.a_lo = c.take(M * deep * f);
+    w.w_hi = c.take(wmax * f);
+    w.w_lo = c.take(wmax * f);
+    const size_t biggest = std::max({M * 2 * s.D, M * static_cast<size_t>(s.Dm), M * static_cast<size_t>(s.P),
+                                     M * static_cast<size_t>(s.D)});
+    w.part_floats = std::min<size_t>(size_t(8) << 20, 4 * biggest);
+    w.part = c.take(w.part_floats * f);
+    w.total = c.off;
+    return w;
+}
+
 bool all_weights(const ssm_block_weights* w) {
     return w && w->in_proj_w && w->in_proj_b && w->conv_w && w->conv_b && w->x_proj_w && w->x_proj_b &&
            w->dt_proj_w && w->dt_proj_b && w->A_log && w->D && w->out_proj_w && w->out_proj_b && w->norm_w;
@@ -349,6 +379,79 @@ ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_bloc
         run.check(ssm_scan_fwd(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, g,
                                at<char>(ctx, c.scan), c.total - c.scan, at<char>(workspace, ws.scanf),
                                ws.total - ws.scanf, stream));
+    }
+    // 10-11. out_proj + residual
+    {
+        Op A = run.split(g, D, M, D, false, ahi, alo);
+        Op W = run.split(w->out_proj_w, D, Dm, D, false, whi, wlo);
+        run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
+    }
+    return run.status;
+}
+
+size_t ssm_block_step_workspace_bytes(const ssm_block_desc* d) {
+    Dims s;
+    if (check_desc(d, s) != SSM_OK || s.L != 1) return 0;
+    return step_layout(s).total;
+}
+
+ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
+                          float* conv_state, float* h, float* out, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (s.L != 1) return SSM_ERR_SHAPE;
+    if (s.M == 0) return SSM_OK;
+    if (!x || !out || !h || !workspace || !all_weights(w) || (s.K > 1 && !conv_state)) return SSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(h) || !aligned16(workspace) ||
+        (s.K > 1 && !aligned16(conv_state)))
+        return SSM_ERR_ALIGN;
+    const StepWs ws = step_layout(s);
+    if (workspace_bytes < ws.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+
+    const int M = static_cast<int>(s.M), Dm = s.Dm, D = s.D, N = s.N, R = s.R, P = s.P;
+    float* xn = at<float>(workspace, ws.xn);
+    float* inv = at<float>(workspace, ws.inv);
+    float* xz = at<float>(workspace, ws.xz);
+    float* u = at<float>(workspace, ws.u);
+    float* xd = at<float>(workspace, ws.xd);
+    float* draw = at<float>(workspace, ws.draw);
+    float* g = at<float>(workspace, ws.g);
+    float* ahi = at<float>(workspace, ws.a_hi);
+    float* alo = at<float>(workspace, ws.a_lo);
+    float* whi = at<float>(workspace, ws.w_hi);
+    float* wlo = at<float>(workspace, ws.w_lo);
+
+    Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
+    // 1. RMSNorm
+    run.cuda(ssm::launch_rmsnorm_fwd(x, w->norm_w, M, Dm, kRmsEps, xn, inv, stream));
+    // 2. in_proj (x_in | z)
+    {
+        Op A = run.split(xn, Dm, M, Dm, false, ahi, alo);
+        Op W = run.split(w->in_proj_w, Dm, 2 * D, Dm, false, whi, wlo);
+        run.gemm(A, W, xz, 2 * D, w->in_proj_b, nullptr, 0);
+    }
+    // 4-5. one position of the causal conv1d + SiLU from the carried conv state
+    if (run.ok())
+        run.check(ssm_conv1d_silu_step(M, D, s.K, xz, 2 * D, w->conv_w, w->conv_b, conv_state, u, D, stream));
+    // 6. x_proj -> (dt | B | C)
+    {
+        Op A = run.split(u, D, M, D, false, ahi, alo);
+        Op W = run.split(w->x_proj_w, D, P, D, false, whi, wlo);
+        run.gemm(A, W, xd, P, w->x_proj_b, nullptr, 0);
+    }
+    // 7. dt_proj -> delta_raw
+    {
+        Op A = run.split(xd, P, M, R, false, ahi, alo);
+        Op W = run.split(w->dt_proj_w, R, D, R, false, whi, wlo);
+        run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
+    }
+    // 8-9. one position of the selective scan from the carried state, SiLU(z) gate
+    if (run.ok()) {
+        ssm_scan_desc sd = scan_desc_of(s);
+        run.check(ssm_scan_step(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, h, g, stream));
     }
     // 10-11. out_proj + residual
     {

@@ -243,3 +243,16 @@ def test_conv_step_validation(lib):
     assert g(1, 5, 8, 1, None, 0, None, None) == 0                # no state for kconv 1
     assert g(1, 5, 8, 4, p, 0, ctypes.c_void_p(8), None) == 3
     assert g(1, 5, 8, 4, p, 0, None, None) == 1
+
+
+def test_block_step_validation(lib):
+    d = _bdesc(seqlen=1)
+    assert binding.ssm_block_step_workspace_bytes(d) > 0
+    assert binding.ssm_block_step_workspace_bytes(_bdesc(seqlen=2)) == 0
+    w = binding.BlockWeights()
+    p = ctypes.c_void_p(16)
+    f = lib.ssm_block_step
+    assert f(ctypes.byref(_bdesc(seqlen=2)), p, ctypes.byref(w), p, p, p, p, 1 << 30, None) == 2
+    assert f(ctypes.byref(d), p, ctypes.byref(w), p, p, p, p, 1 << 30, None) == 1   # no weights
+    assert f(ctypes.byref(_bdesc(seqlen=1, batch=0)), None, ctypes.byref(w), None, None, None, None,
+             0, None) == 0
