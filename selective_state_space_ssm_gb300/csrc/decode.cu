@@ -13,10 +13,9 @@
 // Design (GB300): a decode step touches every state once, so it is bound by
 // HBM: 2 * dstate * 4 bytes of state per (batch row, channel) against a few
 // bytes of activations.  The state is laid out [batch][dstate][dinner] so that
-// a thread owning 2 adjacent channels reads and writes one 8-byte vector per
-// state (256 contiguous bytes per warp instruction); all dstate loads of a
-// thread are issued before any arithmetic, which keeps 128 bytes per thread in
-// flight at about 80 registers (7 CTAs of 128 threads per SM).
+// the lanes of a warp (consecutive channels) read and write 128 contiguous
+// bytes per state; every state load of a row is issued before its arithmetic
+// and the next row's loads overlap the current row's work.
 #include "decode_args.cuh"
 #include "ssm_common.cuh"
 
@@ -31,101 +30,75 @@ constexpr int kConvRows = 4;     // batch rows per conv-step thread
 __device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4f(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-// 2 adjacent activations (8-byte aligned for fp32, 4-byte for bf16).
-__device__ __forceinline__ void load2(const float* p, float (&v)[2]) {
-    const float2 t = *reinterpret_cast<const float2*>(p);
-    v[0] = t.x; v[1] = t.y;
-}
-__device__ __forceinline__ void load2(const __nv_bfloat16* p, float (&v)[2]) {
-    const uint32_t t = *reinterpret_cast<const uint32_t*>(p);
-    v[0] = __uint_as_float(t << 16);
-    v[1] = __uint_as_float(t & 0xffff0000u);
-}
-__device__ __forceinline__ void store2(float* p, const float (&v)[2]) {
-    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
-}
-__device__ __forceinline__ void store2(__nv_bfloat16* p, const float (&v)[2]) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(v[0], v[1]);
-    *reinterpret_cast<__nv_bfloat162*>(p) = t;
-}
-
 __device__ __forceinline__ float silu_f(float x) { return x * rcp(1.0f + ex2(-x * kLog2e)); }
 
 }  // namespace
 
-// One thread = 2 adjacent channels, all dstate states of them, for the
-// kStepRows batch rows of its CTA.  A log2(e) of its channels is computed once
-// (vector loads of their A_log rows) and kept in shared memory for the rows;
-// the states of the next row are loaded while the current one is computed and
-// stored, so reads and writes of the state overlap within a CTA.  FULL:
-// dstate == NT, so the per-state guards and strides are compile-time.
+// One thread = one channel, all dstate states of it (in packed pairs), for the
+// kStepRows batch rows of its CTA (a 64 x 4096 batch: 1024 CTAs of 128
+// threads, 7 per SM by the 72-register budget).  A log2(e) of the channel is computed once
+// into shared memory; the next row's states are loaded while the current row
+// is computed and stored.  FULL: dstate == NT.
 template <typename T, int NT, int DISC, bool GATE, bool FULL>
-__global__ void __launch_bounds__(kStepThreads, 4)
+__global__ void __launch_bounds__(kStepThreads, 7)
 scan_step_kernel(const ScanStepArgs a) {
-    constexpr int CH = 2 * kStepThreads;          // channels per CTA
-    constexpr int AS = CH + 2;                    // padded row
+    constexpr int NP = NT / 2;                    // state pairs
     constexpr int RB = kStepRows;
-    __shared__ __align__(16) float As[NT * AS];   // A log2(e), [n][local channel]
-    __shared__ float Bs[RB][NT], Cs[RB][NT];
+    __shared__ float2 As[NP * kStepThreads];      // A log2(e), [pair][local channel]
+    __shared__ __align__(8) float Bs[RB][NT];
+    __shared__ __align__(8) float Cs[RB][NT];
     const int b0 = blockIdx.y * RB;
     const int nrow = min(RB, a.batch - b0);
-    const int cbase = blockIdx.x * CH;
     const int N = FULL ? NT : a.dstate, Dn = a.dinner;
-    const int d0 = cbase + 2 * threadIdx.x;
-    const bool active = d0 < Dn;
+    const int d = blockIdx.x * kStepThreads + threadIdx.x;
+    const bool active = d < Dn;
 
-    // one row's inputs: the states and the channels' u, delta_raw, z
     struct Row {
-        float2 h[NT];                              // (channel d0, channel d0+1) per state
-        float u[2], xr[2], z[2];
+        float2 h[NP];                              // states (2p, 2p+1)
+        float u, xr, z;
     };
     auto load_row = [&](Row& w, int b) {
-        const float* hp = a.h + static_cast<size_t>(b) * N * Dn + d0;
+        const float* hp = a.h + static_cast<size_t>(b) * N * Dn + d;
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
-            w.h[n] = n < N ? *reinterpret_cast<const float2*>(hp + static_cast<size_t>(n) * Dn)
-                           : make_float2(0.f, 0.f);
-        load2(static_cast<const T*>(a.u) + b * a.ld_u + d0, w.u);
-        load2(static_cast<const T*>(a.dr) + b * a.ld_dr + d0, w.xr);
-        if (GATE) load2(static_cast<const T*>(a.z) + b * a.ld_z + d0, w.z);
+        for (int p = 0; p < NP; ++p) {
+            w.h[p].x = 2 * p < N ? hp[static_cast<size_t>(2 * p) * Dn] : 0.0f;
+            w.h[p].y = 2 * p + 1 < N ? hp[static_cast<size_t>(2 * p + 1) * Dn] : 0.0f;
+        }
+        w.u = Act<T>::load(static_cast<const T*>(a.u) + b * a.ld_u + d);
+        w.xr = Act<T>::load(static_cast<const T*>(a.dr) + b * a.ld_dr + d);
+        w.z = GATE ? Act<T>::load(static_cast<const T*>(a.z) + b * a.ld_z + d) : 0.0f;
     };
-    // the longest loads first
     Row cur, nxt;
-    if (active) load_row(cur, b0);
+    if (active) load_row(cur, b0);                 // the longest loads first
 
-    for (int i = threadIdx.x; i < nrow * N; i += kStepThreads) {
-        const int r = i / N, n = i - r * N;
-        Bs[r][n] = Act<T>::load(static_cast<const T*>(a.B) + (b0 + r) * a.ld_B + n);
-        Cs[r][n] = Act<T>::load(static_cast<const T*>(a.C) + (b0 + r) * a.ld_C + n);
+    // the rows' B and C, zero past dstate so that packed pairs need no guard
+    for (int i = threadIdx.x; i < nrow * NT; i += kStepThreads) {
+        const int r = i / NT, n = i % NT;
+        Bs[r][n] = n < N ? Act<T>::load(static_cast<const T*>(a.B) + (b0 + r) * a.ld_B + n) : 0.0f;
+        Cs[r][n] = n < N ? Act<T>::load(static_cast<const T*>(a.C) + (b0 + r) * a.ld_C + n) : 0.0f;
     }
-    // A log2(e) = -2^(clamp(A_log) log2(e)) log2(e) of this thread's two channels
-    // (the 2N contiguous floats of their A_log rows), kept in shared memory
-    // [n][channel] for the rows; only this thread reads its entries back
+    // A log2(e) = -2^(clamp(A_log) log2(e)) log2(e) of this channel (0 past
+    // dstate: a = 1 there, and B = C = 0 keep those states at 0)
     if (active) {
-        const float* al = a.A_log + static_cast<size_t>(d0) * N;
+        const float* al = a.A_log + static_cast<size_t>(d) * N;
         auto a2 = [](float v) { return -ex2(fminf(fmaxf(v, kALogLo), kALogHi) * kLog2e) * kLog2e; };
-        if (NT == 16 && N == 16 && (reinterpret_cast<uintptr_t>(al) & 15u) == 0) {   // 8 x 16-byte loads
-            float4 q[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) q[k] = reinterpret_cast<const float4*>(al)[k];
+        if (FULL && NT == 16 && (reinterpret_cast<uintptr_t>(al) & 15u) == 0) {   // 4 x 16-byte loads
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 c0 = q[k], c1 = q[4 + k];         // states 4k..4k+3 of each channel
-                *reinterpret_cast<float2*>(&As[(4 * k + 0) * AS + 2 * threadIdx.x]) = make_float2(a2(c0.x), a2(c1.x));
-                *reinterpret_cast<float2*>(&As[(4 * k + 1) * AS + 2 * threadIdx.x]) = make_float2(a2(c0.y), a2(c1.y));
-                *reinterpret_cast<float2*>(&As[(4 * k + 2) * AS + 2 * threadIdx.x]) = make_float2(a2(c0.z), a2(c1.z));
-                *reinterpret_cast<float2*>(&As[(4 * k + 3) * AS + 2 * threadIdx.x]) = make_float2(a2(c0.w), a2(c1.w));
+                const float4 q = reinterpret_cast<const float4*>(al)[k];
+                As[(2 * k) * kStepThreads + threadIdx.x] = make_float2(a2(q.x), a2(q.y));
+                As[(2 * k + 1) * kStepThreads + threadIdx.x] = make_float2(a2(q.z), a2(q.w));
             }
         } else {
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-                if (n < N)
-                    *reinterpret_cast<float2*>(&As[n * AS + 2 * threadIdx.x]) = make_float2(a2(al[n]), a2(al[N + n]));
+            for (int p = 0; p < NP; ++p)
+                As[p * kStepThreads + threadIdx.x] =
+                    make_float2(2 * p < N ? a2(al[2 * p]) : 0.0f, 2 * p + 1 < N ? a2(al[2 * p + 1]) : 0.0f);
         }
     }
     __syncthreads();
     if (!active) return;
-    const float Dv[2] = {a.D ? a.D[d0] : 0.0f, a.D ? a.D[d0 + 1] : 0.0f};
+    const float Dv = a.D ? a.D[d] : 0.0f;
 
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
@@ -133,59 +106,52 @@ scan_step_kernel(const ScanStepArgs a) {
         const int b = b0 + r;
         if (r + 1 < nrow) load_row(nxt, b + 1);   // next row in flight during this one
 
-        float dt[2], bs[2], gz[2] = {1.0f, 1.0f};
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (GATE) {
-                float sz;
-                softplus_sigmoid(cur.xr[c], cur.z[c], dt[c], sz);
-                gz[c] = cur.z[c] * sz;                         // silu(z)
-            } else {
-                float e;
-                dt[c] = softplus_e(cur.xr[c], e);
-            }
-            bs[c] = DISC == 0 ? dt[c] * cur.u[c] : cur.u[c];   // Euler: delta*u; ZOH: u
+        float dt, gz = 1.0f;
+        if (GATE) {
+            float sz;
+            softplus_sigmoid(cur.xr, cur.z, dt, sz);
+            gz = cur.z * sz;                               // silu(z)
+        } else {
+            float e;
+            dt = softplus_e(cur.xr, e);
         }
-        // both channels at once: packed f32x2 multiplies and FMAs
-        const float2 dt2 = make_float2(dt[0], dt[1]), bs2 = make_float2(bs[0], bs[1]);
+        const float bs = DISC == 0 ? dt * cur.u : cur.u;   // Euler: delta*u; ZOH: u
+        const float2 dt2 = f2(dt), bs2 = f2(bs);
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            if (n >= N) break;
-            const float2 A2 = *reinterpret_cast<const float2*>(&As[n * AS + 2 * threadIdx.x]);  // A log2(e)
-            const float Bn = Bs[r][n], Cn = Cs[r][n];
+        for (int p = 0; p < NP; ++p) {
+            if (2 * p >= N) break;
+            const float2 A2 = As[p * kStepThreads + threadIdx.x];
+            const float2 Bp = *reinterpret_cast<const float2*>(&Bs[r][2 * p]);
+            const float2 Cp = *reinterpret_cast<const float2*>(&Cs[r][2 * p]);
             const float2 x = mul2(dt2, A2);
             const float2 av = make_float2(ex2(x.x), ex2(x.y));
             float2 bu;
             if (DISC == 0) {
-                bu = mul2(bs2, f2(Bn));
+                bu = mul2(bs2, Bp);
             } else {
                 // beta/B = expm1(delta A)/A, without cancellation for small delta A
                 float cf[2];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const float Ac = (c ? A2.y : A2.x) * kLn2;
-                    const float xn = dt[c] * Ac;
-                    const float ae = c ? av.y : av.x;
-                    cf[c] = fabsf(xn) < 0.5f ? dt[c] * phi1_series(xn) : (ae - 1.0f) / Ac;
+                for (int e = 0; e < 2; ++e) {
+                    const float Ae = (e ? A2.y : A2.x) * kLn2;
+                    const float xn = dt * Ae;
+                    const float ae = e ? av.y : av.x;
+                    cf[e] = fabsf(xn) < 0.5f ? dt * phi1_series(xn) : (Ae != 0.0f ? (ae - 1.0f) / Ae : dt);
                 }
-                bu = mul2(mul2(make_float2(cf[0], cf[1]), bs2), f2(Bn));
+                bu = mul2(mul2(make_float2(cf[0], cf[1]), bs2), Bp);
             }
-            cur.h[n] = fma2(av, cur.h[n], bu);
-            acc = fma2(f2(Cn), cur.h[n], acc);
+            cur.h[p] = fma2(av, cur.h[p], bu);
+            acc = fma2(Cp, cur.h[p], acc);
         }
-        float y[2];
-        const float accv[2] = {acc.x, acc.y};
+        const float yv = fmaf(Dv, cur.u, acc.x + acc.y);
+        float* hp = a.h + static_cast<size_t>(b) * N * Dn + d;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const float yv = fmaf(Dv[c], cur.u[c], accv[c]);
-            y[c] = GATE ? yv * gz[c] : yv;
+        for (int p = 0; p < NP; ++p) {
+            if (2 * p < N) hp[static_cast<size_t>(2 * p) * Dn] = cur.h[p].x;
+            if (2 * p + 1 < N) hp[static_cast<size_t>(2 * p + 1) * Dn] = cur.h[p].y;
         }
-        float* hp = a.h + static_cast<size_t>(b) * N * Dn + d0;
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-            if (n < N) *reinterpret_cast<float2*>(hp + static_cast<size_t>(n) * Dn) = cur.h[n];
-        store2(static_cast<T*>(a.out) + b * a.ld_out + d0, y);
+        static_cast<T*>(a.out)[b * a.ld_out + d] = Act<T>::from_f(GATE ? yv * gz : yv);
         if (r + 1 < nrow) cur = nxt;
     }
 }
@@ -265,9 +231,7 @@ conv_state_fill_kernel(const ConvStateFillArgs a) {
 
 template <typename T, int NT>
 static cudaError_t launch_step_nt(int disc, bool gate, const ScanStepArgs& a, cudaStream_t st) {
-    const dim3 grid((a.dinner / 2 + kStepThreads - 1) / kStepThreads, (a.batch + kStepRows - 1) / kStepRows);
-    // compile-time dstate for Euler B when the states fill NT (the ZOH path
-    // would spill with it)
+    const dim3 grid((a.dinner + kStepThreads - 1) / kStepThreads, (a.batch + kStepRows - 1) / kStepRows);
     const bool full = a.dstate == NT;
     if (disc == 0) {
         if (gate) {
