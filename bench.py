@@ -16,6 +16,11 @@ replicas (weak scaling): the scan has no cross-rank exchange on this path.
 
 --impl reference times the fp64 CPU oracle on the host cores (a bounded
 sample of the same workload per step) and prints the same metric.
+
+Other lines (not the benchmark's headline): --block times the whole Mamba-1
+block forward + backward on the block workload; --decode times single-token
+decode (conv1d+SiLU step + scan step of 48 layers from carried states,
+replayed from a CUDA graph) on the decode workload.
 """
 from __future__ import annotations
 

@@ -6,7 +6,10 @@
  * engine 2026.7.12 -> 2026.9.27"): the selective scan forward (mamba1CpuForward
  * steps 8-9) and backward (mamba1CpuBackward steps 9-8), and the causal
  * depthwise conv1d + SiLU (forward steps 4-5, backward steps 5-4), plus the
- * primitives of src/training/cpu_ops.ts they use (softplus, silu, sigmoid).
+ * primitives of src/training/cpu_ops.ts they use (softplus, silu, sigmoid);
+ * the whole block (steps 1-11 and their backward) with its projections on
+ * the tensor cores; and single-token decode (the same recurrences one
+ * position at a time from caller-held states).
  *
  * Conventions shared by every entry point
  * ---------------------------------------

@@ -1,6 +1,7 @@
 /*
  * ssm_oracle.c -- plain, slow, sequential fp64 CPU oracle for the Mamba-1 (S6)
- * selective scan, its causal depthwise conv1d+SiLU, and the whole Mamba-1 block.
+ * selective scan, its causal depthwise conv1d+SiLU, the whole Mamba-1 block,
+ * and their single-position (decode) forms with caller-held states.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * load this file; only the tests, the smoke check and the benchmark's CPU
