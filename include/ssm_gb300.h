@@ -305,6 +305,16 @@ ssm_status ssm_conv1d_state_from_prompt(int32_t batch, int32_t seqlen, int32_t d
                                         int32_t kconv, const float* x, int64_t ld_x,
                                         float* conv_state, cudaStream_t stream);
 
+/* ssm_block_fwd that also leaves, for every batch row, the states after the
+ * last position (prefill before ssm_block_step): conv_state (batch, dconv-1,
+ * dinner) and h (batch, dstate, dinner), each 16-byte aligned and may be NULL
+ * (not written).  The forward starts from zero states (new sequences).
+ * seqlen = 0 writes zero states.  Other arguments as ssm_block_fwd. */
+ssm_status ssm_block_fwd_state(const ssm_block_desc* desc, const float* x,
+                               const ssm_block_weights* weights, float* out,
+                               void* ctx, size_t ctx_bytes, float* conv_state, float* h,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* One decode step of the whole block (mamba1_cpu.ts mamba1CpuForward steps
  * 1-11 at a single position): desc->seqlen must be 1 (SSM_ERR_SHAPE) and x,
  * out are (batch, dmodel) fp32, row b = the next token of sequence b.  The

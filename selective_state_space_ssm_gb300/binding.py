@@ -29,7 +29,8 @@ __all__ = [
     "scan_fwd", "scan_bwd", "conv1d_silu", "conv1d_silu_bwd", "block_fwd", "block_bwd",
     "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_state_from_prompt",
-    "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step",
+    "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step", "ssm_block_fwd_state",
+    "block_fwd_state",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -48,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "ssm_device_faults", "ssm_block_ctx_bytes", "ssm_block_workspace_bytes", "ssm_block_fwd",
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
     "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
-    "ssm_block_step_workspace_bytes", "ssm_block_step",
+    "ssm_block_step_workspace_bytes", "ssm_block_step", "ssm_block_fwd_state",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -146,6 +147,10 @@ def load():
             # batch, seqlen, dinner, kconv, x, ld_x, conv_state, stream
             "ssm_conv1d_state_from_prompt": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp]),
             "ssm_block_step_workspace_bytes": (sz, [ctypes.POINTER(BlockDesc)]),
+            # desc, x, weights, out, ctx, ctx_bytes, conv_state, h, ws, ws_bytes, stream
+            "ssm_block_fwd_state": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
+                                                   ctypes.POINTER(BlockWeights), vp, vp, sz, vp, vp,
+                                                   vp, sz, vp]),
             # desc, x, weights, conv_state, h, out, ws, ws_bytes, stream
             "ssm_block_step": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
                                               ctypes.POINTER(BlockWeights), vp, vp, vp, vp, sz, vp]),
@@ -341,6 +346,14 @@ def ssm_block_fwd(desc, x, weights, out, ctx, workspace, stream=None):
     _check("ssm_block_fwd", st)
 
 
+def ssm_block_fwd_state(desc, x, weights, out, ctx, conv_state, h, workspace, stream=None):
+    w = _block_ptrs(BlockWeights, weights)
+    st = load().ssm_block_fwd_state(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(out),
+                                    _ptr(ctx), _nbytes(ctx), _ptr(conv_state), _ptr(h),
+                                    _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check("ssm_block_fwd_state", st)
+
+
 def ssm_block_step_workspace_bytes(desc: BlockDesc) -> int:
     return load().ssm_block_step_workspace_bytes(ctypes.byref(desc))
 
@@ -490,6 +503,23 @@ def block_fwd(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
     ws = _bytes_tensor(ssm_block_workspace_bytes(desc), x)
     ssm_block_fwd(desc, x, weights, out, ctx, ws, stream)
     return out, ctx, ws
+
+
+def block_fwd_state(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
+    """Prefill: the block forward over a prompt, also returning the states
+    after its last position.  Returns (out, conv_state, h): conv_state
+    (batch, dconv-1, dinner) and h (batch, dstate, dinner) fp32."""
+    import torch
+    desc = block_desc(dims, disc)
+    out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ctx = _bytes_tensor(ssm_block_ctx_bytes(desc), x)
+    ws = _bytes_tensor(ssm_block_workspace_bytes(desc), x)
+    B, D = dims["batch"], dims["dinner"]
+    conv_state = torch.empty((B, dims["dconv"] - 1, D), dtype=torch.float32, device=x.device)
+    h = torch.empty((B, dims["dstate"], D), dtype=torch.float32, device=x.device)
+    ssm_block_fwd_state(desc, x, weights, out, ctx, conv_state if dims["dconv"] > 1 else None, h, ws,
+                        stream)
+    return out, conv_state, h
 
 
 def block_step(x, weights, dims, conv_state, h, *, disc=SSM_DISC_EULER, workspace=None,

@@ -273,10 +273,10 @@ size_t ssm_scan_bwd_workspace_bytes(const ssm_scan_desc* d) {
 
 }  // extern "C"
 
-namespace {
+namespace ssm_host {
 
-// The forward behind ssm_scan_fwd (h_init = h_last = null) and
-// ssm_scan_fwd_state (ctx = null).
+// The forward behind ssm_scan_fwd (h_init = h_last = null), ssm_scan_fwd_state
+// (ctx = null) and the block's prefill.
 ssm_status scan_fwd_impl(const ssm_scan_desc* d, const void* u, const void* delta_raw,
                          const float* A_log, const void* B, const void* C, const float* D,
                          const void* z, void* out, void* ctx, size_t ctx_bytes, const float* h_init,
@@ -371,7 +371,7 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* d, const void* u, const void* delt
     return e == cudaSuccess ? SSM_OK : fail_cuda(e);
 }
 
-}  // namespace
+}  // namespace ssm_host
 
 extern "C" {
 
@@ -379,7 +379,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* d, const void* u, const void* delta
                         const float* A_log, const void* B, const void* C, const float* D,
                         const void* z, void* out, void* ctx, size_t ctx_bytes, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
-    return scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, ctx, ctx_bytes, nullptr, nullptr,
+    return ssm_host::scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, ctx, ctx_bytes, nullptr, nullptr,
                          workspace, workspace_bytes, stream);
 }
 
@@ -387,7 +387,7 @@ ssm_status ssm_scan_fwd_state(const ssm_scan_desc* d, const void* u, const void*
                               const float* A_log, const void* B, const void* C, const float* D,
                               const void* z, void* out, const float* h_init, float* h_last,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, nullptr, 0, h_init, h_last,
+    return ssm_host::scan_fwd_impl(d, u, delta_raw, A_log, B, C, D, z, out, nullptr, 0, h_init, h_last,
                          workspace, workspace_bytes, stream);
 }
 

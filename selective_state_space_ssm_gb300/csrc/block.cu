@@ -322,13 +322,34 @@ size_t ssm_block_workspace_bytes(const ssm_block_desc* d) {
     return ws_layout(s).total;
 }
 
-ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
-                         float* out, void* ctx, size_t ctx_bytes, void* workspace,
-                         size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The block forward; with conv_state / h non-null it also leaves the states
+// after the last position (prefill for ssm_block_step).
+ssm_status block_fwd_impl(const ssm_block_desc* d, const float* x, const ssm_block_weights* w, float* out,
+                          void* ctx, size_t ctx_bytes, float* conv_state, float* h, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
     Dims s;
     ssm_status st = check_desc(d, s);
     if (st != SSM_OK) return st;
-    if (s.M == 0) return SSM_OK;
+    if ((conv_state && !aligned16(conv_state)) || (h && !aligned16(h))) return SSM_ERR_ALIGN;
+    if (s.M == 0) {
+        // no position: the states of a new sequence are zero
+        if (!conv_state && !h) return SSM_OK;
+        if ((st = check_device()) != SSM_OK) return st;
+        const size_t f = sizeof(float);
+        if (conv_state && s.K > 1) {
+            cudaError_t e = cudaMemsetAsync(conv_state, 0, size_t(s.B) * (s.K - 1) * s.D * f, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+        if (h) {
+            cudaError_t e = cudaMemsetAsync(h, 0, size_t(s.B) * s.N * s.D * f, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+        return SSM_OK;
+    }
     if (!x || !out || !ctx || !workspace || !all_weights(w)) return SSM_ERR_NULL;
     if (!aligned16(x) || !aligned16(out) || !aligned16(ctx) || !aligned16(workspace))
         return SSM_ERR_ALIGN;
@@ -373,12 +394,15 @@ ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_bloc
         Op W = run.split(w->dt_proj_w, R, D, R, false, whi, wlo);
         run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
     }
-    // 8-9. selective scan with the SiLU(z) gate
+    // the conv's state after the last position (its last kconv-1 inputs)
+    if (run.ok() && conv_state)
+        run.check(ssm_conv1d_state_from_prompt(s.B, s.L, D, s.K, xz, 2 * D, conv_state, stream));
+    // 8-9. selective scan with the SiLU(z) gate (and the state after the last position)
     if (run.ok()) {
         ssm_scan_desc sd = scan_desc_of(s);
-        run.check(ssm_scan_fwd(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, g,
-                               at<char>(ctx, c.scan), c.total - c.scan, at<char>(workspace, ws.scanf),
-                               ws.total - ws.scanf, stream));
+        run.check(ssm_host::scan_fwd_impl(&sd, u, draw, w->A_log, xd + R, xd + R + N, w->D, xz + D, g,
+                                          at<char>(ctx, c.scan), c.total - c.scan, nullptr, h,
+                                          at<char>(workspace, ws.scanf), ws.total - ws.scanf, stream));
     }
     // 10-11. out_proj + residual
     {
@@ -387,6 +411,23 @@ ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_bloc
         run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
     }
     return run.status;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_block_fwd(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
+                         float* out, void* ctx, size_t ctx_bytes, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    return block_fwd_impl(d, x, w, out, ctx, ctx_bytes, nullptr, nullptr, workspace, workspace_bytes,
+                          stream);
+}
+
+ssm_status ssm_block_fwd_state(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
+                               float* out, void* ctx, size_t ctx_bytes, float* conv_state, float* h,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return block_fwd_impl(d, x, w, out, ctx, ctx_bytes, conv_state, h, workspace, workspace_bytes, stream);
 }
 
 size_t ssm_block_step_workspace_bytes(const ssm_block_desc* d) {

@@ -41,3 +41,30 @@ def test_block_decode_equals_forward(lib, case):
     got = np.stack(outs, 1).reshape(b * L, dm)
     e = parity.rel_l2(got, ref)
     assert e <= parity.TOL_FWD_F32, e
+
+
+@pytest.mark.parametrize("disc", [0, 1])
+def test_block_prefill_then_decode(lib, disc):
+    """ssm_block_fwd_state over a prompt, then ssm_block_step for the rest of
+    the sequence from the states it left: the whole sequence's block output."""
+    import torch
+    dm, di, r, n, k, b, P, L = 64, 128, 8, 16, 4, 2, 150, 156
+    inp = workloads.block_inputs(dm, di, r, n, k, b, L, seed=90 + disc, perturb=True)
+    ref = oracle.block_fwd(inp["x"], inp["weights"], inp["dims"], disc).reshape(b, L, dm)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda")
+    w = {key: g(v) for key, v in inp["weights"].items()}
+    xs = inp["x"].reshape(b, L, dm)
+    out_p, conv_state, h = lib.block_fwd_state(g(xs[:, :P].reshape(-1, dm)), w,
+                                               dict(inp["dims"], seqlen=P), disc=disc)
+    outs = [out_p.double().cpu().numpy().reshape(b, P, dm)]
+    for t in range(P, L):
+        o = lib.block_step(g(xs[:, t]), w, inp["dims"], conv_state, h, disc=disc)
+        outs.append(o.double().cpu().numpy().reshape(b, 1, dm))
+    torch.cuda.synchronize()
+    assert lib.ssm_device_faults() == 0
+    got = np.concatenate(outs, 1)
+    e = parity.rel_l2(got, ref)
+    assert e <= parity.TOL_FWD_F32, e
+    # the decoded positions alone, against the same tolerance
+    e2 = parity.rel_l2(got[:, P:], ref[:, P:])
+    assert e2 <= parity.TOL_FWD_F32, e2
