@@ -78,7 +78,8 @@ typedef enum ssm_disc { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_disc;
  *   u, delta_raw, z, out, dout, du, ddelta_raw, dz : (M, dinner), dtype
  *   B, C, dB, dC                                   : (M, dstate), dtype
  *   A_log : (dinner, dstate) fp32, packed;  D : (dinner) fp32
- * 0 <= dstate <= 16.  batch, seqlen or dinner may be 0 (empty problem). */
+ * 0 <= dstate <= 16; batch <= 65535.  batch, seqlen or dinner may be 0 (empty
+ * problem). */
 typedef struct ssm_scan_desc {
     int32_t batch, seqlen, dinner, dstate;
     int32_t dtype;  /* ssm_dtype */

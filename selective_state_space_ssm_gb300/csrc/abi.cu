@@ -125,8 +125,10 @@ ssm_status validate(const ssm_scan_desc* d, Lds& r) {
     const int64_t bcs[] = {r.B, r.C, r.dB, r.dC};
     for (int64_t v : bcs)
         if (v < N || v > (int64_t(1) << 31)) return SSM_ERR_SHAPE;
-    // every flat index must fit comfortably in 64 bits and TMA coordinates in int32
+    // every flat index must fit comfortably in 64 bits and TMA coordinates in
+    // int32; batch rows map to the grid's y dimension (at most 65535)
     if (static_cast<int64_t>(d->batch) * d->seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (d->batch > 65535) return SSM_ERR_SHAPE;
     const int64_t es = d->dtype == SSM_BF16 ? 2 : 4;
     if ((D * es) % 16 != 0) return SSM_ERR_ALIGN;
     for (int64_t v : acts)

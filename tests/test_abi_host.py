@@ -72,7 +72,7 @@ def _fwd(lib, d, ptr=16, ctx=None, ctx_bytes=0):
 @pytest.mark.parametrize("kw,status", [
     (dict(dstate=17), 2), (dict(dstate=-1), 2), (dict(batch=-1), 2), (dict(dtype=3), 4),
     (dict(disc=2), 4), (dict(dinner=6), 3), (dict(ld_u=66), 3), (dict(ld_u=32), 2),
-    (dict(ld_B=8), 2),
+    (dict(ld_B=8), 2), (dict(batch=65536, seqlen=1), 2),
 ])
 def test_scan_fwd_rejects_bad_descriptor(lib, kw, status):
     assert _fwd(lib, _desc(**kw)) == status
