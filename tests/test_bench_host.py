@@ -1,0 +1,28 @@
+"""bench.py's algorithmic byte and exponential counts (the roofline's
+numerators) against values worked out by hand from the workload shapes."""
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_scan_algorithmic_counts():
+    # B8 L2048 D4096 N16 bf16 (M = 16384 rows, 2-byte activations):
+    # forward  4 M D s (u, delta_raw, z in; out) + 2 M N s (B, C) + A_log, D
+    #        = 536870912 + 1048576 + 278528
+    # backward 7 M D s + 4 M N s + 2 (A_log, D and their gradients)
+    #        = 939524096 + 2097152 + 557056
+    fwd, bwd, exps = bench.algorithmic(dict(batch=8, seqlen=2048, dinner=4096, dstate=16, dtype="bf16"))
+    assert fwd == 538_198_016
+    assert bwd == 942_178_304
+    assert exps == 1_073_741_824     # one exp(delta A) per (row, channel, state)
+
+
+def test_decode_bytes():
+    scan, conv = bench.decode_bytes(dict(batch=64, dinner=4096, dstate=16, dconv=4))
+    # state read + written, u / delta_raw / z read and out written, B and C, A_log and D
+    assert scan == 2 * 64 * 16 * 4096 * 4 + 4 * 64 * 4096 * 4 + 2 * 64 * 16 * 4 + 4096 * 16 * 4 + 4096 * 4
+    assert scan == 38_035_456
+    # x, the 3 state slots in and out, out; taps and bias
+    assert conv == 64 * 4096 * 4 * (1 + 2 * 3 + 1) + 4096 * 4 * 4 + 4096 * 4
