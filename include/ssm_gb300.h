@@ -322,14 +322,24 @@ ssm_status ssm_block_fwd_state(const ssm_block_desc* desc, const float* x,
  * conv1d and the scan continue from conv_state (batch, dconv-1, dinner) and
  * h (batch, dstate, dinner), laid out as for ssm_conv1d_silu_step and
  * ssm_scan_step and updated in place (zeros for new sequences).  The
- * projections run as in ssm_block_fwd (with batch rows); workspace (16-byte
- * aligned) must hold ssm_block_step_workspace_bytes(desc) bytes (0 for an
- * invalid descriptor).  Other rules as ssm_block_fwd. */
+ * projections run as in ssm_block_fwd (with batch rows); weights_split, if
+ * not NULL, holds their TF32 halves made by ssm_block_split_weights for these
+ * weights (else they are split at every call).  workspace (16-byte aligned)
+ * must hold ssm_block_step_workspace_bytes(desc) bytes (0 for an invalid
+ * descriptor).  Other rules as ssm_block_fwd. */
 size_t ssm_block_step_workspace_bytes(const ssm_block_desc* desc);
 ssm_status ssm_block_step(const ssm_block_desc* desc, const float* x,
-                          const ssm_block_weights* weights, float* conv_state, float* h,
-                          float* out, void* workspace, size_t workspace_bytes,
-                          cudaStream_t stream);
+                          const ssm_block_weights* weights, const void* weights_split,
+                          float* conv_state, float* h, float* out, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/* The TF32 hi/lo halves of the four projection weights, made once for many
+ * ssm_block_step calls with the same weights (decode): split (16-byte
+ * aligned) must hold ssm_block_weights_split_bytes(desc) bytes; batch and
+ * seqlen of desc do not matter. */
+size_t ssm_block_weights_split_bytes(const ssm_block_desc* desc);
+ssm_status ssm_block_split_weights(const ssm_block_desc* desc, const ssm_block_weights* weights,
+                                   void* split, size_t split_bytes, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);

@@ -30,7 +30,8 @@ __all__ = [
     "ssm_scan_fwd_state", "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_state_from_prompt",
     "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step", "ssm_block_fwd_state",
-    "block_fwd_state",
+    "block_fwd_state", "ssm_block_weights_split_bytes", "ssm_block_split_weights",
+    "block_split_weights",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -50,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
     "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "ssm_block_step_workspace_bytes", "ssm_block_step", "ssm_block_fwd_state",
+    "ssm_block_weights_split_bytes", "ssm_block_split_weights",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -151,9 +153,14 @@ def load():
             "ssm_block_fwd_state": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
                                                    ctypes.POINTER(BlockWeights), vp, vp, sz, vp, vp,
                                                    vp, sz, vp]),
-            # desc, x, weights, conv_state, h, out, ws, ws_bytes, stream
+            # desc, x, weights, weights_split, conv_state, h, out, ws, ws_bytes, stream
             "ssm_block_step": (ctypes.c_int, [ctypes.POINTER(BlockDesc), vp,
-                                              ctypes.POINTER(BlockWeights), vp, vp, vp, vp, sz, vp]),
+                                              ctypes.POINTER(BlockWeights), vp, vp, vp, vp, vp, sz,
+                                              vp]),
+            "ssm_block_weights_split_bytes": (sz, [ctypes.POINTER(BlockDesc)]),
+            # desc, weights, split, split_bytes, stream
+            "ssm_block_split_weights": (ctypes.c_int, [ctypes.POINTER(BlockDesc),
+                                                       ctypes.POINTER(BlockWeights), vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -358,12 +365,24 @@ def ssm_block_step_workspace_bytes(desc: BlockDesc) -> int:
     return load().ssm_block_step_workspace_bytes(ctypes.byref(desc))
 
 
-def ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream=None):
+def ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream=None,
+                   weights_split=None):
     w = _block_ptrs(BlockWeights, weights)
-    st = load().ssm_block_step(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(conv_state),
-                               _ptr(h), _ptr(out), _ptr(workspace), _nbytes(workspace),
-                               _stream(stream))
+    st = load().ssm_block_step(ctypes.byref(desc), _ptr(x), ctypes.byref(w), _ptr(weights_split),
+                               _ptr(conv_state), _ptr(h), _ptr(out), _ptr(workspace),
+                               _nbytes(workspace), _stream(stream))
     _check("ssm_block_step", st)
+
+
+def ssm_block_weights_split_bytes(desc: BlockDesc) -> int:
+    return load().ssm_block_weights_split_bytes(ctypes.byref(desc))
+
+
+def ssm_block_split_weights(desc, weights, split, stream=None):
+    w = _block_ptrs(BlockWeights, weights)
+    st = load().ssm_block_split_weights(ctypes.byref(desc), ctypes.byref(w), _ptr(split),
+                                        _nbytes(split), _stream(stream))
+    _check("ssm_block_split_weights", st)
 
 
 def ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, workspace, stream=None):
@@ -522,17 +541,26 @@ def block_fwd_state(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
     return out, conv_state, h
 
 
+def block_split_weights(weights, dims, *, stream=None):
+    """The projection weights' TF32 halves for repeated block_step calls."""
+    desc = block_desc(dict(dims, seqlen=1))
+    split = _bytes_tensor(ssm_block_weights_split_bytes(desc), weights["wInProj"])
+    ssm_block_split_weights(desc, weights, split, stream)
+    return split
+
+
 def block_step(x, weights, dims, conv_state, h, *, disc=SSM_DISC_EULER, workspace=None,
-               stream=None):
+               weights_split=None, stream=None):
     """One decode step of the block: x (batch, dmodel); conv_state (batch,
     dconv-1, dinner) and h (batch, dstate, dinner) fp32 are updated in place.
+    weights_split: from block_split_weights (None: split at this call).
     Returns out (batch, dmodel)."""
     import torch
     desc = block_desc(dict(dims, batch=x.shape[0], seqlen=1), disc)
     out = torch.empty_like(x, memory_format=torch.contiguous_format)
     if workspace is None:
         workspace = _bytes_tensor(ssm_block_step_workspace_bytes(desc), x)
-    ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream)
+    ssm_block_step(desc, x, weights, conv_state, h, out, workspace, stream, weights_split)
     return out
 
 

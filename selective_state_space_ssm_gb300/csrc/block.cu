@@ -259,6 +259,30 @@ StepWs step_layout(const Dims& s) {
     return w;
 }
 
+// TF32 hi/lo halves of the four projection weights, (rows, round4(cols))
+// each, for decode steps that reuse them: in_proj (2 dinner, dmodel), x_proj
+// (dtrank + 2 dstate, dinner), dt_proj (dinner, dtrank), out_proj (dmodel,
+// dinner).
+struct SplitW {
+    size_t hi[4], lo[4], total;
+    int rows[4], cols[4];
+};
+SplitW split_layout(const Dims& s) {
+    SplitW w;
+    const int rows[4] = {2 * s.D, s.P, s.D, s.Dm};
+    const int cols[4] = {s.Dm, s.D, s.R, s.D};
+    Carve c;
+    for (int i = 0; i < 4; ++i) {
+        w.rows[i] = rows[i];
+        w.cols[i] = cols[i];
+        const size_t bytes = static_cast<size_t>(rows[i]) * round4(cols[i]) * sizeof(float);
+        w.hi[i] = c.take(bytes);
+        w.lo[i] = c.take(bytes);
+    }
+    w.total = c.off;
+    return w;
+}
+
 bool all_weights(const ssm_block_weights* w) {
     return w && w->in_proj_w && w->in_proj_b && w->conv_w && w->conv_b && w->x_proj_w && w->x_proj_b &&
            w->dt_proj_w && w->dt_proj_b && w->A_log && w->D && w->out_proj_w && w->out_proj_b && w->norm_w;
@@ -430,6 +454,30 @@ ssm_status ssm_block_fwd_state(const ssm_block_desc* d, const float* x, const ss
     return block_fwd_impl(d, x, w, out, ctx, ctx_bytes, conv_state, h, workspace, workspace_bytes, stream);
 }
 
+size_t ssm_block_weights_split_bytes(const ssm_block_desc* d) {
+    Dims s;
+    if (check_desc(d, s) != SSM_OK) return 0;
+    return split_layout(s).total;
+}
+
+ssm_status ssm_block_split_weights(const ssm_block_desc* d, const ssm_block_weights* w, void* split,
+                                   size_t split_bytes, cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (!split || !all_weights(w)) return SSM_ERR_NULL;
+    if (!aligned16(split)) return SSM_ERR_ALIGN;
+    const SplitW sw = split_layout(s);
+    if (split_bytes < sw.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+    const float* src[4] = {w->in_proj_w, w->x_proj_w, w->dt_proj_w, w->out_proj_w};
+    Run run{stream};
+    for (int i = 0; i < 4; ++i)
+        run.split(src[i], sw.cols[i], sw.rows[i], sw.cols[i], false, at<float>(split, sw.hi[i]),
+                  at<float>(split, sw.lo[i]));
+    return run.status;
+}
+
 size_t ssm_block_step_workspace_bytes(const ssm_block_desc* d) {
     Dims s;
     if (check_desc(d, s) != SSM_OK || s.L != 1) return 0;
@@ -437,8 +485,8 @@ size_t ssm_block_step_workspace_bytes(const ssm_block_desc* d) {
 }
 
 ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_block_weights* w,
-                          float* conv_state, float* h, float* out, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+                          const void* weights_split, float* conv_state, float* h, float* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Dims s;
     ssm_status st = check_desc(d, s);
     if (st != SSM_OK) return st;
@@ -448,8 +496,18 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     if (!aligned16(x) || !aligned16(out) || !aligned16(h) || !aligned16(workspace) ||
         (s.K > 1 && !aligned16(conv_state)))
         return SSM_ERR_ALIGN;
+    if (weights_split && !aligned16(weights_split)) return SSM_ERR_ALIGN;
     const StepWs ws = step_layout(s);
     if (workspace_bytes < ws.total) return SSM_ERR_WORKSPACE;
+    const SplitW sw = split_layout(s);
+    // weight operand i: the caller's halves, or split now into the workspace
+    auto weight = [&](Run& run, int i, const float* W) {
+        if (weights_split)
+            return Op{at<float>(weights_split, sw.hi[i]), at<float>(weights_split, sw.lo[i]), sw.rows[i],
+                      sw.cols[i], round4(sw.cols[i])};
+        return run.split(W, sw.cols[i], sw.rows[i], sw.cols[i], false, at<float>(workspace, ws.w_hi),
+                         at<float>(workspace, ws.w_lo));
+    };
     if ((st = check_device()) != SSM_OK) return st;
 
     const int M = static_cast<int>(s.M), Dm = s.Dm, D = s.D, N = s.N, R = s.R, P = s.P;
@@ -462,8 +520,6 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     float* g = at<float>(workspace, ws.g);
     float* ahi = at<float>(workspace, ws.a_hi);
     float* alo = at<float>(workspace, ws.a_lo);
-    float* whi = at<float>(workspace, ws.w_hi);
-    float* wlo = at<float>(workspace, ws.w_lo);
 
     Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
     // 1. RMSNorm
@@ -471,7 +527,7 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     // 2. in_proj (x_in | z)
     {
         Op A = run.split(xn, Dm, M, Dm, false, ahi, alo);
-        Op W = run.split(w->in_proj_w, Dm, 2 * D, Dm, false, whi, wlo);
+        Op W = weight(run, 0, w->in_proj_w);
         run.gemm(A, W, xz, 2 * D, w->in_proj_b, nullptr, 0);
     }
     // 4-5. one position of the causal conv1d + SiLU from the carried conv state
@@ -480,13 +536,13 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     // 6. x_proj -> (dt | B | C)
     {
         Op A = run.split(u, D, M, D, false, ahi, alo);
-        Op W = run.split(w->x_proj_w, D, P, D, false, whi, wlo);
+        Op W = weight(run, 1, w->x_proj_w);
         run.gemm(A, W, xd, P, w->x_proj_b, nullptr, 0);
     }
     // 7. dt_proj -> delta_raw
     {
         Op A = run.split(xd, P, M, R, false, ahi, alo);
-        Op W = run.split(w->dt_proj_w, R, D, R, false, whi, wlo);
+        Op W = weight(run, 2, w->dt_proj_w);
         run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
     }
     // 8-9. one position of the selective scan from the carried state, SiLU(z) gate
@@ -497,7 +553,7 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     // 10-11. out_proj + residual
     {
         Op A = run.split(g, D, M, D, false, ahi, alo);
-        Op W = run.split(w->out_proj_w, D, Dm, D, false, whi, wlo);
+        Op W = weight(run, 3, w->out_proj_w);
         run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
     }
     return run.status;

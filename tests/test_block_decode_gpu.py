@@ -29,18 +29,24 @@ def test_block_decode_equals_forward(lib, case):
     ref = oracle.block_fwd(inp["x"], inp["weights"], inp["dims"], disc)
     g = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda")
     w = {key: g(v) for key, v in inp["weights"].items()}
-    conv_state = torch.zeros((b, k - 1, di), dtype=torch.float32, device="cuda")
-    h = torch.zeros((b, n, di), dtype=torch.float32, device="cuda")
     xs = inp["x"].reshape(b, L, dm)
-    outs = []
-    for t in range(L):
-        o = lib.block_step(g(xs[:, t]), w, inp["dims"], conv_state, h, disc=disc)
-        outs.append(o.double().cpu().numpy())
-    torch.cuda.synchronize()
-    assert lib.ssm_device_faults() == 0
-    got = np.stack(outs, 1).reshape(b * L, dm)
-    e = parity.rel_l2(got, ref)
-    assert e <= parity.TOL_FWD_F32, e
+    split = lib.block_split_weights(w, inp["dims"])
+    runs = []
+    for ws in (None, split):            # weights split at each call, or once beforehand
+        conv_state = torch.zeros((b, k - 1, di), dtype=torch.float32, device="cuda")
+        h = torch.zeros((b, n, di), dtype=torch.float32, device="cuda")
+        outs = []
+        for t in range(L):
+            o = lib.block_step(g(xs[:, t]), w, inp["dims"], conv_state, h, disc=disc, weights_split=ws)
+            outs.append(o.double().cpu().numpy())
+        torch.cuda.synchronize()
+        assert lib.ssm_device_faults() == 0
+        got = np.stack(outs, 1).reshape(b * L, dm)
+        e = parity.rel_l2(got, ref)
+        assert e <= parity.TOL_FWD_F32, e
+        runs.append(got)
+    # the same halves either way: identical bits
+    assert np.array_equal(runs[0], runs[1])
 
 
 @pytest.mark.parametrize("disc", [0, 1])
