@@ -304,3 +304,32 @@ def block_bwd(x, weights, dims, dout, disc=EULER):
                                   _p(dx), ctypes.byref(gptrs))
     _check(rc, "block_bwd")
     return dx, grads
+
+
+def stack_fwd(x, layers, dims, disc=EULER):
+    """A stack of blocks, as the pages' model runs its layers (the LM's
+    embedding, final norm and head aside): hidden_0 = x, hidden_{i+1} =
+    block_i(hidden_i), each block with its own residual.  layers: one weight
+    dict per layer.  Returns (out, hidden_in) with hidden_in[i] the input of
+    layer i (what a checkpointed backward keeps)."""
+    hidden_in = []
+    h = _f64(x)
+    for w in layers:
+        hidden_in.append(h)
+        h = block_fwd(h, w, dims, disc)
+    return h, hidden_in
+
+
+def stack_bwd(x, layers, dims, dout, disc=EULER):
+    """Backward through the stack, layers last to first, each layer's forward
+    recomputed from its saved input (the pages' activation checkpointing; the
+    oracle's block backward always recomputes its own forward, so keeping the
+    caches would give the same numbers).  Returns (dx, grads) with grads[i]
+    the gradient dict of layer i."""
+    _, hidden_in = stack_fwd(x, layers, dims, disc)
+    d = _f64(dout)
+    grads = [None] * len(layers)
+    for i in range(len(layers) - 1, -1, -1):
+        d, grads[i] = block_bwd(hidden_in[i], layers[i], dims, d, disc)
+    return d, grads
+

@@ -331,3 +331,33 @@ def test_block_backward_finite_differences(disc):
         n = w[name].size
         _fd_check(loss_w, {name: w[name].copy()}, name, grads[name],
                   range(n) if n <= 12 else rng.choice(n, 12, False))
+
+
+# ---------------------------------------------------------------- layer stack
+
+def test_stack_backward_finite_differences():
+    """Two blocks stacked (the pages' layer loop with activation checkpointing):
+    the chain rule through both layers against central differences of the
+    stacked forward, for the input and a parameter of each layer."""
+    x, w0, dout = _tiny_block(6)
+    _, w1, _ = _tiny_block(7)
+    layers = [w0, w1]
+    dx, grads = oracle.stack_bwd(x, layers, TINY_BLOCK, dout, EULER)
+    rng = np.random.default_rng(9)
+
+    def loss_x(a):
+        return float((oracle.stack_fwd(a["x"], layers, TINY_BLOCK, EULER)[0] * dout).sum())
+
+    _fd_check(loss_x, {"x": x}, "x", dx, rng.choice(x.size, 12, False))
+    for li, name in ((0, "wInProj"), (0, "A_log"), (1, "wXProj"), (1, "normWeight")):
+        def loss_w(a, li=li, name=name):
+            ls = [dict(w) for w in layers]
+            ls[li][name] = a[name]
+            return float((oracle.stack_fwd(x, ls, TINY_BLOCK, EULER)[0] * dout).sum())
+
+        _fd_check(loss_w, {name: layers[li][name]}, name, grads[li][name],
+                  rng.choice(layers[li][name].size, 6, False))
+    # one layer is the block itself
+    out1, hin = oracle.stack_fwd(x, [w0], TINY_BLOCK, EULER)
+    np.testing.assert_array_equal(out1, oracle.block_fwd(x, w0, TINY_BLOCK, EULER))
+    np.testing.assert_array_equal(hin[0], x)
