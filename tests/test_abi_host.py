@@ -260,3 +260,34 @@ def test_block_step_validation(lib):
     sizes = [(2 * 128, 64), (8 + 2 * 16, 128), (128, 8), (64, 128)]
     assert binding.ssm_block_weights_split_bytes(d) == sum(2 * _a256(r * c * 4) for r, c in sizes)
     assert lib.ssm_block_split_weights(ctypes.byref(d), ctypes.byref(w), p, 1 << 30, None) == 1
+
+
+def test_block_fwd_state_validation(lib):
+    p = ctypes.c_void_p(256)
+    w = _weights(256)
+    big = 1 << 40
+
+    def fwd(d, conv_state=p, h=p):
+        return lib.ssm_block_fwd_state(ctypes.byref(d), p, ctypes.byref(w), p, p, big, conv_state, h,
+                                       p, big, None)
+
+    assert fwd(_bdesc(), h=ctypes.c_void_p(264)) == 3            # state not 16-byte aligned
+    assert fwd(_bdesc(), conv_state=ctypes.c_void_p(260)) == 3
+    assert fwd(_bdesc(dstate=17)) == 2
+    # no position and no state asked for: nothing to do
+    assert fwd(_bdesc(seqlen=0), conv_state=None, h=None) == 0
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert fwd(_bdesc()) == 7
+        assert fwd(_bdesc(seqlen=0)) == 7                        # zero states need the device
+
+
+def test_scan_fwd_state_empty_and_sizes(lib):
+    p = ctypes.c_void_p(16)
+    f = lambda d, hi, hl: lib.ssm_scan_fwd_state(ctypes.byref(d), p, p, p, p, p, None, None, p,
+                                                 hi, hl, None, 0, None)
+    # an empty batch or no channels: nothing to copy, no device needed
+    assert f(_desc(batch=0, seqlen=0), p, p) == 0
+    assert f(_desc(dinner=0), p, p) == 0
+    # no final state asked for and no rows: nothing to do
+    assert f(_desc(seqlen=0), p, None) == 0
