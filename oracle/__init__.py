@@ -89,10 +89,13 @@ def _load():
             lib.ssm_oracle_scan_fwd_state.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp,
                                                       _dp, _dp, _dp]
             lib.ssm_oracle_conv1d_silu_step.argtypes = [i, i, i, _dp, _dp, _dp, _dp, _dp]
+            lib.ssm_oracle_linear_fwd.argtypes = [l, i, i, _dp, _dp, _dp, _dp]
+            lib.ssm_oracle_rmsnorm_fwd.argtypes = [l, i, _dp, _dp, _dp, _dp]
             for fn in ("ssm_oracle_scan_chain", "ssm_oracle_scan_fwd", "ssm_oracle_scan_bwd",
                        "ssm_oracle_conv1d_silu_fwd", "ssm_oracle_conv1d_silu_bwd",
                        "ssm_oracle_block_fwd", "ssm_oracle_block_bwd", "ssm_oracle_scan_step",
-                       "ssm_oracle_scan_fwd_state", "ssm_oracle_conv1d_silu_step"):
+                       "ssm_oracle_scan_fwd_state", "ssm_oracle_conv1d_silu_step",
+                       "ssm_oracle_linear_fwd", "ssm_oracle_rmsnorm_fwd"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -270,6 +273,31 @@ def conv1d_silu_step(state, x, w, bias):
                                          _p(out))
     _check(rc, "conv1d_silu_step")
     return out, sn
+
+
+def linear_fwd(X, W, b=None):
+    """cpu_ops.ts linearForward: Y (M, Nout) = X (M, K) W^T + b with W (Nout, K)
+    (the routine the block oracle calls for its four projections)."""
+    lib = _load()
+    X, W = _f64(X), _f64(W)
+    bb = None if b is None else _f64(b)
+    M, K = X.shape
+    Nout = W.shape[0]
+    Y = np.empty((M, Nout))
+    _check(lib.ssm_oracle_linear_fwd(M, K, Nout, _p(X), _p(W), _p(bb), _p(Y)), "linear_fwd")
+    return Y
+
+
+def rmsnorm_fwd(x, w):
+    """cpu_ops.ts rmsNormForward: inv = 1/sqrt(mean(x^2) + 1e-6) per row,
+    y = x * inv * w (the routine the block oracle calls).  Returns (y, inv)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    M, Dm = x.shape
+    y = np.empty_like(x)
+    inv = np.empty(M)
+    _check(lib.ssm_oracle_rmsnorm_fwd(M, Dm, _p(x), _p(w), _p(y), _p(inv)), "rmsnorm_fwd")
+    return y, inv
 
 
 def _block_args(dims, weights):

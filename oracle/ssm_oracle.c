@@ -443,6 +443,21 @@ static void rmsnorm_fwd_(const double* x, const double* w, size_t M, int Dm,
     }
 }
 
+/* Exported for the pins of the block's primitives (cpu_ops.ts linearForward
+ * and rmsNormForward): the same routines the block forward calls. */
+int ssm_oracle_linear_fwd(long M, int K, int Nout, const double* X, const double* W,
+                          const double* b, double* Y) {
+    if (M < 0 || K < 0 || Nout < 0) return 1;
+    linear_fwd_(X, W, b, (size_t)M, K, Nout, Y);
+    return 0;
+}
+int ssm_oracle_rmsnorm_fwd(long M, int Dm, const double* x, const double* w, double* y,
+                           double* inv) {
+    if (M < 0 || Dm <= 0) return 1;
+    rmsnorm_fwd_(x, w, (size_t)M, Dm, y, inv);
+    return 0;
+}
+
 /* cpu_ops.ts rmsNormBackward: dx and dw added into. */
 static void rmsnorm_bwd_(const double* dY, const double* x, const double* w, const double* inv,
                          size_t M, int Dm, double* dx, double* dw) {

@@ -361,3 +361,54 @@ def test_stack_backward_finite_differences():
     out1, hin = oracle.stack_fwd(x, [w0], TINY_BLOCK, EULER)
     np.testing.assert_array_equal(out1, oracle.block_fwd(x, w0, TINY_BLOCK, EULER))
     np.testing.assert_array_equal(hin[0], x)
+
+
+# ---------------------------------------------------------------- block primitives
+# cpu_ops.ts linearForward / rmsNormForward (page "@seanhogg/builderforce-memory-
+# engine 2026.7.14 -> 2026.9.28"), pinned by a hand-worked product and by
+# properties the definition fixes (not by re-typing it).
+
+def test_linear_hand_worked_example():
+    # Y = X W^T + b with W stored (out, in): worked by hand
+    X = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]])
+    W = np.array([[1.0, 0.0, -1.0], [2.0, 1.0, 0.0]])
+    b = np.array([10.0, -1.0])
+    np.testing.assert_array_equal(oracle.linear_fwd(X, W, b), [[8.0, 3.0], [8.0, 12.0]])
+    np.testing.assert_array_equal(oracle.linear_fwd(X, W), [[-2.0, 4.0], [-2.0, 13.0]])
+    # one output feature picks one input column: W = e_k rows
+    E = np.eye(3)[[2, 0]]
+    np.testing.assert_array_equal(oracle.linear_fwd(X, E), X[:, [2, 0]])
+
+
+def test_rmsnorm_mean_square_of_output():
+    # with unit weight every output row has mean square ms / (ms + eps), ms = mean(x^2)
+    rng = np.random.default_rng(3)
+    eps = 1e-6
+    for scale in (1e-4, 1e-3, 3e-3, 1.0, 50.0):
+        x = rng.normal(size=(5, 24)) * scale
+        y, inv = oracle.rmsnorm_fwd(x, np.ones(24))
+        ms = (x * x).mean(-1)
+        np.testing.assert_allclose((y * y).mean(-1), ms / (ms + eps), rtol=1e-12)
+        np.testing.assert_allclose(inv * inv * (ms + eps), 1.0, rtol=1e-12)
+
+
+def test_rmsnorm_constant_row():
+    # a row of equal values c gives w * c / sqrt(c^2 + eps), whatever the width
+    w = np.array([0.5, -2.0, 1.0, 3.0, 0.25])
+    for c in (1e-3, -2.5, 4e-4):
+        y, _ = oracle.rmsnorm_fwd(np.full((1, 5), c), w)
+        np.testing.assert_allclose(y[0], w * c / math.sqrt(c * c + 1e-6), rtol=1e-13)
+
+
+def test_rmsnorm_weight_scales_each_feature_and_scale_invariance():
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(6, 16))
+    w = rng.normal(size=16)
+    y1, _ = oracle.rmsnorm_fwd(x, np.ones(16))
+    yw, _ = oracle.rmsnorm_fwd(x, w)
+    np.testing.assert_allclose(yw, y1 * w, rtol=1e-14, atol=0)
+    # far from the eps term the output does not depend on the input's scale
+    y1000, _ = oracle.rmsnorm_fwd(1000.0 * x, w)
+    np.testing.assert_allclose(y1000, yw, rtol=2e-6)
+    ym, _ = oracle.rmsnorm_fwd(-x, w)
+    np.testing.assert_array_equal(ym, -yw)
