@@ -42,8 +42,12 @@ if ROOT not in sys.path:
 METRIC = "Mamba-1 selective scan fwd+bwd Mtokens/s; achieved % of HBM/SFU roofline"
 WORKLOAD = "mamba1p4b_scan_bf16"
 SM_COUNT = 152
-EX2_PER_CLK_PER_SM = 32          # MUFU ex2 rate of sm_103, measured with a dependency-free ex2 loop
-FP32_LANES_PER_CLK_PER_SM = 128  # FFMA lanes (packed f32x2 does not raise it)
+PIPE_RATES = os.path.join(ROOT, "profiles", "pipe_rates_gb300.json")
+# Used only when the committed pipe-rate measurement is absent (then labelled
+# "assumed" in the line): MUFU ex2 and fp32 FFMA lanes per clock per SM.
+EX2_PER_CLK_PER_SM_ASSUMED = 32.0
+FP32_LANES_PER_CLK_PER_SM_ASSUMED = 128.0
+CLOCK_WINDOW_S = 0.6             # minimum span of clock samples around a timed region
 
 
 def parse():
@@ -65,6 +69,10 @@ def parse():
     p.add_argument("--decode", action="store_true",
                    help="time single-token decode (conv1d+SiLU step + scan step per layer) on "
                         "the decode workload instead of the scan step")
+    p.add_argument("--measure-pipes", metavar="OUT_JSON", default=None,
+                   help="measure the MUFU ex2 and fp32 FFMA / FFMA2 rates of the GPU with the "
+                        "library's probe kernels (CUDA events + sampled SM clock), write them "
+                        "to OUT_JSON and print them")
     return p.parse_args()
 
 
@@ -89,6 +97,18 @@ def max_over_ranks(ms, ws, device):
 def whole_job_rate(tokens_per_rank, ws, ms):
     """Mtokens/s of the whole job: all ranks' tokens over the slowest rank's time."""
     return ws * tokens_per_rank / (ms * 1e-3) / 1e6
+
+
+def pipe_rates():
+    """Per-SM, per-clock MUFU ex2 and fp32 FFMA lane rates: the committed
+    measurement (bench.py --measure-pipes) if present, else the assumed values."""
+    try:
+        with open(PIPE_RATES) as f:
+            rec = json.load(f)
+        return (float(rec["ex2_per_clk_per_sm"]), float(rec["ffma_lanes_per_clk_per_sm"]),
+                f"measured ({os.path.relpath(PIPE_RATES, ROOT)})")
+    except (OSError, ValueError, KeyError):
+        return EX2_PER_CLK_PER_SM_ASSUMED, FP32_LANES_PER_CLK_PER_SM_ASSUMED, "assumed"
 
 
 def measured_peaks():
@@ -144,9 +164,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.perf_counter(), line.strip()))
 
-    def window(self, t0, t1):
-        """Keep only the samples read between host times t0 and t1."""
+    def window(self, t0, t1, timed=None):
+        """Keep only the samples read between host times t0 and t1; `timed`
+        (a, b) is the timed region inside it, whose samples are also counted."""
         self.t0, self.t1 = t0, t1
+        self.timed = timed
 
     def stop(self):
         if self.proc is None:
@@ -159,6 +181,8 @@ class ClockSampler:
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         t0, t1 = getattr(self, "t0", -math.inf), getattr(self, "t1", math.inf)
+        timed = getattr(self, "timed", None)
+        n_timed = 0
         for ts, ln in self.lines:
             if not t0 <= ts <= t1:
                 continue
@@ -170,12 +194,31 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            if timed and timed[0] <= ts <= timed[1]:
+                n_timed += 1
             for nm, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        res = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if timed:
+            res["samples_in_timed_region"] = n_timed
+        return res
+
+
+def clock_soak(step, sync, t_start, min_span=CLOCK_WINDOW_S):
+    """Repeat `step` (untimed) until at least min_span seconds have passed
+    since t_start, so that a short timed region still gets clock samples of
+    the same load right after it.  Returns the soak's end time."""
+    n = 0
+    while time.perf_counter() - t_start < min_span:
+        step()
+        n += 1
+        if n % 8 == 0:
+            sync()
+    sync()
+    return time.perf_counter()
 
 
 # ----------------------------------------------------------------- traffic record
@@ -332,8 +375,17 @@ def run_gb300(args):
         ev[i][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
-    clocks.window(h0 + 0.05, time.perf_counter())
+    h1 = time.perf_counter()
+
+    def step_untimed():
+        fwd()
+        bwd()
+
+    h2 = clock_soak(step_untimed, torch.cuda.synchronize, h0)
+    clocks.window(h0, h2, timed=(h0, h1))
     clk = clocks.stop()
+    clk["window"] = (f"nvidia-smi every 50 ms over the timed region ({h1 - h0:.3f} s) and an "
+                     f"untimed repeat of the same step right after it, {h2 - h0:.3f} s in all")
     barrier()
     ms_total = start.elapsed_time(end)
     t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
@@ -347,8 +399,10 @@ def run_gb300(args):
     # ---- roofline (spec definition: max(bytes / HBM, exps / SFU) per pass)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
-    sm_mhz = clk["sm_mhz"] or float(peaks.get("sm_max_mhz", 2070.0))
-    sfu_rate = EX2_PER_CLK_PER_SM * SM_COUNT * sm_mhz * 1e6      # ex2 / s
+    ex2_clk, ffma_clk, rate_kind = pipe_rates()
+    clock_known = bool(clk.get("sm_mhz"))
+    sm_mhz = clk["sm_mhz"] if clock_known else float(peaks.get("sm_max_mhz", 2070.0))
+    sfu_rate = ex2_clk * SM_COUNT * sm_mhz * 1e6                 # ex2 / s
     fwd_b, bwd_b, exps = algorithmic(cfg)
     bound_fwd = max(fwd_b / (hbm * 1e9), exps / sfu_rate)
     bound_bwd = max(bwd_b / (hbm * 1e9), exps / sfu_rate)
@@ -365,7 +419,12 @@ def run_gb300(args):
         "frac": round(achieved_bwd / peak_bwd, 4),
         "traffic": traffic,
         "peak_source": f"{peak_kind} hbm_gbs" if bwd_hbm_bound else
-                       f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {SM_COUNT} SMs x {sm_mhz:.0f} MHz",
+                       f"{rate_kind} {ex2_clk:.1f} ex2/clk/SM x {SM_COUNT} SMs x {sm_mhz:.0f} MHz",
+        "sfu_rate": {"ex2_per_clk_per_sm": ex2_clk, "source": rate_kind, "sm_mhz": sm_mhz,
+                     "clock": "median sampled" if clock_known else
+                              "NOT SAMPLED: max clock assumed, SFU terms invalid"},
+        "valid": clock_known,
+        "step_ms_x_mhz": round((t_fwd + t_bwd) * sm_mhz, 1),
         "step_frac": round((bound_fwd + bound_bwd) / ((t_fwd + t_bwd) * 1e-3), 4),
         "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4),
         "fwd_frac": round(bound_fwd / (t_fwd * 1e-3), 4),
@@ -527,7 +586,14 @@ def run_block(args):
         bwd()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    clocks.window(h0 + 0.05, time.perf_counter())
+    h1 = time.perf_counter()
+
+    def step_untimed():
+        fwd()
+        bwd()
+
+    h2 = clock_soak(step_untimed, torch.cuda.synchronize, h0)
+    clocks.window(h0, h2, timed=(h0, h1))
     clk = clocks.stop()
     if ssm.ssm_device_faults():
         raise RuntimeError("kernel wait timeout in the timed region")
@@ -690,7 +756,7 @@ def run_decode(args):
     ms_step = timed(g_step.replay, Kst)
     ms_scans = timed(g_scan.replay, Kst)
     ms_eager = timed(step, max(1, Kst // 5))
-    clocks.window(h0 + 0.05, time.perf_counter())
+    clocks.window(h0, time.perf_counter())
     clk = clocks.stop()
     ms_scan_launch = ms_scans / NL
     value = Bn / (ms_step * 1e-3)
@@ -730,6 +796,67 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- pipe rates
+
+def run_measure_pipes(args):
+    """MUFU ex2, fp32 FFMA and packed FFMA2 lane-operations per clock per SM,
+    from the library's probe kernels (ssm_probe_pipe): each kind launched
+    repeatedly for about half a second, timed with CUDA events, divided by the
+    SM count and the median SM clock sampled meanwhile."""
+    import torch
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    ssm.load()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = nsm * 8                       # 8 CTAs of 256 threads: 64 warps per SM
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {"gpu_name": torch.cuda.get_device_name(dev), "sm_count": nsm}
+    for kind, name, iters in ((0, "ex2", 4096), (1, "ffma", 16384), (2, "ffma2", 16384)):
+        for _ in range(3):
+            ssm.ssm_probe_pipe(kind, blocks, iters, sink, stream)
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        times = []
+        h0 = time.perf_counter()
+        while time.perf_counter() - h0 < 0.6:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ssm.ssm_probe_pipe(kind, blocks, iters, sink, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        clocks.window(h0, time.perf_counter())
+        clk = clocks.stop()
+        ops = blocks * 256 * iters * 8
+        ms = statistics.median(times)
+        mhz = clk["sm_mhz"]
+        per_clk = ops / (ms * 1e-3) / (mhz * 1e6) / nsm if mhz else None
+        res[name] = {"lane_ops_per_launch": ops, "median_ms": round(ms, 4), "launches": len(times),
+                     "per_s": ops / (ms * 1e-3), "sm_mhz_median": mhz,
+                     "per_clk_per_sm": round(per_clk, 2) if per_clk else None,
+                     "clock_reasons": clk["reasons"], "clock_samples": clk["samples"]}
+    res["ex2_per_clk_per_sm"] = res["ex2"]["per_clk_per_sm"]
+    res["ffma_lanes_per_clk_per_sm"] = res["ffma"]["per_clk_per_sm"]
+    res["ffma2_lanes_per_clk_per_sm"] = res["ffma2"]["per_clk_per_sm"]
+    res["how"] = ("ssm_probe_pipe: CTAs of 256 threads (8 per SM), each thread 8 independent "
+                  "chains (ex2: x <- 2^-x; ffma: x <- a x + b; ffma2: the same on 4 packed pairs); "
+                  "median CUDA-event time per launch over about 0.6 s, divided by the SM count and "
+                  "the median SM clock nvidia-smi read meanwhile")
+    res["command"] = "python bench.py --measure-pipes OUT_JSON"
+    if args.measure_pipes:
+        with open(args.measure_pipes, "w") as f:
+            json.dump(res, f, indent=1)
+    print(json.dumps(res), flush=True)
+
+
 # ----------------------------------------------------------------- reference leg
 
 def run_reference(args):
@@ -767,6 +894,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.measure_pipes:
+        run_measure_pipes(args)
     elif args.block:
         run_block(args)
     elif args.decode:

@@ -235,8 +235,10 @@ ssm_status ssm_block_bwd(const ssm_block_desc* desc, const float* x,
  *    exceed 2^21 (8 MiB); larger problems return SSM_ERR_WORKSPACE and launch
  *    nothing.
  *  - The first call on a device looks up the scratch's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture.
+ *    device and CUDA context, with that device current); make that first call
+ *    before any stream capture.  A call after the context was destroyed and
+ *    made again (cudaDeviceReset, or the primary context released and
+ *    retained anew) looks the address up again, since the array may have moved.
  *  - Every call on a device shares the one scratch array, and it keeps the
  *    last call's contents; each call writes every partial it reads, so nothing
  *    has to start at zero.  Calls that overlap on the GPU (for example on two
@@ -340,6 +342,19 @@ ssm_status ssm_block_step(const ssm_block_desc* desc, const float* x,
 size_t ssm_block_weights_split_bytes(const ssm_block_desc* desc);
 ssm_status ssm_block_split_weights(const ssm_block_desc* desc, const ssm_block_weights* weights,
                                    void* split, size_t split_bytes, cudaStream_t stream);
+
+/* ---- Measurement helper (no counterpart in the pages) ------------------
+ * Throughput probe of one arithmetic pipe, used by the benchmark to measure
+ * the rates its roofline divides by: kind 0 = MUFU ex2 (ex2.approx.ftz.f32),
+ * 1 = scalar fp32 FFMA, 2 = packed f32x2 FFMA2.  Launches `blocks` CTAs of
+ * 256 threads; each thread runs 8 independent dependency chains (4 packed
+ * pairs for kind 2) of `iters` steps, i.e. blocks*256*iters*8 lane-operations,
+ * and writes one float per thread to sink (blocks*256 floats, device).  The
+ * caller times the launch (CUDA events) and reads the SM clock.  Returns
+ * SSM_ERR_SHAPE for a kind outside 0..2 or non-positive sizes, SSM_ERR_NULL
+ * for a NULL sink, SSM_ERR_LAUNCH if the launch fails. */
+ssm_status ssm_probe_pipe(int32_t kind, int32_t blocks, int32_t iters, float* sink,
+                          cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ssm_status_string(ssm_status status);

@@ -31,12 +31,17 @@ __all__ = [
     "scan_fwd_state", "scan_step", "conv1d_silu_step", "conv1d_state_from_prompt",
     "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step", "ssm_block_fwd_state",
     "block_fwd_state", "ssm_block_weights_split_bytes", "ssm_block_split_weights",
-    "block_split_weights",
+    "block_split_weights", "ssm_conv1d_silu_bwd_noalloc", "ssm_probe_pipe",
+    "SSM_OK", "SSM_ERR_NULL", "SSM_ERR_SHAPE", "SSM_ERR_ALIGN", "SSM_ERR_DTYPE",
+    "SSM_ERR_WORKSPACE", "SSM_ERR_LAUNCH", "SSM_ERR_DEVICE",
     "EXPORTED_SYMBOLS",
 ]
 
 SSM_F32, SSM_BF16 = 0, 1
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
+# ssm_status codes (include/ssm_gb300.h)
+(SSM_OK, SSM_ERR_NULL, SSM_ERR_SHAPE, SSM_ERR_ALIGN, SSM_ERR_DTYPE, SSM_ERR_WORKSPACE,
+ SSM_ERR_LAUNCH, SSM_ERR_DEVICE) = range(8)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libssm_gb300.so"
@@ -51,7 +56,8 @@ EXPORTED_SYMBOLS = (
     "ssm_block_bwd", "ssm_linear_workspace_bytes", "ssm_linear_fwd", "ssm_scan_fwd_state",
     "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "ssm_block_step_workspace_bytes", "ssm_block_step", "ssm_block_fwd_state",
-    "ssm_block_weights_split_bytes", "ssm_block_split_weights",
+    "ssm_block_weights_split_bytes", "ssm_block_split_weights", "ssm_conv1d_silu_bwd_noalloc",
+    "ssm_probe_pipe",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -161,6 +167,12 @@ def load():
             # desc, weights, split, split_bytes, stream
             "ssm_block_split_weights": (ctypes.c_int, [ctypes.POINTER(BlockDesc),
                                                        ctypes.POINTER(BlockWeights), vp, sz, vp]),
+            # batch, seqlen, dinner, kconv, x, ld_x, w, bias, dout, ld_dout, dx, ld_dx, dw,
+            # dbias, stream
+            "ssm_conv1d_silu_bwd_noalloc": (ctypes.c_int, [i32, i32, i32, i32, vp, i64, vp, vp, vp,
+                                                           i64, vp, i64, vp, vp, vp]),
+            # kind, blocks, iters, sink, stream
+            "ssm_probe_pipe": (ctypes.c_int, [i32, i32, i32, vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -270,6 +282,24 @@ def ssm_conv1d_silu_bwd(batch, x, w, bias, dout, dx, dw, dbias, workspace=None, 
                                     _ptr(dw), _ptr(dbias), _ptr(workspace), _nbytes(workspace),
                                     _stream(stream))
     _check("ssm_conv1d_silu_bwd", st)
+
+
+def ssm_conv1d_silu_bwd_noalloc(batch, x, w, bias, dout, dx, dw, dbias, stream=None):
+    """ssm_conv1d_silu_bwd with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate)."""
+    M, dinner = x.shape
+    st = load().ssm_conv1d_silu_bwd_noalloc(batch, M // batch, dinner, w.shape[1], _ptr(x),
+                                            _ld(x), _ptr(w), _ptr(bias), _ptr(dout), _ld(dout),
+                                            _ptr(dx), _ld(dx), _ptr(dw), _ptr(dbias),
+                                            _stream(stream))
+    _check("ssm_conv1d_silu_bwd_noalloc", st)
+
+
+def ssm_probe_pipe(kind, blocks, iters, sink, stream=None):
+    """Launch the pipe-throughput probe: kind 0 = MUFU ex2, 1 = fp32 FFMA,
+    2 = packed FFMA2; blocks x 256 threads x iters x 8 lane-operations; sink
+    holds blocks*256 floats."""
+    _check("ssm_probe_pipe", load().ssm_probe_pipe(kind, blocks, iters, _ptr(sink), _stream(stream)))
 
 
 def ssm_scan_fwd_state(desc, u, delta_raw, A_log, B, C, D, z, out, h_init=None, h_last=None,

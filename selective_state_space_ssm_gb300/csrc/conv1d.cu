@@ -13,6 +13,8 @@
 // 512 contiguous bytes per warp) and walks a run of kRun rows, keeping the
 // last K rows of x (and, backward, of dpre) in registers, so each element is
 // read from HBM once plus a (K-1)/kRun halo.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -247,24 +249,62 @@ cudaError_t launch_conv1d_bwd(const ConvArgs& a, cudaStream_t st) {
 // (8 MiB) until the process exits.
 static __device__ __align__(256) float g_conv_bwd_scratch[kConvNoAllocScratchFloats];
 
-// Device address of g_conv_bwd_scratch on the current device, looked up once
-// per device (the name is only a host-side stand-in; the kernel needs this
-// address).  Returns the cudaGetSymbolAddress error, if any.
+// Identity of the calling thread's current CUDA context (cuCtxGetId: unique
+// for the life of the process, so a context destroyed and created again --
+// cudaDeviceReset, or the primary context released and retained anew -- gets
+// a new one), or 0 when no context is current or the driver cannot say.
+static unsigned long long current_context_id() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_conv_bwd_scratch in the current device's context (the
+// array's name is only a host-side stand-in; the kernel needs this address).
+// It is looked up with cudaGetSymbolAddress once per device and context and
+// kept keyed on the context's identity, so a call after a device reset (the
+// module reloaded, perhaps at another address) looks it up again; if the
+// context cannot be identified it is looked up at every call.  Returns the
+// cudaGetSymbolAddress error, if any.
 cudaError_t conv1d_noalloc_scratch(float** out) {
+    struct Entry {
+        unsigned long long ctx;
+        float* addr;
+    };
     static std::mutex mu;
-    static float* addr[64] = {};
+    static Entry cache[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_conv_bwd_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = static_cast<float*>(p);
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && cache[dev].ctx == ctx && cache[dev].addr) {
+        *out = cache[dev].addr;
+        return cudaSuccess;
     }
-    *out = addr[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_conv_bwd_scratch);   // also makes the primary context current
+    if (e != cudaSuccess) return e;
+    cache[dev].ctx = current_context_id();
+    cache[dev].addr = static_cast<float*>(p);
+    *out = cache[dev].addr;
     return cudaSuccess;
 }
 

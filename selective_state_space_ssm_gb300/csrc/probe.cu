@@ -1,0 +1,78 @@
+// probe.cu -- throughput probes of three arithmetic pipes of the SM: the MUFU
+// ex2 unit, scalar fp32 FFMA and packed f32x2 FFMA2.  The scan's roofline
+// divides its exponential count by the ex2 rate and its fp32 lane-operation
+// count by the FFMA rate; these kernels measure both on the device at hand
+// (the benchmark times them with CUDA events and the sampled SM clock).
+//
+// Every thread runs 8 independent dependency chains (4 packed pairs for
+// FFMA2), so with 8 warps per SMSP the pipe, not the chain latency, sets the
+// rate.  The chains stay bounded (ex2: x <- 2^-x converges to ~0.64; FFMA:
+// x <- a x + b with |a| < 1), and each thread's sum is stored so nothing is
+// dead code.
+#include <cuda_runtime.h>
+
+#include "ssm_gb300.h"
+
+namespace {
+
+__device__ __forceinline__ float ex2_neg(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(-x));
+    return y;
+}
+
+constexpr int kProbeThreads = 256;
+
+template <int KIND>
+__global__ void __launch_bounds__(kProbeThreads) pipe_probe_kernel(int iters, float a, float b,
+                                                                   float* sink) {
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    float x[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = 0.25f + 0.01f * c + 1e-6f * (tid & 255);
+    if constexpr (KIND == 0) {
+#pragma unroll 1
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = ex2_neg(x[c]);
+    } else if constexpr (KIND == 1) {
+#pragma unroll 1
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = fmaf(x[c], a, b);
+    } else {
+        float2 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = make_float2(x[2 * c], x[2 * c + 1]);
+        const float2 a2 = make_float2(a, a), b2 = make_float2(b, b);
+#pragma unroll 1
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = __ffma2_rn(v[c], a2, b2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            x[2 * c] = v[c].x;
+            x[2 * c + 1] = v[c].y;
+        }
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) s += x[c];
+    sink[tid] = s;
+}
+
+}  // namespace
+
+extern "C" ssm_status ssm_probe_pipe(int32_t kind, int32_t blocks, int32_t iters, float* sink,
+                                     cudaStream_t stream) {
+    if (kind < 0 || kind > 2 || blocks <= 0 || iters <= 0) return SSM_ERR_SHAPE;
+    if (!sink) return SSM_ERR_NULL;
+    // the inner loop is unrolled by 8 chains; a and b keep the fma chains in (0, 1)
+    const float a = 0.999f, b = 0.0005f;
+    switch (kind) {
+        case 0: pipe_probe_kernel<0><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+        case 1: pipe_probe_kernel<1><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+        default: pipe_probe_kernel<2><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}

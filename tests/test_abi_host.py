@@ -291,3 +291,19 @@ def test_scan_fwd_state_empty_and_sizes(lib):
     assert f(_desc(dinner=0), p, p) == 0
     # no final state asked for and no rows: nothing to do
     assert f(_desc(seqlen=0), p, None) == 0
+
+
+def test_noalloc_conv_bwd_refuses_problems_beyond_its_scratch(lib):
+    # ceil(seqlen/64) * batch * dinner * (kconv+1) floats must fit the library's
+    # 2^21-float scratch; the check comes before any device access (a problem
+    # that fills it exactly runs in tests/test_zz_no_alloc.py)
+    fn = lib.ssm_conv1d_silu_bwd_noalloc
+    p = ctypes.c_void_p(256)
+
+    def call(batch, seqlen, dinner, kconv):
+        return fn(batch, seqlen, dinner, kconv, p, 0, p, p, p, 0, p, 0, p, p, None)
+
+    assert call(64, 4096, 1024, 4) == binding.SSM_ERR_WORKSPACE
+    # 16 runs x 2 x 8192 x 8 = 2^21 floats fill it exactly; one more run of rows is too many
+    assert call(2, 1025, 8192, 7) == binding.SSM_ERR_WORKSPACE
+    assert call(2, 1000, 8192, 9) == binding.SSM_ERR_SHAPE

@@ -4,58 +4,59 @@ Some callers cannot hand the library scratch memory -- a runtime or plugin
 interface that owns every device buffer, or a loop where a cudaMalloc (which
 may synchronise the device) is not allowed.  For them the library keeps a
 fixed scratch array in its device image.  This test calls that entry point
-through the C ABI twice in a row and checks each result against the regular
-entry point (which takes a caller workspace), within the gradient tolerance
-of the other parity tests.  It lives in its own file, collected last.
+through the C ABI twice in a row, on two different problems (the second one
+fills the scratch exactly, with kconv 7, strided x / dx and a ragged last
+run of rows), and checks each result against the fp64 oracle within the
+gradient tolerance of the other parity tests and, bit for bit, against the
+regular entry point that takes a caller workspace (the same kernels in the
+same order).  It lives in its own file, collected last.  The refusal of a
+problem larger than the scratch needs no GPU and is in test_abi_host.py.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
+import oracle
 from selective_state_space_ssm_gb300 import workloads
 
 import parity
 
 pytestmark = pytest.mark.gpu
 
-
-def _noalloc_fn(lib_handle):
-    fn = lib_handle.ssm_conv1d_silu_bwd_noalloc
-    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
-    fn.argtypes = [i32, i32, i32, i32, vp, i64, vp, vp, vp, i64, vp, i64, vp, vp, vp]
-    fn.restype = ctypes.c_int
-    return fn
+SCRATCH_FLOATS = 1 << 21
+# (batch, seqlen, dinner, kconv, extra columns of the x / dx buffers)
+CASES = [(4, 300, 256, 4, 0),
+         (2, 1000, 8192, 7, 64)]
 
 
-def test_noalloc_matches_workspace_entry_point(lib):
+def _needed_floats(batch, seqlen, dinner, kconv):
+    return -(-seqlen // 64) * batch * dinner * (kconv + 1)
+
+
+def test_noalloc_matches_oracle_and_workspace_entry_point(lib):
     import torch
-    handle = lib.load()
-    fn = _noalloc_fn(handle)
-    Bt, L, D, K = 4, 300, 256, 4
-    for call in range(2):
+    assert _needed_floats(*CASES[1][:4]) == SCRATCH_FLOATS   # the second call fills it
+    for call, (Bt, L, D, K, pad) in enumerate(CASES):
         inp = workloads.conv_inputs(Bt, L, D, K, seed=40 + call)
-        x = torch.from_numpy(inp["x"]).cuda()
+        M = Bt * L
+
+        def strided(a):
+            buf = torch.zeros((M, D + pad), dtype=torch.float32, device="cuda")
+            buf[:, :D] = torch.from_numpy(a).cuda()
+            return buf[:, :D]
+
+        x = strided(inp["x"])
+        g = torch.from_numpy(inp["dout"]).cuda()
         w = torch.from_numpy(inp["w"]).cuda()
         b = torch.from_numpy(inp["bias"]).cuda()
-        g = torch.from_numpy(inp["dout"]).cuda()
         ref_dx, ref_dw, ref_db = lib.conv1d_silu_bwd(x, w, b, g, batch=Bt)
-        dx = torch.full_like(x, float("nan"))
+        dx = strided(np.full((M, D), np.nan, dtype=np.float32))
         dw = torch.full_like(w, float("nan"))
         db = torch.full_like(b, float("nan"))
-        stream = torch.cuda.current_stream().cuda_stream
-        st = fn(Bt, L, D, K, x.data_ptr(), 0, w.data_ptr(), b.data_ptr(), g.data_ptr(), 0,
-                dx.data_ptr(), 0, dw.data_ptr(), db.data_ptr(), stream)
-        assert st == 0, lib.ssm_status_string(st)
+        lib.ssm_conv1d_silu_bwd_noalloc(Bt, x, w, b, g, dx, dw, db)
         torch.cuda.synchronize()
         for got, ref in ((dx, ref_dx), (dw, ref_dw), (db, ref_db)):
-            assert parity.rel_l2(got.cpu().numpy(), ref.cpu().numpy()) <= parity.TOL_GRAD_F32
-
-
-def test_noalloc_rejects_problems_beyond_its_scratch(lib):
-    handle = lib.load()
-    fn = _noalloc_fn(handle)
-    p = ctypes.c_void_p(256)
-    # ceil(4096/64) * 64 * 1024 * 5 floats > 2^21
-    st = fn(64, 4096, 1024, 4, p, 0, p, p, p, 0, p, 0, p, p, None)
-    assert st == 5
+            assert torch.equal(got, ref)
+        odx, odw, odb = oracle.conv1d_silu_bwd(inp["x"], inp["w"], inp["bias"], inp["dout"],
+                                               batch=Bt)
+        for got, ref in ((dx, odx), (dw, odw), (db, odb)):
+            assert parity.rel_l2(got.cpu().numpy(), ref) <= parity.TOL_GRAD_F32
