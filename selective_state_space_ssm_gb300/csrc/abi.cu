@@ -192,7 +192,7 @@ bool bc_tma_ok(const ssm_scan_desc* d, const void* B, const void* C, int64_t ldB
 }
 
 struct BwdLayout {
-    int ncl, nseg, seg_chunks;
+    int cw, ncl, nseg, seg_chunks;
     size_t off_cg, off_cdl, off_sg, off_sds, off_sd0;
     size_t off_bc, off_dA, off_dD, total;
 };
@@ -224,13 +224,12 @@ FwdLayout fwd_layout(const ssm_scan_desc* d) {
 
 BwdLayout bwd_layout(const ssm_scan_desc* d) {
     BwdLayout l{};
-    l.ncl = static_cast<int>((static_cast<int64_t>(d->dinner) + ssm::kBwdChannels - 1) /
-                             ssm::kBwdChannels);
+    l.cw = ssm::bwd_channels(d->batch, d->dinner);
+    l.ncl = static_cast<int>((static_cast<int64_t>(d->dinner) + l.cw - 1) / l.cw);
     const size_t M = static_cast<size_t>(d->batch) * d->seqlen;
     const size_t NT = nt_of(d->dstate);
     const int nchunks = static_cast<int>(nchunks_of(d->seqlen));
-    const int g = ssm::bwd_segments(d->batch, d->dinner, d->seqlen,
-                                    ssm::bwd_warps_per_cta(nt_of(d->dstate)));
+    const int g = ssm::bwd_segments(d->batch, d->dinner, d->seqlen, l.cw);
     l.seg_chunks = nchunks > 0 ? (nchunks + g - 1) / g : 1;
     l.nseg = nchunks > 0 ? (nchunks + l.seg_chunks - 1) / l.seg_chunks : 1;
     const size_t planes = static_cast<size_t>(d->batch) * l.nseg;   // dA / dD partial planes
@@ -434,7 +433,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         const bool bct = bc_tma_ok(d, B, C, r.B, r.C);
         const bool ysaved = z != nullptr && ctx != nullptr;
         const void* ybuf = ysaved ? static_cast<const char*>(ctx) + ctx_y_offset(d) : u;
-        const int bc = ssm::kBwdChannels;
+        const int bc = lay.cw;
         if (!encode_act(&maps.u, u, d->dtype, d->dinner, d->seqlen, d->batch, r.u, ssm::kChunk, bc) ||
             !encode_act(&maps.dr, delta_raw, d->dtype, d->dinner, d->seqlen, d->batch, r.delta,
                         ssm::kChunk, bc) ||
@@ -483,6 +482,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* d, const void* u, const void* delta
         a.ld_dz = r.dz;
         a.nck = static_cast<int>(nck_of(d->seqlen));
         a.ncl = lay.ncl;
+        a.cw = lay.cw;
         a.bc_tma = bct ? 1 : 0;
         cudaError_t e = ssm::launch_scan_bwd(d->dtype, nt, d->disc, z != nullptr, maps, a, stream);
         if (e != cudaSuccess) return fail_cuda(e);

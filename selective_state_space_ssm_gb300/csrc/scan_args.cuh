@@ -35,18 +35,23 @@ inline int fwd_seg_tiles(int seqlen, int g) {
     return (ntiles + g - 1) / g;
 }
 
-// Backward: a CTA owns 32 channels of one batch row; its NT/8 warps split the
-// states (8 per warp), each lane 2 channels x 4 states.  Every CTA writes its
-// own dB/dC partial plane.
+// Backward: one warp per CTA covers 32 or 16 channels x all states (each lane
+// owns 4 or 2 channels x dstate/4 states); every CTA writes its own dB/dC
+// partial plane.  The 16-channel kernel is held to 128 registers so that 14
+// CTAs fit an SM.
 constexpr int kBwdStages = 2;
-constexpr int kBwdChannels = 32;
-inline int bwd_warps_per_cta(int nt) { return nt / 8; }
-// Time segments of the backward: one unless the problem's warps (32-channel
-// tiles x warps per tile) leave the SMs with fewer than 2 warps each; then
-// enough segments (of at least 32 chunks) for about 6 warps per SM.
-inline int bwd_segments(int batch, int dinner, int seqlen, int warps_per_tile) {
-    const long long warps = static_cast<long long>(batch) *
-                            ((dinner + kBwdChannels - 1) / kBwdChannels) * warps_per_tile;
+constexpr int kBwdMinBlocks16 = 14;
+// Channels per backward CTA: 32 when 32-channel CTAs already give at least 6
+// warps per SM on the 152 SMs of a GB300, else 16 (twice the warps).
+inline int bwd_channels(int batch, int dinner) {
+    const long long ctas32 = static_cast<long long>(batch) * ((dinner + 31) / 32);
+    return ctas32 >= 152LL * 6 ? 32 : 16;
+}
+// Time segments of the backward: one unless the CTAs of cw channels leave the
+// SMs with fewer than 2 warps each; then enough segments (of at least 32
+// chunks) for about 6 warps per SM.
+inline int bwd_segments(int batch, int dinner, int seqlen, int cw) {
+    const long long warps = static_cast<long long>(batch) * ((dinner + cw - 1) / cw);
     if (warps <= 0 || warps >= 152LL * 2) return 1;
     long long g = (152LL * 6 + warps - 1) / warps;
     const long long gmax = ((seqlen + kChunk - 1) / kChunk) / 32;
@@ -95,7 +100,8 @@ struct ScanBwdArgs {
     int batch, seqlen, dinner, dstate;
     int64_t ld_B, ld_C, ld_du, ld_ddelta, ld_dz;
     int nck;
-    int ncl;             // CTA columns = ceil(dinner / 32) = dB/dC partial planes
+    int ncl;             // CTA columns = ceil(dinner / cw) = dB/dC partial planes
+    int cw;              // channels per CTA (bwd_channels)
     // Time segments (walked in parallel when the channels alone give too few
     // warps): nseg segments of seg_chunks chunks.  Segment sg < nseg-1 starts
     // its reverse walk from carry_g[b][sg][NT][dinner] (dL/dh at the first step
@@ -140,7 +146,7 @@ struct FwdMaps {
 cudaError_t launch_scan_fwd(int dtype, int nt, int disc, bool gate, const FwdMaps& maps,
                             const ScanFwdArgs& a, cudaStream_t stream);
 // Tensor maps of the backward: u, delta_raw, z, dout, the saved pre-gate y
-// (all 32 channels x kChunk steps boxes) and the checkpoints (32 x NT box).
+// (all cw channels x kChunk steps boxes) and the checkpoints (cw x NT box).
 struct BwdMaps {
     CUtensorMap u, dr, z, dout, y, ck, B, C;
 };

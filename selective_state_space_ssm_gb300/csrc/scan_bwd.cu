@@ -11,19 +11,19 @@
 //   dA_log   = dA * A inside (-10, 5), exactly 0 at or beyond the bounds
 //   ddelta_raw = ddelta * sigmoid(delta_raw)
 //
-// Design (GB300): the forward saved h every kChunk (= 8) steps.  A CTA owns
-// 32 channels of one batch row and walks the chunks last to first; its NT/8
-// warps split the states, so the B8 x D4096 problem runs 2048 warps (about 13
-// per SM) with 8 chains per lane.  For each chunk a prologue computes the
-// per-(step, channel) scalars once for the CTA (delta, delta*u, dy and the two
-// sigmoids, shared memory); pass B recomputes h forward from the checkpoint,
-// keeping a_t h_{t-1} in registers; the reverse pass runs g over the chunk in
-// two halves, each followed by the epilogue of its steps (du, ddelta_raw, dz,
-// dD).  Sums over states leave as per-group partials through shared memory;
-// sums over channels (dB, dC) as per-channel-pair partials that the warp adds
-// into the CTA's partial plane (no inter-CTA synchronisation; an earlier
-// cluster/DSMEM exchange paid a cluster-scope release fence per chunk).
-// scan_reduce_kernel adds the planes and finishes dA_log and dD.
+// Design (GB300): the forward saved h every kChunk (= 8) steps.  A warp-sized
+// CTA owns 32 channels of one batch row and walks the chunks last to first.
+// For each chunk it recomputes h forward from the checkpoint (pass B), keeping
+// a_t h_{t-1} in registers, then runs the reverse recurrence for g over
+// the chunk.  Each lane owns 4 channels x dstate/4 states (16 chains), so the
+// sums over states (y, sum g B, sum g A a h) and over channels (dB, dC) are
+// mostly register accumulations.  Per step, a lane's dB/dC partials (its 4
+// channels) go to shared memory by channel group; once per chunk the warp
+// adds the 8 groups with float4 loads and writes the rows of its own partial
+// plane with plain vector stores (no inter-CTA synchronisation: an earlier
+// cluster/DSMEM exchange cost a cluster-scope release fence per chunk, about
+// 16% of the kernel); scan_reduce_kernel adds the planes and also finishes
+// dA_log and dD.
 #include <algorithm>
 
 #include "scan_args.cuh"
@@ -31,81 +31,35 @@
 
 namespace ssm {
 
-// Two adjacent activation elements as fp32 (loads from a TMA tile, stores to
-// global memory): one 32-bit access for bf16, one 64-bit access for fp32.
-template <typename T> struct Pair;
-template <> struct Pair<float> {
-    static __device__ __forceinline__ float2 ld(const float* p) {
-        return *reinterpret_cast<const float2*>(p);
+// Loads CPL consecutive floats (CPL = 2 or 4) from shared memory.
+template <int CPL>
+__device__ __forceinline__ void ld_cpl(const float* p, float (&v)[CPL]) {
+    if constexpr (CPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        v[0] = t.x; v[1] = t.y;
     }
-    static __device__ __forceinline__ void st(float* p, float2 v) {
-        *reinterpret_cast<float2*>(p) = v;
-    }
-};
-template <> struct Pair<__nv_bfloat16> {
-    static __device__ __forceinline__ float2 ld(const __nv_bfloat16* p) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16* p, float2 v) {
-        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
-    }
-};
-
-// delta = softplus(x) together with sigmoid(x) and sigmoid(z), from
-// e = exp(-|x|), ez = exp(-z) and one reciprocal r = 1/((2+e)(1+ez)(1+e)):
-// 1/(2+e) = r(1+ez)(1+e), sigmoid(z) = 1/(1+ez) = r(2+e)(1+e) and
-// 1/(1+e) = r(2+e)(1+ez).  ez is capped at 2^100 (see softplus_sigmoid).
-__device__ __forceinline__ void softplus_sig_xz(float x, float z, float& dt, float& sdr, float& sz) {
-    const float e = ex2(-fabsf(x) * kLog2e);
-    const float ez = ex2(fminf(-z * kLog2e, 100.0f));
-    const float a = 2.0f + e, b = 1.0f + ez, c = 1.0f + e;
-    const float ab = a * b;
-    const float r = rcp(ab * c);
-    const float inv_c = r * ab;
-    sz = r * (a * c);
-    dt = fmaxf(x, 0.0f) + log1p_unit(e, r * (b * c));
-    sdr = x >= 0.0f ? inv_c : e * inv_c;
 }
-// The same without a gate: r = 1/((2+e)(1+e)).
-__device__ __forceinline__ void softplus_sig_x(float x, float& dt, float& sdr) {
-    const float e = ex2(-fabsf(x) * kLog2e);
-    const float a = 2.0f + e, c = 1.0f + e;
-    const float r = rcp(a * c);
-    const float inv_c = r * a;
-    dt = fmaxf(x, 0.0f) + log1p_unit(e, r * c);
-    sdr = x >= 0.0f ? inv_c : e * inv_c;
+template <int CPL>
+__device__ __forceinline__ void st_cpl(float* p, const float (&v)[CPL]) {
+    if constexpr (CPL == 4)
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    else
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
 }
 
-// ZOH coefficient beta/B = (exp(delta A) - 1)/A = delta phi1(delta A) and its
-// A-derivative delta^2 phi2(delta A), from x2 = delta A log2(e) and a = exp(delta A).
-__device__ __forceinline__ float zoh_cf(float x2, float a, float dt, float inv_a) {
-    const float xn = x2 * kLn2;
-    return fabsf(xn) < 0.5f ? dt * phi1_series(xn) : (a - 1.0f) * inv_a;
-}
-__device__ __forceinline__ float zoh_dcf(float x2, float a, float dt, float inv_a) {
-    const float xn = x2 * kLn2;
-    return fabsf(xn) < 0.5f ? dt * dt * phi2_series(xn) : (xn * a - (a - 1.0f)) * inv_a * inv_a;
-}
-
-// A CTA owns 32 channels of one batch row for its time segment; its NT/8
-// warps split the states (warp w: states 8w .. 8w+7).  Lane (pi, sq) of a
-// warp owns channels 2pi, 2pi+1 and states 8w+4sq .. +3: 8 chains, held as
-// state pairs in packed f32x2 registers.  The per-(step, channel) scalars
-// (delta, delta*u, dy) are stored duplicated in shared memory, so one 16-byte
-// load gives the broadcast pairs of both channels.  Sums over the states of a
-// (step, channel) (sum g B, sum g A a h) leave as per-group partials (NT/4
-// groups) that the epilogue adds; sums over the channels of a (step, state)
-// (dB, dC) leave as per-channel-pair partials that the warp adds and writes to
-// the CTA's partial plane.
-template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(4 * NT, DISC == 0 ? (NT == 16 ? 7 : 14) : (NT == 16 ? 6 : 12))
+// CW = channels per CTA (one warp): 32 (each lane 4 channels) or 16 (each lane
+// 2 channels: half the work per warp and fewer registers, so twice the warps
+// when the problem has few channels).
+template <typename T, int NT, int DISC, bool GATE, int CW>
+__global__ void __launch_bounds__(32, CW == 16 ? kBwdMinBlocks16 : 1)
 scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr int TC = kChunk;
     constexpr int S = kBwdStages;
-    constexpr int CW = kBwdChannels;
-    constexpr int NW = NT / 8;                  // warps
-    constexpr int NTH = 32 * NW;
+    constexpr int CPL = CW / 8;                 // channels per lane
+    constexpr int NS = NT / 4;                  // states per lane
     constexpr int NTEN = GATE ? 5 : 3;          // u, delta_raw, dout, [z, y]
     constexpr int TILE = TC * CW;
     constexpr int BCT = TC * NT;                // elements per B or C tile
@@ -113,71 +67,71 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
     constexpr uint32_t kBCBytes = 2 * BCT * sizeof(T);
     constexpr uint32_t kCkBytes = NT * CW * sizeof(float);
-    constexpr bool ZOH = DISC == 1;
-    constexpr int HS = TC / 2;                  // steps per half chunk (flush / epilogue)
-    constexpr int NG = 2 * NW;                  // state groups of a (step, channel)
-    constexpr int NQ = ZOH ? 3 : 2;             // state sums per (step, channel)
-    constexpr int PPJ = 16 * 8 + 8;             // padded partial row: 16 channel pairs x 8 states
-    constexpr int PART = HS * NQ * NG * CW;     // floats of the state-sum partials
-    constexpr int PBUF = NW * HS * PPJ;         // floats of one dB or dC partial buffer
-    constexpr int PROW = PART > PBUF ? PART : PBUF;
-    constexpr int PI = 128 / NTH;               // prologue pair-items per thread and chunk
-    constexpr int EI = 64 / NTH;                // epilogue pair-items per thread and half
-    constexpr int kSu = ZOH ? 2 : 0;            // the state sum that multiplies u in ddelta
+    constexpr int BCN = 2 * TC * NT;
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
-    static_assert(TC == 8 && (NT == 8 || NT == 16), "lane layout below");
+    static_assert((CPL == 2 || CPL == 4) && TC == 8, "lane layout below");
+    constexpr int SPL = 32 / CW;                // steps per lane-iteration of pro/epilogue
+    constexpr bool ZOH = DISC == 1;
+    constexpr int NQN = ZOH ? 3 : 2;            // state sums kept per (step, channel)
+    constexpr int PR = CW == 32 ? TC : 4;       // steps per dB/dC flush
+    constexpr int PJ = 9 * NT;                  // padded partial row: conflict-free float4 sums
 
     extern __shared__ __align__(128) unsigned char smem[];
-    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
-    float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [S][NT][CW]
-    float* bcs = cks + S * NT * CW;             // [TC][NT] B | [TC][NT] C (fp32)
-    float* Pd = bcs + 2 * BCT;                  // [TC][CW][2] delta, each value twice
-    float* Pbu = Pd + 2 * TILE;                 // [TC][CW][2] delta*u (Euler) | u (ZOH)
-    float* Pdy = Pbu + 2 * TILE;                // [TC][CW][2] dy = dout * silu(z)
-    float* Psdr = Pdy + 2 * TILE;               // [TC][CW] sigmoid(delta_raw)
-    float* Psz = Psdr + TILE;                   // [TC][CW] sigmoid(z)
-    float* part = Psz + TILE;                   // [HS][NQ][NG][CW] state sums; dC partials in pass B
-    float* pbufB = part + PROW;                 // [NW][HS][PPJ] dB partials
-    uint64_t* full = reinterpret_cast<uint64_t*>(pbufB + PBUF);   // [S]
+    T* tiles = reinterpret_cast<T*>(smem);                               // [S][STAGE]
+    float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][CW]
+    float* bcs = cks + S * NT * CW;                                      // [TC][NT] B | [TC][NT] C
+    float* Pd = bcs + BCN;                                               // [TC][CW] delta
+    float* Pbs = Pd + TILE;                                              // [TC][CW] delta*u | u
+    float* Pdy = Pbs + TILE;                                             // [TC][CW] dy
+    float* part = Pdy + TILE;                                            // [TC][NQN][4][CW]
+    float* pbuf = part + TC * NQN * 4 * CW;                              // [PR][PJ] dB or dC by channel group
+    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + PR * PJ);        // [S]
 
-    const int tid = threadIdx.x;
-    const int w = tid >> 5, lane = tid & 31;
-    const int pi = lane & 15, sq = lane >> 4;
-    const int cl = 2 * pi;                      // this lane's first channel (local)
-    const int n0 = 8 * w + 4 * sq;              // this lane's first state
-    const int grp = 2 * w + sq;                 // its state group
-    const int cp = tid & 15;                    // channel pair of this thread's pro/epilogue items
+    const int lane = threadIdx.x;
+    const int cg = lane >> 2, ng = lane & 3;     // channel group (CPL channels), state group (NS states)
+    const int cbase = cg * CPL;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
     const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
     const int nchunks = (L + TC - 1) / TC;
-    const int sg = blockIdx.z;                  // time segment: chunks [kcb, kce), last to first
+    // this CTA's time segment: chunks [kcb, kce), walked last to first
+    const int sg = blockIdx.z;
     const int kcb = sg * a.seg_chunks;
     const int kce = min(nchunks, kcb + a.seg_chunks);
     const int nit = kce - kcb;
     const size_t plane_b = static_cast<size_t>(b) * a.nseg + sg;   // dA / dD plane
     const size_t row0 = static_cast<size_t>(b) * L;
+    // prologue / epilogue layout: lane = (channel pc, step phase pj)
+    const int pc = lane % CW, pj = lane / CW;
+    const int dch = c0 + pc;
+    const bool lane_ok = dch < Dn;
+    // column of channel c in state-group row k of `part`: rotated (CW = 32) or
+    // xor-swizzled (CW = 16) so that the per-step writes and the epilogue's
+    // reads hit distinct banks
+    auto part_col = [](int c, int k) {
+        return CW == 32 ? ((c + 8 * k) & 31) : (c ^ (8 * (k >> 1)));
+    };
 
-    // per (channel, state pair) constants: A log2(e) (0 on padding) [and 1/A]
-    float2 A2[2][2], iA[2][2];
+    // per (channel, state) constants of this lane's chains: A log2(e) (0 on
+    // padding states and channels) [and 1/A for ZOH]
+    float2 A2r[CPL][NS / 2], iAr[CPL][NS / 2];
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci)
+    for (int i = 0; i < CPL; ++i)
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            float v[2], r[2];
+        for (int p = 0; p < NS / 2; ++p) {
+            float v[2], w[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int d = c0 + cl + ci, n = n0 + 2 * p + e;
+                const int d = c0 + cbase + i, n = ng * NS + 2 * p + e;
                 const bool ok = d < Dn && n < N;
                 const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
                 v[e] = ok ? A * kLog2e : 0.0f;
-                r[e] = 1.0f / A;
+                w[e] = 1.0f / A;
             }
-            A2[ci][p] = make_float2(v[0], v[1]);
-            iA[ci][p] = make_float2(r[0], r[1]);
+            A2r[i][p] = make_float2(v[0], v[1]);
+            iAr[i][p] = make_float2(w[0], w[1]);
         }
-    float2 Dp = make_float2(0.0f, 0.0f);   // D of the items' channel pair (D needs only 4-byte alignment)
-    if (a.D && c0 + 2 * cp < Dn) Dp = make_float2(a.D[c0 + 2 * cp], a.D[c0 + 2 * cp + 1]);
+    const float Dd = (lane_ok && a.D) ? a.D[dch] : 0.0f;
 
     const T* Bp = static_cast<const T*>(a.B);
     const T* Cp = static_cast<const T*>(a.C);
@@ -186,7 +140,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         const int kc = kce - 1 - it;
         const int s = it % S;
         T* dst = tiles + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], kActBytes + (kc > 0 ? kCkBytes : 0u) + (bc_tma ? kBCBytes : 0u));
+        mbar_arrive_expect_tx(&full[s], kActBytes + (kc > 0 ? kCkBytes : 0u) +
+                                            (bc_tma ? kBCBytes : 0u));
         if (bc_tma) {
             tma_load_3d(dst + NTEN * TILE, &maps.B, &full[s], 0, kc * TC, b);
             tma_load_3d(dst + NTEN * TILE + BCT, &maps.C, &full[s], 0, kc * TC, b);
@@ -198,74 +153,116 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             tma_load_3d(dst + 3 * TILE, &maps.z, &full[s], c0, kc * TC, b);
             tma_load_3d(dst + 4 * TILE, &maps.y, &full[s], c0, kc * TC, b);
         }
-        if (kc > 0) tma_load_2d(cks + s * NT * CW, &maps.ck, &full[s], c0, (b * a.nck + kc - 1) * NT);
+        if (kc > 0)
+            tma_load_2d(cks + s * NT * CW, &maps.ck, &full[s], c0, (b * a.nck + kc - 1) * NT);
     };
-    if (tid == 0) {
+    if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    if (tid == 0)
+    __syncwarp();
+    if (lane == 0)
         for (int it = 0; it < S && it < nit; ++it) issue(it);
+    __syncwarp();
 
-    // carries of the reverse recurrence: g = dL/dh after this segment, delta of
-    // the step after it
-    float2 g[2][2], dA[2][2];
-    float dl_next[2] = {0.0f, 0.0f};
+    // The carries of the reverse recurrence (g) and the dA accumulators live in
+    // registers only during the reverse pass and epilogue; between chunks they
+    // are parked in the (then idle) state-sum buffer, so pass B can hold the
+    // chunk's a h_{t-1} values in registers.
+    float* stash = part;
+    static_assert(2 * CPL * NS * 32 <= TC * NQN * 4 * CW, "stash fits in the partials buffer");
+    float2 dA[CPL][NS / 2], g[CPL][NS / 2];
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci)
+    for (int i = 0; i < CPL; ++i)
 #pragma unroll
-        for (int p = 0; p < 2; ++p) g[ci][p] = dA[ci][p] = make_float2(0.0f, 0.0f);
+        for (int p = 0; p < NS / 2; ++p) dA[i][p] = g[i][p] = make_float2(0.f, 0.f);
+    auto park = [&]() {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i)
+#pragma unroll
+            for (int p = 0; p < NS / 2; ++p) {
+                reinterpret_cast<float2*>(stash)[(i * NS / 2 + p) * 32 + lane] = g[i][p];
+                reinterpret_cast<float2*>(stash)[((CPL + i) * NS / 2 + p) * 32 + lane] = dA[i][p];
+            }
+    };
+    auto unpark = [&]() {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i)
+#pragma unroll
+            for (int p = 0; p < NS / 2; ++p) {
+                g[i][p] = reinterpret_cast<const float2*>(stash)[(i * NS / 2 + p) * 32 + lane];
+                dA[i][p] = reinterpret_cast<const float2*>(stash)[((CPL + i) * NS / 2 + p) * 32 + lane];
+            }
+    };
+    float dl_next[CPL];                         // delta of the step after this chunk
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) dl_next[i] = 0.0f;
     if (sg + 1 < a.nseg) {
+        // dL/dh and delta at the first step of the next segment
 #pragma unroll
-        for (int ci = 0; ci < 2; ++ci) {
-            const int d = c0 + cl + ci;
+        for (int i = 0; i < CPL; ++i) {
+            const int d = c0 + cbase + i;
             if (d < Dn) {
-                dl_next[ci] = a.carry_dl[plane_b * Dn + d];
+                dl_next[i] = a.carry_dl[plane_b * Dn + d];
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const float* cq = a.carry_g + (plane_b * NT + n0 + 2 * p) * Dn + d;
-                    g[ci][p] = make_float2(cq[0], cq[Dn]);
+                for (int p = 0; p < NS / 2; ++p) {
+                    const float* cp = a.carry_g + (plane_b * NT + ng * NS + 2 * p) * Dn + d;
+                    g[i][p] = make_float2(cp[0], cp[Dn]);
                 }
             }
         }
     }
-    float2 dDacc[EI];
-#pragma unroll
-    for (int m = 0; m < EI; ++m) dDacc[m] = make_float2(0.0f, 0.0f);
+    park();
+    float dD_acc = 0.0f;
 
     T* dup = static_cast<T*>(a.du);
     T* ddp = static_cast<T*>(a.ddelta);
     T* dzp = static_cast<T*>(a.dz);
-    float* plane = a.ws_bc + static_cast<size_t>(blockIdx.x) * a.batch * L * 2 * NT;
-
-    // Adds the 16 channel-pair partials of every (step, state) of this warp's
-    // rows [tf, tf + HS) and writes them to the plane (qoff 0: dB, NT: dC).
-    // Lane -> (step jj, state pair sp, half hf of the channel pairs).
-    auto flush = [&](const float* pb, int qoff, int tf, int nrows) {
-        const int o = lane >> 1, hf = lane & 1;
-        const int jj = o >> 2, sp = o & 3;
-        const float* rp = pb + jj * PPJ + 2 * sp + 64 * hf;
-        float2 acc = *reinterpret_cast<const float2*>(rp);
-#pragma unroll
-        for (int k = 1; k < 8; ++k) acc = add2(acc, *reinterpret_cast<const float2*>(rp + 8 * k));
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-        if (hf == 0 && jj < nrows)
-            *reinterpret_cast<float2*>(plane + (row0 + tf + jj) * 2 * NT + qoff + 8 * w + 2 * sp) = acc;
-    };
-
     bool ok = true;
     int waited = 0;
+
+    // this CTA's partial plane of dB|dC: [batch][seqlen][2][NT]
+    float* plane = a.ws_bc + static_cast<size_t>(blockIdx.x) * a.batch * L * 2 * NT;
+    // dB or dC partials of one step, summed over this lane's CPL channels, go
+    // to pbuf by channel group; flush() adds the 8 groups (the CTA's channels)
+    // for PR steps and writes those rows of the plane, float4 per lane.
+    auto store_partial = [&](int j, const float2 (&v)[NS / 2]) {
+        float* pp = pbuf + (j % PR) * PJ + cg * NT + ng * NS;
+        if constexpr (NS == 4)
+            *reinterpret_cast<float4*>(pp) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        else
+            *reinterpret_cast<float2*>(pp) = v[0];
+    };
+    auto flush = [&](int coff, int tf, int nrows) {
+        constexpr int NM = NT / 4;
+        __syncwarp();
+        if (lane < PR * NM) {
+            const int j = lane / NM, m = lane % NM;
+            float4 acc = *reinterpret_cast<const float4*>(pbuf + j * PJ + 4 * m);
+#pragma unroll
+            for (int c = 1; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(pbuf + j * PJ + c * NT + 4 * m);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            if (j < nrows)
+                *reinterpret_cast<float4*>(plane + (static_cast<size_t>(b) * L + tf + j) * 2 * NT + coff +
+                                           4 * m) = acc;
+        }
+        __syncwarp();
+    };
+
     for (int it = 0; it < nit; ++it) {
         const int kc = kce - 1 - it;
         const int t0 = kc * TC;
         const int jmax = min(TC, L - t0);
         const int s = it % S;
+
         if (ok) ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
-        ok = __syncthreads_and(ok) != 0;
-        if (!ok) break;
-        waited = it + 1;
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) waited = it + 1;
 
         const T* tu = tiles + s * STAGE;
         const T* tr = tu + TILE;
@@ -273,281 +270,359 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         const T* tz = tu + 3 * TILE;
         const T* ty = tu + 4 * TILE;
         const float* ck = cks + s * NT * CW;
-
-        // fp32 B and C of the chunk, [TC][NT] each (states past dstate and
-        // steps past seqlen are 0): fp32 TMA tiles in place, bf16 widened.
-        const float* Bf;
-        {
-            const T* Bs = tu + NTEN * TILE;
-            if (bc_tma && sizeof(T) == 4) {
-                Bf = reinterpret_cast<const float*>(Bs);
-            } else if (bc_tma) {
-                for (int g8 = tid; g8 < 2 * BCT / 8; g8 += NTH) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                    float f[8];
+        if (ok) {
+            // fp32 B and C of this chunk: [TC][NT] each.  fp32 TMA tiles are used
+            // in place; bf16 tiles are widened into bcs, 8 values per lane.
+            const float* Bf;
+            const float* Cf;
+            {
+                const T* Bs = tu + NTEN * TILE;
+                if (bc_tma && sizeof(T) == 4) {
+                    Bf = reinterpret_cast<const float*>(Bs);
+                } else if (bc_tma) {
+                    for (int g8 = lane; g8 < BCN / 8; g8 += 32) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        float f[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f[2 * q] = __uint_as_float(wv[q] << 16);
-                        f[2 * q + 1] = __uint_as_float(wv[q] & 0xffff0000u);
-                    }
-                    *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
-                }
-                Bf = bcs;
-            } else {
-                for (int e = tid; e < 2 * BCT; e += NTH) {
-                    const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = t0 + j;
-                    float v = 0.0f;
-                    if (t < L && n < N) {
-                        const size_t r = row0 + t;
-                        v = isC ? Act<T>::load(Cp + r * a.ld_C + n) : Act<T>::load(Bp + r * a.ld_B + n);
-                    }
-                    bcs[e] = v;
-                }
-                Bf = bcs;
-            }
-        }
-        const float* Cf = Bf + BCT;
-
-        // ---- prologue: per (step, channel pair) delta, delta*u | u, dy and the
-        //      two sigmoids.  Past seqlen the tiles are zero: dy = 0 there.
-#pragma unroll
-        for (int m = 0; m < PI; ++m) {
-            const int j = (tid >> 4) + (NTH / 16) * m;
-            const int c = 2 * cp;
-            const float2 u2 = Pair<T>::ld(tu + j * CW + c);
-            const float2 x2 = Pair<T>::ld(tr + j * CW + c);
-            const float2 o2 = Pair<T>::ld(tg + j * CW + c);
-            float dt[2], sdr[2], sz[2] = {0.0f, 0.0f}, dy[2];
-            if (GATE) {
-                const float2 z2 = Pair<T>::ld(tz + j * CW + c);
-                softplus_sig_xz(x2.x, z2.x, dt[0], sdr[0], sz[0]);
-                softplus_sig_xz(x2.y, z2.y, dt[1], sdr[1], sz[1]);
-                dy[0] = o2.x * z2.x * sz[0];
-                dy[1] = o2.y * z2.y * sz[1];
-            } else {
-                softplus_sig_x(x2.x, dt[0], sdr[0]);
-                softplus_sig_x(x2.y, dt[1], sdr[1]);
-                dy[0] = o2.x;
-                dy[1] = o2.y;
-            }
-            const float bu0 = ZOH ? u2.x : dt[0] * u2.x;
-            const float bu1 = ZOH ? u2.y : dt[1] * u2.y;
-            const int o = (j * CW + c) * 2;
-            *reinterpret_cast<float4*>(Pd + o) = make_float4(dt[0], dt[0], dt[1], dt[1]);
-            *reinterpret_cast<float4*>(Pbu + o) = make_float4(bu0, bu0, bu1, bu1);
-            *reinterpret_cast<float4*>(Pdy + o) = make_float4(dy[0], dy[0], dy[1], dy[1]);
-            *reinterpret_cast<float2*>(Psdr + j * CW + c) = make_float2(sdr[0], sdr[1]);
-            if (GATE) *reinterpret_cast<float2*>(Psz + j * CW + c) = make_float2(sz[0], sz[1]);
-        }
-        __syncthreads();
-
-        // ---- pass B: h from the chunk's checkpoint, a_t h_{t-1} kept in
-        //      registers; dC partials (over this lane's two channels) flushed
-        //      every HS steps through `part`.
-        float2 ah[TC][2][2];
-        {
-            float2 h[2][2];
-#pragma unroll
-            for (int ci = 0; ci < 2; ++ci)
-#pragma unroll
-                for (int p = 0; p < 2; ++p)
-                    h[ci][p] = kc > 0 ? make_float2(ck[(n0 + 2 * p) * CW + cl + ci],
-                                                    ck[(n0 + 2 * p + 1) * CW + cl + ci])
-                                      : make_float2(0.0f, 0.0f);
-            float* pc = part + w * HS * PPJ;
-#pragma unroll
-            for (int j = 0; j < TC; ++j) {
-                const float4 dl = *reinterpret_cast<const float4*>(Pd + (j * CW + cl) * 2);
-                const float4 bu = *reinterpret_cast<const float4*>(Pbu + (j * CW + cl) * 2);
-                const float4 dy = *reinterpret_cast<const float4*>(Pdy + (j * CW + cl) * 2);
-                const float4 Bq = *reinterpret_cast<const float4*>(Bf + j * NT + n0);
-                float2 dC[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-#pragma unroll
-                for (int ci = 0; ci < 2; ++ci) {
-                    const float2 dlc = ci ? make_float2(dl.z, dl.w) : make_float2(dl.x, dl.y);
-                    const float2 buc = ci ? make_float2(bu.z, bu.w) : make_float2(bu.x, bu.y);
-                    const float2 dyc = ci ? make_float2(dy.z, dy.w) : make_float2(dy.x, dy.y);
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const float2 Bv = p ? make_float2(Bq.z, Bq.w) : make_float2(Bq.x, Bq.y);
-                        const float2 x = mul2(dlc, A2[ci][p]);
-                        const float2 av = make_float2(ex2(x.x), ex2(x.y));
-                        const float2 ahv = mul2(av, h[ci][p]);
-                        if (!ZOH) {
-                            h[ci][p] = fma2(buc, Bv, ahv);
-                        } else {
-                            const float2 cf = make_float2(zoh_cf(x.x, av.x, dlc.x, iA[ci][p].x),
-                                                          zoh_cf(x.y, av.y, dlc.x, iA[ci][p].y));
-                            h[ci][p] = fma2(mul2(cf, buc), Bv, ahv);
+                        for (int q = 0; q < 4; ++q) {
+                            f[2 * q] = __uint_as_float(w[q] << 16);
+                            f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
                         }
-                        ah[j][ci][p] = ahv;
-                        dC[p] = fma2(dyc, h[ci][p], dC[p]);
+                        *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
                     }
-                }
-                *reinterpret_cast<float4*>(pc + (j % HS) * PPJ + pi * 8 + 4 * sq) =
-                    make_float4(dC[0].x, dC[0].y, dC[1].x, dC[1].y);
-                if (j % HS == HS - 1) {
-                    __syncwarp();
-                    flush(pc, NT, t0 + j + 1 - HS, jmax - (j + 1 - HS));
-                    __syncwarp();
-                }
-            }
-        }
-        __syncthreads();   // `part` changes role: state sums from here on
-
-        // ---- reverse pass, in two halves (steps 7..4, then 3..0), each followed
-        //      by the dB flush and the epilogue of its steps.
-        float2 an[2][2];                        // a of the step after the current one
-#pragma unroll
-        for (int ci = 0; ci < 2; ++ci)
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const float2 x = mul2(f2(dl_next[ci]), A2[ci][p]);
-                an[ci][p] = make_float2(ex2(x.x), ex2(x.y));
-            }
-#pragma unroll
-        for (int hb = 1; hb >= 0; --hb) {
-            const int jb = hb * HS;
-#pragma unroll
-            for (int jl = HS - 1; jl >= 0; --jl) {
-                const int j = jb + jl;
-                const float4 dl = *reinterpret_cast<const float4*>(Pd + (j * CW + cl) * 2);
-                const float4 bu = *reinterpret_cast<const float4*>(Pbu + (j * CW + cl) * 2);
-                const float4 dy = *reinterpret_cast<const float4*>(Pdy + (j * CW + cl) * 2);
-                const float4 Bq = *reinterpret_cast<const float4*>(Bf + j * NT + n0);
-                const float4 Cq = *reinterpret_cast<const float4*>(Cf + j * NT + n0);
-                float2 dB[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-                float sums[NQ][2];
-#pragma unroll
-                for (int ci = 0; ci < 2; ++ci) {
-                    const float2 dlc = ci ? make_float2(dl.z, dl.w) : make_float2(dl.x, dl.y);
-                    const float2 buc = ci ? make_float2(bu.z, bu.w) : make_float2(bu.x, bu.y);
-                    const float2 dyc = ci ? make_float2(dy.z, dy.w) : make_float2(dy.x, dy.y);
-                    float2 Sg = make_float2(0.0f, 0.0f), Eg = Sg, Sa = Sg;
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const float2 Bv = p ? make_float2(Bq.z, Bq.w) : make_float2(Bq.x, Bq.y);
-                        const float2 Cv = p ? make_float2(Cq.z, Cq.w) : make_float2(Cq.x, Cq.y);
-                        // g_t = C_t dy_t + a_{t+1} g_{t+1}
-                        const float2 gv = fma2(an[ci][p], g[ci][p], mul2(Cv, dyc));
-                        g[ci][p] = gv;
-                        const float2 q = mul2(gv, ah[j][ci][p]);      // g a_t h_{t-1}
-                        Eg = fma2(A2[ci][p], q, Eg);
-                        const float2 x = mul2(dlc, A2[ci][p]);
-                        const float2 av = make_float2(ex2(x.x), ex2(x.y));   // a_t
-                        if (!ZOH) {
-                            dA[ci][p] = fma2(dlc, q, dA[ci][p]);
-                            Sg = fma2(gv, Bv, Sg);
-                            dB[p] = fma2(buc, gv, dB[p]);
-                        } else {
-                            const float2 cf = make_float2(zoh_cf(x.x, av.x, dlc.x, iA[ci][p].x),
-                                                          zoh_cf(x.y, av.y, dlc.x, iA[ci][p].y));
-                            const float2 dcf = make_float2(zoh_dcf(x.x, av.x, dlc.x, iA[ci][p].x),
-                                                           zoh_dcf(x.y, av.y, dlc.x, iA[ci][p].y));
-                            const float2 gB = mul2(gv, Bv);
-                            dA[ci][p] = fma2(dlc, q, fma2(mul2(gB, buc), dcf, dA[ci][p]));
-                            Sg = fma2(gB, cf, Sg);
-                            Sa = fma2(gB, av, Sa);
-                            dB[p] = fma2(mul2(buc, cf), gv, dB[p]);
+                    Bf = bcs;
+                } else {
+                    for (int e = lane; e < BCN; e += 32) {
+                        const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = t0 + j;
+                        float v = 0.0f;
+                        if (t < L && n < N) {
+                            const size_t r = row0 + t;
+                            v = isC ? Act<T>::load(Cp + r * a.ld_C + n) : Act<T>::load(Bp + r * a.ld_B + n);
                         }
-                        an[ci][p] = av;
+                        bcs[e] = v;
                     }
-                    sums[0][ci] = Sg.x + Sg.y;
-                    sums[1][ci] = Eg.x + Eg.y;
-                    if (ZOH) sums[NQ - 1][ci] = Sa.x + Sa.y;
+                    Bf = bcs;
                 }
-                float* pp = part + (jl * NQ * NG + grp) * CW + cl;
+                Cf = Bf + BCT;
+            }
+
+            // ---- prologue (lane = channel, step parity): delta, delta*u (or u),
+            //      dy.  All TC steps run: past seqlen the tiles, B and C are
+            //      zero, so dy = 0 and the extra steps add nothing.
+            {
+                // loads, math and stores in separate passes, so that the steps'
+                // independent chains overlap (stores could alias later loads)
+                constexpr int NJ = TC / SPL;
+                float uvA[NJ], xrA[NJ], goA[NJ], zvA[NJ];
 #pragma unroll
-                for (int qn = 0; qn < NQ; ++qn)
-                    *reinterpret_cast<float2*>(pp + qn * NG * CW) = make_float2(sums[qn][0], sums[qn][1]);
-                *reinterpret_cast<float4*>(pbufB + (w * HS + jl) * PPJ + pi * 8 + 4 * sq) =
-                    make_float4(dB[0].x, dB[0].y, dB[1].x, dB[1].y);
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * jj + pj;
+                    uvA[jj] = Act<T>::to_f(tu[j * CW + pc]);
+                    xrA[jj] = Act<T>::to_f(tr[j * CW + pc]);
+                    goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
+                    zvA[jj] = GATE ? Act<T>::to_f(tz[j * CW + pc]) : 0.0f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    float dt, dy = goA[jj];
+                    if (GATE) {
+                        float sz;
+                        softplus_sigmoid(xrA[jj], zvA[jj], dt, sz);
+                        dy = goA[jj] * zvA[jj] * sz;
+                    } else {
+                        float e;
+                        dt = softplus_e(xrA[jj], e);
+                    }
+                    xrA[jj] = dt;                               // reuse: delta
+                    goA[jj] = dy;                               // reuse: dy
+                    uvA[jj] = ZOH ? uvA[jj] : dt * uvA[jj];     // reuse: delta*u | u
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * jj + pj;
+                    Pd[j * CW + pc] = xrA[jj];
+                    Pbs[j * CW + pc] = uvA[jj];
+                    Pdy[j * CW + pc] = goA[jj];
+                }
             }
             __syncwarp();
-            flush(pbufB + w * HS * PPJ, 0, t0 + jb, jmax - jb);
-            __syncthreads();   // every warp's state sums of these steps are in `part`
 
-            // ---- epilogue of steps jb .. jb+HS-1 (thread -> step, channel pair):
-            //      du, ddelta_raw, dz, dD
+            // ---- pass B: h from the checkpoint, a_t h_{t-1} kept in registers;
+            //      dC partials (over this lane's channels) to pbuf.
+            float2 ah[TC][CPL][NS / 2];
+            {
+                float2 h[CPL][NS / 2];
 #pragma unroll
-            for (int m = 0; m < EI; ++m) {
-                const int jl = (tid >> 4) + (NTH / 16) * m;
-                const int j = jb + jl;
-                const int c = 2 * cp;
-                const float* pp = part + jl * NQ * NG * CW + c;
-                float2 sm[NQ];
+                for (int i = 0; i < CPL; ++i)
 #pragma unroll
-                for (int qn = 0; qn < NQ; ++qn) {
-                    float2 v = *reinterpret_cast<const float2*>(pp + qn * NG * CW);
+                    for (int p = 0; p < NS / 2; ++p)
+                        h[i][p] = kc > 0 ? make_float2(ck[(ng * NS + 2 * p) * CW + cbase + i],
+                                                       ck[(ng * NS + 2 * p + 1) * CW + cbase + i])
+                                         : make_float2(0.f, 0.f);
+                // a step's inputs are loaded one step ahead: a partial-sum store
+                // could alias them, so they could not move above it otherwise
+                float dlN[CPL], bsN[CPL], dyN[CPL];
+                float2 BN[NS / 2];
+                auto load_b = [&](int j) {
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlN);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsN);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyN);
 #pragma unroll
-                    for (int gq = 1; gq < NG; ++gq)
-                        v = add2(v, *reinterpret_cast<const float2*>(pp + (qn * NG + gq) * CW));
-                    sm[qn] = v;
+                    for (int p = 0; p < NS / 2; ++p)
+                        BN[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                };
+                load_b(0);
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    float dlA[CPL], bsA[CPL], dyA[CPL];
+                    float2 Bv[NS / 2];
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+                        dlA[i] = dlN[i];
+                        bsA[i] = bsN[i];
+                        dyA[i] = dyN[i];
+                    }
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) Bv[p] = BN[p];
+                    if (j + 1 < TC) load_b(j + 1);
+                    float2 dC[NS / 2];
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) dC[p] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) {
+                            const float2 x = mul2(f2(dlA[i]), A2r[i][p]);
+                            const float2 av = make_float2(ex2(x.x), ex2(x.y));
+                            const float2 ahv = mul2(av, h[i][p]);
+                            float2 bu = f2(bsA[i]);
+                            if (!ZOH) {
+                                h[i][p] = fma2(bu, Bv[p], ahv);
+                            } else {
+                                const float xn0 = x.x * kLn2, xn1 = x.y * kLn2;
+                                const float cf0 = fabsf(xn0) < 0.5f ? dlA[i] * phi1_series(xn0)
+                                                                    : (av.x - 1.0f) * iAr[i][p].x;
+                                const float cf1 = fabsf(xn1) < 0.5f ? dlA[i] * phi1_series(xn1)
+                                                                    : (av.y - 1.0f) * iAr[i][p].y;
+                                bu = mul2(mul2(make_float2(cf0, cf1), f2(bsA[i])), Bv[p]);
+                                h[i][p] = add2(ahv, bu);
+                            }
+                            ah[j][i][p] = ahv;
+                            dC[p] = fma2(f2(dyA[i]), h[i][p], dC[p]);
+                        }
+                    }
+                    store_partial(j, dC);
+                    if (j % PR == PR - 1) flush(NT, t0 + j + 1 - PR, jmax - (j + 1 - PR));
                 }
-                const float4 dl4 = *reinterpret_cast<const float4*>(Pd + (j * CW + c) * 2);
-                const float4 dy4 = *reinterpret_cast<const float4*>(Pdy + (j * CW + c) * 2);
-                const float2 dl2 = make_float2(dl4.x, dl4.z), dy2 = make_float2(dy4.x, dy4.z);
-                const float2 sdr2 = *reinterpret_cast<const float2*>(Psdr + j * CW + c);
-                const float2 u2 = Pair<T>::ld(tu + j * CW + c);
-                const float2 du2 = ZOH ? fma2(Dp, dy2, sm[0]) : fma2(dl2, sm[0], mul2(Dp, dy2));
-                const float2 dd2 = mul2(fma2(u2, sm[kSu], mul2(sm[1], f2(kLn2))), sdr2);
-                float2 dz2 = make_float2(0.0f, 0.0f);
-                if (GATE) {
-                    const float2 sz2 = *reinterpret_cast<const float2*>(Psz + j * CW + c);
-                    const float2 z2 = Pair<T>::ld(tz + j * CW + c);
-                    const float2 o2 = Pair<T>::ld(tg + j * CW + c);
-                    const float2 y2 = Pair<T>::ld(ty + j * CW + c);
-                    const float2 one = f2(1.0f);
-                    const float2 t1 = fma2(z2, add2(one, mul2(f2(-1.0f), sz2)), one);   // 1 + z (1 - sz)
-                    dz2 = mul2(mul2(mul2(o2, y2), sz2), t1);
+            }
+
+            // ---- reverse pass: g_t = C_t dy_t + a_{t+1} g_{t+1}; state sums to
+            //      shared partials, dB partials to pbuf.
+            unpark();
+            __syncwarp();
+            {
+                float2 an[CPL][NS / 2];
+#pragma unroll
+                for (int i = 0; i < CPL; ++i)
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        const float2 x = mul2(f2(dl_next[i]), A2r[i][p]);
+                        an[i][p] = make_float2(ex2(x.x), ex2(x.y));
+                    }
+                // inputs one step ahead (see pass B)
+                float dlN[CPL], bsN[CPL], dyN[CPL];
+                float2 BN[NS / 2], CN[NS / 2];
+                auto load_r = [&](int j) {
+                    ld_cpl<CPL>(Pd + j * CW + cbase, dlN);
+                    ld_cpl<CPL>(Pbs + j * CW + cbase, bsN);
+                    ld_cpl<CPL>(Pdy + j * CW + cbase, dyN);
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        BN[p] = *reinterpret_cast<const float2*>(Bf + j * NT + ng * NS + 2 * p);
+                        CN[p] = *reinterpret_cast<const float2*>(Cf + j * NT + ng * NS + 2 * p);
+                    }
+                };
+                load_r(TC - 1);
+#pragma unroll
+                for (int j = TC - 1; j >= 0; --j) {
+                    float dlA[CPL], bsA[CPL], dyA[CPL];
+                    float2 Bv[NS / 2], Cv[NS / 2];
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+                        dlA[i] = dlN[i];
+                        bsA[i] = bsN[i];
+                        dyA[i] = dyN[i];
+                    }
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) {
+                        Bv[p] = BN[p];
+                        Cv[p] = CN[p];
+                    }
+                    if (j > 0) load_r(j - 1);
+                    float2 dB[NS / 2];
+#pragma unroll
+                    for (int p = 0; p < NS / 2; ++p) dB[p] = make_float2(0.f, 0.f);
+                    float sums[NQN][CPL];
+#pragma unroll
+                    for (int i = 0; i < CPL; ++i) {
+                        float2 Sg = make_float2(0.f, 0.f), Eg = make_float2(0.f, 0.f);
+                        float2 Sa = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int p = 0; p < NS / 2; ++p) {
+                            const float2 A2p = A2r[i][p];
+                            // g_t = C_t dy_t + a_{t+1} g_{t+1}
+                            const float2 gv = fma2(an[i][p], g[i][p], mul2(Cv[p], f2(dyA[i])));
+                            g[i][p] = gv;
+                            const float2 q = mul2(gv, ah[j][i][p]);        // g a_t h_{t-1}
+                            Eg = fma2(A2p, q, Eg);
+                            const float2 x = mul2(f2(dlA[i]), A2p);
+                            const float2 av = make_float2(ex2(x.x), ex2(x.y));   // a_t
+                            float2 dAv = dA[i][p];
+                            if (!ZOH) {
+                                dAv = fma2(f2(dlA[i]), q, dAv);
+                                Sg = fma2(gv, Bv[p], Sg);
+                                dB[p] = fma2(f2(bsA[i]), gv, dB[p]);
+                            } else {
+                                const float dt = dlA[i], uv = bsA[i];
+                                float cf[2], dcf[2];
+#pragma unroll
+                                for (int ee = 0; ee < 2; ++ee) {
+                                    const float xn = (ee ? x.y : x.x) * kLn2;
+                                    const float ae = ee ? av.y : av.x;
+                                    const float ia = ee ? iAr[i][p].y : iAr[i][p].x;
+                                    const bool small = fabsf(xn) < 0.5f;
+                                    cf[ee] = small ? dt * phi1_series(xn) : (ae - 1.0f) * ia;
+                                    dcf[ee] = small ? dt * dt * phi2_series(xn)
+                                                    : (xn * ae - (ae - 1.0f)) * ia * ia;
+                                }
+                                const float2 gB = mul2(gv, Bv[p]);
+                                dAv = fma2(f2(dt), q, fma2(mul2(gB, f2(uv)), make_float2(dcf[0], dcf[1]), dAv));
+                                Sg = fma2(gB, make_float2(cf[0], cf[1]), Sg);
+                                Sa = fma2(gB, av, Sa);
+                                dB[p] = fma2(mul2(f2(uv), make_float2(cf[0], cf[1])), gv, dB[p]);
+                            }
+                            dA[i][p] = dAv;
+                            an[i][p] = av;
+                        }
+                        sums[0][i] = Sg.x + Sg.y;
+                        sums[1][i] = Eg.x + Eg.y;
+                        if (ZOH) sums[NQN - 1][i] = Sa.x + Sa.y;
+                    }
+#pragma unroll
+                    for (int qn = 0; qn < NQN; ++qn)
+                        st_cpl<CPL>(part + ((j * NQN + qn) * 4 + ng) * CW + part_col(cbase, ng), sums[qn]);
+                    store_partial(j, dB);
+                    if (j % PR == 0) flush(0, t0 + j, jmax - j);
                 }
-                if (j < jmax) {
-                    dDacc[m] = fma2(dy2, u2, dDacc[m]);
-                    if (c0 + c < Dn) {
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) dl_next[i] = Pd[cbase + i];   // delta of step t0
+        }
+        __syncwarp();
+
+        if (ok) {
+            // ---- epilogue (lane = channel, step parity): finish du,
+            //      ddelta_raw, dz, dD
+            if (lane_ok) {
+                // loads, math and stores in separate passes (see the prologue),
+                // two steps at a time for 32-channel CTAs (register pressure)
+                constexpr int NJALL = TC / SPL;
+                constexpr int NJ = (CW == 32) ? 2 : NJALL;   // steps per load/compute/store block
+#pragma unroll 1
+                for (int jb = 0; jb < NJALL; jb += NJ) {
+                float Sg[NJ], Eg[NJ], Sa[NJ], uvA[NJ], xrA[NJ], dtA[NJ], dyA2[NJ], zvA[NJ], goA[NJ], yvA[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    float sm[NQN];
+#pragma unroll
+                    for (int qn = 0; qn < NQN; ++qn) {
+                        // the 4 state groups' sums; a step-phase-1 lane reads
+                        // them in the order 1,0,3,2 (other banks, same sum)
+                        const float* pp = part + (j * NQN + qn) * 4 * CW;
+                        float v[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int kk = k ^ pj;
+                            v[k] = pp[kk * CW + part_col(pc, kk)];
+                        }
+                        sm[qn] = (v[0] + v[1]) + (v[2] + v[3]);
+                    }
+                    Sg[jj] = sm[0];
+                    Eg[jj] = sm[1] * kLn2;
+                    Sa[jj] = sm[NQN - 1];
+                    uvA[jj] = Act<T>::to_f(tu[j * CW + pc]);
+                    xrA[jj] = Act<T>::to_f(tr[j * CW + pc]);
+                    dtA[jj] = Pd[j * CW + pc];
+                    dyA2[jj] = Pdy[j * CW + pc];
+                    if (GATE) {
+                        zvA[jj] = Act<T>::to_f(tz[j * CW + pc]);
+                        goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
+                        yvA[jj] = Act<T>::to_f(ty[j * CW + pc]);
+                    }
+                }
+                float duO[NJ], ddO[NJ], dzO[NJ];
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    duO[jj] = ZOH ? fmaf(Dd, dyA2[jj], Sg[jj]) : fmaf(dtA[jj], Sg[jj], Dd * dyA2[jj]);
+                    ddO[jj] = fmaf(uvA[jj], ZOH ? Sa[jj] : Sg[jj], Eg[jj]) * sigmoidf_(xrA[jj]);
+                    if (j < jmax) dD_acc = fmaf(dyA2[jj], uvA[jj], dD_acc);
+                    if (GATE) {
+                        const float sz = sigmoidf_(zvA[jj]);
+                        dzO[jj] = goA[jj] * yvA[jj] * sz * (1.0f + zvA[jj] * (1.0f - sz));
+                    }
+                }
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int j = SPL * (jb + jj) + pj;
+                    if (j < jmax) {
                         const size_t r = row0 + t0 + j;
-                        Pair<T>::st(dup + r * a.ld_du + c0 + c, du2);
-                        Pair<T>::st(ddp + r * a.ld_ddelta + c0 + c, dd2);
-                        if (GATE) Pair<T>::st(dzp + r * a.ld_dz + c0 + c, dz2);
+                        dup[r * a.ld_du + dch] = Act<T>::from_f(duO[jj]);
+                        ddp[r * a.ld_ddelta + dch] = Act<T>::from_f(ddO[jj]);
+                        if (GATE) dzp[r * a.ld_dz + dch] = Act<T>::from_f(dzO[jj]);
                     }
                 }
             }
-            __syncthreads();   // `part` and the dB rows are reused by the next half
+            }
+            __syncwarp();
+            park();
         }
-#pragma unroll
-        for (int ci = 0; ci < 2; ++ci) dl_next[ci] = Pd[(cl + ci) * 2];   // delta of step t0
 
         // ---- release this TMA stage
-        if (tid == 0 && it + S < nit) issue(it + S);
+        __syncwarp();
+        if (lane == 0 && ok && it + S < nit) issue(it + S);
     }
 
-    if (!ok) {
-        // a wait gave up: drain the copies still in flight (bounded) before exit
-        if (tid == 0)
-            for (int it = waited; it < nit && it < waited + S; ++it)
-                mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
-        return;
+    if (lane == 0 && !ok) {
+        for (int it = waited; it < nit && it < waited + S; ++it)
+            mbar_wait(&full[it % S], (it / S) & 1, kFaultDrain);
     }
+    __syncwarp();
+    unpark();
+    if (ok) {
 #pragma unroll
-    for (int ci = 0; ci < 2; ++ci) {
-        const int d = c0 + cl + ci;
-        if (d < Dn)
-            *reinterpret_cast<float4*>(a.ws_dA + (plane_b * Dn + d) * NT + n0) =
-                make_float4(dA[ci][0].x, dA[ci][0].y, dA[ci][1].x, dA[ci][1].y);
-    }
-    // dD: the threads of a channel pair hold the sums over steps jl (mod 4)
-    float* red = part;
+        for (int i = 0; i < CPL; ++i) {
+            const int d = c0 + cbase + i;
+            if (d < Dn) {
 #pragma unroll
-    for (int m = 0; m < EI; ++m)
-        *reinterpret_cast<float2*>(red + ((tid >> 4) + (NTH / 16) * m) * CW + 2 * cp) = dDacc[m];
-    __syncthreads();
-    if (tid < 16) {
-        float2 v = *reinterpret_cast<const float2*>(red + 2 * cp);
-#pragma unroll
-        for (int k = 1; k < HS; ++k) v = add2(v, *reinterpret_cast<const float2*>(red + k * CW + 2 * cp));
-        const int d = c0 + 2 * cp;
-        if (d < Dn) *reinterpret_cast<float2*>(a.ws_dD + plane_b * Dn + d) = v;
+                for (int p = 0; p < NS / 2; ++p) {
+                    float* dst = a.ws_dA + (plane_b * Dn + d) * NT + ng * NS + 2 * p;
+                    dst[0] = dA[i][p].x;
+                    dst[1] = dA[i][p].y;
+                }
+            }
+        }
+        if constexpr (SPL == 2) {
+            // the two step-phase lanes of a channel each hold half of its dD sum
+            const float dD_other = __shfl_xor_sync(0xffffffffu, dD_acc, 16);
+            if (lane_ok && pj == 0) a.ws_dD[plane_b * Dn + dch] = dD_acc + dD_other;
+        } else {
+            if (lane_ok) a.ws_dD[plane_b * Dn + dch] = dD_acc;
+        }
     }
 }
 
@@ -785,31 +860,27 @@ __global__ void scan_reduce_kernel(const ScanReduceArgs a) {
     }
 }
 
-template <typename T, int NT, int DISC, bool GATE>
+template <typename T, int NT, int DISC, bool GATE, int CW>
 static size_t bwd_smem_bytes() {
-    constexpr int TC = kChunk, CW = kBwdChannels, NW = NT / 8;
+    constexpr int TC = kChunk;
     constexpr int NTEN = GATE ? 5 : 3;
-    constexpr int NQ = DISC == 1 ? 3 : 2;
-    constexpr int HS = TC / 2, NG = 2 * NW, PPJ = 16 * 8 + 8;
-    constexpr int PART = HS * NQ * NG * CW, PBUF = NW * HS * PPJ;
+    constexpr int NQN = DISC == 1 ? 3 : 2;
     return kBwdStages * (NTEN * TC * CW + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
            + kBwdStages * NT * CW * sizeof(float)      // checkpoint tiles
-           + 2 * TC * NT * sizeof(float)               // fp32 B | C
-           + 3 * 2 * TC * CW * sizeof(float)           // delta, delta*u | u, dy (duplicated)
-           + 2 * TC * CW * sizeof(float)               // sigmoid(delta_raw), sigmoid(z)
-           + (PART > PBUF ? PART : PBUF) * sizeof(float)   // state sums | dC partials
-           + PBUF * sizeof(float)                      // dB partials
+           + 2 * TC * NT * sizeof(float)               // fp32 B|C (bf16 or unaligned B/C)
+           + 3 * TC * CW * sizeof(float)               // delta, delta*u, dy
+           + TC * NQN * 4 * CW * sizeof(float)         // state-sum partials
+           + (CW == 32 ? TC : 4) * 9 * NT * sizeof(float)   // dB or dC partials by channel group
            + kBwdStages * sizeof(uint64_t);
 }
 
-template <typename T, int NT, int DISC, bool GATE>
-static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
-    const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE>();
-    auto kern = scan_bwd_kernel<T, NT, DISC, GATE>;
+template <typename T, int NT, int DISC, bool GATE, int CW>
+static cudaError_t launch_bwd_cw(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
+    const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE, CW>();
+    auto kern = scan_bwd_kernel<T, NT, DISC, GATE, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    constexpr int CW = kBwdChannels;
     if (a.nseg > 1) {
         // segment pass (segments 1 .. nseg-1), then the combine of the carries
         constexpr int NTEN1 = GATE ? 3 : 2;
@@ -828,8 +899,14 @@ static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaS
         if (e != cudaSuccess) return e;
     }
     kern<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch), static_cast<unsigned>(a.nseg)),
-           4 * NT, smem, st>>>(maps, a);
+           32, smem, st>>>(maps, a);
     return cudaGetLastError();
+}
+
+template <typename T, int NT, int DISC, bool GATE>
+static cudaError_t launch_bwd_t(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
+    return a.cw == 32 ? launch_bwd_cw<T, NT, DISC, GATE, 32>(maps, a, st)
+                      : launch_bwd_cw<T, NT, DISC, GATE, 16>(maps, a, st);
 }
 
 template <typename T, int NT>

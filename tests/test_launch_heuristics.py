@@ -1,7 +1,7 @@
-"""The launch heuristics of the scan (warps per backward CTA, time segments
-of the forward and the backward), compiled from the kernels' own header with
-the host compiler: the configurations the documentation quotes for the
-benchmark workloads."""
+"""The launch heuristics of the scan (channels per backward CTA, time
+segments of the forward and the backward), compiled from the kernels' own
+header with the host compiler: the configurations the documentation quotes
+for the benchmark workloads."""
 import os
 import shutil
 import subprocess
@@ -19,16 +19,16 @@ int main() {
     const int shapes[][3] = {{8, 1024, 1536}, {8, 2048, 4096}, {1, 65536, 2048}, {1, 64, 32}};
     for (const auto& s : shapes) {
         const int b = s[0], L = s[1], D = s[2];
-        const int nw = ssm::bwd_warps_per_cta(16);
+        const int cw = ssm::bwd_channels(b, D);
         const int gf = ssm::fwd_segments(b, D, L);
         const int tiles = ssm::fwd_seg_tiles(L, gf);
         const int nt = (L + ssm::kFwdTile - 1) / ssm::kFwdTile;
         const int nseg_f = (nt + tiles - 1) / tiles;
-        const int gb = ssm::bwd_segments(b, D, L, nw);
+        const int gb = ssm::bwd_segments(b, D, L, cw);
         const int nch = (L + ssm::kChunk - 1) / ssm::kChunk;
         const int sc = (nch + gb - 1) / gb;
         const int nseg_b = (nch + sc - 1) / sc;
-        std::printf("%d %d %d %d %d %d\n", b, L, D, nw, nseg_f, nseg_b);
+        std::printf("%d %d %d %d %d %d\n", b, L, D, cw, nseg_f, nseg_b);
     }
     return 0;
 }
@@ -49,15 +49,15 @@ def table(tmp_path_factory):
     return {r[:3]: r[3:] for r in rows}
 
 
-def test_benchmark_workload_runs_one_segment(table):
-    # B8 L2048 D4096 (dstate 16): 1024 CTAs of 2 warps (states split in two), one wave
-    assert table[(8, 2048, 4096)] == (2, 1, 1)
+def test_benchmark_workload_runs_one_segment_with_32_channel_backward(table):
+    # B8 L2048 D4096: 1024 CTAs of 32 channels fill the 152 SMs (>= 6 warps each)
+    assert table[(8, 2048, 4096)] == (32, 1, 1)
 
 
 def test_few_channel_workloads(table):
-    # B8 L1024 D1536: 384 CTAs of 2 warps (5 per SM), no segments
-    assert table[(8, 1024, 1536)] == (2, 1, 1)
+    # B8 L1024 D1536: 16-channel backward CTAs (twice the warps), no segments
+    assert table[(8, 1024, 1536)] == (16, 1, 1)
     # B1 L65536 D2048: time segments in both passes (15 forward, 8 backward)
-    assert table[(1, 65536, 2048)] == (2, 15, 8)
+    assert table[(1, 65536, 2048)] == (16, 15, 8)
     # the tiny problem: too short to split
-    assert table[(1, 64, 32)] == (2, 1, 1)
+    assert table[(1, 64, 32)] == (16, 1, 1)

@@ -1,10 +1,10 @@
 """GPU parity of ssm_scan_fwd / ssm_scan_bwd against the fp64 oracle on small
 shapes that span several tiles and chunks with ragged tails.  The backward
-runs CTAs of 32 channels whose dstate/8 warps split the states (dstate <= 8:
-one warp, else two); the backward scans time segments in parallel when the
-problem has fewer than 2 warps per SM.  The forward scans time segments in
-parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512 (the B2
-L1000 case and the two marked below)."""
+uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
+otherwise; the wide cases below (short sequences, many channels) run the
+32-channel kernel, the rest the 16-channel one.  The forward scans time
+segments in parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512
+(the B2 L1000 case and the two marked below)."""
 import numpy as np
 import pytest
 
@@ -29,7 +29,7 @@ CASES = [
     # time-segmented forward (few channels, seqlen >= 512): ragged last segment
     (1, 777, 96, 16, "bf16", 1, False, 0.5, 0.02),
     (3, 1030, 40, 5, "f32", 0, True, 0.3, 0.0),
-    # wide problems (4 * 256 = 1024 backward CTAs of 32 channels)
+    # 32-channel backward CTAs (4 * 256 = 1024 CTAs of 32 channels)
     (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
     (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
     (8, 17, 3680, 6, "f32", 0, False, 0.3, 0.0),    # ragged dinner (not a multiple of 32), NT = 8
