@@ -69,7 +69,7 @@ __device__ __forceinline__ float fwd_step(float2 (&h)[NL / 2], const float2 (&A2
 // per step pair; the y partials of the two halves are added the same way,
 // and each lane finishes the outputs of its own steps.
 template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(64, NT == 16 ? 7 : 8)
+__global__ void __maxnreg__(144)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     constexpr int CW = kFwdChannels;                    // channels per CTA (32)
     constexpr int TS = kFwdTile;                        // steps per tile (16)
@@ -181,8 +181,6 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     for (; k < ke; ++k) {
         const int s = (k - kb) % S;
         ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
-        ok = __syncthreads_and(ok) != 0;
-        if (!ok) break;
 
         const T* tu = tiles + s * STAGE;
         const T* tr = tu + TILE;
@@ -196,7 +194,7 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             if (bc_tma && sizeof(T) == 4) {
                 Bf = reinterpret_cast<const float*>(Bs);
             } else if (bc_tma) {
-                for (int g8 = tid; g8 < 2 * BCT / 8; g8 += NTH) {
+                for (int g8 = tid; ok && g8 < 2 * BCT / 8; g8 += NTH) {
                     const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
                     float f[8];
@@ -224,7 +222,9 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         }
         // the staging buffer of this tile was last read by the stores of tile k-2
         if (tid == 0 && k - kb >= 2) bulk_wait_read_1();
-        __syncthreads();
+        // every thread's wait succeeded, B|C are staged, the staging buffer is free
+        ok = __syncthreads_and(ok) != 0;
+        if (!ok) break;
         const int jmax = min(TS, L - k * TS);
 
         // Phase A: the per-step scalars of this lane's own steps j = 2i + half.
@@ -252,32 +252,39 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             odu[i] = Dd * uv;
         }
 
-        // Phase B: the recurrence over all TS steps (past seqlen the tiles and
-        // B|C are zero, so the extra steps evolve a state that is never stored,
-        // or, when the final state is asked for, leave it unchanged).  Per step
-        // pair the lanes of a channel swap their delta and delta*u; after it
-        // they swap y partials so that each lane holds the y of its own step.
-        float yo[TH];
-        float2 hck[NCK][NQ];                            // states at the chunk ends
+        // The lanes of a channel swap their delta and delta*u, so that each
+        // holds them for every step of the tile.
+        float dts[TS], bss[TS];
 #pragma unroll
         for (int i = 0; i < TH; ++i) {
             const float pdt = __shfl_xor_sync(0xffffffffu, odt[i], 16);
             const float pbs = __shfl_xor_sync(0xffffffffu, obs[i], 16);
+            dts[2 * i] = half ? pdt : odt[i];
+            dts[2 * i + 1] = half ? odt[i] : pdt;
+            bss[2 * i] = half ? pbs : obs[i];
+            bss[2 * i + 1] = half ? obs[i] : pbs;
+        }
+
+        // Phase B: the recurrence over all TS steps (past seqlen the tiles and
+        // B|C are zero, so the extra steps evolve a state that is never stored,
+        // or, when the final state is asked for, leave it unchanged).  After
+        // each step pair the lanes swap y partials: each keeps the y of its
+        // own step.
+        float yo[TH];
+        float2 hck[NCK][NQ];                            // states at the chunk ends
+#pragma unroll
+        for (int i = 0; i < TH; ++i) {
             float yp[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int j = 2 * i + e;
-                const bool own = e == half;
-                const float dt = own ? odt[i] : pdt;
-                const float bs = own ? obs[i] : pbs;
                 yp[e] = fwd_step<NL, DISC>(h, A2, Anat, invA, Bf + j * NT + n0, Bf + BCT + j * NT + n0,
-                                           dt, bs);
+                                           dts[j], bss[j]);
                 if ((j + 1) % kChunk == 0) {
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) hck[j / kChunk][q] = h[q];
                 }
             }
-            // this lane keeps its own step's partial and sends the other one
             const float keep = half ? yp[1] : yp[0];
             const float send = half ? yp[0] : yp[1];
             yo[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16) + odu[i];
