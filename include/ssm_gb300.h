@@ -95,7 +95,7 @@ size_t ssm_scan_ctx_bytes(const ssm_scan_desc* desc);
 
 /* Bytes of device scratch that ssm_scan_fwd / ssm_scan_bwd need.  The
  * forward needs none unless the problem has few channels for its length
- * (batch * ceil(dinner/32) < 152 and seqlen >= 512): it then scans time
+ * (batch * ceil(dinner/32) < 304 and seqlen >= 512): it then scans time
  * segments in parallel and keeps per-segment states (about
  * 2 * batch * segments * 16 * dinner floats). */
 size_t ssm_scan_fwd_workspace_bytes(const ssm_scan_desc* desc);

@@ -12,18 +12,17 @@ namespace ssm {
 // the backward recomputes h inside each chunk of kChunk steps.
 constexpr int kChunk = 8;
 
-// Forward: a CTA of two warps owns 32 channels; the two lanes of a channel
-// hold half of its states each.
+// Forward: one lane per channel (all states of it), one warp of 32 channels
+// per CTA.
 constexpr int kFwdChannels = 32;
-constexpr int kFwdWarps = 2;    // warps per forward CTA
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
-// Time segments of the forward: one per batch row unless the CTAs' warps
-// (2 per 32 channels) leave the 152 SMs with fewer than 2 warps each
-// (measured: at 2.5 warps per SM the segment pass costs more than it gains);
-// then enough segments (of at least 256 steps) for about 6 warps per SM.
+// Time segments of the forward: one per batch row unless batch x ceil(dinner/32)
+// warps leave the 152 SMs with fewer than 2 warps each (measured: at 2.5 warps
+// per SM the segment pass costs more than it gains); then enough segments (of
+// at least 256 steps) for about 6 warps per SM.
 inline int fwd_segments(int batch, int dinner, int seqlen) {
-    const long long warps = static_cast<long long>(batch) * ((dinner + 31) / 32) * kFwdWarps;
+    const long long warps = static_cast<long long>(batch) * ((dinner + 31) / 32);
     if (warps <= 0 || warps >= 152LL * 2) return 1;
     long long g = (152LL * 6 + warps - 1) / warps;
     const long long gmax = seqlen / 256;

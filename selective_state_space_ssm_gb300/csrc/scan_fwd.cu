@@ -7,14 +7,13 @@
 //   out_t = y_t * silu(z_t)
 // with beta = delta*B (Euler) or expm1(delta A)/A * B (ZOH).
 //
-// Design (GB300): the NT states of a (batch row, channel) chain live in the
-// registers of two lanes (NT/2 each) for the whole sequence, so every element
-// costs one ex2 and four fp32 lane-operations (two packed f32x2 instructions
-// per state pair).  A CTA of two warps owns 32 channels; it streams u /
-// delta_raw / z tiles of kFwdTile steps x 32 channels and the B/C tiles of
-// the same steps (shared by the 32 channels) with TMA, kFwdStages tiles in
-// flight.  Every kChunk steps the state is written to the context buffer for
-// the backward.
+// Design (GB300): one thread owns one (batch row, channel) chain and keeps all
+// dstate states of it in registers for the whole sequence, so every element
+// costs one ex2 and four fp32 ops (two packed f32x2 instructions per state
+// pair) and nothing crosses threads.  A warp-sized CTA streams u / delta_raw /
+// z tiles of kFwdTile steps x 32 channels and the B/C tiles of the same steps
+// (shared by the 32 channels) with TMA, 4 tiles in flight.  Every kChunk
+// steps the state is written to the context buffer for the backward.
 #include "scan_args.cuh"
 #include "ssm_common.cuh"
 
@@ -60,25 +59,56 @@ __device__ __forceinline__ float fwd_step(float2 (&h)[NL / 2], const float2 (&A2
     return s.x + s.y;
 }
 
-// Lane layout: a CTA of two warps owns 32 channels of one batch row (warp w:
-// channels 16w .. 16w+15).  The two lanes of a channel (lane c and c+16 of
-// its warp) split its states: each holds NT/2 of them in registers, so the
-// B8 x D4096 problem runs 2048 warps.  The lane pair also splits the
-// per-step scalars (softplus, silu(z), D u): each lane computes them for
-// every other step and the pair exchange delta and delta*u with one shuffle
-// per step pair; the y partials of the two halves are added the same way,
-// and each lane finishes the outputs of its own steps.
+// fp32 B and C of one tile, [TS][NT] each (states past dstate and steps past
+// seqlen read 0).  fp32 TMA tiles are used in place; bf16 TMA tiles are
+// widened into bcs 8 values per lane; B/C that are not TMA-aligned are read
+// straight from global memory into bcs.  Returns the B pointer (C follows
+// TS*NT floats later).
+template <typename T, int NT, int TS>
+__device__ __forceinline__ const float* fwd_stage_bc(float* bcs, const T* Bs, bool from_tma,
+                                                     const T* Bp, const T* Cp, int64_t ldB,
+                                                     int64_t ldC, size_t row0, int k, int L, int N,
+                                                     int lane) {
+    constexpr int BCT = TS * NT;
+    if (from_tma && sizeof(T) == 4) return reinterpret_cast<const float*>(Bs);
+    if (from_tma) {
+        for (int g8 = lane; g8 < 2 * BCT / 8; g8 += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                f[2 * q] = __uint_as_float(w[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            }
+            *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        return bcs;
+    }
+    for (int e = lane; e < 2 * BCT; e += 32) {
+        const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = k * TS + j;
+        float v = 0.0f;
+        if (t < L && n < N) {
+            const size_t r = row0 + t;
+            v = isC ? Act<T>::load(Cp + r * ldC + n) : Act<T>::load(Bp + r * ldB + n);
+        }
+        bcs[e] = v;
+    }
+    return bcs;
+}
+
+// Lane layout: a warp-sized CTA owns 32 channels of one batch row, one
+// channel per lane with all NT states of it in registers, so nothing per step
+// is computed twice and no value crosses lanes.
 template <typename T, int NT, int DISC, bool GATE>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(32, 1)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     constexpr int CW = kFwdChannels;                    // channels per CTA (32)
-    constexpr int TS = kFwdTile;                        // steps per tile (16)
+    constexpr int TS = kFwdTile;
     constexpr int S = kFwdStages;
-    constexpr int NTH = 64;
     constexpr int NTEN = GATE ? 3 : 2;
-    constexpr int NL = NT / 2;                          // states per lane
-    constexpr int NQ = NL / 2;                          // state pairs per lane
-    constexpr int TH = TS / 2;                          // own steps per lane and tile
+    constexpr int NQ = NT / 2;                          // state pairs per lane
     constexpr int TILE = TS * CW;                       // elements per activation tile
     constexpr int BCT = TS * NT;                        // elements per B or C tile
     constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
@@ -86,7 +116,6 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     constexpr int STAGE = NTEN * TILE + 2 * BCT;        // elements per stage
     static_assert(TS % kChunk == 0, "tiles hold whole checkpoint chunks");
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
-    static_assert(NL % 4 == 0, "float4 B/C loads per lane");
 
     constexpr int NCK = TS / kChunk;                    // chunk boundaries per tile
     extern __shared__ __align__(128) unsigned char smem[];
@@ -96,14 +125,10 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     T* ost = reinterpret_cast<T*>(ckst + 2 * NCK * NT * CW);                // [2][2][TS][CW] out | y
     uint64_t* full = reinterpret_cast<uint64_t*>(ost + 2 * 2 * TILE);        // [S]
 
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int half = lane >> 4;                         // which half of the states
-    const int cl = (tid >> 5) * 16 + (lane & 15);       // channel within the CTA
-    const int n0 = half * NL;                           // first state of this lane
+    const int lane = threadIdx.x;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
-    const int d = c0 + cl;
+    const int d = c0 + lane;
     const bool active = d < a.dinner;
     const int L = a.seqlen, N = a.dstate;
     const int ntiles = (L + TS - 1) / TS;
@@ -111,14 +136,14 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     const bool bc_tma = a.bc_tma != 0;
 
     // Per-(channel, state) constants: A*log2(e) as the ex2 argument scale (0 on
-    // padding states and inactive channels, where B = C = 0 or u = 0 keeps h at 0).
+    // padding states and inactive lanes, where B = C = 0 or u = 0 keeps h at 0).
     float2 A2[NQ], Anat[NQ], invA[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         float v[2], w[2], r[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = n0 + 2 * q + e;
+            const int n = 2 * q + e;
             const bool ok = active && n < N;
             const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
             v[e] = ok ? A * kLog2e : 0.0f;
@@ -139,15 +164,14 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         h[q] = make_float2(0.0f, 0.0f);
-        const int n = n0 + 2 * q;
         if (g > 0 && active) {
-            const float* hp = a.h0 + ((static_cast<size_t>(b) * a.nseg + g) * NT + n) * a.dinner + d;
+            const float* hp = a.h0 + ((static_cast<size_t>(b) * a.nseg + g) * NT + 2 * q) * a.dinner + d;
             h[q] = make_float2(hp[0], hp[a.dinner]);
         } else if (g == 0 && active && a.h_init) {
             // caller's initial state [batch][dstate][dinner]
-            const float* hp = a.h_init + (static_cast<size_t>(b) * N + n) * a.dinner + d;
-            if (n < N) h[q].x = hp[0];
-            if (n + 1 < N) h[q].y = hp[a.dinner];
+            const float* hp = a.h_init + (static_cast<size_t>(b) * N + 2 * q) * a.dinner + d;
+            if (2 * q < N) h[q].x = hp[0];
+            if (2 * q + 1 < N) h[q].y = hp[a.dinner];
         }
     }
 
@@ -166,77 +190,41 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         }
     };
 
-    if (tid == 0) {
+    if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    if (tid == 0)
+    __syncwarp();
+    if (lane == 0)
         for (int k = kb; k < kb + S && k < ke; ++k) issue(k);
 
     const bool save_y = GATE && a.ysave != nullptr;
     const bool save_ck = a.ctx != nullptr && a.nck > 0;
     int k = kb;
-    bool ok = true;
     for (; k < ke; ++k) {
         const int s = (k - kb) % S;
-        ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
+        bool ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
 
         const T* tu = tiles + s * STAGE;
         const T* tr = tu + TILE;
         const T* tz = tu + 2 * TILE;
-        // fp32 B and C of the tile, [TS][NT] each (states past dstate and steps
-        // past seqlen read 0): fp32 TMA tiles in place, bf16 widened, B/C that
-        // are not TMA-aligned read from global memory.
-        const float* Bf;
-        {
-            const T* Bs = tu + NTEN * TILE;
-            if (bc_tma && sizeof(T) == 4) {
-                Bf = reinterpret_cast<const float*>(Bs);
-            } else if (bc_tma) {
-                for (int g8 = tid; ok && g8 < 2 * BCT / 8; g8 += NTH) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(Bs + 8 * g8);
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                    float f[8];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f[2 * q] = __uint_as_float(wv[q] << 16);
-                        f[2 * q + 1] = __uint_as_float(wv[q] & 0xffff0000u);
-                    }
-                    *reinterpret_cast<float4*>(bcs + 8 * g8) = make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4*>(bcs + 8 * g8 + 4) = make_float4(f[4], f[5], f[6], f[7]);
-                }
-                Bf = bcs;
-            } else {
-                for (int e = tid; e < 2 * BCT; e += NTH) {
-                    const int isC = e >= BCT, j = (e % BCT) / NT, n = e % NT, t = k * TS + j;
-                    float v = 0.0f;
-                    if (t < L && n < N) {
-                        const size_t r = row0 + t;
-                        v = isC ? Act<T>::load(Cp + r * a.ld_C + n) : Act<T>::load(Bp + r * a.ld_B + n);
-                    }
-                    bcs[e] = v;
-                }
-                Bf = bcs;
-            }
-        }
-        // the staging buffer of this tile was last read by the stores of tile k-2
-        if (tid == 0 && k - kb >= 2) bulk_wait_read_1();
-        // every thread's wait succeeded, B|C are staged, the staging buffer is free
-        ok = __syncthreads_and(ok) != 0;
-        if (!ok) break;
+        const float* Bf = fwd_stage_bc<T, NT, TS>(bcs, tu + NTEN * TILE, bc_tma, Bp, Cp, a.ld_B,
+                                                  a.ld_C, row0, k, L, N, lane);
+        __syncwarp();
         const int jmax = min(TS, L - k * TS);
 
-        // Phase A: the per-step scalars of this lane's own steps j = 2i + half.
-        float odt[TH], obs[TH], ogz[TH], odu[TH];
+        // Phase A: the per-step scalars of the whole tile (independent across
+        // steps, so their dependency chains overlap).
+        float dtv[TS], bsv[TS], gzv[TS], duv[TS];
 #pragma unroll
-        for (int i = 0; i < TH; ++i) {
-            const int j = 2 * i + half;
-            const float uv = Act<T>::to_f(tu[j * CW + cl]);
-            const float xr = Act<T>::to_f(tr[j * CW + cl]);
+        for (int j = 0; j < TS; ++j) {
+            const float uv = Act<T>::to_f(tu[j * CW + lane]);
+            const float xr = Act<T>::to_f(tr[j * CW + lane]);
             float dt, gz = 1.0f;
             if (GATE) {
-                const float zv = Act<T>::to_f(tz[j * CW + cl]);
+                const float zv = Act<T>::to_f(tz[j * CW + lane]);
                 float sz;
                 softplus_sigmoid(xr, zv, dt, sz);
                 gz = zv * sz;                                   // silu(z)
@@ -244,61 +232,46 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
                 float e;
                 dt = softplus_e(xr, e);
             }
-            float bs = DISC == 0 ? dt * uv : uv;               // Euler: delta*u; ZOH: u
-            if (a.h_last && j >= jmax) dt = bs = 0.0f;         // past seqlen: keep the state
-            odt[i] = dt;
-            obs[i] = bs;
-            ogz[i] = gz;
-            odu[i] = Dd * uv;
+            dtv[j] = dt;
+            bsv[j] = DISC == 0 ? dt * uv : uv;                  // Euler: delta*u; ZOH: u
+            gzv[j] = gz;
+            duv[j] = Dd * uv;
+        }
+        if (a.h_last && jmax < TS) {
+            // steps past seqlen: delta = 0 keeps the state exactly (a = 1,
+            // beta u = 0), so it is the state after the last step at the end
+#pragma unroll
+            for (int j = 0; j < TS; ++j)
+                if (j >= jmax) dtv[j] = bsv[j] = 0.0f;
         }
 
-        // The lanes of a channel swap their delta and delta*u, so that each
-        // holds them for every step of the tile.
-        float dts[TS], bss[TS];
-#pragma unroll
-        for (int i = 0; i < TH; ++i) {
-            const float pdt = __shfl_xor_sync(0xffffffffu, odt[i], 16);
-            const float pbs = __shfl_xor_sync(0xffffffffu, obs[i], 16);
-            dts[2 * i] = half ? pdt : odt[i];
-            dts[2 * i + 1] = half ? odt[i] : pdt;
-            bss[2 * i] = half ? pbs : obs[i];
-            bss[2 * i + 1] = half ? obs[i] : pbs;
-        }
-
-        // Phase B: the recurrence over all TS steps (past seqlen the tiles and
-        // B|C are zero, so the extra steps evolve a state that is never stored,
-        // or, when the final state is asked for, leave it unchanged).  After
-        // each step pair the lanes swap y partials: each keeps the y of its
-        // own step.
-        float yo[TH];
-        float2 hck[NCK][NQ];                            // states at the chunk ends
-#pragma unroll
-        for (int i = 0; i < TH; ++i) {
-            float yp[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = 2 * i + e;
-                yp[e] = fwd_step<NL, DISC>(h, A2, Anat, invA, Bf + j * NT + n0, Bf + BCT + j * NT + n0,
-                                           dts[j], bss[j]);
-                if ((j + 1) % kChunk == 0) {
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) hck[j / kChunk][q] = h[q];
-                }
-            }
-            const float keep = half ? yp[1] : yp[0];
-            const float send = half ? yp[0] : yp[1];
-            yo[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16) + odu[i];
-        }
-
-        // Outputs of the own steps and the chunk-end states to the staging
-        // tiles, then TMA tile stores by one thread.
+        // Phase B: the recurrence.  Every tile runs all TS steps: past seqlen
+        // the TMA tiles and B|C are zero, so the extra steps only evolve a
+        // state that is never stored (or, when the final state is asked for,
+        // leave it unchanged: see above).  Outputs go to a staging tile in shared
+        // memory (double-buffered) and leave by TMA store; the store of tile
+        // k-2 must have finished reading its buffer first.
+        if (lane == 0 && k - kb >= 2) bulk_wait_read_1();
+        __syncwarp();
         T* so = ost + ((k - kb) & 1) * 2 * TILE;
         float* sc = ckst + ((k - kb) & 1) * NCK * NT * CW;
+        // The recurrence first, the staging stores after it: a store could
+        // alias the next step's B|C loads, which would then have to wait.
+        float yv[TS];
+        float2 hck[NCK][NQ];                            // states at the chunk ends
 #pragma unroll
-        for (int i = 0; i < TH; ++i) {
-            const int j = 2 * i + half;
-            so[j * CW + cl] = Act<T>::from_f(GATE ? yo[i] * ogz[i] : yo[i]);
-            if (save_y) so[TILE + j * CW + cl] = Act<T>::from_f(yo[i]);
+        for (int j = 0; j < TS; ++j) {
+            yv[j] = fwd_step<NT, DISC>(h, A2, Anat, invA, Bf + j * NT, Bf + BCT + j * NT, dtv[j], bsv[j]) +
+                    duv[j];
+            if ((j + 1) % kChunk == 0) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) hck[j / kChunk][q] = h[q];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < TS; ++j) {
+            so[j * CW + lane] = Act<T>::from_f(GATE ? yv[j] * gzv[j] : yv[j]);
+            if (save_y) so[TILE + j * CW + lane] = Act<T>::from_f(yv[j]);
         }
         if (save_ck) {
             // state after the last step of a chunk = checkpoint of the next one
@@ -306,13 +279,13 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             for (int m = 0; m < NCK; ++m)
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
-                    sc[(m * NT + n0 + 2 * q) * CW + cl] = hck[m][q].x;
-                    sc[(m * NT + n0 + 2 * q + 1) * CW + cl] = hck[m][q].y;
+                    sc[(m * NT + 2 * q) * CW + lane] = hck[m][q].x;
+                    sc[(m * NT + 2 * q + 1) * CW + lane] = hck[m][q].y;
                 }
         }
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        __syncwarp();
+        if (lane == 0) {
             tma_store_3d(&maps.out, so, c0, k * TS, b);
             if (save_y) tma_store_3d(&maps.y, so + TILE, c0, k * TS, b);
             if (save_ck) {
@@ -327,19 +300,18 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             if (k + S < ke) issue(k + S);
         }
     }
-    if (!ok && tid == 0) {
+    if (k < ke && lane == 0) {
         // A wait gave up: drain the copies still in flight (bounded) before exit.
         for (int kk = k; kk < ke && kk < k + S; ++kk)
             mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
     }
-    if (tid == 0) bulk_wait_all();   // the staged stores have left shared memory
-    if (a.h_last && ok && ke == ntiles && active) {
+    if (lane == 0) bulk_wait_all();   // the staged stores have left shared memory
+    if (a.h_last && k == ke && ke == ntiles && active) {
         float* hp = a.h_last + static_cast<size_t>(b) * N * a.dinner + d;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            const int n = n0 + 2 * q;
-            if (n < N) hp[static_cast<size_t>(n) * a.dinner] = h[q].x;
-            if (n + 1 < N) hp[static_cast<size_t>(n + 1) * a.dinner] = h[q].y;
+            if (2 * q < N) hp[static_cast<size_t>(2 * q) * a.dinner] = h[q].x;
+            if (2 * q + 1 < N) hp[static_cast<size_t>(2 * q + 1) * a.dinner] = h[q].y;
         }
     }
 }
@@ -547,7 +519,7 @@ static cudaError_t launch_fwd_t(const FwdMaps& m, const ScanFwdArgs& a, cudaStre
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    kern<<<dim3(gx, a.batch, a.nseg), 64, smem, st>>>(m, a);
+    kern<<<dim3(gx, a.batch, a.nseg), 32, smem, st>>>(m, a);
     return cudaGetLastError();
 }
 

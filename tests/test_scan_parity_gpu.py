@@ -3,7 +3,7 @@ shapes that span several tiles and chunks with ragged tails.  The backward
 uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
 otherwise; the wide cases below (short sequences, many channels) run the
 32-channel kernel, the rest the 16-channel one.  The forward scans time
-segments in parallel when batch * ceil(dinner / 32) < 152 and seqlen >= 512
+segments in parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512
 (the B2 L1000 case and the two marked below)."""
 import numpy as np
 import pytest
