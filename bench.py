@@ -105,7 +105,9 @@ def pipe_rates():
     try:
         with open(PIPE_RATES) as f:
             rec = json.load(f)
-        return (float(rec["ex2_per_clk_per_sm"]), float(rec["ffma_lanes_per_clk_per_sm"]),
+        fp32 = max(float(rec["ffma_lanes_per_clk_per_sm"]),
+                   float(rec.get("ffma2_lanes_per_clk_per_sm", 0.0)))
+        return (float(rec["ex2_per_clk_per_sm"]), fp32,
                 f"measured ({os.path.relpath(PIPE_RATES, ROOT)})")
     except (OSError, ValueError, KeyError):
         return EX2_PER_CLK_PER_SM_ASSUMED, FP32_LANES_PER_CLK_PER_SM_ASSUMED, "assumed"

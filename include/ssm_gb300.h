@@ -350,9 +350,11 @@ ssm_status ssm_block_split_weights(const ssm_block_desc* desc, const ssm_block_w
  * 256 threads; each thread runs 8 independent dependency chains (4 packed
  * pairs for kind 2) of `iters` steps, i.e. blocks*256*iters*8 lane-operations,
  * and writes one float per thread to sink (blocks*256 floats, device).  The
- * caller times the launch (CUDA events) and reads the SM clock.  Returns
- * SSM_ERR_SHAPE for a kind outside 0..2 or non-positive sizes, SSM_ERR_NULL
- * for a NULL sink, SSM_ERR_LAUNCH if the launch fails. */
+ * caller times the launch (CUDA events) and reads the SM clock.  Kinds 3 and
+ * 4 are for counting instructions, not rates: 4 packed chains whose FFMA2
+ * multiplier is a scalar broadcast to both halves (3) or a pair (4).
+ * Returns SSM_ERR_SHAPE for a kind outside 0..4 or non-positive sizes,
+ * SSM_ERR_NULL for a NULL sink, SSM_ERR_LAUNCH if the launch fails. */
 ssm_status ssm_probe_pipe(int32_t kind, int32_t blocks, int32_t iters, float* sink,
                           cudaStream_t stream);
 

@@ -31,21 +31,21 @@ __global__ void __launch_bounds__(kProbeThreads) pipe_probe_kernel(int iters, fl
 #pragma unroll
     for (int c = 0; c < 8; ++c) x[c] = 0.25f + 0.01f * c + 1e-6f * (tid & 255);
     if constexpr (KIND == 0) {
-#pragma unroll 1
+#pragma unroll 4
         for (int it = 0; it < iters; ++it)
 #pragma unroll
             for (int c = 0; c < 8; ++c) x[c] = ex2_neg(x[c]);
     } else if constexpr (KIND == 1) {
-#pragma unroll 1
+#pragma unroll 4
         for (int it = 0; it < iters; ++it)
 #pragma unroll
             for (int c = 0; c < 8; ++c) x[c] = fmaf(x[c], a, b);
-    } else {
+    } else if constexpr (KIND == 2) {
         float2 v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[c] = make_float2(x[2 * c], x[2 * c + 1]);
         const float2 a2 = make_float2(a, a), b2 = make_float2(b, b);
-#pragma unroll 1
+#pragma unroll 4
         for (int it = 0; it < iters; ++it)
 #pragma unroll
             for (int c = 0; c < 4; ++c) v[c] = __ffma2_rn(v[c], a2, b2);
@@ -53,6 +53,37 @@ __global__ void __launch_bounds__(kProbeThreads) pipe_probe_kernel(int iters, fl
         for (int c = 0; c < 4; ++c) {
             x[2 * c] = v[c].x;
             x[2 * c + 1] = v[c].y;
+        }
+    } else {
+        // 3: a packed FFMA2 whose multiplier is a scalar that changes every
+        // step, broadcast to both halves; 4: the same multiplier kept as a
+        // pair (updated with FFMA2).  Their instruction counts per step show
+        // what a scalar-to-pair broadcast costs.
+        float2 v[4], s2[4];
+        float s1[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            v[c] = make_float2(x[2 * c], x[2 * c + 1]);
+            s1[c] = 0.5f + 0.01f * c;
+            s2[c] = make_float2(s1[c], s1[c]);
+        }
+        const float2 a2 = make_float2(a, a), b2 = make_float2(b, b);
+#pragma unroll 1
+        for (int it = 0; it < iters; ++it)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if constexpr (KIND == 3) {
+                    s1[c] = fmaf(s1[c], a, b);
+                    v[c] = __ffma2_rn(v[c], make_float2(s1[c], s1[c]), b2);
+                } else {
+                    s2[c] = __ffma2_rn(s2[c], a2, b2);
+                    v[c] = __ffma2_rn(v[c], s2[c], b2);
+                }
+            }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            x[2 * c] = v[c].x + s1[c];
+            x[2 * c + 1] = v[c].y + s2[c].y;
         }
     }
     float s = 0.0f;
@@ -65,14 +96,16 @@ __global__ void __launch_bounds__(kProbeThreads) pipe_probe_kernel(int iters, fl
 
 extern "C" ssm_status ssm_probe_pipe(int32_t kind, int32_t blocks, int32_t iters, float* sink,
                                      cudaStream_t stream) {
-    if (kind < 0 || kind > 2 || blocks <= 0 || iters <= 0) return SSM_ERR_SHAPE;
+    if (kind < 0 || kind > 4 || blocks <= 0 || iters <= 0) return SSM_ERR_SHAPE;
     if (!sink) return SSM_ERR_NULL;
     // the inner loop is unrolled by 8 chains; a and b keep the fma chains in (0, 1)
     const float a = 0.999f, b = 0.0005f;
     switch (kind) {
         case 0: pipe_probe_kernel<0><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
         case 1: pipe_probe_kernel<1><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
-        default: pipe_probe_kernel<2><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+        case 2: pipe_probe_kernel<2><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+        case 3: pipe_probe_kernel<3><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
+        default: pipe_probe_kernel<4><<<blocks, kProbeThreads, 0, stream>>>(iters, a, b, sink); break;
     }
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
