@@ -222,6 +222,38 @@ ssm_status ssm_block_bwd(const ssm_block_desc* desc, const float* x,
                          const ssm_block_grads* grads,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---- A stack of blocks with activation checkpointing (the model of the
+ * pages "@seanhogg/builderforce-memory-engine 2026.7.14 -> 2026.9.28",
+ * src/training/model_cpu.js: forwardInternal runs the layers one after
+ * another; cpuModelBackward walks them last to first and, with activation
+ * checkpointing, recomputes each layer's forward from that layer's saved
+ * input before its backward -- the same gradients as keeping every
+ * activation).  Here: hidden_0 = x, hidden_{i+1} = block_i(hidden_i) for
+ * i < layers (each block with its own residual), out = hidden_layers.
+ *  - weights / grads: arrays of `layers` structs, one per layer, as for
+ *    ssm_block_fwd / ssm_block_bwd (all pointers required).
+ *  - ctx (ssm_stack_ctx_bytes, 16-byte aligned; may be NULL for one layer)
+ *    keeps only the layer inputs hidden_1 .. hidden_{layers-1}, (layers-1) x
+ *    batch*seqlen x dmodel fp32 -- not the per-layer block contexts.
+ *  - workspace (ssm_stack_workspace_bytes, 16-byte aligned) holds one block
+ *    context and one block workspace that every layer reuses, plus three
+ *    (batch*seqlen, dmodel) buffers for the backward.
+ *  - ssm_stack_bwd recomputes each layer's forward once (one extra block
+ *    forward per layer), then runs its backward; dx and every layer's
+ *    gradients are written.  x, weights and ctx must be those of the
+ *    matching ssm_stack_fwd call.
+ * Other rules as ssm_block_fwd / ssm_block_bwd; layers < 1 is SSM_ERR_SHAPE;
+ * 0 for an invalid descriptor from the size queries. */
+size_t ssm_stack_ctx_bytes(const ssm_block_desc* desc, int32_t layers);
+size_t ssm_stack_workspace_bytes(const ssm_block_desc* desc, int32_t layers);
+ssm_status ssm_stack_fwd(const ssm_block_desc* desc, int32_t layers, const float* x,
+                         const ssm_block_weights* weights, float* out, void* ctx, size_t ctx_bytes,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+ssm_status ssm_stack_bwd(const ssm_block_desc* desc, int32_t layers, const float* x,
+                         const ssm_block_weights* weights, const float* dout, const void* ctx,
+                         size_t ctx_bytes, float* dx, const ssm_block_grads* grads,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ssm_conv1d_silu_bwd without a workspace argument: the same result as
  * ssm_conv1d_silu_bwd, but the per-run dw/dbias partial sums live in scratch
  * that the library reserves once, as a fixed 8 MiB array in the device image,

@@ -32,6 +32,8 @@ __all__ = [
     "ssm_block_step_workspace_bytes", "ssm_block_step", "block_step", "ssm_block_fwd_state",
     "block_fwd_state", "ssm_block_weights_split_bytes", "ssm_block_split_weights",
     "block_split_weights", "ssm_conv1d_silu_bwd_noalloc", "ssm_probe_pipe",
+    "ssm_stack_ctx_bytes", "ssm_stack_workspace_bytes", "ssm_stack_fwd", "ssm_stack_bwd",
+    "stack_fwd", "stack_bwd",
     "SSM_OK", "SSM_ERR_NULL", "SSM_ERR_SHAPE", "SSM_ERR_ALIGN", "SSM_ERR_DTYPE",
     "SSM_ERR_WORKSPACE", "SSM_ERR_LAUNCH", "SSM_ERR_DEVICE",
     "EXPORTED_SYMBOLS",
@@ -57,7 +59,8 @@ EXPORTED_SYMBOLS = (
     "ssm_scan_step", "ssm_conv1d_silu_step", "ssm_conv1d_state_from_prompt",
     "ssm_block_step_workspace_bytes", "ssm_block_step", "ssm_block_fwd_state",
     "ssm_block_weights_split_bytes", "ssm_block_split_weights", "ssm_conv1d_silu_bwd_noalloc",
-    "ssm_probe_pipe",
+    "ssm_probe_pipe", "ssm_stack_ctx_bytes", "ssm_stack_workspace_bytes", "ssm_stack_fwd",
+    "ssm_stack_bwd",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -173,6 +176,16 @@ def load():
                                                            i64, vp, i64, vp, vp, vp]),
             # kind, blocks, iters, sink, stream
             "ssm_probe_pipe": (ctypes.c_int, [i32, i32, i32, vp, vp]),
+            "ssm_stack_ctx_bytes": (sz, [ctypes.POINTER(BlockDesc), i32]),
+            "ssm_stack_workspace_bytes": (sz, [ctypes.POINTER(BlockDesc), i32]),
+            # desc, layers, x, weights[layers], out, ctx, ctx_bytes, ws, ws_bytes, stream
+            "ssm_stack_fwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc), i32, vp,
+                                             ctypes.POINTER(BlockWeights), vp, vp, sz, vp, sz, vp]),
+            # desc, layers, x, weights[layers], dout, ctx, ctx_bytes, dx, grads[layers], ws,
+            # ws_bytes, stream
+            "ssm_stack_bwd": (ctypes.c_int, [ctypes.POINTER(BlockDesc), i32, vp,
+                                             ctypes.POINTER(BlockWeights), vp, vp, sz, vp,
+                                             ctypes.POINTER(BlockGrads), vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -425,6 +438,32 @@ def ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, workspace, stream=None
     _check("ssm_block_bwd", st)
 
 
+def ssm_stack_ctx_bytes(desc: BlockDesc, layers: int) -> int:
+    return load().ssm_stack_ctx_bytes(ctypes.byref(desc), layers)
+
+
+def ssm_stack_workspace_bytes(desc: BlockDesc, layers: int) -> int:
+    return load().ssm_stack_workspace_bytes(ctypes.byref(desc), layers)
+
+
+def ssm_stack_fwd(desc, x, layers, out, ctx, workspace, stream=None):
+    """layers: list of weight dicts keyed by BLOCK_PARAM_NAMES, one per layer."""
+    ws = (BlockWeights * len(layers))(*[_block_ptrs(BlockWeights, w) for w in layers])
+    st = load().ssm_stack_fwd(ctypes.byref(desc), len(layers), _ptr(x), ws, _ptr(out), _ptr(ctx),
+                              _nbytes(ctx), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    _check("ssm_stack_fwd", st)
+
+
+def ssm_stack_bwd(desc, x, layers, dout, ctx, dx, grads, workspace, stream=None):
+    """grads: list of gradient dicts (written), one per layer."""
+    ws = (BlockWeights * len(layers))(*[_block_ptrs(BlockWeights, w) for w in layers])
+    gs = (BlockGrads * len(grads))(*[_block_ptrs(BlockGrads, g) for g in grads])
+    st = load().ssm_stack_bwd(ctypes.byref(desc), len(layers), _ptr(x), ws, _ptr(dout), _ptr(ctx),
+                              _nbytes(ctx), _ptr(dx), gs, _ptr(workspace), _nbytes(workspace),
+                              _stream(stream))
+    _check("ssm_stack_bwd", st)
+
+
 # ----------------------------------------------------------------- allocating helpers
 
 def _bytes_tensor(nbytes, like):
@@ -603,4 +642,30 @@ def block_bwd(x, weights, dims, dout, ctx, *, disc=SSM_DISC_EULER, workspace=Non
     grads = {n: torch.empty_like(weights[n]) for n in BLOCK_PARAM_NAMES}
     ws = workspace if workspace is not None else _bytes_tensor(ssm_block_workspace_bytes(desc), x)
     ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, ws, stream)
+    return dx, grads
+
+
+def stack_fwd(x, layers, dims, *, disc=SSM_DISC_EULER, stream=None):
+    """Allocate out, the stack context (the layers' inputs; None for one
+    layer) and the workspace and run ssm_stack_fwd.  Returns (out, ctx,
+    workspace)."""
+    import torch
+    desc = block_desc(dims, disc)
+    out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ctx = _bytes_tensor(ssm_stack_ctx_bytes(desc, len(layers)), x)
+    ws = _bytes_tensor(ssm_stack_workspace_bytes(desc, len(layers)), x)
+    ssm_stack_fwd(desc, x, layers, out, ctx, ws, stream)
+    return out, ctx, ws
+
+
+def stack_bwd(x, layers, dims, dout, ctx, *, disc=SSM_DISC_EULER, workspace=None, stream=None):
+    """Allocate dx and every layer's gradients and run ssm_stack_bwd.  Returns
+    (dx, grads) with grads a list of dicts keyed by BLOCK_PARAM_NAMES."""
+    import torch
+    desc = block_desc(dims, disc)
+    dx = torch.empty_like(x, memory_format=torch.contiguous_format)
+    grads = [{n: torch.empty_like(w[n]) for n in BLOCK_PARAM_NAMES} for w in layers]
+    ws = workspace if workspace is not None else _bytes_tensor(
+        ssm_stack_workspace_bytes(desc, len(layers)), x)
+    ssm_stack_bwd(desc, x, layers, dout, ctx, dx, grads, ws, stream)
     return dx, grads

@@ -660,3 +660,123 @@ ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_bloc
 }
 
 }  // extern "C"
+
+// ---- A stack of blocks with activation checkpointing (the pages' model runs
+// its layers one after another, each block with its own residual, and its
+// backward recomputes every layer's forward from the layer's saved input
+// instead of keeping all layers' activations).  Host orchestration over the
+// block entry points above: one block context and one block workspace are
+// reused by every layer.
+namespace {
+
+struct StackWs {
+    size_t bctx, bws, tmp, g0, g1, total;
+};
+StackWs stack_ws_layout(const ssm_block_desc* d, const Dims& s) {
+    StackWs l{};
+    Carve cv;
+    const size_t act = static_cast<size_t>(s.M) * s.Dm * sizeof(float);
+    l.bctx = cv.take(ssm_block_ctx_bytes(d));
+    l.bws = cv.take(ssm_block_workspace_bytes(d));
+    l.tmp = cv.take(act);   // the recomputed forward's output (not needed, but written)
+    l.g0 = cv.take(act);    // dL/d(hidden) of alternate layers
+    l.g1 = cv.take(act);
+    l.total = cv.off;
+    return l;
+}
+size_t stack_ctx_bytes_of(const Dims& s, int layers) {
+    return static_cast<size_t>(layers - 1) * align256(static_cast<size_t>(s.M) * s.Dm * sizeof(float));
+}
+// Input of layer i (> 0): the output of layer i-1, kept in the stack context.
+float* stack_hidden(void* ctx, const Dims& s, int i) {
+    return reinterpret_cast<float*>(static_cast<char*>(ctx) +
+                                    static_cast<size_t>(i - 1) *
+                                        align256(static_cast<size_t>(s.M) * s.Dm * sizeof(float)));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_stack_ctx_bytes(const ssm_block_desc* d, int32_t layers) {
+    Dims s;
+    if (layers < 1 || check_desc(d, s) != SSM_OK) return 0;
+    return stack_ctx_bytes_of(s, layers);
+}
+
+size_t ssm_stack_workspace_bytes(const ssm_block_desc* d, int32_t layers) {
+    Dims s;
+    if (layers < 1 || check_desc(d, s) != SSM_OK) return 0;
+    return stack_ws_layout(d, s).total;
+}
+
+ssm_status ssm_stack_fwd(const ssm_block_desc* d, int32_t layers, const float* x,
+                         const ssm_block_weights* weights, float* out, void* ctx, size_t ctx_bytes,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (layers < 1) return SSM_ERR_SHAPE;
+    if (!weights) return SSM_ERR_NULL;
+    for (int i = 0; i < layers; ++i)
+        if (!all_weights(&weights[i])) return SSM_ERR_NULL;
+    if (s.M == 0) return SSM_OK;
+    if (!x || !out || !workspace || (layers > 1 && !ctx)) return SSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(workspace) || (ctx && !aligned16(ctx)))
+        return SSM_ERR_ALIGN;
+    const StackWs l = stack_ws_layout(d, s);
+    if (ctx_bytes < stack_ctx_bytes_of(s, layers) || workspace_bytes < l.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+    char* w = static_cast<char*>(workspace);
+    const float* h = x;
+    for (int i = 0; i < layers && st == SSM_OK; ++i) {
+        float* o = (i + 1 < layers) ? stack_hidden(ctx, s, i + 1) : out;
+        st = ssm_block_fwd(d, h, &weights[i], o, w + l.bctx, l.bws - l.bctx, w + l.bws, l.tmp - l.bws,
+                           stream);
+        h = o;
+    }
+    return st;
+}
+
+ssm_status ssm_stack_bwd(const ssm_block_desc* d, int32_t layers, const float* x,
+                         const ssm_block_weights* weights, const float* dout, const void* ctx,
+                         size_t ctx_bytes, float* dx, const ssm_block_grads* grads, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    Dims s;
+    ssm_status st = check_desc(d, s);
+    if (st != SSM_OK) return st;
+    if (layers < 1) return SSM_ERR_SHAPE;
+    if (!weights || !grads) return SSM_ERR_NULL;
+    for (int i = 0; i < layers; ++i)
+        if (!all_weights(&weights[i]) || !all_grads(&grads[i])) return SSM_ERR_NULL;
+    if (s.M == 0) {
+        // no rows: every gradient is zero (the block backward writes them)
+        for (int i = 0; i < layers && st == SSM_OK; ++i)
+            st = ssm_block_bwd(d, x, &weights[i], dout, ctx, 0, dx, &grads[i], workspace, 0, stream);
+        return st;
+    }
+    if (!x || !dout || !dx || !workspace || (layers > 1 && !ctx)) return SSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(dout) || !aligned16(dx) || !aligned16(workspace) ||
+        (ctx && !aligned16(ctx)))
+        return SSM_ERR_ALIGN;
+    const StackWs l = stack_ws_layout(d, s);
+    if (ctx_bytes < stack_ctx_bytes_of(s, layers) || workspace_bytes < l.total) return SSM_ERR_WORKSPACE;
+    if ((st = check_device()) != SSM_OK) return st;
+    char* w = static_cast<char*>(workspace);
+    void* hidden_ctx = const_cast<void*>(ctx);
+    const float* g = dout;   // dL/d(output of the current layer)
+    for (int i = layers - 1; i >= 0 && st == SSM_OK; --i) {
+        const float* h = i == 0 ? x : stack_hidden(hidden_ctx, s, i);
+        // recompute the layer's forward from its saved input, then its backward
+        st = ssm_block_fwd(d, h, &weights[i], reinterpret_cast<float*>(w + l.tmp), w + l.bctx,
+                           l.bws - l.bctx, w + l.bws, l.tmp - l.bws, stream);
+        if (st != SSM_OK) break;
+        float* dh = i == 0 ? dx : reinterpret_cast<float*>(w + ((i & 1) ? l.g1 : l.g0));
+        st = ssm_block_bwd(d, h, &weights[i], g, w + l.bctx, l.bws - l.bctx, dh, &grads[i], w + l.bws,
+                           l.tmp - l.bws, stream);
+        g = dh;
+    }
+    return st;
+}
+
+}  // extern "C"

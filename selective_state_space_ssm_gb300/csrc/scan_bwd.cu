@@ -85,7 +85,9 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     float* Pdy = Pbs + TILE;                                             // [TC][CW] dy
     float* part = Pdy + TILE;                                            // [TC][NQN][4][CW]
     float* pbuf = part + TC * NQN * 4 * CW;                              // [PR][PJ] dB or dC by channel group
-    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + PR * PJ);        // [S]
+    float* Psdr = pbuf + PR * PJ;                                        // [TC][CW] sigmoid(delta_raw)
+    float* Psz = Psdr + TILE;                                            // [TC][CW] sigmoid(z)
+    uint64_t* full = reinterpret_cast<uint64_t*>(Psz + TILE);            // [S]
 
     const int lane = threadIdx.x;
     const int cg = lane >> 2, ng = lane & 3;     // channel group (CPL channels), state group (NS states)
@@ -324,17 +326,19 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                     goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
                     zvA[jj] = GATE ? Act<T>::to_f(tz[j * CW + pc]) : 0.0f;
                 }
+                float sxA[NJ];
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
-                    float dt, dy = goA[jj];
+                    float dt, sx, dy = goA[jj];
                     if (GATE) {
                         float sz;
-                        softplus_sigmoid(xrA[jj], zvA[jj], dt, sz);
+                        softplus_sig_xz(xrA[jj], zvA[jj], dt, sx, sz);
                         dy = goA[jj] * zvA[jj] * sz;
+                        zvA[jj] = sz;                           // reuse: sigmoid(z)
                     } else {
-                        float e;
-                        dt = softplus_e(xrA[jj], e);
+                        softplus_sig_x(xrA[jj], dt, sx);
                     }
+                    sxA[jj] = sx;
                     xrA[jj] = dt;                               // reuse: delta
                     goA[jj] = dy;                               // reuse: dy
                     uvA[jj] = ZOH ? uvA[jj] : dt * uvA[jj];     // reuse: delta*u | u
@@ -345,6 +349,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                     Pd[j * CW + pc] = xrA[jj];
                     Pbs[j * CW + pc] = uvA[jj];
                     Pdy[j * CW + pc] = goA[jj];
+                    Psdr[j * CW + pc] = sxA[jj];
+                    if (GATE) Psz[j * CW + pc] = zvA[jj];
                 }
             }
             __syncwarp();
@@ -533,7 +539,8 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 constexpr int NJ = (CW == 32) ? 2 : NJALL;   // steps per load/compute/store block
 #pragma unroll 1
                 for (int jb = 0; jb < NJALL; jb += NJ) {
-                float Sg[NJ], Eg[NJ], Sa[NJ], uvA[NJ], xrA[NJ], dtA[NJ], dyA2[NJ], zvA[NJ], goA[NJ], yvA[NJ];
+                float Sg[NJ], Eg[NJ], Sa[NJ], uvA[NJ], sxA[NJ], dtA[NJ], dyA2[NJ], zvA[NJ], szA[NJ], goA[NJ],
+                    yvA[NJ];
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
                     const int j = SPL * (jb + jj) + pj;
@@ -555,10 +562,11 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                     Eg[jj] = sm[1] * kLn2;
                     Sa[jj] = sm[NQN - 1];
                     uvA[jj] = Act<T>::to_f(tu[j * CW + pc]);
-                    xrA[jj] = Act<T>::to_f(tr[j * CW + pc]);
+                    sxA[jj] = Psdr[j * CW + pc];
                     dtA[jj] = Pd[j * CW + pc];
                     dyA2[jj] = Pdy[j * CW + pc];
                     if (GATE) {
+                        szA[jj] = Psz[j * CW + pc];
                         zvA[jj] = Act<T>::to_f(tz[j * CW + pc]);
                         goA[jj] = Act<T>::to_f(tg[j * CW + pc]);
                         yvA[jj] = Act<T>::to_f(ty[j * CW + pc]);
@@ -569,10 +577,10 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 for (int jj = 0; jj < NJ; ++jj) {
                     const int j = SPL * (jb + jj) + pj;
                     duO[jj] = ZOH ? fmaf(Dd, dyA2[jj], Sg[jj]) : fmaf(dtA[jj], Sg[jj], Dd * dyA2[jj]);
-                    ddO[jj] = fmaf(uvA[jj], ZOH ? Sa[jj] : Sg[jj], Eg[jj]) * sigmoidf_(xrA[jj]);
+                    ddO[jj] = fmaf(uvA[jj], ZOH ? Sa[jj] : Sg[jj], Eg[jj]) * sxA[jj];
                     if (j < jmax) dD_acc = fmaf(dyA2[jj], uvA[jj], dD_acc);
                     if (GATE) {
-                        const float sz = sigmoidf_(zvA[jj]);
+                        const float sz = szA[jj];
                         dzO[jj] = goA[jj] * yvA[jj] * sz * (1.0f + zvA[jj] * (1.0f - sz));
                     }
                 }
@@ -871,6 +879,7 @@ static size_t bwd_smem_bytes() {
            + 3 * TC * CW * sizeof(float)               // delta, delta*u, dy
            + TC * NQN * 4 * CW * sizeof(float)         // state-sum partials
            + (CW == 32 ? TC : 4) * 9 * NT * sizeof(float)   // dB or dC partials by channel group
+           + 2 * TC * CW * sizeof(float)               // sigmoid(delta_raw), sigmoid(z)
            + kBwdStages * sizeof(uint64_t);
 }
 

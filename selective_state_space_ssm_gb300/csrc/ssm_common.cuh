@@ -117,6 +117,32 @@ __device__ __forceinline__ void softplus_sigmoid(float x, float z, float& sp, fl
     sig_z = r * a;
 }
 
+// softplus(x) together with sigmoid(x) and sigmoid(z), from e = exp(-|x|),
+// ez = exp(-z) and one reciprocal r = 1/((2+e)(1+ez)(1+e)): 1/(2+e) =
+// r(1+ez)(1+e), sigmoid(z) = 1/(1+ez) = r(2+e)(1+e), 1/(1+e) = r(2+e)(1+ez).
+// ez is capped at 2^100 as in softplus_sigmoid; the product stays below 2^103.
+__device__ __forceinline__ void softplus_sig_xz(float x, float z, float& sp, float& sig_x,
+                                                float& sig_z) {
+    const float e = ex2(-fabsf(x) * kLog2e);
+    const float ez = ex2(fminf(-z * kLog2e, 100.0f));
+    const float a = 2.0f + e, b = 1.0f + ez, c = 1.0f + e;
+    const float ab = a * b;
+    const float r = rcp(ab * c);
+    const float inv_c = r * ab;
+    sig_z = r * (a * c);
+    sp = fmaxf(x, 0.0f) + log1p_unit(e, r * (b * c));
+    sig_x = x >= 0.0f ? inv_c : e * inv_c;
+}
+// The same without a gate: r = 1/((2+e)(1+e)).
+__device__ __forceinline__ void softplus_sig_x(float x, float& sp, float& sig_x) {
+    const float e = ex2(-fabsf(x) * kLog2e);
+    const float a = 2.0f + e, c = 1.0f + e;
+    const float r = rcp(a * c);
+    const float inv_c = r * a;
+    sp = fmaxf(x, 0.0f) + log1p_unit(e, r * c);
+    sig_x = x >= 0.0f ? inv_c : e * inv_c;
+}
+
 // A = -exp(clamp(A_log, -10, 5)), returned pre-scaled by log2(e) so that
 // exp(delta * A) = ex2(delta * A2).
 __device__ __forceinline__ float a2_from_alog(float a_log) {
