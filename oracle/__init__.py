@@ -40,7 +40,7 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c99", "-Wall", "-Wno-maybe-uninitialized",
+        cmd = ["gcc", "-O2", "-std=c99", "-Wall", "-Wno-maybe-uninitialized", "-pthread",
                "-fno-fast-math", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
@@ -90,12 +90,13 @@ def _load():
                                                       _dp, _dp, _dp]
             lib.ssm_oracle_conv1d_silu_step.argtypes = [i, i, i, _dp, _dp, _dp, _dp, _dp]
             lib.ssm_oracle_linear_fwd.argtypes = [l, i, i, _dp, _dp, _dp, _dp]
+            lib.ssm_oracle_scan_mt.argtypes = [i, i, i, i, i, i] + [_dp] * 17
             lib.ssm_oracle_rmsnorm_fwd.argtypes = [l, i, _dp, _dp, _dp, _dp]
             for fn in ("ssm_oracle_scan_chain", "ssm_oracle_scan_fwd", "ssm_oracle_scan_bwd",
                        "ssm_oracle_conv1d_silu_fwd", "ssm_oracle_conv1d_silu_bwd",
                        "ssm_oracle_block_fwd", "ssm_oracle_block_bwd", "ssm_oracle_scan_step",
                        "ssm_oracle_scan_fwd_state", "ssm_oracle_conv1d_silu_step",
-                       "ssm_oracle_linear_fwd", "ssm_oracle_rmsnorm_fwd"):
+                       "ssm_oracle_linear_fwd", "ssm_oracle_rmsnorm_fwd", "ssm_oracle_scan_mt"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -114,7 +115,7 @@ def _check(rc, what):
         raise MemoryError(f"oracle {what} failed (rc={rc})")
 
 
-def scan_fwd(u, delta_raw, A_log, B, C, D, z=None, disc=EULER, batch=None):
+def scan_fwd(u, delta_raw, A_log, B, C, D, z=None, disc=EULER, batch=None, threads=1):
     """Selective scan forward.  u, delta_raw, z: (M, dinner); B, C: (M, dstate);
     A_log: (dinner, dstate); D: (dinner).  ``batch`` splits M = batch*seqlen.
     Returns (out, y) where y is the pre-gate scan output and out = y*silu(z)."""
@@ -127,15 +128,22 @@ def scan_fwd(u, delta_raw, A_log, B, C, D, z=None, disc=EULER, batch=None):
     seqlen = M // batch
     out = np.empty((M, dinner))
     y = np.empty((M, dinner))
-    rc = lib.ssm_oracle_scan_fwd(batch, seqlen, dinner, dstate, int(disc), _p(u), _p(dr), _p(Al),
-                                 _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(out), _p(y))
+    if threads > 1:   # the same chains on several host threads (timing of the CPU baseline)
+        rc = lib.ssm_oracle_scan_mt(int(threads), batch, seqlen, dinner, dstate, int(disc), _p(u),
+                                    _p(dr), _p(Al), _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(out), _p(y),
+                                    None, None, None, None, None, None, None, None)
+    else:
+        rc = lib.ssm_oracle_scan_fwd(batch, seqlen, dinner, dstate, int(disc), _p(u), _p(dr),
+                                     _p(Al), _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(out), _p(y))
     _check(rc, "scan_fwd")
     return out, y
 
 
-def scan_bwd(u, delta_raw, A_log, B, C, D, z, dout, disc=EULER, batch=None):
+def scan_bwd(u, delta_raw, A_log, B, C, D, z, dout, disc=EULER, batch=None, threads=1):
     """Selective scan backward.  Returns a dict with du, ddelta_raw, dA_log, dB, dC,
-    dD and dz (dz is None when z is None)."""
+    dD and dz (dz is None when z is None).  threads > 1 runs the chains of
+    disjoint channel blocks on that many host threads (dB, dC added in thread
+    order)."""
     lib = _load()
     u, dr, Al, Bm, Cm, Dv, g = map(_f64, (u, delta_raw, A_log, B, C, D, dout))
     zz = None if z is None else _f64(z)
@@ -150,9 +158,15 @@ def scan_bwd(u, delta_raw, A_log, B, C, D, z, dout, disc=EULER, batch=None):
     dC = np.empty((M, dstate))
     dD = np.empty((dinner,))
     dz = None if zz is None else np.empty((M, dinner))
-    rc = lib.ssm_oracle_scan_bwd(batch, seqlen, dinner, dstate, int(disc), _p(u), _p(dr), _p(Al),
-                                 _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(g), _p(du), _p(ddr), _p(dAl),
-                                 _p(dB), _p(dC), _p(dD), _p(dz))
+    if threads > 1:
+        rc = lib.ssm_oracle_scan_mt(int(threads), batch, seqlen, dinner, dstate, int(disc), _p(u),
+                                    _p(dr), _p(Al), _p(Bm), _p(Cm), _p(Dv), _p(zz), None, None,
+                                    _p(g), _p(du), _p(ddr), _p(dAl), _p(dB), _p(dC), _p(dD),
+                                    _p(dz))
+    else:
+        rc = lib.ssm_oracle_scan_bwd(batch, seqlen, dinner, dstate, int(disc), _p(u), _p(dr),
+                                     _p(Al), _p(Bm), _p(Cm), _p(Dv), _p(zz), _p(g), _p(du),
+                                     _p(ddr), _p(dAl), _p(dB), _p(dC), _p(dD), _p(dz))
     _check(rc, "scan_bwd")
     return dict(du=du, ddelta_raw=ddr, dA_log=dAl, dB=dB, dC=dC, dD=dD, dz=dz)
 

@@ -230,6 +230,100 @@ int ssm_oracle_scan_bwd(int batch, int seqlen, int dinner, int dstate, int disc,
     return 0;
 }
 
+/* ---------------- the same, over several host threads ----------------
+ * Timing aid for the CPU baseline: the chains of channels [d0, d1) of every
+ * batch row go to one POSIX thread, which runs ssm_oracle_scan_chain on each
+ * of them exactly as the sequential drivers above do.  du, ddt_raw, dz, out,
+ * y, dA_log and dD of a channel are written by its own thread only; dB and dC
+ * (sums over channels) are accumulated per thread and then added in thread
+ * order, so the result does not depend on the scheduling. */
+#include <pthread.h>
+
+typedef struct {
+    int batch, seqlen, dinner, dstate, disc, d0, d1, rc;
+    const double *u, *dt_raw, *A_log, *B, *C, *Dv, *z, *dout;
+    double *out, *y, *du, *ddt_raw, *dA_log, *dB, *dC, *dD, *dz;
+} scan_job_;
+
+static void* scan_job_run_(void* p) {
+    scan_job_* j = (scan_job_*)p;
+    j->rc = 0;
+    for (int b = 0; b < j->batch && !j->rc; ++b) {
+        size_t r0 = (size_t)b * j->seqlen;
+        for (int d = j->d0; d < j->d1 && !j->rc; ++d) {
+            size_t o = r0 * j->dinner + d;
+            const int bwd = j->dout != NULL;
+            j->rc = ssm_oracle_scan_chain(
+                j->seqlen, j->dstate, j->disc, j->u + o, j->dt_raw + o,
+                j->A_log + (size_t)d * j->dstate, j->B + r0 * j->dstate, j->C + r0 * j->dstate,
+                j->Dv[d], j->z ? j->z + o : NULL, j->dinner, j->dstate,
+                bwd ? NULL : j->out + o, (!bwd && j->y) ? j->y + o : NULL,
+                bwd ? j->dout + o : NULL, bwd ? j->du + o : NULL, bwd ? j->ddt_raw + o : NULL,
+                (bwd && j->z) ? j->dz + o : NULL, bwd ? j->dA_log + (size_t)d * j->dstate : NULL,
+                bwd ? j->dD + d : NULL, bwd ? j->dB + r0 * j->dstate : NULL,
+                bwd ? j->dC + r0 * j->dstate : NULL);
+        }
+    }
+    return NULL;
+}
+
+/* Forward (dout == NULL) or backward of the whole scan on `threads` threads;
+ * arguments as ssm_oracle_scan_fwd / ssm_oracle_scan_bwd. */
+int ssm_oracle_scan_mt(int threads, int batch, int seqlen, int dinner, int dstate, int disc,
+                       const double* u, const double* dt_raw, const double* A_log,
+                       const double* B, const double* C, const double* Dv, const double* z,
+                       double* out, double* y, const double* dout,
+                       double* du, double* ddt_raw, double* dA_log, double* dB, double* dC,
+                       double* dD, double* dz) {
+    if (threads < 1) threads = 1;
+    if (threads > dinner) threads = dinner > 0 ? dinner : 1;
+    const size_t M = (size_t)batch * seqlen, nbc = M * dstate;
+    scan_job_* jobs = (scan_job_*)calloc((size_t)threads, sizeof(scan_job_));
+    pthread_t* tids = (pthread_t*)calloc((size_t)threads, sizeof(pthread_t));
+    double* part = dout ? (double*)calloc((size_t)threads * 2 * (nbc ? nbc : 1), sizeof(double)) : NULL;
+    if (!jobs || !tids || (dout && !part)) {
+        free(jobs); free(tids); free(part);
+        return -1;
+    }
+    if (dout) {
+        memset(dA_log, 0, (size_t)dinner * dstate * sizeof(double));
+        memset(dD, 0, (size_t)dinner * sizeof(double));
+    }
+    int rc = 0, started = 0;
+    for (int t = 0; t < threads; ++t) {
+        scan_job_* j = &jobs[t];
+        j->batch = batch; j->seqlen = seqlen; j->dinner = dinner; j->dstate = dstate; j->disc = disc;
+        j->d0 = (int)((long)dinner * t / threads);
+        j->d1 = (int)((long)dinner * (t + 1) / threads);
+        j->u = u; j->dt_raw = dt_raw; j->A_log = A_log; j->B = B; j->C = C; j->Dv = Dv; j->z = z;
+        j->dout = dout; j->out = out; j->y = y; j->du = du; j->ddt_raw = ddt_raw;
+        j->dA_log = dA_log; j->dD = dD; j->dz = dz;
+        if (dout) {
+            j->dB = part + (size_t)t * 2 * nbc;
+            j->dC = j->dB + nbc;
+        }
+        if (pthread_create(&tids[t], NULL, scan_job_run_, j) != 0) { rc = -1; break; }
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) {
+        pthread_join(tids[t], NULL);
+        if (jobs[t].rc) rc = jobs[t].rc;
+    }
+    if (dout && !rc) {
+        for (size_t i = 0; i < nbc; ++i) {
+            double sb = 0.0, sc = 0.0;
+            for (int t = 0; t < threads; ++t) {
+                sb += part[(size_t)t * 2 * nbc + i];
+                sc += part[(size_t)t * 2 * nbc + nbc + i];
+            }
+            dB[i] = sb;
+            dC[i] = sc;
+        }
+    }
+    free(jobs); free(tids); free(part);
+    return rc;
+}
+
 /* ---------------- causal depthwise conv1d + SiLU ---------------- */
 
 /* mamba1_cpu.ts steps 4-5: pre[r,d] = bias[d] + sum_{k<K, t>=k} w[d*K+k] * x[r-k, d]

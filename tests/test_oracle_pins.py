@@ -412,3 +412,21 @@ def test_rmsnorm_weight_scales_each_feature_and_scale_invariance():
     np.testing.assert_allclose(y1000, yw, rtol=2e-6)
     ym, _ = oracle.rmsnorm_fwd(-x, w)
     np.testing.assert_array_equal(ym, -yw)
+
+
+def test_threaded_scan_equals_sequential():
+    """The host-threaded driver used for the CPU baseline runs the same chain
+    routine on channel blocks: per-channel outputs are identical, dB / dC
+    (sums over channels, added per thread) equal up to summation order."""
+    inp = workloads.scan_inputs(2, 120, 40, 5, seed=3, A_log_noise=0.3, clamp_frac=0.05)
+    args = (inp["u"], inp["delta_raw"], inp["A_log"], inp["B"], inp["C"], inp["D"], inp["z"])
+    for disc in (EULER, ZOH):
+        o1, y1 = oracle.scan_fwd(*args, disc, batch=2)
+        o2, y2 = oracle.scan_fwd(*args, disc, batch=2, threads=7)
+        assert np.array_equal(o1, o2) and np.array_equal(y1, y2)
+        a = oracle.scan_bwd(*args, inp["dout"], disc, batch=2)
+        b = oracle.scan_bwd(*args, inp["dout"], disc, batch=2, threads=7)
+        for k in ("du", "ddelta_raw", "dz", "dA_log", "dD"):
+            assert np.array_equal(a[k], b[k]), k
+        for k in ("dB", "dC"):
+            np.testing.assert_allclose(b[k], a[k], rtol=1e-12, atol=1e-13)
