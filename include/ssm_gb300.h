@@ -403,11 +403,19 @@ int ssm_abi_version(void);
 /* Fault bits recorded by the kernels since the last call, then cleared:
  * every wait of a kernel on an asynchronous copy is bounded, and a wait that
  * gives up sets a bit here (1: forward copy wait, 2: backward copy wait,
- * 4: drain after a failed wait, 8: block GEMM pipeline wait) instead of
- * hanging; that call's outputs are
+ * 4: drain after a failed wait, 8: block GEMM pipeline wait, 16: the
+ * self-test below) instead of hanging; that call's outputs are
  * then invalid.  Synchronous: call it after the work has completed.  Returns
  * 0 when no sm_103 device is current. */
 unsigned ssm_device_faults(void);
+
+/* Self-test of the bounded waits (no counterpart in the pages): launches one
+ * CTA that arms an mbarrier for a 16-byte copy that is never issued and waits
+ * on it with at most poll_limit polls (1 <= poll_limit <= 2^20, else
+ * SSM_ERR_SHAPE).  The wait gives up, the kernel returns, and the next
+ * ssm_device_faults() reports bit 16 -- the path every kernel's waits take
+ * when a copy does not arrive, without faulting or hanging the GPU. */
+ssm_status ssm_selftest_bounded_wait(uint32_t poll_limit, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ __all__ = [
     "block_fwd_state", "ssm_block_weights_split_bytes", "ssm_block_split_weights",
     "block_split_weights", "ssm_conv1d_silu_bwd_noalloc", "ssm_probe_pipe",
     "ssm_stack_ctx_bytes", "ssm_stack_workspace_bytes", "ssm_stack_fwd", "ssm_stack_bwd",
-    "stack_fwd", "stack_bwd",
+    "stack_fwd", "stack_bwd", "ssm_selftest_bounded_wait",
     "SSM_OK", "SSM_ERR_NULL", "SSM_ERR_SHAPE", "SSM_ERR_ALIGN", "SSM_ERR_DTYPE",
     "SSM_ERR_WORKSPACE", "SSM_ERR_LAUNCH", "SSM_ERR_DEVICE",
     "EXPORTED_SYMBOLS",
@@ -60,7 +60,7 @@ EXPORTED_SYMBOLS = (
     "ssm_block_step_workspace_bytes", "ssm_block_step", "ssm_block_fwd_state",
     "ssm_block_weights_split_bytes", "ssm_block_split_weights", "ssm_conv1d_silu_bwd_noalloc",
     "ssm_probe_pipe", "ssm_stack_ctx_bytes", "ssm_stack_workspace_bytes", "ssm_stack_fwd",
-    "ssm_stack_bwd",
+    "ssm_stack_bwd", "ssm_selftest_bounded_wait",
 )
 
 # The block's 13 parameters: the pages' names (Mamba1CpuWeights) in their order,
@@ -176,6 +176,7 @@ def load():
                                                            i64, vp, i64, vp, vp, vp]),
             # kind, blocks, iters, sink, stream
             "ssm_probe_pipe": (ctypes.c_int, [i32, i32, i32, vp, vp]),
+            "ssm_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, vp]),
             "ssm_stack_ctx_bytes": (sz, [ctypes.POINTER(BlockDesc), i32]),
             "ssm_stack_workspace_bytes": (sz, [ctypes.POINTER(BlockDesc), i32]),
             # desc, layers, x, weights[layers], out, ctx, ctx_bytes, ws, ws_bytes, stream
@@ -436,6 +437,12 @@ def ssm_block_bwd(desc, x, weights, dout, ctx, dx, grads, workspace, stream=None
                               _nbytes(ctx), _ptr(dx), ctypes.byref(g), _ptr(workspace),
                               _nbytes(workspace), _stream(stream))
     _check("ssm_block_bwd", st)
+
+
+def ssm_selftest_bounded_wait(poll_limit, stream=None):
+    """Run the bounded-wait self-test kernel (a wait that must give up)."""
+    _check("ssm_selftest_bounded_wait", load().ssm_selftest_bounded_wait(poll_limit,
+                                                                        _stream(stream)))
 
 
 def ssm_stack_ctx_bytes(desc: BlockDesc, layers: int) -> int:

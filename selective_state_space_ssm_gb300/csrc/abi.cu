@@ -738,12 +738,13 @@ int ssm_last_cuda_error(void) { return g_last_cuda_error; }
 int ssm_abi_version(void) { return SSM_GB300_ABI_VERSION; }
 
 unsigned ssm_device_faults(void) {
-    unsigned f1 = 0, f2 = 0, f3 = 0;
+    unsigned f1 = 0, f2 = 0, f3 = 0, f4 = 0;
     if (check_device() != SSM_OK) return 0;
     ssm::read_clear_fault_fwd(&f1);
     ssm::read_clear_fault_bwd(&f2);
     ssm::read_clear_fault_gemm(&f3);
-    return f1 | f2 | f3;
+    ssm::read_clear_fault_probe(&f4);
+    return f1 | f2 | f3 | f4;
 }
 
 }  // extern "C"

@@ -11,9 +11,24 @@
 // dead code.
 #include <cuda_runtime.h>
 
+#include "ssm_common.cuh"
 #include "ssm_gb300.h"
 
 namespace {
+
+// Self-test of the bounded waits: arm an mbarrier for 16 bytes of a copy that
+// is never issued and wait on it with at most `limit` polls.  The wait gives
+// up, records kFaultSelftest in this file's fault word and the kernel returns
+// (nothing is in flight, so the barrier can simply be abandoned).
+__global__ void bounded_wait_selftest_kernel(uint32_t limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ssm::mbar_init(&bar, 1);
+        ssm::fence_mbar_init();
+        ssm::mbar_arrive_expect_tx(&bar, 16);
+        ssm::mbar_wait(&bar, 0, ssm::kFaultSelftest, limit);
+    }
+}
 
 __device__ __forceinline__ float ex2_neg(float x) {
     float y;
@@ -109,3 +124,18 @@ extern "C" ssm_status ssm_probe_pipe(int32_t kind, int32_t blocks, int32_t iters
     }
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
+
+extern "C" ssm_status ssm_selftest_bounded_wait(uint32_t poll_limit, cudaStream_t stream) {
+    if (poll_limit == 0 || poll_limit > (1u << 20)) return SSM_ERR_SHAPE;
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(poll_limit);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+namespace ssm {
+cudaError_t read_clear_fault_probe(unsigned* out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_ssm_fault, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_ssm_fault, &zero, sizeof(unsigned));
+}
+}  // namespace ssm

@@ -157,5 +157,7 @@ cudaError_t launch_scan_reduce(const ScanReduceArgs& a, cudaStream_t stream);
 // Read and clear the fault word of the forward / backward translation unit.
 cudaError_t read_clear_fault_fwd(unsigned* out);
 cudaError_t read_clear_fault_bwd(unsigned* out);
+// ... and of the probe / self-test translation unit.
+cudaError_t read_clear_fault_probe(unsigned* out);
 
 }  // namespace ssm

@@ -26,6 +26,7 @@ constexpr float kALogHi = 5.0f;     // mamba1_cpu.ts A_LOG_CLAMP_HI
 constexpr unsigned kFaultFwdWait = 1u;
 constexpr unsigned kFaultBwdWait = 2u;
 constexpr unsigned kFaultDrain = 4u;
+constexpr unsigned kFaultSelftest = 16u;   // the bounded-wait self-test (probe.cu)
 
 // mbarrier polls before a wait gives up (each try_wait may itself suspend for
 // a hardware-chosen time slice, so this is far beyond any legitimate wait).
@@ -205,10 +206,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (and records `fault`) if it did not complete within kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned fault) {
+// (and records `fault`) if it did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned fault,
+                                          uint32_t limit = kWaitLimit) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
