@@ -137,6 +137,29 @@ def algorithmic(cfg):
     return fwd_bytes, bwd_bytes, exps
 
 
+# fp32 lane-operations per (step, channel, state) element that the
+# recurrences need at the least (Euler B): forward delta*A, delta*u*B, the
+# h update and the C.h readout (4); backward h recomputed (4: delta*A, a*h,
+# + delta*u*B, dC) and the reverse pass (8: C*dy, the g update, g*a*h, the
+# sums over states into ddelta and over time into dA, g*B, dB, delta*A).
+FP32_OPS_FWD, FP32_OPS_BWD = 4, 12
+
+
+def alu_roofline(cfg, t_fwd, t_bwd, lanes_per_clk, sm_mhz, rate_kind):
+    """The same step against the fp32 pipe: the recurrences' minimal fp32
+    lane-operations per element over the measured FFMA lane rate."""
+    el = cfg["batch"] * cfg["seqlen"] * cfg["dinner"] * cfg["dstate"]
+    peak = lanes_per_clk * SM_COUNT * sm_mhz * 1e6              # lane-ops / s
+    f, b = FP32_OPS_FWD * el, FP32_OPS_BWD * el
+    return {"unit": "Tlane-op/s", "peak": round(peak / 1e12, 3),
+            "peak_source": f"{rate_kind} {lanes_per_clk:.1f} fp32 lanes/clk/SM x {SM_COUNT} SMs x "
+                           f"{sm_mhz:.0f} MHz",
+            "ops_per_element": {"fwd": FP32_OPS_FWD, "bwd": FP32_OPS_BWD},
+            "fwd_frac": round(f / peak / (t_fwd * 1e-3), 4),
+            "bwd_frac": round(b / peak / (t_bwd * 1e-3), 4),
+            "step_frac": round((f + b) / peak / ((t_fwd + t_bwd) * 1e-3), 4)}
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -435,6 +458,7 @@ def run_gb300(args):
                               "NOT SAMPLED: max clock assumed, SFU terms invalid"},
         "valid": clock_known,
         "step_ms_x_mhz": round((t_fwd + t_bwd) * sm_mhz, 1),
+        "alu": alu_roofline(cfg, t_fwd, t_bwd, ffma_clk, sm_mhz, rate_kind),
         "step_frac": round((bound_fwd + bound_bwd) / ((t_fwd + t_bwd) * 1e-3), 4),
         "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4),
         "fwd_frac": round(bound_fwd / (t_fwd * 1e-3), 4),

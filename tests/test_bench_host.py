@@ -26,3 +26,15 @@ def test_decode_bytes():
     assert scan == 38_035_456
     # x, the 3 state slots in and out, out; taps and bias
     assert conv == 64 * 4096 * 4 * (1 + 2 * 3 + 1) + 4096 * 4 * 4 + 4096 * 4
+
+
+def test_alu_roofline_counts_the_recurrences_minimal_fp32_work():
+    import bench
+    cfg = dict(batch=8, seqlen=2048, dinner=4096, dstate=16)
+    el = 8 * 2048 * 4096 * 16
+    r = bench.alu_roofline(cfg, 1.0, 3.0, 128.0, 2000.0, "test")
+    peak = 128.0 * 152 * 2000e6
+    assert abs(r["peak"] - peak / 1e12) < 1e-3
+    assert abs(r["fwd_frac"] - 4 * el / peak / 1e-3) < 1e-4
+    assert abs(r["bwd_frac"] - 12 * el / peak / 3e-3) < 1e-4
+    assert abs(r["step_frac"] - 16 * el / peak / 4e-3) < 1e-4
