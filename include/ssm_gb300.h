@@ -157,11 +157,14 @@ ssm_status ssm_conv1d_silu_bwd(int32_t batch, int32_t seqlen, int32_t dinner, in
 
 /* Linear layer (cpu_ops.ts linearForward): Y (M, N) = X (M, K) W^T + bias
  * (+ R), fp32, on the tensor cores as three TF32 products of hi/lo splits
- * with the partial sums drained to fp32 every 128 K (about fp32 accuracy).
- * W is (N, K) as torch.nn.Linear stores it; row strides ldx, ldw, ldr, ldy in
- * elements (0 = packed); bias (N) and R (M, N) may be NULL; R may alias Y.
- * workspace (16-byte aligned) must hold ssm_linear_workspace_bytes(M, N, K)
- * bytes.  K = 0 is rejected (SSM_ERR_SHAPE). */
+ * that the GEMM forms from the fp32 tiles itself, with the partial sums
+ * drained to fp32 every 128 K (about fp32 accuracy).  W is (N, K) as
+ * torch.nn.Linear stores it; row strides ldx, ldw, ldr, ldy in elements
+ * (0 = packed); bias (N) and R (M, N) may be NULL; R may alias Y.  X and W
+ * are read in place when 16-byte aligned with a row stride that is a multiple
+ * of 4 elements, else copied into the workspace first.  workspace (16-byte
+ * aligned) must hold ssm_linear_workspace_bytes(M, N, K) bytes.  K = 0 is
+ * rejected (SSM_ERR_SHAPE). */
 size_t ssm_linear_workspace_bytes(int32_t M, int32_t N, int32_t K);
 ssm_status ssm_linear_fwd(int32_t M, int32_t N, int32_t K, const float* X, int64_t ldx,
                           const float* W, int64_t ldw, const float* bias, const float* R,
@@ -357,8 +360,9 @@ ssm_status ssm_block_fwd_state(const ssm_block_desc* desc, const float* x,
  * h (batch, dstate, dinner), laid out as for ssm_conv1d_silu_step and
  * ssm_scan_step and updated in place (zeros for new sequences).  The
  * projections run as in ssm_block_fwd (with batch rows); weights_split, if
- * not NULL, holds their TF32 halves made by ssm_block_split_weights for these
- * weights (else they are split at every call).  workspace (16-byte aligned)
+ * not NULL, holds the copies made by ssm_block_split_weights for these
+ * weights (else the weights are read in place, or copied into the workspace
+ * when not 16-byte aligned).  workspace (16-byte aligned)
  * must hold ssm_block_step_workspace_bytes(desc) bytes (0 for an invalid
  * descriptor).  Other rules as ssm_block_fwd. */
 size_t ssm_block_step_workspace_bytes(const ssm_block_desc* desc);
@@ -367,10 +371,11 @@ ssm_status ssm_block_step(const ssm_block_desc* desc, const float* x,
                           float* conv_state, float* h, float* out, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
-/* The TF32 hi/lo halves of the four projection weights, made once for many
- * ssm_block_step calls with the same weights (decode): split (16-byte
- * aligned) must hold ssm_block_weights_split_bytes(desc) bytes; batch and
- * seqlen of desc do not matter. */
+/* The four projection weights as the GEMM reads them (16-byte aligned copies,
+ * rows padded to a multiple of 4 floats), made once for many ssm_block_step
+ * calls with the same weights (decode): split (16-byte aligned) must hold
+ * ssm_block_weights_split_bytes(desc) bytes; batch and seqlen of desc do not
+ * matter.  (The GEMM forms the TF32 hi/lo halves itself.) */
 size_t ssm_block_weights_split_bytes(const ssm_block_desc* desc);
 ssm_status ssm_block_split_weights(const ssm_block_desc* desc, const ssm_block_weights* weights,
                                    void* split, size_t split_bytes, cudaStream_t stream);

@@ -618,7 +618,7 @@ def block_fwd_state(x, weights, dims, *, disc=SSM_DISC_EULER, stream=None):
 
 
 def block_split_weights(weights, dims, *, stream=None):
-    """The projection weights' TF32 halves for repeated block_step calls."""
+    """The projection weights prepared once (aligned copies) for repeated block_step calls."""
     desc = block_desc(dict(dims, seqlen=1))
     split = _bytes_tensor(ssm_block_weights_split_bytes(desc), weights["wInProj"])
     ssm_block_split_weights(desc, weights, split, stream)

@@ -2,7 +2,7 @@
 // (mamba1_cpu.ts mamba1CpuForward steps 1-11 and mamba1CpuBackward steps
 // 11-1; linear and RMSNorm as cpu_ops.ts defines them).  Host-side
 // orchestration only: every step runs in this library's kernels (RMSNorm,
-// TF32 split, tcgen05 GEMM, conv1d+SiLU, selective scan, column sums), in
+// operand transposes, tcgen05 GEMM, conv1d+SiLU, selective scan, column sums), in
 // stream order on the caller's stream, in caller-owned memory.
 #include <algorithm>
 #include <cstring>
@@ -106,7 +106,7 @@ Ctx ctx_layout(const Dims& s) {
 
 // Scratch shared by forward and backward (regions reused in stream order).
 struct Ws {
-    size_t a_hi, a_lo, b_hi, b_lo, w_hi, w_lo;            // TF32 splits
+    size_t a_hi, b_hi, w_hi;                              // copies of GEMM operands (transposed / aligned)
     size_t dg, du, ddelta, dxd, dxz, dxn;                 // backward activations
     size_t scan, conv, red, scanf, part, part_floats, total;
 };
@@ -123,11 +123,8 @@ Ws ws_layout(const Dims& s) {
     Carve c;
     Ws w;
     w.a_hi = c.take(static_cast<size_t>(ldM * wide) * f);
-    w.a_lo = c.take(static_cast<size_t>(ldM * wide) * f);
     w.b_hi = c.take(static_cast<size_t>(ldM * deep) * f);
-    w.b_lo = c.take(static_cast<size_t>(ldM * deep) * f);
     w.w_hi = c.take(wmax * f);
-    w.w_lo = c.take(wmax * f);
     w.dg = c.take(M * s.D * f);
     w.du = c.take(M * s.D * f);
     w.ddelta = c.take(M * s.D * f);
@@ -152,15 +149,16 @@ Ws ws_layout(const Dims& s) {
     return w;
 }
 
-// One GEMM operand: hi/lo TF32 halves of a (rows, cols) matrix, row stride ld.
+// One GEMM operand: a K-major (rows, cols) fp32 matrix with row stride ld
+// (16-byte aligned base and row stride, as TMA needs).
 struct Op {
-    const float* hi;
-    const float* lo;
+    const float* p;
     int rows, cols;
     int64_t ld;
 };
 
-bool encode_op(CUtensorMap* m, const float* p, const Op& o) {
+bool encode_op(CUtensorMap* m, const Op& o) {
+    const float* p = o.p;
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows)};
@@ -187,11 +185,14 @@ struct Run {
         if (ok() && s != SSM_OK) status = s;
     }
 
-    // Split x (rows, cols; stride ldx) into hi/lo, transposed or not.
-    Op split(const float* x, int64_t ldx, int rows, int cols, bool transpose, float* hi, float* lo) {
-        Op o{hi, lo, transpose ? cols : rows, transpose ? rows : cols, 0};
+    // x (rows, cols; stride ldx) as a GEMM operand, transposed or not: used in
+    // place when it is K-major and TMA-aligned, else copied (transposed) into buf.
+    Op operand(const float* x, int64_t ldx, int rows, int cols, bool transpose, float* buf) {
+        if (!transpose && aligned16(x) && (ldx * static_cast<int64_t>(sizeof(float))) % 16 == 0)
+            return Op{x, rows, cols, ldx};
+        Op o{buf, transpose ? cols : rows, transpose ? rows : cols, 0};
         o.ld = round4(o.cols);
-        if (ok()) cuda(ssm::launch_split_tf32(x, ldx, rows, cols, transpose ? 1 : 0, hi, lo, o.ld, st));
+        if (ok()) cuda(ssm::launch_operand_copy(x, ldx, rows, cols, transpose ? 1 : 0, buf, o.ld, st));
         return o;
     }
 
@@ -200,8 +201,7 @@ struct Run {
               int64_t ldr) {
         if (!ok()) return;
         ssm::GemmMaps maps;
-        if (!encode_op(&maps.a_hi, A.hi, A) || !encode_op(&maps.a_lo, A.lo, A) ||
-            !encode_op(&maps.b_hi, B.hi, B) || !encode_op(&maps.b_lo, B.lo, B)) {
+        if (!encode_op(&maps.a, A) || !encode_op(&maps.b, B)) {
             status = SSM_ERR_DEVICE;
             return;
         }
@@ -231,7 +231,7 @@ const T* at(const void* base, size_t off) {
 
 // Scratch of one decode step of the block (M = batch rows of one position).
 struct StepWs {
-    size_t xn, inv, xz, u, xd, draw, g, a_hi, a_lo, w_hi, w_lo, part, part_floats, total;
+    size_t xn, inv, xz, u, xd, draw, g, a_hi, w_hi, part, part_floats, total;
 };
 StepWs step_layout(const Dims& s) {
     const size_t f = sizeof(float), M = static_cast<size_t>(s.M);
@@ -248,9 +248,7 @@ StepWs step_layout(const Dims& s) {
     w.draw = c.take(M * s.D * f);
     w.g = c.take(M * s.D * f);
     w.a_hi = c.take(M * deep * f);
-    w.a_lo = c.take(M * deep * f);
     w.w_hi = c.take(wmax * f);
-    w.w_lo = c.take(wmax * f);
     const size_t biggest = std::max({M * 2 * s.D, M * static_cast<size_t>(s.Dm), M * static_cast<size_t>(s.P),
                                      M * static_cast<size_t>(s.D)});
     w.part_floats = std::min<size_t>(size_t(8) << 20, 4 * biggest);
@@ -259,12 +257,12 @@ StepWs step_layout(const Dims& s) {
     return w;
 }
 
-// TF32 hi/lo halves of the four projection weights, (rows, round4(cols))
-// each, for decode steps that reuse them: in_proj (2 dinner, dmodel), x_proj
-// (dtrank + 2 dstate, dinner), dt_proj (dinner, dtrank), out_proj (dmodel,
-// dinner).
+// The four projection weights as the GEMM reads them -- 16-byte aligned
+// copies with rows padded to a multiple of 4 floats -- for decode steps that
+// reuse them: in_proj (2 dinner, dmodel), x_proj (dtrank + 2 dstate, dinner),
+// dt_proj (dinner, dtrank), out_proj (dmodel, dinner).
 struct SplitW {
-    size_t hi[4], lo[4], total;
+    size_t hi[4], total;
     int rows[4], cols[4];
 };
 SplitW split_layout(const Dims& s) {
@@ -277,7 +275,6 @@ SplitW split_layout(const Dims& s) {
         w.cols[i] = cols[i];
         const size_t bytes = static_cast<size_t>(rows[i]) * round4(cols[i]) * sizeof(float);
         w.hi[i] = c.take(bytes);
-        w.lo[i] = c.take(bytes);
     }
     w.total = c.off;
     return w;
@@ -299,8 +296,8 @@ extern "C" {
 size_t ssm_linear_workspace_bytes(int32_t M, int32_t N, int32_t K) {
     if (M < 0 || N < 0 || K < 0) return 0;
     const size_t f = sizeof(float);
-    return 2 * align256(static_cast<size_t>(M) * round4(K) * f) +
-           2 * align256(static_cast<size_t>(N) * round4(K) * f);
+    return align256(static_cast<size_t>(M) * round4(K) * f) +
+           align256(static_cast<size_t>(N) * round4(K) * f);
 }
 
 ssm_status ssm_linear_fwd(int32_t M, int32_t N, int32_t K, const float* X, int64_t ldx,
@@ -323,13 +320,11 @@ ssm_status ssm_linear_fwd(int32_t M, int32_t N, int32_t K, const float* X, int64
     if (K == 0) return SSM_ERR_SHAPE;
     const size_t f = sizeof(float);
     const size_t xa = align256(static_cast<size_t>(M) * round4(K) * f);
-    float* xhi = static_cast<float*>(workspace);
-    float* xlo = at<float>(workspace, xa);
-    float* whi = at<float>(workspace, 2 * xa);
-    float* wlo = at<float>(workspace, 2 * xa + align256(static_cast<size_t>(N) * round4(K) * f));
+    float* xbuf = static_cast<float*>(workspace);
+    float* wbuf = at<float>(workspace, xa);
     Run run{stream};
-    Op A = run.split(X, ldx, M, K, false, xhi, xlo);
-    Op B = run.split(W, ldw, N, K, false, whi, wlo);
+    Op A = run.operand(X, ldx, M, K, false, xbuf);
+    Op B = run.operand(W, ldw, N, K, false, wbuf);
     run.gemm(A, B, Y, ldy, bias, R, ldr);
     return run.status;
 }
@@ -391,31 +386,29 @@ ssm_status block_fwd_impl(const ssm_block_desc* d, const float* x, const ssm_blo
     float* draw = at<float>(ctx, c.draw);
     float* g = at<float>(ctx, c.g);
     float* ahi = at<float>(workspace, ws.a_hi);
-    float* alo = at<float>(workspace, ws.a_lo);
     float* whi = at<float>(workspace, ws.w_hi);
-    float* wlo = at<float>(workspace, ws.w_lo);
 
     Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
     // 1. RMSNorm
     run.cuda(ssm::launch_rmsnorm_fwd(x, w->norm_w, M, Dm, kRmsEps, xn, inv, stream));
     // 2. in_proj (x_in | z)
     {
-        Op A = run.split(xn, Dm, M, Dm, false, ahi, alo);
-        Op W = run.split(w->in_proj_w, Dm, 2 * D, Dm, false, whi, wlo);
+        Op A = run.operand(xn, Dm, M, Dm, false, ahi);
+        Op W = run.operand(w->in_proj_w, Dm, 2 * D, Dm, false, whi);
         run.gemm(A, W, xz, 2 * D, w->in_proj_b, nullptr, 0);
     }
     // 4-5. causal conv1d + SiLU on the x_in columns
     if (run.ok()) run.check(ssm_conv1d_silu(s.B, s.L, D, s.K, xz, 2 * D, w->conv_w, w->conv_b, u, D, stream));
     // 6. x_proj -> (dt | B | C)
     {
-        Op A = run.split(u, D, M, D, false, ahi, alo);
-        Op W = run.split(w->x_proj_w, D, P, D, false, whi, wlo);
+        Op A = run.operand(u, D, M, D, false, ahi);
+        Op W = run.operand(w->x_proj_w, D, P, D, false, whi);
         run.gemm(A, W, xd, P, w->x_proj_b, nullptr, 0);
     }
     // 7. dt_proj -> delta_raw
     {
-        Op A = run.split(xd, P, M, R, false, ahi, alo);
-        Op W = run.split(w->dt_proj_w, R, D, R, false, whi, wlo);
+        Op A = run.operand(xd, P, M, R, false, ahi);
+        Op W = run.operand(w->dt_proj_w, R, D, R, false, whi);
         run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
     }
     // the conv's state after the last position (its last kconv-1 inputs)
@@ -430,8 +423,8 @@ ssm_status block_fwd_impl(const ssm_block_desc* d, const float* x, const ssm_blo
     }
     // 10-11. out_proj + residual
     {
-        Op A = run.split(g, D, M, D, false, ahi, alo);
-        Op W = run.split(w->out_proj_w, D, Dm, D, false, whi, wlo);
+        Op A = run.operand(g, D, M, D, false, ahi);
+        Op W = run.operand(w->out_proj_w, D, Dm, D, false, whi);
         run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
     }
     return run.status;
@@ -473,8 +466,8 @@ ssm_status ssm_block_split_weights(const ssm_block_desc* d, const ssm_block_weig
     const float* src[4] = {w->in_proj_w, w->x_proj_w, w->dt_proj_w, w->out_proj_w};
     Run run{stream};
     for (int i = 0; i < 4; ++i)
-        run.split(src[i], sw.cols[i], sw.rows[i], sw.cols[i], false, at<float>(split, sw.hi[i]),
-                  at<float>(split, sw.lo[i]));
+        run.cuda(ssm::launch_operand_copy(src[i], sw.cols[i], sw.rows[i], sw.cols[i], 0,
+                                          at<float>(split, sw.hi[i]), round4(sw.cols[i]), stream));
     return run.status;
 }
 
@@ -500,13 +493,12 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     const StepWs ws = step_layout(s);
     if (workspace_bytes < ws.total) return SSM_ERR_WORKSPACE;
     const SplitW sw = split_layout(s);
-    // weight operand i: the caller's halves, or split now into the workspace
+    // weight operand i: the caller's prepared copy, or the weight itself
+    // (copied into the workspace only if it is not TMA-aligned)
     auto weight = [&](Run& run, int i, const float* W) {
         if (weights_split)
-            return Op{at<float>(weights_split, sw.hi[i]), at<float>(weights_split, sw.lo[i]), sw.rows[i],
-                      sw.cols[i], round4(sw.cols[i])};
-        return run.split(W, sw.cols[i], sw.rows[i], sw.cols[i], false, at<float>(workspace, ws.w_hi),
-                         at<float>(workspace, ws.w_lo));
+            return Op{at<float>(weights_split, sw.hi[i]), sw.rows[i], sw.cols[i], round4(sw.cols[i])};
+        return run.operand(W, sw.cols[i], sw.rows[i], sw.cols[i], false, at<float>(workspace, ws.w_hi));
     };
     if ((st = check_device()) != SSM_OK) return st;
 
@@ -519,14 +511,13 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     float* draw = at<float>(workspace, ws.draw);
     float* g = at<float>(workspace, ws.g);
     float* ahi = at<float>(workspace, ws.a_hi);
-    float* alo = at<float>(workspace, ws.a_lo);
 
     Run run{stream, at<float>(workspace, ws.part), ws.part_floats};
     // 1. RMSNorm
     run.cuda(ssm::launch_rmsnorm_fwd(x, w->norm_w, M, Dm, kRmsEps, xn, inv, stream));
     // 2. in_proj (x_in | z)
     {
-        Op A = run.split(xn, Dm, M, Dm, false, ahi, alo);
+        Op A = run.operand(xn, Dm, M, Dm, false, ahi);
         Op W = weight(run, 0, w->in_proj_w);
         run.gemm(A, W, xz, 2 * D, w->in_proj_b, nullptr, 0);
     }
@@ -535,13 +526,13 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
         run.check(ssm_conv1d_silu_step(M, D, s.K, xz, 2 * D, w->conv_w, w->conv_b, conv_state, u, D, stream));
     // 6. x_proj -> (dt | B | C)
     {
-        Op A = run.split(u, D, M, D, false, ahi, alo);
+        Op A = run.operand(u, D, M, D, false, ahi);
         Op W = weight(run, 1, w->x_proj_w);
         run.gemm(A, W, xd, P, w->x_proj_b, nullptr, 0);
     }
     // 7. dt_proj -> delta_raw
     {
-        Op A = run.split(xd, P, M, R, false, ahi, alo);
+        Op A = run.operand(xd, P, M, R, false, ahi);
         Op W = weight(run, 2, w->dt_proj_w);
         run.gemm(A, W, draw, D, w->dt_proj_b, nullptr, 0);
     }
@@ -552,7 +543,7 @@ ssm_status ssm_block_step(const ssm_block_desc* d, const float* x, const ssm_blo
     }
     // 10-11. out_proj + residual
     {
-        Op A = run.split(g, D, M, D, false, ahi, alo);
+        Op A = run.operand(g, D, M, D, false, ahi);
         Op W = weight(run, 3, w->out_proj_w);
         run.gemm(A, W, out, Dm, w->out_proj_b, x, Dm);
     }
@@ -600,11 +591,8 @@ ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_bloc
     const float* draw = at<float>(ctx, c.draw);
     const float* g = at<float>(ctx, c.g);
     float* ahi = at<float>(workspace, ws.a_hi);
-    float* alo = at<float>(workspace, ws.a_lo);
     float* bhi = at<float>(workspace, ws.b_hi);
-    float* blo = at<float>(workspace, ws.b_lo);
     float* whi = at<float>(workspace, ws.w_hi);
-    float* wlo = at<float>(workspace, ws.w_lo);
     float* dg = at<float>(workspace, ws.dg);
     float* du = at<float>(workspace, ws.du);
     float* ddelta = at<float>(workspace, ws.ddelta);
@@ -621,12 +609,12 @@ ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_bloc
     auto linear_bwd = [&](const float* dY, int64_t lddy, int nout, const float* X, int64_t ldx, int k,
                           const float* W, float* dX, int64_t lddx, bool accumulate, float* dW, float* db) {
         if (dX) {
-            Op A = run.split(dY, lddy, M, nout, false, ahi, alo);
-            Op Wt = run.split(W, k, nout, k, true, whi, wlo);   // (k, nout)
+            Op A = run.operand(dY, lddy, M, nout, false, ahi);
+            Op Wt = run.operand(W, k, nout, k, true, whi);   // (k, nout)
             run.gemm(A, Wt, dX, lddx, nullptr, accumulate ? dX : nullptr, lddx);
         }
-        Op At = run.split(dY, lddy, M, nout, true, ahi, alo);   // (nout, M)
-        Op Xt = run.split(X, ldx, M, k, true, bhi, blo);        // (k, M)
+        Op At = run.operand(dY, lddy, M, nout, true, ahi);   // (nout, M)
+        Op Xt = run.operand(X, ldx, M, k, true, bhi);        // (k, M)
         run.gemm(At, Xt, dW, k, nullptr, nullptr, 0);
         if (run.ok()) run.cuda(ssm::launch_colsum(dY, lddy, M, nout, db, red, stream));
     };

@@ -1,19 +1,25 @@
 // gemm.cu -- fp32-accurate tensor-core GEMM for the Mamba-1 block projections
 // (cpu_ops.ts linearForward / linearBackward: Y = X W^T + b, dX = dY W,
-// dW = dY^T X), plus the TF32 hi/lo split and deterministic column sums.
+// dW = dY^T X), plus operand copies (transposes) and deterministic column
+// sums.
 //
 // sm_103a design: one CTA computes a 128 x 128 tile of C = A B^T with
 // tcgen05.mma (kind::tf32, cta_group::1, M = 128, N = 128, K = 8 per
-// instruction) accumulating in tensor memory.  Warp 0 streams 128 x 32 fp32
-// tiles of A_hi, A_lo, B_hi, B_lo with TMA (128-byte swizzle) through a
-// three-stage mbarrier pipeline; one thread of warp 1 issues the MMAs
-// (A_hi B_hi + A_hi B_lo + A_lo B_hi per k-step: the three-pass TF32 split,
-// which keeps the product at about fp32 accuracy); warps 2-5 read the
-// accumulator back with tcgen05.ld and apply bias / residual.  The tensor
-// core's fp32 accumulation drifts in one direction (its error grows linearly
-// with K), so the accumulator is double-buffered in tensor memory and read back
-// into fp32 registers every kGemmGroup K-blocks.  Every mbarrier
-// wait is bounded; tensor memory is always released.
+// instruction) accumulating in tensor memory, as three TF32 products
+// A_hi B_hi + A_hi B_lo + A_lo B_hi (about fp32 accuracy).  The tensor core
+// reads a tf32 operand from an fp32 word and ignores its low 13 mantissa
+// bits, so the raw fp32 tiles serve as the "hi" operands: warp 0 streams
+// 128 x 32 fp32 tiles of A and B with TMA (128-byte swizzle) through a
+// three-stage mbarrier pipeline, and the four epilogue warps (2-5) write the
+// "lo" tiles (x minus x with its low 13 mantissa bits cleared: exact) next to
+// them in shared memory, at the same swizzled offsets; one thread of warp 1
+// issues the MMAs.  Compared with splitting the operands into hi/lo arrays
+// beforehand, half the operand bytes cross L2 and no split pass runs.  The
+// tensor core's fp32 accumulation drifts in one direction (its error grows
+// linearly with K), so the accumulator is double-buffered in tensor memory and
+// read back into fp32 registers every kGemmGroup K-blocks by the same
+// epilogue warps, one group behind the conversion.  Every mbarrier wait is
+// bounded; tensor memory is always released.
 #include <algorithm>
 
 #include "gemm_args.cuh"
@@ -24,6 +30,8 @@ namespace ssm {
 constexpr unsigned kFaultGemm = 8u;
 constexpr uint32_t kTmemCols = 2 * kGemmBN;                     // two fp32 accumulators
 constexpr uint32_t kOpTileBytes = kGemmBM * kGemmBK * 4;         // 16 KB (BM == BN)
+// A stage holds [A raw][B raw][A lo][B lo], 16 KB each.
+constexpr int kTileFloats = kGemmBM * kGemmBK;
 static_assert(kGemmBM == kGemmBN, "square tiles share one tile size");
 
 // Shared-memory matrix descriptor of a K-major operand tile laid out by TMA
@@ -99,9 +107,10 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * 4 * kOpTileBytes);
-    uint64_t* empty = full + S;
-    uint64_t* acc_full = empty + S;    // [2] a partial accumulator is complete
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * 4 * kOpTileBytes);   // raw tiles landed
+    uint64_t* conv = full + S;           // [S] the lo tiles are written (one arrival per epilogue warp)
+    uint64_t* empty = conv + S;          // [S] the MMAs have read the stage
+    uint64_t* acc_full = empty + S;      // [2] a partial accumulator is complete
     uint64_t* acc_empty = acc_full + 2;  // [2] the epilogue has read it back
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
@@ -118,6 +127,7 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&conv[s], 4);      // one arrival per epilogue warp
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -136,18 +146,16 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {   // TMA producer
+        if (lane == 0) {   // TMA producer: the raw fp32 tiles of A and B
             int kb = 0;
             for (; kb < nk; ++kb) {
                 const int s = kb % S;
                 if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, kFaultGemm)) break;
                 unsigned char* st = smem + s * 4 * kOpTileBytes;
-                mbar_arrive_expect_tx(&full[s], 4 * kOpTileBytes);
+                mbar_arrive_expect_tx(&full[s], 2 * kOpTileBytes);
                 const int kx = (kb0 + kb) * kGemmBK;
-                tma_load_2d(st, &maps.a_hi, &full[s], kx, m0);
-                tma_load_2d(st + kOpTileBytes, &maps.a_lo, &full[s], kx, m0);
-                tma_load_2d(st + 2 * kOpTileBytes, &maps.b_hi, &full[s], kx, n0);
-                tma_load_2d(st + 3 * kOpTileBytes, &maps.b_lo, &full[s], kx, n0);
+                tma_load_2d(st, &maps.a, &full[s], kx, m0);
+                tma_load_2d(st + kOpTileBytes, &maps.b, &full[s], kx, n0);
             }
             // copies still in flight land before the CTA may exit (bounded)
             for (int j = std::max(0, kb - S); j < kb; ++j)
@@ -165,7 +173,7 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 const int kb1 = std::min(nk, (gi + 1) * G);
                 for (int kb = gi * G; kb < kb1; ++kb) {
                     const int s = kb % S;
-                    if (!mbar_wait(&full[s], (kb / S) & 1, kFaultGemm)) {
+                    if (!mbar_wait(&conv[s], (kb / S) & 1, kFaultGemm)) {
                         ok = false;
                         break;
                     }
@@ -175,8 +183,8 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     for (int kk = 0; kk < kGemmBK / 8; ++kk) {
                         const uint32_t off = kk * 32;   // 8 tf32 = 32 bytes along K
                         const uint64_t ahi = umma_desc_sw128(st + off);
-                        const uint64_t alo = umma_desc_sw128(st + kOpTileBytes + off);
-                        const uint64_t bhi = umma_desc_sw128(st + 2 * kOpTileBytes + off);
+                        const uint64_t bhi = umma_desc_sw128(st + kOpTileBytes + off);
+                        const uint64_t alo = umma_desc_sw128(st + 2 * kOpTileBytes + off);
                         const uint64_t blo = umma_desc_sw128(st + 3 * kOpTileBytes + off);
                         umma_tf32(d, ahi, bhi, (kb != gi * G || kk != 0) ? 1u : 0u);
                         umma_tf32(d, ahi, blo, 1u);
@@ -187,17 +195,19 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 umma_commit(&acc_full[buf]);  // this group's partial sum is complete
             }
         }
-    } else {   // warps 2..5: epilogue, TMEM lane quadrant = warp % 4
+    } else {   // warps 2..5: lo tiles, then the epilogue; TMEM lane quadrant = warp % 4
         const int q = warp & 3;
+        const int et = threadIdx.x - 64;   // 0..127
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
         // Each group's partial sum (at most G K-blocks, accumulated by the tensor
-        // core) is added into fp32 registers here, so the tensor core's own
+        // core) is added into fp32 registers, so the tensor core's own
         // accumulation never spans more than G * kGemmBK products.
         float acc[kGemmBN];
 #pragma unroll
         for (int j = 0; j < kGemmBN; ++j) acc[j] = 0.0f;
         bool got = true;
-        for (int gi = 0; gi < ngroups; ++gi) {
+        int drained = 0;
+        auto drain = [&](int gi) {
             const int buf = gi & 1;
             got = mbar_wait(&acc_full[buf], (gi >> 1) & 1, kFaultGemm) && got;
             __syncwarp();
@@ -213,8 +223,38 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            if (!got) break;
+        };
+        for (int kb = 0; kb < nk && got; ++kb) {
+            const int s = kb % S;
+            // lo = x - (x with its low 13 mantissa bits cleared), for both raw
+            // tiles of the stage, at the same (swizzled) offsets
+            got = mbar_wait(&full[s], (kb / S) & 1, kFaultGemm) && got;
+            if (got) {
+                const float4* src = reinterpret_cast<const float4*>(smem + s * 4 * kOpTileBytes);
+                float4* dst = reinterpret_cast<float4*>(smem + s * 4 * kOpTileBytes + 2 * kOpTileBytes);
+#pragma unroll
+                for (int i0 = 0; i0 < 2 * kTileFloats / 4 / 128; i0 += 4) {
+                    float4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[u] = src[et + 128 * (i0 + u)];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float4 w;
+                        w.x = v[u].x - __uint_as_float(__float_as_uint(v[u].x) & 0xFFFFE000u);
+                        w.y = v[u].y - __uint_as_float(__float_as_uint(v[u].y) & 0xFFFFE000u);
+                        w.z = v[u].z - __uint_as_float(__float_as_uint(v[u].z) & 0xFFFFE000u);
+                        w.w = v[u].w - __uint_as_float(__float_as_uint(v[u].w) & 0xFFFFE000u);
+                        dst[et + 128 * (i0 + u)] = w;
+                    }
+                }
+                fence_proxy_async_smem();   // the tensor core reads them through the async proxy
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[s]);
+            // read back the groups that are a full group behind the conversion
+            while (got && drained < (kb + 1) / G - 1) drain(drained++);
         }
+        while (got && drained < ngroups) drain(drained++);
         // The operand stages are idle once the last group is complete: each
         // warp turns its 32 x 32 sub-tiles around through a padded slice of
         // stage 0 so that global stores run along rows.
@@ -288,7 +328,7 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs a) {
 cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.ksplit < 1 || (a.ksplit > 1 && !a.part)) return cudaErrorInvalidValue;
-    const size_t smem = kGemmStages * 4 * kOpTileBytes + (2 * kGemmStages + 4) * 8 + 16 + 1024;
+    const size_t smem = kGemmStages * 4 * kOpTileBytes + (3 * kGemmStages + 4) * 8 + 16 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -302,30 +342,21 @@ cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStre
     return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- TF32 split
+// ---------------------------------------------------------------- operand copies
 
-__device__ __forceinline__ float tf32_round(float v) {
-    uint32_t u = __float_as_uint(v);
-    u = (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;   // round to nearest even, 10 bits
-    return __uint_as_float(u);
-}
-
-__global__ void split_tf32_kernel(const float* __restrict__ x, int64_t ldx, int rows, int cols,
-                                  float* __restrict__ hi, float* __restrict__ lo, int64_t ldo) {
+__global__ void copy2d_kernel(const float* __restrict__ x, int64_t ldx, int rows, int cols,
+                              float* __restrict__ out, int64_t ldo) {
     const int64_t total = static_cast<int64_t>(rows) * cols;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / cols, c = i % cols;
-        const float v = x[r * ldx + c];
-        const float h = tf32_round(v);
-        hi[r * ldo + c] = h;
-        lo[r * ldo + c] = v - h;
+        out[r * ldo + c] = x[r * ldx + c];
     }
 }
 
-// Transposing split through a 32 x 33 shared tile: out is (cols, rows).
-__global__ void split_tf32_t_kernel(const float* __restrict__ x, int64_t ldx, int rows, int cols,
-                                    float* __restrict__ hi, float* __restrict__ lo, int64_t ldo) {
+// Transpose through a 32 x 33 shared tile: out is (cols, rows).
+__global__ void transpose_kernel(const float* __restrict__ x, int64_t ldx, int rows, int cols,
+                                 float* __restrict__ out, int64_t ldo) {
     __shared__ float tile[32][33];
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
@@ -336,25 +367,20 @@ __global__ void split_tf32_t_kernel(const float* __restrict__ x, int64_t ldx, in
     __syncthreads();
     for (int k = ty; k < 32; k += 8) {
         const int c = c0 + k, r = r0 + tx;
-        if (c < cols && r < rows) {
-            const float v = tile[tx][k];
-            const float h = tf32_round(v);
-            hi[static_cast<int64_t>(c) * ldo + r] = h;
-            lo[static_cast<int64_t>(c) * ldo + r] = v - h;
-        }
+        if (c < cols && r < rows) out[static_cast<int64_t>(c) * ldo + r] = tile[tx][k];
     }
 }
 
-cudaError_t launch_split_tf32(const float* x, int64_t ldx, int rows, int cols, int transpose,
-                              float* hi, float* lo, int64_t ldo, cudaStream_t st) {
+cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols, int transpose,
+                                float* out, int64_t ldo, cudaStream_t st) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     if (transpose) {
         dim3 grid((cols + 31) / 32, (rows + 31) / 32);
-        split_tf32_t_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, hi, lo, ldo);
+        transpose_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
     } else {
         const int64_t total = static_cast<int64_t>(rows) * cols;
         const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, 152 * 32));
-        split_tf32_kernel<<<blocks, 256, 0, st>>>(x, ldx, rows, cols, hi, lo, ldo);
+        copy2d_kernel<<<blocks, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
     }
     return cudaGetLastError();
 }

@@ -21,8 +21,10 @@ constexpr int kGemmGroup = 4;
 
 // C[m, n] = sum_k A[m, k] B[n, k] (+ bias[n]) (+ R[m, n]), fp32 in and out,
 // computed as three TF32 tensor-core products of hi/lo splits
-// (A_hi B_hi + A_hi B_lo + A_lo B_hi) accumulated in fp32 in tensor memory.
-// A_hi/A_lo are (M, K) and B_hi/B_lo are (N, K), row-major, K-contiguous.
+// (A_hi B_hi + A_hi B_lo + A_lo B_hi) accumulated in fp32 in tensor memory;
+// the kernel forms the splits itself from the fp32 tiles.  A is (M, K) and B
+// is (N, K), row-major, K-contiguous, each with a row stride whose byte size
+// is a multiple of 16 and a 16-byte-aligned base (TMA).
 struct GemmArgs {
     float* C;
     const float* bias;   // may be null
@@ -44,16 +46,16 @@ inline int gemm_ksplit(int M, int N, int K, size_t part_floats) {
     return ks < 1 ? 1 : static_cast<int>(ks);
 }
 struct GemmMaps {
-    CUtensorMap a_hi, a_lo, b_hi, b_lo;
+    CUtensorMap a, b;
 };
 
 cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st);
 
-// hi = x rounded to TF32 (10 mantissa bits), lo = x - hi, for a (rows, cols)
-// fp32 matrix with row stride ldx.  transpose = 0 writes (rows, cols) with
-// row stride ldo; transpose = 1 writes the transpose (cols, rows).
-cudaError_t launch_split_tf32(const float* x, int64_t ldx, int rows, int cols, int transpose,
-                              float* hi, float* lo, int64_t ldo, cudaStream_t st);
+// Copy of a (rows, cols) fp32 matrix with row stride ldx into out with row
+// stride ldo: as it is (transpose = 0) or transposed to (cols, rows)
+// (transpose = 1) -- GEMM operands that are not K-major or not TMA-aligned.
+cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols, int transpose,
+                                float* out, int64_t ldo, cudaStream_t st);
 
 // out[n] = sum_m x[m, n] (fixed-order partial sums, no atomics); ws must hold
 // colsum_ws_floats(rows, cols) floats.

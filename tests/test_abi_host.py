@@ -256,9 +256,9 @@ def test_block_step_validation(lib):
     assert f(ctypes.byref(d), p, ctypes.byref(w), None, p, p, p, p, 1 << 30, None) == 1   # no weights
     assert f(ctypes.byref(_bdesc(seqlen=1, batch=0)), None, ctypes.byref(w), None, None, None, None,
              None, 0, None) == 0
-    # the split weights: 8 halves of (rows, round4(cols)) floats, 256-byte aligned regions
+    # the prepared weights: 4 copies of (rows, round4(cols)) floats, 256-byte aligned regions
     sizes = [(2 * 128, 64), (8 + 2 * 16, 128), (128, 8), (64, 128)]
-    assert binding.ssm_block_weights_split_bytes(d) == sum(2 * _a256(r * c * 4) for r, c in sizes)
+    assert binding.ssm_block_weights_split_bytes(d) == sum(_a256(r * c * 4) for r, c in sizes)
     assert lib.ssm_block_split_weights(ctypes.byref(d), ctypes.byref(w), p, 1 << 30, None) == 1
 
 
