@@ -30,7 +30,9 @@ namespace ssm {
 constexpr unsigned kFaultGemm = 8u;
 constexpr uint32_t kTmemCols = 2 * kGemmBN;                     // two fp32 accumulators
 constexpr uint32_t kOpTileBytes = kGemmBM * kGemmBK * 4;         // 16 KB (BM == BN)
-// A stage holds [A raw][B raw][A lo][B lo], 16 KB each.
+constexpr uint32_t kPairBytes = 2 * kOpTileBytes;                // [A][B] of one K-block
+// Shared memory: kGemmStages raw stages [A raw][B raw], then kGemmLoBufs
+// buffers [A lo][B lo], 32 KB each.
 constexpr int kTileFloats = kGemmBM * kGemmBK;
 static_assert(kGemmBM == kGemmBN, "square tiles share one tile size");
 
@@ -103,13 +105,15 @@ __device__ __forceinline__ void tmem_wait_ld() {
 __global__ void __launch_bounds__(192, 1)
 gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     constexpr int S = kGemmStages;
+    constexpr int NL = kGemmLoBufs;
     constexpr int G = kGemmGroup;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * 4 * kOpTileBytes);   // raw tiles landed
-    uint64_t* conv = full + S;           // [S] the lo tiles are written (one arrival per epilogue warp)
-    uint64_t* empty = conv + S;          // [S] the MMAs have read the stage
+    unsigned char* lobuf = smem + S * kPairBytes;                                 // [NL][A lo][B lo]
+    uint64_t* full = reinterpret_cast<uint64_t*>(lobuf + NL * kPairBytes);        // [S] raw tiles landed
+    uint64_t* conv = full + S;           // [NL] the lo tiles are written (one arrival per epilogue warp)
+    uint64_t* empty = conv + NL;         // [S] the MMAs of that K-block are done (stage and its lo buffer free)
     uint64_t* acc_full = empty + S;      // [2] a partial accumulator is complete
     uint64_t* acc_empty = acc_full + 2;  // [2] the epilogue has read it back
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
@@ -127,9 +131,9 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&conv[s], 4);      // one arrival per epilogue warp
             mbar_init(&empty[s], 1);
         }
+        for (int l = 0; l < NL; ++l) mbar_init(&conv[l], 4);   // one arrival per epilogue warp
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
@@ -151,8 +155,8 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             for (; kb < nk; ++kb) {
                 const int s = kb % S;
                 if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, kFaultGemm)) break;
-                unsigned char* st = smem + s * 4 * kOpTileBytes;
-                mbar_arrive_expect_tx(&full[s], 2 * kOpTileBytes);
+                unsigned char* st = smem + s * kPairBytes;
+                mbar_arrive_expect_tx(&full[s], kPairBytes);
                 const int kx = (kb0 + kb) * kGemmBK;
                 tma_load_2d(st, &maps.a, &full[s], kx, m0);
                 tma_load_2d(st + kOpTileBytes, &maps.b, &full[s], kx, n0);
@@ -172,25 +176,26 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 const uint32_t d = tmem + static_cast<uint32_t>(buf * kGemmBN);
                 const int kb1 = std::min(nk, (gi + 1) * G);
                 for (int kb = gi * G; kb < kb1; ++kb) {
-                    const int s = kb % S;
-                    if (!mbar_wait(&conv[s], (kb / S) & 1, kFaultGemm)) {
+                    const int s = kb % S, l = kb % NL;
+                    if (!mbar_wait(&conv[l], (kb / NL) & 1, kFaultGemm)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = smem_u32(smem + s * 4 * kOpTileBytes);
+                    const uint32_t st = smem_u32(smem + s * kPairBytes);
+                    const uint32_t lt = smem_u32(lobuf + l * kPairBytes);
 #pragma unroll
                     for (int kk = 0; kk < kGemmBK / 8; ++kk) {
                         const uint32_t off = kk * 32;   // 8 tf32 = 32 bytes along K
                         const uint64_t ahi = umma_desc_sw128(st + off);
                         const uint64_t bhi = umma_desc_sw128(st + kOpTileBytes + off);
-                        const uint64_t alo = umma_desc_sw128(st + 2 * kOpTileBytes + off);
-                        const uint64_t blo = umma_desc_sw128(st + 3 * kOpTileBytes + off);
+                        const uint64_t alo = umma_desc_sw128(lt + off);
+                        const uint64_t blo = umma_desc_sw128(lt + kOpTileBytes + off);
                         umma_tf32(d, ahi, bhi, (kb != gi * G || kk != 0) ? 1u : 0u);
                         umma_tf32(d, ahi, blo, 1u);
                         umma_tf32(d, alo, bhi, 1u);
                     }
-                    umma_commit(&empty[s]);   // stage s is free once these MMAs finish
+                    umma_commit(&empty[s]);   // stage s and lo buffer l are free once these MMAs finish
                 }
                 umma_commit(&acc_full[buf]);  // this group's partial sum is complete
             }
@@ -225,13 +230,16 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
         };
         for (int kb = 0; kb < nk && got; ++kb) {
-            const int s = kb % S;
+            const int s = kb % S, l = kb % NL;
             // lo = x - (x with its low 13 mantissa bits cleared), for both raw
-            // tiles of the stage, at the same (swizzled) offsets
+            // tiles of the stage, at the same (swizzled) offsets in lo buffer l,
+            // once the MMAs of block kb - NL have finished reading that buffer
             got = mbar_wait(&full[s], (kb / S) & 1, kFaultGemm) && got;
+            if (kb >= NL)
+                got = mbar_wait(&empty[(kb - NL) % S], ((kb - NL) / S) & 1, kFaultGemm) && got;
             if (got) {
-                const float4* src = reinterpret_cast<const float4*>(smem + s * 4 * kOpTileBytes);
-                float4* dst = reinterpret_cast<float4*>(smem + s * 4 * kOpTileBytes + 2 * kOpTileBytes);
+                const float4* src = reinterpret_cast<const float4*>(smem + s * kPairBytes);
+                float4* dst = reinterpret_cast<float4*>(lobuf + l * kPairBytes);
 #pragma unroll
                 for (int i0 = 0; i0 < 2 * kTileFloats / 4 / 128; i0 += 4) {
                     float4 v[4];
@@ -250,7 +258,7 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 fence_proxy_async_smem();   // the tensor core reads them through the async proxy
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[s]);
+            if (lane == 0) mbar_arrive(&conv[l]);
             // read back the groups that are a full group behind the conversion
             while (got && drained < (kb + 1) / G - 1) drain(drained++);
         }
@@ -328,7 +336,8 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs a) {
 cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.ksplit < 1 || (a.ksplit > 1 && !a.part)) return cudaErrorInvalidValue;
-    const size_t smem = kGemmStages * 4 * kOpTileBytes + (3 * kGemmStages + 4) * 8 + 16 + 1024;
+    const size_t smem = (kGemmStages + kGemmLoBufs) * kPairBytes +
+                        (2 * kGemmStages + kGemmLoBufs + 4) * 8 + 16 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -10,11 +10,13 @@
 namespace ssm {
 
 // TN GEMM tile: 128 x 128 output, K in blocks of 32 fp32 (one 128-byte
-// swizzle row), three-stage TMA pipeline.
+// swizzle row); kGemmStages raw fp32 A|B stages in flight by TMA and
+// kGemmLoBufs buffers of their TF32 "lo" parts.
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 128;
 constexpr int kGemmBK = 32;
-constexpr int kGemmStages = 3;
+constexpr int kGemmStages = 5;
+constexpr int kGemmLoBufs = 2;
 // K-blocks accumulated by the tensor core before the partial sum is added into
 // fp32 registers (bounds the tensor core's accumulation drift at 128 products).
 constexpr int kGemmGroup = 4;
