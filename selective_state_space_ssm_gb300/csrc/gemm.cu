@@ -3,24 +3,25 @@
 // dW = dY^T X), plus operand copies (transposes) and deterministic column
 // sums.
 //
-// sm_103a design: one CTA computes a 128 x 128 tile of C = A B^T with
-// tcgen05.mma (kind::tf32, cta_group::1, M = 128, N = 128, K = 8 per
-// instruction) accumulating in tensor memory, as three TF32 products
-// A_hi B_hi + A_hi B_lo + A_lo B_hi (about fp32 accuracy).  The tensor core
-// reads a tf32 operand from an fp32 word and ignores its low 13 mantissa
-// bits, so the raw fp32 tiles serve as the "hi" operands: warp 0 streams
-// 128 x 32 fp32 tiles of A and B with TMA (128-byte swizzle) through a
-// three-stage mbarrier pipeline, and the four epilogue warps (2-5) write the
-// "lo" tiles (x minus x with its low 13 mantissa bits cleared: exact) next to
-// them in shared memory, at the same swizzled offsets; one thread of warp 1
-// issues the MMAs.  Compared with splitting the operands into hi/lo arrays
-// beforehand, half the operand bytes cross L2 and no split pass runs.  The
-// tensor core's fp32 accumulation drifts in one direction (its error grows
-// linearly with K), so the accumulator is double-buffered in tensor memory and
-// read back into fp32 registers every kGemmGroup K-blocks by the same
-// epilogue warps, one group behind the conversion.  Every mbarrier wait is
+// sm_103a design: a persistent, warp-specialized kernel (one CTA per SM walks
+// 128 x 128 tiles of C = A B^T) on tcgen05.mma (kind::tf32, cta_group::1,
+// M = 128, N = 128, K = 8 per instruction) accumulating in tensor memory, as
+// three TF32 products A_hi B_hi + A_hi B_lo + A_lo B_hi (about fp32 accuracy;
+// hi = x with its low 13 mantissa bits cleared, lo = x - hi, exact).  A TMA
+// producer streams raw 128 x 32 fp32 tiles of A and B (128-byte swizzle);
+// converter warps write A's hi and lo parts into tensor memory (tcgen05.st,
+// one row per thread; the MMAs read A from there) and B's lo part into a
+// shared-memory tile at the raw tile's swizzled offsets, while the raw B tile
+// itself serves as B_hi (the tensor core reads a tf32 operand from an fp32
+// word and ignores its low 13 mantissa bits); one thread issues the MMAs; an
+// epilogue warpgroup reads the accumulator back.  The tensor core's fp32
+// accumulation drifts in one direction (its error grows linearly with K), so
+// the accumulator is double-buffered in tensor memory and read back into
+// fp32 registers every kGemmGroup K-blocks, and the tile is stored after its
+// last group while the MMAs of the next tile run.  Every mbarrier wait is
 // bounded; tensor memory is always released.
 #include <algorithm>
+#include <type_traits>
 
 #include "gemm_args.cuh"
 #include "ssm_common.cuh"
@@ -28,11 +29,16 @@
 namespace ssm {
 
 constexpr unsigned kFaultGemm = 8u;
-constexpr uint32_t kTmemCols = 2 * kGemmBN;                     // two fp32 accumulators
 constexpr uint32_t kOpTileBytes = kGemmBM * kGemmBK * 4;         // 16 KB (BM == BN)
 constexpr uint32_t kPairBytes = 2 * kOpTileBytes;                // [A][B] of one K-block
-// Shared memory: kGemmStages raw stages [A raw][B raw], then kGemmLoBufs
-// buffers [A lo][B lo], 32 KB each.
+// Tensor memory: two fp32 accumulators (columns [0, 2 BN)), then kGemmLoBufs
+// A operand buffers of 2 BK columns each: [A_hi | A_lo] of one K-block.
+constexpr uint32_t kAccCols = 2 * kGemmBN;
+constexpr uint32_t kABufCols = 2 * kGemmBK;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAccCols + kGemmLoBufs * kABufCols <= kTmemCols, "tensor memory budget");
+// Shared memory: kGemmStages raw stages [A raw][B raw] of 32 KB, then
+// kGemmLoBufs B_lo tiles of 16 KB.
 constexpr int kTileFloats = kGemmBM * kGemmBK;
 static_assert(kGemmBM == kGemmBN, "square tiles share one tile size");
 
@@ -81,6 +87,15 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint6
         "l"(adesc), "l"(bdesc), "r"(kIdescTF32), "r"(acc)
         : "memory");
 }
+// The same with A read from tensor memory (128 lanes = rows, 8 columns = K).
+__device__ __forceinline__ void umma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(kIdescTF32), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -101,39 +116,94 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Sixteen consecutive 32-bit columns of this thread's tensor-memory lane (no
+// memory clobber: it touches no memory that C++ code reads or writes).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+// A global store in the global state space (so that it is not ordered
+// against later shared-memory loads as a generic store would be).
+__device__ __forceinline__ void st_global_f32(float* p, float v) {
+    asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+// Register split between the warpgroups (see the kernel).
+__device__ __forceinline__ void regs_shrink() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemmRegsSmall)); }
+__device__ __forceinline__ void regs_conv() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemmRegsConv)); }
+__device__ __forceinline__ void regs_grow() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGemmRegsEpi)); }
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
-__global__ void __launch_bounds__(192, 1)
+// One output tile of the persistent schedule: tile t of a GEMM has n-tile
+// t % ntn, m-tile (t / ntn) % ntm and K slice t / (ntn ntm); its K-blocks are
+// [kb0, kb0 + nk) of the full K range.
+struct GemmTile {
+    int m0, n0, z, kb0, nk;
+};
+
+// Warp roles (512 threads, persistent, one CTA per SM):
+//   warp 0        TMA producer: raw fp32 A | B tiles into kGemmStages stages
+//   warp 1        tensor-memory allocation; one thread issues the MMAs
+//   warps 2-3     3/8 of each B lo tile into shared memory
+//   warps 4-7     for even K-blocks: A hi | lo into tensor memory (warp w
+//                 writes lanes 32 (w % 4) ..) and the rest of the B lo tile
+//   warps 8-11    epilogue: every group's partial accumulator into fp32
+//                 registers, then the tile's stores
+//   warps 12-15   as warps 4-7, for odd K-blocks
+// (one converter warp per K-block and quadrant could not keep up with the
+// MMAs: its loads, conversion and tensor-memory stores form a chain longer
+// than one K-block's MMAs).  The epilogue warpgroup holds a 128-float row of
+// running sums per thread, so the other three warpgroups hand it registers
+// (setmaxnreg): 128 x (kGemmRegsSmall + 2 x kGemmRegsConv + kGemmRegsEpi) must not exceed the
+// 512 x (launch registers) the CTA starts with, which the launcher checks.
+__global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     constexpr int S = kGemmStages;
     constexpr int NL = kGemmLoBufs;
     constexpr int G = kGemmGroup;
+    static_assert(NL <= S, "a lo buffer is reused only after its stage's MMAs finished");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* lobuf = smem + S * kPairBytes;                                 // [NL][A lo][B lo]
-    uint64_t* full = reinterpret_cast<uint64_t*>(lobuf + NL * kPairBytes);        // [S] raw tiles landed
-    uint64_t* conv = full + S;           // [NL] the lo tiles are written (one arrival per epilogue warp)
-    uint64_t* empty = conv + NL;         // [S] the MMAs of that K-block are done (stage and its lo buffer free)
+    unsigned char* lobuf = smem + S * kPairBytes;                                 // [NL][B lo]
+    float* ebuf = reinterpret_cast<float*>(lobuf + NL * kOpTileBytes);            // [4][32][33] epilogue
+    uint64_t* full = reinterpret_cast<uint64_t*>(ebuf + 4 * 32 * 33);             // [S] raw tiles landed
+    uint64_t* conv = full + S;           // [NL] A hi/lo and B lo written (one arrival per converter warp)
+    uint64_t* empty = conv + NL;         // [S] the MMAs of that K-block are done (stage and its lo buffers free)
     uint64_t* acc_full = empty + S;      // [2] a partial accumulator is complete
     uint64_t* acc_empty = acc_full + 2;  // [2] the epilogue has read it back
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kGemmBN, m0 = blockIdx.y * kGemmBM;
-    // this CTA's K range (split-K: blockIdx.z of ksplit slices, partial sums to
-    // a.part, added up by gemm_splitk_reduce_kernel)
+    // Persistent schedule: CTA i computes tiles i, i + gridDim.x, ...  Every
+    // role walks the same sequence, and the barrier phases run on across
+    // tiles (K-block counter j, accumulator-group counter gg).
+    const int ntn = (a.N + kGemmBN - 1) / kGemmBN;
+    const int ntm = (a.M + kGemmBM - 1) / kGemmBM;
+    const int ntiles = ntn * ntm * a.ksplit;
     const int nk_all = (a.K + kGemmBK - 1) / kGemmBK;
     const int per = (nk_all + a.ksplit - 1) / a.ksplit;
-    const int kb0 = blockIdx.z * per;
-    const int nk = max(0, min(per, nk_all - kb0));
-    const int ngroups = (nk + G - 1) / G;
+    auto tile_of = [&](int t) {
+        GemmTile x;
+        const int r = t / ntn;
+        x.n0 = (t % ntn) * kGemmBN;
+        x.m0 = (r % ntm) * kGemmBM;
+        x.z = r / ntm;
+        x.kb0 = x.z * per;
+        x.nk = max(0, min(per, nk_all - x.kb0));
+        return x;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int l = 0; l < NL; ++l) mbar_init(&conv[l], 4);   // one arrival per epilogue warp
+        for (int l = 0; l < NL; ++l) mbar_init(&conv[l], 6);   // 2 B warps + 4 A warps of the K-block's parity
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
@@ -149,158 +219,260 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {   // TMA producer: the raw fp32 tiles of A and B
-            int kb = 0;
-            for (; kb < nk; ++kb) {
-                const int s = kb % S;
-                if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1, kFaultGemm)) break;
+    // TMA producer (one thread): the raw fp32 tiles of A and B
+    auto producer = [&]() {
+        tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.b);
+        int j = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const GemmTile x = tile_of(t);
+            for (int kb = 0; kb < x.nk; ++kb, ++j) {
+                const int s = j % S;
+                if (j >= S && !mbar_wait(&empty[s], ((j / S) - 1) & 1, kFaultGemm)) {
+                    ok = false;
+                    break;
+                }
                 unsigned char* st = smem + s * kPairBytes;
                 mbar_arrive_expect_tx(&full[s], kPairBytes);
-                const int kx = (kb0 + kb) * kGemmBK;
-                tma_load_2d(st, &maps.a, &full[s], kx, m0);
-                tma_load_2d(st + kOpTileBytes, &maps.b, &full[s], kx, n0);
+                const int kx = (x.kb0 + kb) * kGemmBK;
+                tma_load_2d(st, &maps.a, &full[s], kx, x.m0);
+                tma_load_2d(st + kOpTileBytes, &maps.b, &full[s], kx, x.n0);
             }
-            // copies still in flight land before the CTA may exit (bounded)
-            for (int j = std::max(0, kb - S); j < kb; ++j)
-                mbar_wait(&full[j % S], (j / S) & 1, kFaultDrain);
         }
-    } else if (warp == 1) {
-        if (lane == 0) {   // MMA issuer
-            bool ok = true;
-            for (int gi = 0; gi < ngroups && ok; ++gi) {
-                const int buf = gi & 1;
+        // copies still in flight land before the CTA may exit (bounded)
+        for (int jj = max(0, j - S); jj < j; ++jj) mbar_wait(&full[jj % S], (jj / S) & 1, kFaultDrain);
+    };
+
+    // MMA issuer (one thread)
+    auto mma_issuer = [&]() {
+        int j = 0, gg = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const GemmTile x = tile_of(t);
+            const int ng = (x.nk + G - 1) / G;
+            for (int gi = 0; gi < ng && ok; ++gi, ++gg) {
+                const int buf = gg & 1;
                 // the epilogue must have read this buffer's previous group
-                if (gi >= 2 && !mbar_wait(&acc_empty[buf], ((gi >> 1) - 1) & 1, kFaultGemm)) break;
+                if (gg >= 2 && !mbar_wait(&acc_empty[buf], ((gg >> 1) - 1) & 1, kFaultGemm)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(buf * kGemmBN);
-                const int kb1 = std::min(nk, (gi + 1) * G);
-                for (int kb = gi * G; kb < kb1; ++kb) {
-                    const int s = kb % S, l = kb % NL;
-                    if (!mbar_wait(&conv[l], (kb / NL) & 1, kFaultGemm)) {
+                const int kb1 = min(x.nk, (gi + 1) * G);
+                for (int kb = gi * G; kb < kb1; ++kb, ++j) {
+                    const int s = j % S, l = j % NL;
+                    if (!mbar_wait(&conv[l], (j / NL) & 1, kFaultGemm)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + s * kPairBytes);
-                    const uint32_t lt = smem_u32(lobuf + l * kPairBytes);
+                    const uint32_t lt = smem_u32(lobuf + l * kOpTileBytes);
+                    const uint32_t at = tmem + kAccCols + static_cast<uint32_t>(l) * kABufCols;
 #pragma unroll
                     for (int kk = 0; kk < kGemmBK / 8; ++kk) {
                         const uint32_t off = kk * 32;   // 8 tf32 = 32 bytes along K
-                        const uint64_t ahi = umma_desc_sw128(st + off);
+                        const uint32_t ahi = at + kk * 8, alo = at + kGemmBK + kk * 8;
                         const uint64_t bhi = umma_desc_sw128(st + kOpTileBytes + off);
-                        const uint64_t alo = umma_desc_sw128(lt + off);
-                        const uint64_t blo = umma_desc_sw128(lt + kOpTileBytes + off);
-                        umma_tf32(d, ahi, bhi, (kb != gi * G || kk != 0) ? 1u : 0u);
-                        umma_tf32(d, ahi, blo, 1u);
-                        umma_tf32(d, alo, bhi, 1u);
+                        const uint64_t blo = umma_desc_sw128(lt + off);
+                        umma_tf32_ta(d, ahi, bhi, (kb != gi * G || kk != 0) ? 1u : 0u);
+                        umma_tf32_ta(d, ahi, blo, 1u);
+                        umma_tf32_ta(d, alo, bhi, 1u);
                     }
-                    umma_commit(&empty[s]);   // stage s and lo buffer l are free once these MMAs finish
+                    umma_commit(&empty[s]);   // stage s and lo buffers l are free once these MMAs finish
                 }
+                if (!ok) break;
                 umma_commit(&acc_full[buf]);  // this group's partial sum is complete
             }
         }
-    } else {   // warps 2..5: lo tiles, then the epilogue; TMEM lane quadrant = warp % 4
-        const int q = warp & 3;
-        const int et = threadIdx.x - 64;   // 0..127
+        // every MMA has finished before tensor memory is released
+        if (j > 0) mbar_wait(&empty[(j - 1) % S], ((j - 1) / S) & 1, kFaultDrain);
+    };
+
+    // K-block j's lo parts go to lo buffer j % NL once the MMAs of block
+    // j - NL have finished reading it: A hi | lo into tensor memory by the
+    // A warpgroup of j's parity (warps 4-7 even j, 12-15 odd j), B lo into
+    // shared memory at the raw tile's (swizzled) offsets, its first 3/8 by
+    // warps 2-3 (6 float4 per thread), the rest by that A warpgroup (5 float4
+    // per thread).
+    auto converters = [&](bool is_a, int parity) {
+        const int q = warp & 3;                        // A: TMEM lane quadrant
+        const int ar = 32 * q + lane;                  // A: this thread's row (= its TMEM lane)
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAccCols;
+        constexpr int kF4 = kTileFloats / 4;           // float4 per B tile
+        constexpr int kBwarpsF4 = 3 * kF4 / 8;         // B lo float4 of warps 2-3
+        const int bf0 = is_a ? kBwarpsF4 + ar : threadIdx.x - 64;
+        const int bstep = is_a ? 128 : 64;
+        bool got = true;
+        int j = 0;
+        for (int t = blockIdx.x; t < ntiles && got; t += gridDim.x) {
+            const int nk = tile_of(t).nk;
+            for (int kb = 0; kb < nk && got; ++kb, ++j) {
+                if (is_a && (j & 1) != parity) continue;
+                const int s = j % S, l = j % NL;
+                got = mbar_wait(&full[s], (j / S) & 1, kFaultGemm) && got;
+                if (j >= NL)
+                    got = mbar_wait(&empty[(j - NL) % S], ((j - NL) / S) & 1, kFaultGemm) && got;
+                got = __all_sync(0xffffffffu, got);
+                if (got) {
+                    const float4* src =
+                        reinterpret_cast<const float4*>(smem + s * kPairBytes + kOpTileBytes);
+                    float4* dst = reinterpret_cast<float4*>(lobuf + l * kOpTileBytes);
+                    auto b_lo = [&](auto nv) {
+                        constexpr int NV = decltype(nv)::value;
+                        float4 v[NV];
+#pragma unroll
+                        for (int u = 0; u < NV; ++u) v[u] = src[bf0 + bstep * u];
+#pragma unroll
+                        for (int u = 0; u < NV; ++u) {
+                            float4 w;
+                            w.x = v[u].x - __uint_as_float(__float_as_uint(v[u].x) & 0xFFFFE000u);
+                            w.y = v[u].y - __uint_as_float(__float_as_uint(v[u].y) & 0xFFFFE000u);
+                            w.z = v[u].z - __uint_as_float(__float_as_uint(v[u].z) & 0xFFFFE000u);
+                            w.w = v[u].w - __uint_as_float(__float_as_uint(v[u].w) & 0xFFFFE000u);
+                            dst[bf0 + bstep * u] = w;
+                        }
+                        fence_proxy_async_smem();   // the tensor core reads B lo through the async proxy
+                    };
+                    if (!is_a) {
+                        b_lo(std::integral_constant<int, kBwarpsF4 / 64>{});
+                    } else {
+                        // row ar: hi | lo into columns of tensor-memory buffer l
+                        tc_fence_after();
+                        const unsigned char* arow = smem + s * kPairBytes + ar * 128;
+                        const uint32_t adst = a_lane + static_cast<uint32_t>(l) * kABufCols;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            // 16-byte chunks 4h .. 4h + 3 of the row (128-byte
+                            // swizzle: chunk index xor row mod 8)
+                            float4 v4[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                v4[c] = *reinterpret_cast<const float4*>(arow + (((4 * h + c) ^ (ar & 7)) << 4));
+                            uint32_t hi[16], lo[16];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const float xv[4] = {v4[c].x, v4[c].y, v4[c].z, v4[c].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    hi[4 * c + e] = __float_as_uint(xv[e]) & 0xFFFFE000u;
+                                    lo[4 * c + e] = __float_as_uint(xv[e] - __uint_as_float(hi[4 * c + e]));
+                                }
+                            }
+                            tmem_st16(adst + 16 * h, hi);
+                            tmem_st16(adst + kGemmBK + 16 * h, lo);
+                        }
+                        b_lo(std::integral_constant<int, (kF4 - kBwarpsF4) / 128>{});
+                        tmem_wait_st();
+                        tc_fence_before();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[l]);
+            }
+        }
+    };
+
+    // Each group's partial sum (at most G K-blocks, accumulated by the tensor
+    // core) is added into fp32 registers, so the tensor core's own
+    // accumulation never spans more than G * kGemmBK products; after a tile's
+    // last group its rows are stored.
+    auto epilogue = [&]() {
+        const int q = warp & 3;                        // TMEM lane quadrant
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        // Each group's partial sum (at most G K-blocks, accumulated by the tensor
-        // core) is added into fp32 registers, so the tensor core's own
-        // accumulation never spans more than G * kGemmBK products.
         float acc[kGemmBN];
 #pragma unroll
-        for (int j = 0; j < kGemmBN; ++j) acc[j] = 0.0f;
+        for (int c = 0; c < kGemmBN; ++c) acc[c] = 0.0f;
         bool got = true;
-        int drained = 0;
-        auto drain = [&](int gi) {
-            const int buf = gi & 1;
-            got = mbar_wait(&acc_full[buf], (gi >> 1) & 1, kFaultGemm) && got;
-            __syncwarp();
-            tc_fence_after();
+        float* tile = ebuf + q * (32 * 33);
+        int gg = 0;
+        for (int t = blockIdx.x; t < ntiles && got; t += gridDim.x) {
+            const GemmTile x = tile_of(t);
+            const int ng = (x.nk + G - 1) / G;
+            for (int gi = 0; gi < ng && got; ++gi, ++gg) {
+                const int buf = gg & 1;
+                got = mbar_wait(&acc_full[buf], (gg >> 1) & 1, kFaultGemm) && got;
+                got = __all_sync(0xffffffffu, got);
+                if (got) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_base + static_cast<uint32_t>(buf * kGemmBN + c0), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) acc[c0 + c] += __uint_as_float(r[c]);
+                    }
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            }
+            if (!got) break;
+            // each warp turns its 32 x 32 sub-tiles around through its slice of
+            // ebuf so that global stores run along rows
 #pragma unroll
             for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + static_cast<uint32_t>(buf * kGemmBN + c0), r);
-                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[c0 + j] += __uint_as_float(r[j]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        };
-        for (int kb = 0; kb < nk && got; ++kb) {
-            const int s = kb % S, l = kb % NL;
-            // lo = x - (x with its low 13 mantissa bits cleared), for both raw
-            // tiles of the stage, at the same (swizzled) offsets in lo buffer l,
-            // once the MMAs of block kb - NL have finished reading that buffer
-            got = mbar_wait(&full[s], (kb / S) & 1, kFaultGemm) && got;
-            if (kb >= NL)
-                got = mbar_wait(&empty[(kb - NL) % S], ((kb - NL) / S) & 1, kFaultGemm) && got;
-            if (got) {
-                const float4* src = reinterpret_cast<const float4*>(smem + s * kPairBytes);
-                float4* dst = reinterpret_cast<float4*>(lobuf + l * kPairBytes);
+                for (int c = 0; c < 32; ++c) tile[lane * 33 + c] = acc[c0 + c];
+                __syncwarp();
+                // the column of the sub-tile this lane stores, read whole
+                // before any global store is issued
+                float v[32];
 #pragma unroll
-                for (int i0 = 0; i0 < 2 * kTileFloats / 4 / 128; i0 += 4) {
-                    float4 v[4];
+                for (int rr = 0; rr < 32; ++rr) v[rr] = tile[rr * 33 + lane];
+                __syncwarp();
+                const int col = x.n0 + c0 + lane;
+                const int rbase = x.m0 + 32 * q;
+                const int rows = min(32, a.M - rbase);
+                if (col < a.N && rows > 0) {
+                    if (a.ksplit > 1) {
+                        float* P = a.part + static_cast<size_t>(x.z) * a.M * a.N +
+                                   static_cast<size_t>(rbase) * a.N + col;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) v[u] = src[et + 128 * (i0 + u)];
+                        for (int rr = 0; rr < 32; ++rr)
+                            if (rr < rows) st_global_f32(P + static_cast<size_t>(rr) * a.N, v[rr]);
+                    } else {
+                        const float bv = a.bias ? a.bias[col] : 0.0f;
+                        if (a.R) {
+                            const float* Rp = a.R + static_cast<size_t>(rbase) * a.ldr + col;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float4 w;
-                        w.x = v[u].x - __uint_as_float(__float_as_uint(v[u].x) & 0xFFFFE000u);
-                        w.y = v[u].y - __uint_as_float(__float_as_uint(v[u].y) & 0xFFFFE000u);
-                        w.z = v[u].z - __uint_as_float(__float_as_uint(v[u].z) & 0xFFFFE000u);
-                        w.w = v[u].w - __uint_as_float(__float_as_uint(v[u].w) & 0xFFFFE000u);
-                        dst[et + 128 * (i0 + u)] = w;
-                    }
-                }
-                fence_proxy_async_smem();   // the tensor core reads them through the async proxy
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[l]);
-            // read back the groups that are a full group behind the conversion
-            while (got && drained < (kb + 1) / G - 1) drain(drained++);
-        }
-        while (got && drained < ngroups) drain(drained++);
-        // The operand stages are idle once the last group is complete: each
-        // warp turns its 32 x 32 sub-tiles around through a padded slice of
-        // stage 0 so that global stores run along rows.
-        float* tile = reinterpret_cast<float*>(smem) + q * (32 * 33);
+                            for (int rr = 0; rr < 32; ++rr)
+                                if (rr < rows) v[rr] += Rp[static_cast<size_t>(rr) * a.ldr];
+                        }
+                        float* Cp = a.C + static_cast<size_t>(rbase) * a.ldc + col;
 #pragma unroll
-        for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) tile[lane * 33 + j] = acc[c0 + j];
-            __syncwarp();
-            const int col = n0 + c0 + lane;
-            const int rbase = m0 + 32 * q;
-            const int rows = min(32, a.M - rbase);
-            if (got && col < a.N && rows > 0) {
-                if (a.ksplit > 1) {
-                    float* P = a.part + static_cast<size_t>(blockIdx.z) * a.M * a.N;
-#pragma unroll 8
-                    for (int rr = 0; rr < 32; ++rr)
-                        if (rr < rows) P[static_cast<size_t>(rbase + rr) * a.N + col] = tile[rr * 33 + lane];
-                } else {
-                    const float bv = a.bias ? a.bias[col] : 0.0f;
-                    // residual rows fetched 8 at a time so their loads overlap
-#pragma unroll
-                    for (int r0 = 0; r0 < 32; r0 += 8) {
-                        float res[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            res[u] = (a.R && r0 + u < rows)
-                                         ? a.R[static_cast<size_t>(rbase + r0 + u) * a.ldr + col] : 0.0f;
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            if (r0 + u < rows)
-                                a.C[static_cast<size_t>(rbase + r0 + u) * a.ldc + col] =
-                                    tile[(r0 + u) * 33 + lane] + bv + res[u];
+                        for (int rr = 0; rr < 32; ++rr)
+                            if (rr < rows) st_global_f32(Cp + static_cast<size_t>(rr) * a.ldc, v[rr] + bv);
                     }
                 }
             }
-            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < kGemmBN; ++c) acc[c] = 0.0f;
         }
+    };
+
+    // Roles by warpgroup; each warpgroup resizes its registers at one place.
+    if (warp < 4) {
+        regs_shrink();
+        if (warp == 0) {
+            if (lane == 0) producer();
+        } else if (warp == 1) {
+            if (lane == 0) mma_issuer();
+        } else {
+            converters(false, 0);
+        }
+    } else if (warp < 8) {
+        regs_conv();
+        converters(true, 0);
+    } else if (warp < 12) {
+        regs_grow();
+        epilogue();
+    } else {
+        regs_conv();
+        converters(true, 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -336,13 +508,32 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs a) {
 cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.ksplit < 1 || (a.ksplit > 1 && !a.part)) return cudaErrorInvalidValue;
-    const size_t smem = (kGemmStages + kGemmLoBufs) * kPairBytes +
+    const size_t smem = kGemmStages * kPairBytes + kGemmLoBufs * kOpTileBytes + 4 * 32 * 33 * 4 +
                         (2 * kGemmStages + kGemmLoBufs + 4) * 8 + 16 + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kGemmBN - 1) / kGemmBN, (a.M + kGemmBM - 1) / kGemmBM, a.ksplit);
-    gemm_tf32x3_kernel<<<grid, 192, smem, st>>>(maps, a);
+    // The warpgroups' register split must fit in what the CTA is launched
+    // with (otherwise the epilogue's setmaxnreg.inc could never be granted).
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemm_tf32x3_kernel);
+        if (e != cudaSuccess) return e;
+        launch_regs = fa.numRegs;
+    }
+    if (kGemmThreads * launch_regs < 128 * (kGemmRegsSmall + 2 * kGemmRegsConv + kGemmRegsEpi))
+        return cudaErrorInvalidConfiguration;
+    // persistent: one CTA per SM (shared memory allows no more), each walking
+    // its share of the output tiles
+    const long long ntiles = static_cast<long long>((a.N + kGemmBN - 1) / kGemmBN) *
+                             ((a.M + kGemmBM - 1) / kGemmBM) * a.ksplit;
+    int dev = 0, nsm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(std::min<long long>(ntiles, std::max(nsm, 1)));
+    gemm_tf32x3_kernel<<<grid, kGemmThreads, smem, st>>>(maps, a);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.ksplit == 1) return e;
     const size_t total = static_cast<size_t>(a.M) * a.N;

@@ -11,12 +11,20 @@ namespace ssm {
 
 // TN GEMM tile: 128 x 128 output, K in blocks of 32 fp32 (one 128-byte
 // swizzle row); kGemmStages raw fp32 A|B stages in flight by TMA and
-// kGemmLoBufs buffers of their TF32 "lo" parts.
+// kGemmLoBufs K-blocks split ahead of the MMAs (A hi/lo in tensor memory,
+// B lo in shared memory).
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 128;
 constexpr int kGemmBK = 32;
 constexpr int kGemmStages = 5;
-constexpr int kGemmLoBufs = 2;
+constexpr int kGemmLoBufs = 3;
+// 16 warps in four warpgroups; registers per thread after the split: the
+// producer/MMA/B warpgroup kGemmRegsSmall, the two A warpgroups
+// kGemmRegsConv, the epilogue kGemmRegsEpi.
+constexpr int kGemmThreads = 512;
+constexpr int kGemmRegsSmall = 96;
+constexpr int kGemmRegsConv = 88;
+constexpr int kGemmRegsEpi = 240;
 // K-blocks accumulated by the tensor core before the partial sum is added into
 // fp32 registers (bounds the tensor core's accumulation drift at 128 products).
 constexpr int kGemmGroup = 4;

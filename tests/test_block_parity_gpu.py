@@ -24,14 +24,16 @@ NAMES = ("wInProj", "bInProj", "wConv", "bConv", "wXProj", "bXProj", "wDtProj", 
 
 # (dmodel, dinner, dtrank, dstate, dconv, batch, seqlen): several 128-row GEMM
 # tiles with ragged tails, x_proj / dt_proj widths below one tile, dt_proj K
-# below one 32-wide K block, odd sequence lengths, kconv != 4, and (last)
-# weight-gradient GEMMs with a single output tile and 25 K blocks, which the
-# GEMM splits over K.
+# below one 32-wide K block, odd sequence lengths, kconv != 4, and (last two)
+# weight-gradient GEMMs with a single output tile, which the GEMM splits over
+# K: 25 K blocks in 3 slices, and 99 K blocks in 12 slices of 9 whose last one
+# is empty (that slice's partial sum must be zero).
 SMALL = [
     (64, 128, 8, 16, 4, 2, 200),
     (36, 20, 4, 4, 3, 3, 37),
     (128, 256, 16, 8, 2, 1, 129),
     (36, 20, 4, 4, 3, 2, 400),     # weight-gradient GEMMs over 800 rows: split-K
+    (36, 20, 4, 4, 3, 2, 1580),    # over 3160 rows: split-K with an empty last slice
 ]
 
 
