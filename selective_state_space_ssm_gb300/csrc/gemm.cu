@@ -130,6 +130,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void st_global_f32(float* p, float v) {
     asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
+// A global load in the global state space.  The epilogue issues a sub-tile's
+// 32 residual loads back to back with these before adding any of them (as
+// plain loads they were issued one after another, each waiting for the
+// last: 30 us per tile).
+__device__ __forceinline__ float ld_global_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
 // Register split between the warpgroups (see the kernel).
 __device__ __forceinline__ void regs_shrink() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemmRegsSmall)); }
 __device__ __forceinline__ void regs_conv() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGemmRegsConv)); }
@@ -438,9 +447,12 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         const float bv = a.bias ? a.bias[col] : 0.0f;
                         if (a.R) {
                             const float* Rp = a.R + static_cast<size_t>(rbase) * a.ldr + col;
+                            float res[32];
 #pragma unroll
                             for (int rr = 0; rr < 32; ++rr)
-                                if (rr < rows) v[rr] += Rp[static_cast<size_t>(rr) * a.ldr];
+                                res[rr] = ld_global_f32(Rp + static_cast<size_t>(min(rr, rows - 1)) * a.ldr);
+#pragma unroll
+                            for (int rr = 0; rr < 32; ++rr) v[rr] += res[rr];
                         }
                         float* Cp = a.C + static_cast<size_t>(rbase) * a.ldc + col;
 #pragma unroll
