@@ -50,6 +50,21 @@ __device__ __forceinline__ void st_cpl(float* p, const float (&v)[CPL]) {
         *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
 }
 
+// Two adjacent activations (an even element index) as one 4- or 8-byte access.
+template <typename T> struct ActPair;
+template <> struct ActPair<float> {
+    static __device__ __forceinline__ float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    static __device__ __forceinline__ void store(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+};
+template <> struct ActPair<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 load(const __nv_bfloat16* p) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float2 v) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
+    }
+};
+
 // CW = channels per CTA (one warp): 32 (each lane 4 channels) or 16 (each lane
 // 2 channels: half the work per warp and fewer registers, so twice the warps
 // when the problem has few channels).
@@ -216,10 +231,20 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     }
     park();
     float dD_acc = 0.0f;
+    // 32-channel epilogue: lane = (step parity ep, channel pair 2 ecp, 2 ecp + 1)
+    const int ep = lane >> 4, ec = c0 + 2 * (lane & 15);
+    const bool eok0 = ec < Dn, eok1 = ec + 1 < Dn;
+    const float2 eD = make_float2(eok0 && a.D ? a.D[ec] : 0.0f, eok1 && a.D ? a.D[ec + 1] : 0.0f);
+    float2 eDD = make_float2(0.0f, 0.0f);
 
     T* dup = static_cast<T*>(a.du);
     T* ddp = static_cast<T*>(a.ddelta);
     T* dzp = static_cast<T*>(a.dz);
+    // outputs written as channel pairs when every pair is aligned for it
+    const bool pair_st = eok1 &&
+        ((reinterpret_cast<uintptr_t>(dup) | reinterpret_cast<uintptr_t>(ddp) |
+          (GATE ? reinterpret_cast<uintptr_t>(dzp) : 0)) % (2 * sizeof(T))) == 0 &&
+        a.ld_du % 2 == 0 && a.ld_ddelta % 2 == 0 && (!GATE || a.ld_dz % 2 == 0);
     bool ok = true;
     int waited = 0;
 
@@ -310,10 +335,49 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 Cf = Bf + BCT;
             }
 
-            // ---- prologue (lane = channel, step parity): delta, delta*u (or u),
-            //      dy.  All TC steps run: past seqlen the tiles, B and C are
-            //      zero, so dy = 0 and the extra steps add nothing.
-            {
+            // ---- prologue: delta, delta*u (or u), dy, sigmoid(delta_raw),
+            //      sigmoid(z).  All TC steps run: past seqlen the tiles, B and
+            //      C are zero, so dy = 0 and the extra steps add nothing.
+            //      32-channel CTAs: lane = (step parity, channel pair) as in
+            //      the epilogue; 16-channel CTAs: lane = (channel, step parity).
+            if constexpr (CW == 32) {
+                const int ce = ec - c0;
+                float2 uv[TC / 2], xr[TC / 2], go[TC / 2], zv[TC / 2];
+#pragma unroll
+                for (int jj = 0; jj < TC / 2; ++jj) {
+                    const int e = (2 * jj + ep) * CW + ce;
+                    uv[jj] = ActPair<T>::load(tu + e);
+                    xr[jj] = ActPair<T>::load(tr + e);
+                    go[jj] = ActPair<T>::load(tg + e);
+                    zv[jj] = GATE ? ActPair<T>::load(tz + e) : f2(0.0f);
+                }
+                float2 sxv[TC / 2];
+#pragma unroll
+                for (int jj = 0; jj < TC / 2; ++jj) {
+                    float2 dt, sx, dy = go[jj];
+                    if (GATE) {
+                        float2 sz;
+                        softplus_sig_xz2(xr[jj], zv[jj], dt, sx, sz);
+                        dy = mul2(mul2(go[jj], zv[jj]), sz);
+                        zv[jj] = sz;                            // reuse: sigmoid(z)
+                    } else {
+                        softplus_sig_x2(xr[jj], dt, sx);
+                    }
+                    sxv[jj] = sx;
+                    xr[jj] = dt;                                // reuse: delta
+                    go[jj] = dy;                                // reuse: dy
+                    uv[jj] = ZOH ? uv[jj] : mul2(dt, uv[jj]);   // reuse: delta*u | u
+                }
+#pragma unroll
+                for (int jj = 0; jj < TC / 2; ++jj) {
+                    const int e = (2 * jj + ep) * CW + ce;
+                    *reinterpret_cast<float2*>(Pd + e) = xr[jj];
+                    *reinterpret_cast<float2*>(Pbs + e) = uv[jj];
+                    *reinterpret_cast<float2*>(Pdy + e) = go[jj];
+                    *reinterpret_cast<float2*>(Psdr + e) = sxv[jj];
+                    if (GATE) *reinterpret_cast<float2*>(Psz + e) = zv[jj];
+                }
+            } else {
                 // loads, math and stores in separate passes, so that the steps'
                 // independent chains overlap (stores could alias later loads)
                 constexpr int NJ = TC / SPL;
@@ -530,9 +594,80 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         __syncwarp();
 
         if (ok) {
-            // ---- epilogue (lane = channel, step parity): finish du,
-            //      ddelta_raw, dz, dD
-            if (lane_ok) {
+            // ---- epilogue: finish du, ddelta_raw, dz, dD.  32-channel CTAs:
+            //      lane = (step parity, channel pair), paired loads and
+            //      stores and f32x2 arithmetic; 16-channel CTAs: lane =
+            //      (channel, step parity).
+            if constexpr (CW == 32) {
+#pragma unroll 1
+                for (int jb = 0; jb < TC / 2; jb += 2) {
+                    float2 Sg[2], Eg[2], Sa[2], uv[2], sx[2], dt[2], dy[2], sz[2], zv[2], go[2], yv[2];
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * (jb + jj) + ep;
+                        float2 sm[NQN];
+#pragma unroll
+                        for (int qn = 0; qn < NQN; ++qn) {
+                            // the 4 state groups' sums of both channels (a
+                            // pair never wraps around the rotated row)
+                            const float* pp = part + (j * NQN + qn) * 4 * CW;
+                            float2 v[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                v[k] = *reinterpret_cast<const float2*>(pp + k * CW + part_col(ec - c0, k));
+                            sm[qn] = add2(add2(v[0], v[1]), add2(v[2], v[3]));
+                        }
+                        Sg[jj] = sm[0];
+                        Eg[jj] = mul2(sm[1], f2(kLn2));
+                        Sa[jj] = sm[NQN - 1];
+                        const int e = j * CW + (ec - c0);
+                        uv[jj] = ActPair<T>::load(tu + e);
+                        sx[jj] = *reinterpret_cast<const float2*>(Psdr + e);
+                        dt[jj] = *reinterpret_cast<const float2*>(Pd + e);
+                        dy[jj] = *reinterpret_cast<const float2*>(Pdy + e);
+                        if (GATE) {
+                            sz[jj] = *reinterpret_cast<const float2*>(Psz + e);
+                            zv[jj] = ActPair<T>::load(tz + e);
+                            go[jj] = ActPair<T>::load(tg + e);
+                            yv[jj] = ActPair<T>::load(ty + e);
+                        }
+                    }
+                    float2 duO[2], ddO[2], dzO[2];
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * (jb + jj) + ep;
+                        duO[jj] = ZOH ? fma2(eD, dy[jj], Sg[jj]) : fma2(dt[jj], Sg[jj], mul2(eD, dy[jj]));
+                        ddO[jj] = mul2(fma2(uv[jj], ZOH ? Sa[jj] : Sg[jj], Eg[jj]), sx[jj]);
+                        if (j < jmax) eDD = fma2(dy[jj], uv[jj], eDD);
+                        if (GATE) {
+                            // dout y sigmoid(z) (1 + z (1 - sigmoid(z)))
+                            const float2 om = fma2(sz[jj], f2(-1.0f), f2(1.0f));
+                            dzO[jj] = mul2(mul2(mul2(go[jj], yv[jj]), sz[jj]), fma2(zv[jj], om, f2(1.0f)));
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * (jb + jj) + ep;
+                        if (j < jmax && eok0) {
+                            const size_t r = row0 + t0 + j;
+                            if (pair_st) {
+                                ActPair<T>::store(dup + r * a.ld_du + ec, duO[jj]);
+                                ActPair<T>::store(ddp + r * a.ld_ddelta + ec, ddO[jj]);
+                                if (GATE) ActPair<T>::store(dzp + r * a.ld_dz + ec, dzO[jj]);
+                            } else {
+                                dup[r * a.ld_du + ec] = Act<T>::from_f(duO[jj].x);
+                                ddp[r * a.ld_ddelta + ec] = Act<T>::from_f(ddO[jj].x);
+                                if (GATE) dzp[r * a.ld_dz + ec] = Act<T>::from_f(dzO[jj].x);
+                                if (eok1) {
+                                    dup[r * a.ld_du + ec + 1] = Act<T>::from_f(duO[jj].y);
+                                    ddp[r * a.ld_ddelta + ec + 1] = Act<T>::from_f(ddO[jj].y);
+                                    if (GATE) dzp[r * a.ld_dz + ec + 1] = Act<T>::from_f(dzO[jj].y);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else if (lane_ok) {
                 // loads, math and stores in separate passes (see the prologue),
                 // two steps at a time for 32-channel CTAs (register pressure)
                 constexpr int NJALL = TC / SPL;
@@ -624,12 +759,16 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
                 }
             }
         }
-        if constexpr (SPL == 2) {
+        if constexpr (CW == 32) {
+            // the two step-parity lanes of a channel pair each hold half of its dD sums
+            const float ox = __shfl_xor_sync(0xffffffffu, eDD.x, 16);
+            const float oy = __shfl_xor_sync(0xffffffffu, eDD.y, 16);
+            if (ep == 0 && eok0) a.ws_dD[plane_b * Dn + ec] = eDD.x + ox;
+            if (ep == 0 && eok1) a.ws_dD[plane_b * Dn + ec + 1] = eDD.y + oy;
+        } else {
             // the two step-phase lanes of a channel each hold half of its dD sum
             const float dD_other = __shfl_xor_sync(0xffffffffu, dD_acc, 16);
             if (lane_ok && pj == 0) a.ws_dD[plane_b * Dn + dch] = dD_acc + dD_other;
-        } else {
-            if (lane_ok) a.ws_dD[plane_b * Dn + dch] = dD_acc;
         }
     }
 }

@@ -188,6 +188,49 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
+// softplus_sig_xz / softplus_sig_x for two elements at once: the same
+// formulas, the fp32 arithmetic on f32x2 pairs and the ex2 / rcp per element.
+__device__ __forceinline__ float2 log1p_unit2(float2 e, float2 inv2pe) {
+    const float2 s = mul2(e, inv2pe);
+    const float2 s2 = mul2(s, s);
+    float2 p = f2(1.0f / 15.0f);
+    p = fma2(p, s2, f2(1.0f / 13.0f));
+    p = fma2(p, s2, f2(1.0f / 11.0f));
+    p = fma2(p, s2, f2(1.0f / 9.0f));
+    p = fma2(p, s2, f2(1.0f / 7.0f));
+    p = fma2(p, s2, f2(1.0f / 5.0f));
+    p = fma2(p, s2, f2(1.0f / 3.0f));
+    p = fma2(p, s2, f2(1.0f));
+    return mul2(mul2(f2(2.0f), s), p);
+}
+__device__ __forceinline__ void softplus_sig_xz2(float2 x, float2 z, float2& sp, float2& sig_x,
+                                                 float2& sig_z) {
+    const float2 ax = mul2(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 e = make_float2(ex2(ax.x), ex2(ax.y));
+    const float2 zz = mul2(z, f2(-kLog2e));
+    const float2 ez = make_float2(ex2(fminf(zz.x, 100.0f)), ex2(fminf(zz.y, 100.0f)));
+    const float2 a = add2(f2(2.0f), e), b = add2(f2(1.0f), ez), c = add2(f2(1.0f), e);
+    const float2 ab = mul2(a, b);
+    const float2 abc = mul2(ab, c);
+    const float2 r = make_float2(rcp(abc.x), rcp(abc.y));
+    const float2 inv_c = mul2(r, ab);
+    sig_z = mul2(r, mul2(a, c));
+    sp = add2(make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)), log1p_unit2(e, mul2(r, mul2(b, c))));
+    const float2 ei = mul2(e, inv_c);
+    sig_x = make_float2(x.x >= 0.0f ? inv_c.x : ei.x, x.y >= 0.0f ? inv_c.y : ei.y);
+}
+__device__ __forceinline__ void softplus_sig_x2(float2 x, float2& sp, float2& sig_x) {
+    const float2 ax = mul2(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 e = make_float2(ex2(ax.x), ex2(ax.y));
+    const float2 a = add2(f2(2.0f), e), c = add2(f2(1.0f), e);
+    const float2 ac = mul2(a, c);
+    const float2 r = make_float2(rcp(ac.x), rcp(ac.y));
+    const float2 inv_c = mul2(r, a);
+    sp = add2(make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)), log1p_unit2(e, mul2(r, c)));
+    const float2 ei = mul2(e, inv_c);
+    sig_x = make_float2(x.x >= 0.0f ? inv_c.x : ei.x, x.y >= 0.0f ? inv_c.y : ei.y);
+}
+
 // ---------------------------------------------------------------- mbarrier / TMA
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
