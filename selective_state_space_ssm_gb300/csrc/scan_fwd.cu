@@ -216,26 +216,33 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
         const int jmax = min(TS, L - k * TS);
 
         // Phase A: the per-step scalars of the whole tile (independent across
-        // steps, so their dependency chains overlap).
+        // steps, so their dependency chains overlap), two steps at a time in
+        // f32x2 arithmetic.
         float dtv[TS], bsv[TS], gzv[TS], duv[TS];
 #pragma unroll
-        for (int j = 0; j < TS; ++j) {
-            const float uv = Act<T>::to_f(tu[j * CW + lane]);
-            const float xr = Act<T>::to_f(tr[j * CW + lane]);
-            float dt, gz = 1.0f;
+        for (int j = 0; j < TS; j += 2) {
+            const float2 uv = make_float2(Act<T>::to_f(tu[j * CW + lane]), Act<T>::to_f(tu[(j + 1) * CW + lane]));
+            const float2 xr = make_float2(Act<T>::to_f(tr[j * CW + lane]), Act<T>::to_f(tr[(j + 1) * CW + lane]));
+            float2 dt, gz = f2(1.0f);
             if (GATE) {
-                const float zv = Act<T>::to_f(tz[j * CW + lane]);
-                float sz;
-                softplus_sigmoid(xr, zv, dt, sz);
-                gz = zv * sz;                                   // silu(z)
+                const float2 zv =
+                    make_float2(Act<T>::to_f(tz[j * CW + lane]), Act<T>::to_f(tz[(j + 1) * CW + lane]));
+                float2 sz;
+                softplus_sigmoid2(xr, zv, dt, sz);
+                gz = mul2(zv, sz);                              // silu(z)
             } else {
-                float e;
-                dt = softplus_e(xr, e);
+                dt = softplus2(xr);
             }
-            dtv[j] = dt;
-            bsv[j] = DISC == 0 ? dt * uv : uv;                  // Euler: delta*u; ZOH: u
-            gzv[j] = gz;
-            duv[j] = Dd * uv;
+            const float2 bs = DISC == 0 ? mul2(dt, uv) : uv;    // Euler: delta*u; ZOH: u
+            const float2 du = mul2(f2(Dd), uv);
+            dtv[j] = dt.x;
+            dtv[j + 1] = dt.y;
+            bsv[j] = bs.x;
+            bsv[j + 1] = bs.y;
+            gzv[j] = gz.x;
+            gzv[j + 1] = gz.y;
+            duv[j] = du.x;
+            duv[j + 1] = du.y;
         }
         if (a.h_last && jmax < TS) {
             // steps past seqlen: delta = 0 keeps the state exactly (a = 1,

@@ -188,7 +188,8 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
-// softplus_sig_xz / softplus_sig_x for two elements at once: the same
+// softplus_sig_xz / softplus_sig_x / softplus_sigmoid / softplus for two
+// elements at once: the same
 // formulas, the fp32 arithmetic on f32x2 pairs and the ex2 / rcp per element.
 __device__ __forceinline__ float2 log1p_unit2(float2 e, float2 inv2pe) {
     const float2 s = mul2(e, inv2pe);
@@ -218,6 +219,24 @@ __device__ __forceinline__ void softplus_sig_xz2(float2 x, float2 z, float2& sp,
     sp = add2(make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)), log1p_unit2(e, mul2(r, mul2(b, c))));
     const float2 ei = mul2(e, inv_c);
     sig_x = make_float2(x.x >= 0.0f ? inv_c.x : ei.x, x.y >= 0.0f ? inv_c.y : ei.y);
+}
+__device__ __forceinline__ void softplus_sigmoid2(float2 x, float2 z, float2& sp, float2& sig_z) {
+    const float2 ax = mul2(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 e = make_float2(ex2(ax.x), ex2(ax.y));
+    const float2 zz = mul2(z, f2(-kLog2e));
+    const float2 ez = make_float2(ex2(fminf(zz.x, 100.0f)), ex2(fminf(zz.y, 100.0f)));
+    const float2 a = add2(f2(2.0f), e), b = add2(f2(1.0f), ez);
+    const float2 ab = mul2(a, b);
+    const float2 r = make_float2(rcp(ab.x), rcp(ab.y));
+    sp = add2(make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)), log1p_unit2(e, mul2(r, b)));
+    sig_z = mul2(r, a);
+}
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    const float2 ax = mul2(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 e = make_float2(ex2(ax.x), ex2(ax.y));
+    const float2 a = add2(f2(2.0f), e);
+    return add2(make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)),
+                log1p_unit2(e, make_float2(rcp(a.x), rcp(a.y))));
 }
 __device__ __forceinline__ void softplus_sig_x2(float2 x, float2& sp, float2& sig_x) {
     const float2 ax = mul2(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
