@@ -32,7 +32,10 @@ CASES = [
     # 32-channel backward CTAs (4 * 256 = 1024 CTAs of 32 channels)
     (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
     (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
-    (8, 17, 3680, 6, "f32", 0, False, 0.3, 0.0),    # ragged dinner (not a multiple of 32), NT = 8
+    (8, 17, 3680, 6, "f32", 0, False, 0.3, 0.0),    # NT = 8
+    # dinner not a multiple of 32: a ragged last 32-channel tile (8 and 4 channels)
+    (8, 19, 3688, 16, "bf16", 0, True, 0.3, 0.02),
+    (8, 23, 3684, 16, "f32", 1, True, 0.3, 0.02),
 ]
 
 
