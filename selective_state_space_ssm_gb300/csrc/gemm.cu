@@ -583,10 +583,63 @@ __global__ void transpose_kernel(const float* __restrict__ x, int64_t ldx, int r
     }
 }
 
+// Transpose of 64 x 64 tiles with 16-byte loads and stores (x, out 16-byte
+// aligned, ldx and ldo multiples of 4); tiles cut by the matrix edge take
+// single-element accesses.  256 threads, 4 float4 each way per thread.
+__global__ void __launch_bounds__(256) transpose64_kernel(const float* __restrict__ x, int64_t ldx, int rows,
+                                                          int cols, float* __restrict__ out, int64_t ldo) {
+    __shared__ float tile[64][65];
+    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    const int t = threadIdx.x;
+    const bool full = r0 + 64 <= rows && c0 + 64 <= cols;
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = t + 256 * i, rr = idx >> 4, cc = (idx & 15) * 4;
+        const float* src = x + static_cast<int64_t>(r0 + rr) * ldx + c0 + cc;
+        if (full) {
+            v[i] = *reinterpret_cast<const float4*>(src);
+        } else {
+            float e[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) e[k] = (r0 + rr < rows && c0 + cc + k < cols) ? src[k] : 0.0f;
+            v[i] = make_float4(e[0], e[1], e[2], e[3]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = t + 256 * i, rr = idx >> 4, cc = (idx & 15) * 4;
+        tile[rr][cc] = v[i].x;
+        tile[rr][cc + 1] = v[i].y;
+        tile[rr][cc + 2] = v[i].z;
+        tile[rr][cc + 3] = v[i].w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = t + 256 * i, cr = idx >> 4, rc = (idx & 15) * 4;
+        const float4 w = make_float4(tile[rc][cr], tile[rc + 1][cr], tile[rc + 2][cr], tile[rc + 3][cr]);
+        float* dst = out + static_cast<int64_t>(c0 + cr) * ldo + r0 + rc;
+        if (full) {
+            *reinterpret_cast<float4*>(dst) = w;
+        } else if (c0 + cr < cols) {
+            const float e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (r0 + rc + k < rows) dst[k] = e[k];
+        }
+    }
+}
+
 cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols, int transpose,
                                 float* out, int64_t ldo, cudaStream_t st) {
     if (rows == 0 || cols == 0) return cudaSuccess;
-    if (transpose) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0 &&
+                     ldx % 4 == 0 && ldo % 4 == 0;
+    if (transpose && vec) {
+        dim3 grid((cols + 63) / 64, (rows + 63) / 64);
+        transpose64_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
+    } else if (transpose) {
         dim3 grid((cols + 31) / 32, (rows + 31) / 32);
         transpose_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
     } else {
