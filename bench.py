@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 
 METRIC = "Mamba-1 selective scan fwd+bwd Mtokens/s; achieved % of HBM/SFU roofline"
 WORKLOAD = "mamba1p4b_scan_bf16"
+BLOCK_WORKLOAD = "mamba_block_fp32"
 SM_COUNT = 152
 PIPE_RATES = os.path.join(ROOT, "profiles", "pipe_rates_gb300.json")
 # Used only when the committed pipe-rate measurement is absent (then labelled
@@ -73,6 +74,10 @@ def parse():
                    help="measure the MUFU ex2 and fp32 FFMA / FFMA2 rates of the GPU with the "
                         "library's probe kernels (CUDA events + sampled SM clock), write them "
                         "to OUT_JSON and print them")
+    p.add_argument("--measure-gemm-ref", metavar="OUT_JSON", default=None,
+                   help="time the block's projection GEMMs through ssm_linear_fwd (3xTF32) beside "
+                        "the vendor library's single TF32, BF16 and FP32 GEMMs of the same shapes "
+                        "(context for the GEMM's tensor-core rate), write them to OUT_JSON")
     return p.parse_args()
 
 
@@ -582,7 +587,7 @@ def run_block(args):
     dev = torch.device("cuda", local)
     ssm_build.build()
     ssm.load()
-    cfg = dict(workloads.BLOCK_WORKLOADS["mamba_block_fp32"])
+    cfg = dict(workloads.BLOCK_WORKLOADS[BLOCK_WORKLOAD])
     seed = cfg.pop("seed")
     if args.seqlen:
         cfg["seqlen"] = args.seqlen
@@ -897,6 +902,73 @@ def run_measure_pipes(args):
     print(json.dumps(res), flush=True)
 
 
+def run_measure_gemm_ref(args):
+    """The block workload's forward projection GEMMs (M = batch*seqlen rows)
+    through ssm_linear_fwd (three TF32 products, fp32 in and out) and, for
+    context, the vendor library's GEMM of the same shape in TF32 (one
+    product), BF16 and plain FP32, each timed with CUDA events around 20
+    back-to-back launches (median of 5 such runs, after 3 warm-ups).  TFLOP/s
+    count 2*M*N*K once."""
+    import torch
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build, workloads
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    ssm.load()
+    cfg = workloads.BLOCK_WORKLOADS[BLOCK_WORKLOAD]
+    M = cfg["batch"] * cfg["seqlen"]
+    dm, di, r, n = cfg["dmodel"], cfg["dinner"], cfg["dtrank"], cfg["dstate"]
+    shapes = {"in_proj": (M, 2 * di, dm), "x_proj": (M, r + 2 * n, di), "dt_proj": (M, di, r),
+              "out_proj": (M, dm, di)}
+
+    def timed(fn, n=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / n)
+        return statistics.median(ts)
+
+    res = {"gpu_name": torch.cuda.get_device_name(dev), "workload": BLOCK_WORKLOAD, "shapes": {}}
+    old_tf32 = torch.backends.cuda.matmul.allow_tf32
+    try:
+        for name, (m, nn, k) in shapes.items():
+            g = torch.Generator(device=dev).manual_seed(5)
+            X = torch.randn(m, k, device=dev, generator=g)
+            W = torch.randn(nn, k, device=dev, generator=g) / k ** 0.5
+            flop = 2.0 * m * nn * k
+            row = {"M": m, "N": nn, "K": k}
+            ms = timed(lambda: ssm.linear(X, W))
+            row["ssm_linear_3xtf32"] = {"ms": round(ms, 4), "tflops": round(flop / ms / 1e9, 1)}
+            for label, dt, tf32 in (("vendor_tf32", torch.float32, True), ("vendor_bf16", torch.bfloat16, False),
+                                    ("vendor_fp32", torch.float32, False)):
+                torch.backends.cuda.matmul.allow_tf32 = tf32
+                Xd, Wd = X.to(dt), W.to(dt)
+                ms = timed(lambda: Xd @ Wd.t())
+                row[label] = {"ms": round(ms, 4), "tflops": round(flop / ms / 1e9, 1)}
+            res["shapes"][name] = row
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old_tf32
+    res["how"] = ("CUDA events around 20 back-to-back calls, median of 5 (ssm.linear includes its "
+                  "output and workspace allocation from the caching allocator); the vendor rows are "
+                  "torch.matmul")
+    res["command"] = "python bench.py --measure-gemm-ref OUT_JSON"
+    if args.measure_gemm_ref:
+        with open(args.measure_gemm_ref, "w") as f:
+            json.dump(res, f, indent=1)
+    print(json.dumps(res), flush=True)
+
+
 # ----------------------------------------------------------------- reference leg
 
 def run_reference(args):
@@ -937,6 +1009,8 @@ def main():
         run_reference(args)
     elif args.measure_pipes:
         run_measure_pipes(args)
+    elif args.measure_gemm_ref:
+        run_measure_gemm_ref(args)
     elif args.block:
         run_block(args)
     elif args.decode:
