@@ -17,6 +17,9 @@ constexpr int kChunk = 8;
 constexpr int kFwdChannels = 32;
 constexpr int kFwdTile = 16;    // steps per TMA-staged tile
 constexpr int kFwdStages = 4;   // tiles in flight
+// Time segments up to this count run as the warps of one CTA, combined in
+// shared memory; more segments run as separate CTAs combined in global memory.
+constexpr int kFwdChunkWarps = 4;
 // Time segments of the forward: one per batch row unless batch x ceil(dinner/32)
 // warps leave the 152 SMs with fewer than 2 warps each (measured: at 2.5 warps
 // per SM the segment pass costs more than it gains); then enough segments (of

@@ -98,11 +98,206 @@ __device__ __forceinline__ const float* fwd_stage_bc(float* bcs, const T* Bs, bo
     return bcs;
 }
 
+// Segment pass of the time-parallel forward: for segment g of batch row b,
+// run the recurrence from h = 0 and keep only the end state and the sum of
+// delta over the segment.  Since exp(delta_t A) multiplies across steps into
+// exp(A sum_t delta_t), the true state entering segment g+1 is
+//   h_start(g+1) = exp(A sum_g delta) h_start(g) + h_end_from_zero(g),
+// evaluated by scan_fwd_combine_kernel (segments in separate CTAs) or inside
+// the CTA (segments as its warps).  One warp; smem holds the stages and the
+// barriers of the pass.  Returns false if a bounded wait gave up.
+template <typename T, int NT, int DISC>
+__device__ __forceinline__ bool fwd_segsum_run(const FwdMaps& maps, const ScanFwdArgs& a, unsigned char* smem,
+                                               int c0, int b, int g, int lane, float2 (&h)[NT / 2],
+                                               float& dsum) {
+    constexpr int CW = kFwdChannels;
+    constexpr int TS = kFwdTile;
+    constexpr int S = kFwdStages;
+    constexpr int NQ = NT / 2;
+    constexpr int TILE = TS * CW;
+    constexpr int BCT = TS * NT;
+    constexpr int STAGE = 2 * TILE + BCT;               // u, delta_raw, B
+    constexpr uint32_t kActBytes = 2 * TILE * sizeof(T);
+    constexpr uint32_t kBBytes = BCT * sizeof(T);
+    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+
+    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
+    float* bsm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] fp32 B
+    uint64_t* full = reinterpret_cast<uint64_t*>(bsm + BCT);                 // [S]
+
+    const int d = c0 + lane;
+    const bool active = d < a.dinner;
+    const int L = a.seqlen, N = a.dstate;
+    const size_t row0 = static_cast<size_t>(b) * L;
+    const bool bc_tma = a.bc_tma != 0;
+    const int kb = g * a.seg_tiles, ke = kb + a.seg_tiles;   // a full segment (never the last)
+
+    float2 A2[NQ], Anat[NQ], invA[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        float v[2], w[2], r[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = 2 * q + e;
+            const bool ok = active && n < N;
+            const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
+            v[e] = ok ? A * kLog2e : 0.0f;
+            w[e] = A;
+            r[e] = 1.0f / A;
+        }
+        A2[q] = make_float2(v[0], v[1]);
+        Anat[q] = make_float2(w[0], w[1]);
+        invA[q] = make_float2(r[0], r[1]);
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) h[q] = make_float2(0.0f, 0.0f);
+    dsum = 0.0f;
+
+    const T* Bp = static_cast<const T*>(a.B);
+    auto issue = [&](int k) {
+        const int s = (k - kb) % S;
+        T* dst = tiles + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kBBytes : 0u));
+        tma_load_3d(dst, &maps.u, &full[s], c0, k * TS, b);
+        tma_load_3d(dst + TILE, &maps.dr, &full[s], c0, k * TS, b);
+        if (bc_tma) tma_load_3d(dst + 2 * TILE, &maps.B, &full[s], 0, k * TS, b);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int k = kb; k < kb + S && k < ke; ++k) issue(k);
+
+    int k = kb;
+    for (; k < ke; ++k) {
+        const int s = (k - kb) % S;
+        bool ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const T* tu = tiles + s * STAGE;
+        const T* tr = tu + TILE;
+        const T* tb = tu + 2 * TILE;
+        // fp32 B of this tile ([TS][NT]; past dstate 0)
+        const float* Bf;
+        if (bc_tma && sizeof(T) == 4) {
+            Bf = reinterpret_cast<const float*>(tb);
+        } else {
+            for (int e = lane; e < BCT; e += 32) {
+                float v;
+                if (bc_tma) {
+                    v = Act<T>::to_f(tb[e]);
+                } else {
+                    const int j = e / NT, n = e % NT;
+                    v = n < N ? Act<T>::load(Bp + (row0 + static_cast<size_t>(k) * TS + j) * a.ld_B + n)
+                              : 0.0f;
+                }
+                bsm[e] = v;
+            }
+            Bf = bsm;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < TS; ++j) {
+            const float uv = Act<T>::to_f(tu[j * CW + lane]);
+            const float xr = Act<T>::to_f(tr[j * CW + lane]);
+            float e;
+            const float dt = softplus_e(xr, e);
+            dsum += dt;
+            const float bs = DISC == 0 ? dt * uv : uv;
+            const float2 dt2 = f2(dt), bs2 = f2(bs);
+#pragma unroll
+            for (int q4 = 0; q4 < NT / 4; ++q4) {
+                const float4 B4 = *reinterpret_cast<const float4*>(Bf + j * NT + 4 * q4);
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    const int q = 2 * q4 + hq;
+                    const float2 Bq = hq ? make_float2(B4.z, B4.w) : make_float2(B4.x, B4.y);
+                    const float2 x = mul2(dt2, A2[q]);
+                    const float2 av = make_float2(ex2(x.x), ex2(x.y));
+                    float2 bu;
+                    if (DISC == 0) {
+                        bu = mul2(bs2, Bq);
+                    } else {
+                        const float2 xn = mul2(dt2, Anat[q]);
+                        const float c0f = fabsf(xn.x) < 0.5f ? dt * phi1_series(xn.x) : (av.x - 1.0f) * invA[q].x;
+                        const float c1f = fabsf(xn.y) < 0.5f ? dt * phi1_series(xn.y) : (av.y - 1.0f) * invA[q].y;
+                        bu = mul2(mul2(make_float2(c0f, c1f), bs2), Bq);
+                    }
+                    h[q] = fma2(av, h[q], bu);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && k + S < ke) issue(k + S);
+    }
+    if (k < ke && lane == 0) {
+        for (int kk = k; kk < ke && kk < k + S; ++kk)
+            mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
+    }
+    return k == ke;
+}
+
+// Shared memory of fwd_segsum_run: stages of u, delta_raw, B, the fp32 B tile
+// and the barriers.
+template <typename T, int NT>
+constexpr size_t fwd_segsum_smem_bytes() {
+    return kFwdStages * (2 * kFwdTile * kFwdChannels + kFwdTile * NT) * sizeof(T) + kFwdTile * NT * sizeof(float) +
+           kFwdStages * sizeof(uint64_t);
+}
+
+template <typename T, int NT, int DISC>
+__global__ void __launch_bounds__(32, 1)
+scan_fwd_segsum_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NQ = NT / 2;
+    const int lane = threadIdx.x;
+    const int c0 = blockIdx.x * kFwdChannels, b = blockIdx.y, g = blockIdx.z;
+    const int d = c0 + lane;
+    float2 h[NQ];
+    float dsum;
+    const bool done = fwd_segsum_run<T, NT, DISC>(maps, a, smem, c0, b, g, lane, h, dsum);
+    if (d < a.dinner && done) {
+        float* hp = a.seg_h + (static_cast<size_t>(b) * a.nseg + g) * NT * a.dinner + d;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            hp[static_cast<size_t>(2 * q) * a.dinner] = h[q].x;
+            hp[static_cast<size_t>(2 * q + 1) * a.dinner] = h[q].y;
+        }
+        a.seg_ds[(static_cast<size_t>(b) * a.nseg + g) * a.dinner + d] = dsum;
+    }
+}
+
 // Lane layout: a warp-sized CTA owns 32 channels of one batch row, one
 // channel per lane with all NT states of it in registers, so nothing per step
 // is computed twice and no value crosses lanes.
+//
+// CHUNKED: the a.nseg time segments of one 32-channel tile are the warps of
+// one CTA (the sequence split into chunks scanned in parallel).  Each warp but
+// the last first runs its segment from h = 0 (fwd_segsum_run) and leaves the
+// end state and the sum of delta in shared memory; after a CTA barrier each
+// warp combines the segments before it into its start state,
+//   h_start(g+1) = exp(A sum_g delta) h_start(g) + h_end_from_zero(g),
+// then scans its segment as below.  Each warp has its own shared-memory
+// region of fwd_warp_smem_bytes.
 template <typename T, int NT, int DISC, bool GATE>
-__global__ void __launch_bounds__(32, 1)
+constexpr size_t fwd_warp_smem_bytes() {
+    constexpr int NTEN = GATE ? 3 : 2;
+    constexpr int TILE = kFwdTile * kFwdChannels;
+    constexpr int STAGE = NTEN * TILE + 2 * kFwdTile * NT;
+    constexpr size_t bytes = kFwdStages * STAGE * sizeof(T) + 2 * kFwdTile * NT * sizeof(float) +
+                             2 * (kFwdTile / kChunk) * NT * kFwdChannels * sizeof(float) +
+                             2 * 2 * TILE * sizeof(T) + kFwdStages * sizeof(uint64_t);
+    return (bytes + 127) / 128 * 128;
+}
+template <int NT>
+constexpr size_t fwd_chunk_xchg_bytes(int nseg) {
+    return static_cast<size_t>(nseg) * (NT + 1) * kFwdChannels * sizeof(float);
+}
+
+template <typename T, int NT, int DISC, bool GATE, bool CHUNKED>
+__global__ void __launch_bounds__(CHUNKED ? 32 * kFwdChunkWarps : 32, 1)
 scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     constexpr int CW = kFwdChannels;                    // channels per CTA (32)
     constexpr int TS = kFwdTile;
@@ -118,14 +313,16 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
 
     constexpr int NCK = TS / kChunk;                    // chunk boundaries per tile
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_all[];
+    const int wid = CHUNKED ? static_cast<int>(threadIdx.x >> 5) : 0;
+    unsigned char* smem = smem_all + wid * fwd_warp_smem_bytes<T, NT, DISC, GATE>();
     T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
     float* bcs = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] B | C
     float* ckst = bcs + 2 * BCT;                                             // [2][NCK][NT][CW]
     T* ost = reinterpret_cast<T*>(ckst + 2 * NCK * NT * CW);                // [2][2][TS][CW] out | y
     uint64_t* full = reinterpret_cast<uint64_t*>(ost + 2 * 2 * TILE);        // [S]
 
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
     const int d = c0 + lane;
@@ -157,10 +354,51 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     const float Dd = (active && a.D) ? a.D[d] : 0.0f;
     // This CTA's time segment: tiles [kb, ke).  A segment after the first starts
     // from the state the segment pass left in h0 (exact: see the combine).
-    const int g = blockIdx.z;
+    const int g = CHUNKED ? wid : static_cast<int>(blockIdx.z);
     const int kb = g * a.seg_tiles;
     const int ke = min(ntiles, kb + a.seg_tiles);
     float2 h[NQ];
+    if constexpr (CHUNKED) {
+        // segments before the last: end state from h = 0 and the sum of delta,
+        // to shared memory ([nseg][NT][CW] states, then [nseg][CW] sums)
+        float* xh = reinterpret_cast<float*>(smem_all + blockDim.x / 32 * fwd_warp_smem_bytes<T, NT, DISC, GATE>());
+        float* xd = xh + static_cast<size_t>(a.nseg) * NT * CW;
+        if (g + 1 < a.nseg) {
+            float dsum;
+            fwd_segsum_run<T, NT, DISC>(maps, a, smem, c0, b, g, lane, h, dsum);
+            if (lane == 0)
+                for (int s2 = 0; s2 < S; ++s2)
+                    mbar_inval(reinterpret_cast<uint64_t*>(smem + fwd_segsum_smem_bytes<T, NT>() -
+                                                           S * sizeof(uint64_t)) + s2);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                xh[(g * NT + 2 * q) * CW + lane] = h[q].x;
+                xh[(g * NT + 2 * q + 1) * CW + lane] = h[q].y;
+            }
+            xd[g * CW + lane] = dsum;
+        }
+        fence_proxy_async_smem();   // the stages are TMA destinations again below
+        __syncthreads();
+        // start state: the caller's initial state (or 0), then the segments before g
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            h[q] = make_float2(0.0f, 0.0f);
+            if (active && a.h_init) {
+                const float* hp = a.h_init + (static_cast<size_t>(b) * N + 2 * q) * a.dinner + d;
+                if (2 * q < N) h[q].x = hp[0];
+                if (2 * q + 1 < N) h[q].y = hp[a.dinner];
+            }
+        }
+        for (int gp = 0; gp < g; ++gp) {
+            const float ds = xd[gp * CW + lane];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float2 P = make_float2(ex2(A2[q].x * ds), ex2(A2[q].y * ds));
+                h[q] = make_float2(fmaf(P.x, h[q].x, xh[(gp * NT + 2 * q) * CW + lane]),
+                                   fmaf(P.y, h[q].y, xh[(gp * NT + 2 * q + 1) * CW + lane]));
+            }
+        }
+    } else {
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         h[q] = make_float2(0.0f, 0.0f);
@@ -173,6 +411,7 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
             if (2 * q < N) h[q].x = hp[0];
             if (2 * q + 1 < N) h[q].y = hp[a.dinner];
         }
+    }
     }
 
     const T* Bp = static_cast<const T*>(a.B);
@@ -323,158 +562,6 @@ scan_fwd_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
     }
 }
 
-// Segment pass of the time-parallel forward: for segment g of batch row b,
-// run the recurrence from h = 0 and keep only the end state and the sum of
-// delta over the segment.  Since exp(delta_t A) multiplies across steps into
-// exp(A sum_t delta_t), the true state entering segment g+1 is
-//   h_start(g+1) = exp(A sum_g delta) h_start(g) + h_end_from_zero(g),
-// which scan_fwd_combine_kernel evaluates segment by segment.
-template <typename T, int NT, int DISC>
-__global__ void __launch_bounds__(32, 1)
-scan_fwd_segsum_kernel(const __grid_constant__ FwdMaps maps, const ScanFwdArgs a) {
-    constexpr int CW = kFwdChannels;
-    constexpr int TS = kFwdTile;
-    constexpr int S = kFwdStages;
-    constexpr int NQ = NT / 2;
-    constexpr int TILE = TS * CW;
-    constexpr int BCT = TS * NT;
-    constexpr int STAGE = 2 * TILE + BCT;               // u, delta_raw, B
-    constexpr uint32_t kActBytes = 2 * TILE * sizeof(T);
-    constexpr uint32_t kBBytes = BCT * sizeof(T);
-    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
-
-    extern __shared__ __align__(128) unsigned char smem[];
-    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
-    float* bsm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TS][NT] fp32 B
-    uint64_t* full = reinterpret_cast<uint64_t*>(bsm + BCT);                 // [S]
-
-    const int lane = threadIdx.x;
-    const int c0 = blockIdx.x * CW;
-    const int b = blockIdx.y;
-    const int g = blockIdx.z;
-    const int d = c0 + lane;
-    const bool active = d < a.dinner;
-    const int L = a.seqlen, N = a.dstate;
-    const size_t row0 = static_cast<size_t>(b) * L;
-    const bool bc_tma = a.bc_tma != 0;
-    const int kb = g * a.seg_tiles, ke = kb + a.seg_tiles;   // a full segment (never the last)
-
-    float2 A2[NQ], Anat[NQ], invA[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        float v[2], w[2], r[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = 2 * q + e;
-            const bool ok = active && n < N;
-            const float A = ok ? a_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : -1.0f;
-            v[e] = ok ? A * kLog2e : 0.0f;
-            w[e] = A;
-            r[e] = 1.0f / A;
-        }
-        A2[q] = make_float2(v[0], v[1]);
-        Anat[q] = make_float2(w[0], w[1]);
-        invA[q] = make_float2(r[0], r[1]);
-    }
-    float2 h[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) h[q] = make_float2(0.0f, 0.0f);
-    float dsum = 0.0f;
-
-    const T* Bp = static_cast<const T*>(a.B);
-    auto issue = [&](int k) {
-        const int s = (k - kb) % S;
-        T* dst = tiles + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kBBytes : 0u));
-        tma_load_3d(dst, &maps.u, &full[s], c0, k * TS, b);
-        tma_load_3d(dst + TILE, &maps.dr, &full[s], c0, k * TS, b);
-        if (bc_tma) tma_load_3d(dst + 2 * TILE, &maps.B, &full[s], 0, k * TS, b);
-    };
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    if (lane == 0)
-        for (int k = kb; k < kb + S && k < ke; ++k) issue(k);
-
-    int k = kb;
-    for (; k < ke; ++k) {
-        const int s = (k - kb) % S;
-        bool ok = mbar_wait(&full[s], ((k - kb) / S) & 1, kFaultFwdWait);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const T* tu = tiles + s * STAGE;
-        const T* tr = tu + TILE;
-        const T* tb = tu + 2 * TILE;
-        // fp32 B of this tile ([TS][NT]; past dstate 0)
-        const float* Bf;
-        if (bc_tma && sizeof(T) == 4) {
-            Bf = reinterpret_cast<const float*>(tb);
-        } else {
-            for (int e = lane; e < BCT; e += 32) {
-                float v;
-                if (bc_tma) {
-                    v = Act<T>::to_f(tb[e]);
-                } else {
-                    const int j = e / NT, n = e % NT;
-                    v = n < N ? Act<T>::load(Bp + (row0 + static_cast<size_t>(k) * TS + j) * a.ld_B + n)
-                              : 0.0f;
-                }
-                bsm[e] = v;
-            }
-            Bf = bsm;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < TS; ++j) {
-            const float uv = Act<T>::to_f(tu[j * CW + lane]);
-            const float xr = Act<T>::to_f(tr[j * CW + lane]);
-            float e;
-            const float dt = softplus_e(xr, e);
-            dsum += dt;
-            const float bs = DISC == 0 ? dt * uv : uv;
-            const float2 dt2 = f2(dt), bs2 = f2(bs);
-#pragma unroll
-            for (int q4 = 0; q4 < NT / 4; ++q4) {
-                const float4 B4 = *reinterpret_cast<const float4*>(Bf + j * NT + 4 * q4);
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    const int q = 2 * q4 + hq;
-                    const float2 Bq = hq ? make_float2(B4.z, B4.w) : make_float2(B4.x, B4.y);
-                    const float2 x = mul2(dt2, A2[q]);
-                    const float2 av = make_float2(ex2(x.x), ex2(x.y));
-                    float2 bu;
-                    if (DISC == 0) {
-                        bu = mul2(bs2, Bq);
-                    } else {
-                        const float2 xn = mul2(dt2, Anat[q]);
-                        const float c0f = fabsf(xn.x) < 0.5f ? dt * phi1_series(xn.x) : (av.x - 1.0f) * invA[q].x;
-                        const float c1f = fabsf(xn.y) < 0.5f ? dt * phi1_series(xn.y) : (av.y - 1.0f) * invA[q].y;
-                        bu = mul2(mul2(make_float2(c0f, c1f), bs2), Bq);
-                    }
-                    h[q] = fma2(av, h[q], bu);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && k + S < ke) issue(k + S);
-    }
-    if (k < ke && lane == 0) {
-        for (int kk = k; kk < ke && kk < k + S; ++kk)
-            mbar_wait(&full[(kk - kb) % S], ((kk - kb) / S) & 1, kFaultDrain);
-    }
-    if (active && k == ke) {
-        float* hp = a.seg_h + (static_cast<size_t>(b) * a.nseg + g) * NT * a.dinner + d;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            hp[static_cast<size_t>(2 * q) * a.dinner] = h[q].x;
-            hp[static_cast<size_t>(2 * q + 1) * a.dinner] = h[q].y;
-        }
-        a.seg_ds[(static_cast<size_t>(b) * a.nseg + g) * a.dinner + d] = dsum;
-    }
-}
-
 // Combine of the time segments: one thread per (batch row, state, channel)
 // walks the segments in order, from the caller's initial state (or 0), and
 // writes the state entering each segment.
@@ -499,17 +586,32 @@ __global__ void scan_fwd_combine_kernel(const ScanFwdArgs a) {
 
 template <typename T, int NT, int DISC, bool GATE>
 static cudaError_t launch_fwd_t(const FwdMaps& m, const ScanFwdArgs& a, cudaStream_t st) {
-    constexpr int NTEN = GATE ? 3 : 2;
-    constexpr int TILE = kFwdTile * kFwdChannels;
-    constexpr int STAGE = NTEN * TILE + 2 * kFwdTile * NT;
-    const size_t smem = kFwdStages * STAGE * sizeof(T) + 2 * kFwdTile * NT * sizeof(float) +
-                        2 * (kFwdTile / kChunk) * NT * kFwdChannels * sizeof(float) +
-                        2 * 2 * TILE * sizeof(T) + kFwdStages * sizeof(uint64_t);
-    auto kern = scan_fwd_kernel<T, NT, DISC, GATE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    const size_t smem = fwd_warp_smem_bytes<T, NT, DISC, GATE>();
     const unsigned gx = (a.dinner + kFwdChannels - 1) / kFwdChannels;
+    cudaError_t e;
+    if (a.nseg > 1 && a.nseg <= kFwdChunkWarps) {
+        // the segments as the warps of one CTA per (channel tile, batch row),
+        // when those CTAs (one shared-memory region per warp) all fit at once;
+        // otherwise separate CTAs per segment, which fit more per SM
+        auto kc = scan_fwd_kernel<T, NT, DISC, GATE, true>;
+        const size_t smc = a.nseg * smem + fwd_chunk_xchg_bytes<NT>(a.nseg);
+        e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kFwdChunkWarps * smem + fwd_chunk_xchg_bytes<NT>(kFwdChunkWarps)));
+        if (e != cudaSuccess) return e;
+        int dev = 0, nsm = 0, per_sm = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, 32 * a.nseg, smc);
+        if (e != cudaSuccess) return e;
+        if (static_cast<long long>(gx) * a.batch <= static_cast<long long>(nsm) * per_sm) {
+            kc<<<dim3(gx, a.batch, 1), 32 * a.nseg, smc, st>>>(m, a);
+            return cudaGetLastError();
+        }
+    }
+    auto kern = scan_fwd_kernel<T, NT, DISC, GATE, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     if (a.nseg > 1) {
         // segment pass (every segment but the last), then the combine
         constexpr int STG = 2 * kFwdTile * kFwdChannels + kFwdTile * NT;

@@ -4,7 +4,9 @@ uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
 otherwise; the wide cases below (short sequences, many channels) run the
 32-channel kernel, the rest the 16-channel one.  The forward scans time
 segments in parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512
-(the B2 L1000 case and the two marked below)."""
+(the B2 L1000 case and the three marked below): up to 4 segments as the
+warps of one CTA when those CTAs fit on the GPU at once, else one CTA per
+segment."""
 import numpy as np
 import pytest
 
@@ -26,9 +28,11 @@ CASES = [
     (2, 1000, 64, 16, "f32", 0, True, 0.5, 0.02),
     (1, 130, 512, 16, "f32", 1, True, 0.5, 0.02),   # 32 channel tiles
     (2, 24, 16, 0, "f32", 0, True, 0.0, 0.0),       # dstate = 0: y = D u
-    # time-segmented forward (few channels, seqlen >= 512): ragged last segment
+    # time-segmented forward (few channels, seqlen >= 512): ragged last segment;
+    # up to 4 segments run as the warps of one CTA (shared-memory combine)
     (1, 777, 96, 16, "bf16", 1, False, 0.5, 0.02),
     (3, 1030, 40, 5, "f32", 0, True, 0.3, 0.0),
+    (1, 1024, 4096, 16, "bf16", 0, True, 0.5, 0.02),   # 128 CTAs of 4 segment warps
     # 32-channel backward CTAs (4 * 256 = 1024 CTAs of 32 channels)
     (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
     (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
