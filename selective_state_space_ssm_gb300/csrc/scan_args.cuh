@@ -44,6 +44,9 @@ inline int fwd_seg_tiles(int seqlen, int g) {
 // CTAs fit an SM.
 constexpr int kBwdStages = 2;
 constexpr int kBwdMinBlocks16 = 14;
+// Backward time segments up to this count run as the warps of one CTA
+// (16-channel tiles), combined in shared memory.
+constexpr int kBwdChunkWarps = 4;
 // Channels per backward CTA: 32 when 32-channel CTAs already give at least 6
 // warps per SM on the 152 SMs of a GB300, else 16 (twice the warps).
 inline int bwd_channels(int batch, int dinner) {

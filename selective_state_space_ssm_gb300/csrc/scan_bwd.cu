@@ -65,11 +65,221 @@ template <> struct ActPair<__nv_bfloat16> {
     }
 };
 
+// Segment pass of the time-parallel backward: for segment sg >= 1 of batch
+// row b, walk its steps last to first with g = 0 after its last step,
+//   g_t = C_t dy_t + a_{t+1} g_{t+1},
+// and keep g at its first step, the sum of delta over its steps after the
+// first, and delta at its first step.  Because the product of a_s over steps
+// t0+1 .. t1+1 is exp(A (that sum + delta at t1+1)), the true g at the first
+// step of a segment is its zero-carry value plus that product times the true
+// g at the first step of the next segment (scan_bwd_combine_kernel).  A lane
+// owns NT * CW / 32 states of one channel: lane = (channel lane % CW, half
+// lane / CW of the states).  One warp; smem holds the stages and barriers of
+// the pass.  Returns false if a bounded wait gave up.
+template <typename T, int NT, bool GATE, int CW>
+__device__ __forceinline__ bool bwd_segsum_run(const BwdMaps& maps, const ScanBwdArgs& a, unsigned char* smem,
+                                               int c0, int b, int sg, int lane, float2 (&gl)[NT * CW / 64],
+                                               float& dsum, float& dfirst) {
+
+    constexpr int TC = kChunk;
+    constexpr int S = kBwdStages;
+    constexpr int SPL = 32 / CW;                 // lanes per channel
+    constexpr int NL = NT / SPL;                 // states per lane
+    constexpr int NQ = NL / 2;
+    constexpr int TILE = TC * CW;
+    constexpr int BCT = TC * NT;
+    constexpr int NTEN = GATE ? 3 : 2;           // delta_raw, dout, [z]
+    constexpr int STAGE = NTEN * TILE + BCT;     // + C
+    constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
+    constexpr uint32_t kCBytes = BCT * sizeof(T);
+    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
+
+    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
+    float* csm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TC][NT] fp32 C
+    uint64_t* full = reinterpret_cast<uint64_t*>(csm + BCT);                 // [S]
+
+    const int c = lane % CW, half = lane / CW;
+    const int nbase = half * NL;
+    const int d = c0 + c;
+    const bool active = d < a.dinner;
+    const int L = a.seqlen, N = a.dstate;
+    const int nchunks = (L + TC - 1) / TC;
+    const int kcb = sg * a.seg_chunks;
+    const int kce = min(nchunks, kcb + a.seg_chunks);
+    const int nit = kce - kcb;
+    const size_t row0 = static_cast<size_t>(b) * L;
+    const bool bc_tma = a.bc_tma != 0;
+
+    float2 A2[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = nbase + 2 * q + e;
+            const bool ok = active && n < N;
+            v[e] = ok ? a2_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : 0.0f;
+        }
+        A2[q] = make_float2(v[0], v[1]);
+    }
+    float2 an[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) gl[q] = an[q] = make_float2(0.0f, 0.0f);
+    dsum = 0.0f;
+    dfirst = 0.0f;
+
+    const T* Cp = static_cast<const T*>(a.C);
+    auto issue = [&](int it) {
+        const int kc = kce - 1 - it;
+        const int s = it % S;
+        T* dst = tiles + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kCBytes : 0u));
+        tma_load_3d(dst, &maps.dr, &full[s], c0, kc * TC, b);
+        tma_load_3d(dst + TILE, &maps.dout, &full[s], c0, kc * TC, b);
+        if (GATE) tma_load_3d(dst + 2 * TILE, &maps.z, &full[s], c0, kc * TC, b);
+        if (bc_tma) tma_load_3d(dst + NTEN * TILE, &maps.C, &full[s], 0, kc * TC, b);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int it = 0; it < S && it < nit; ++it) issue(it);
+
+    int it = 0;
+    for (; it < nit; ++it) {
+        const int kc = kce - 1 - it;
+        const int s = it % S;
+        bool ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const T* tr = tiles + s * STAGE;
+        const T* tg = tr + TILE;
+        const T* tz = tr + 2 * TILE;
+        const T* tc = tr + NTEN * TILE;
+        const float* Cf;
+        if (bc_tma && sizeof(T) == 4) {
+            Cf = reinterpret_cast<const float*>(tc);
+        } else {
+            for (int e = lane; e < BCT; e += 32) {
+                float v;
+                if (bc_tma) {
+                    v = Act<T>::to_f(tc[e]);
+                } else {
+                    const int j = e / NT, n = e % NT, t = kc * TC + j;
+                    v = (n < N && t < L) ? Act<T>::load(Cp + (row0 + t) * a.ld_C + n) : 0.0f;
+                }
+                csm[e] = v;
+            }
+            Cf = csm;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = TC - 1; j >= 0; --j) {
+            const int t = kc * TC + j;
+            const float xr = Act<T>::to_f(tr[j * CW + c]);
+            const float go = Act<T>::to_f(tg[j * CW + c]);
+            float dt, dy = go;
+            if (GATE) {
+                const float zv = Act<T>::to_f(tz[j * CW + c]);
+                float sz;
+                softplus_sigmoid(xr, zv, dt, sz);
+                dy = go * zv * sz;
+            } else {
+                float e;
+                dt = softplus_e(xr, e);
+            }
+            // past seqlen the tiles are zero: dy = 0 keeps g at 0 there
+            const float2 dy2 = f2(dy), dt2 = f2(dt);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float2 Cq = *reinterpret_cast<const float2*>(Cf + j * NT + nbase + 2 * q);
+                gl[q] = fma2(an[q], gl[q], mul2(Cq, dy2));
+                const float2 x = mul2(dt2, A2[q]);
+                an[q] = make_float2(ex2(x.x), ex2(x.y));
+            }
+            if (t < L) {
+                if (t == kcb * TC) dfirst = dt;
+                else dsum += dt;
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && it + S < nit) issue(it + S);
+    }
+    if (it < nit && lane == 0) {
+        for (int k2 = it; k2 < nit && k2 < it + S; ++k2)
+            mbar_wait(&full[k2 % S], (k2 / S) & 1, kFaultDrain);
+    }
+    return it == nit;
+}
+
+// Shared memory of bwd_segsum_run.
+template <typename T, int NT, bool GATE, int CW>
+constexpr size_t bwd_segsum_smem_bytes() {
+    return kBwdStages * ((GATE ? 3 : 2) * kChunk * CW + kChunk * NT) * sizeof(T) + kChunk * NT * sizeof(float) +
+           kBwdStages * sizeof(uint64_t);
+}
+
+template <typename T, int NT, bool GATE, int CW>
+__global__ void __launch_bounds__(32, 1)
+scan_bwd_segsum_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NL = NT * CW / 32, NQ = NL / 2;
+    const int lane = threadIdx.x;
+    const int c = lane % CW, half = lane / CW, nbase = half * NL;
+    const int c0 = blockIdx.x * CW, b = blockIdx.y, sg = blockIdx.z + 1;   // segments 1 .. nseg-1
+    const int d = c0 + c;
+    float2 gl[NQ];
+    float dsum, dfirst;
+    const bool done = bwd_segsum_run<T, NT, GATE, CW>(maps, a, smem, c0, b, sg, lane, gl, dsum, dfirst);
+    if (d < a.dinner && done) {
+        const size_t pb = static_cast<size_t>(b) * a.nseg + sg;
+        float* gp = a.seg_g + (pb * NT + nbase) * a.dinner + d;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            gp[static_cast<size_t>(2 * q) * a.dinner] = gl[q].x;
+            gp[static_cast<size_t>(2 * q + 1) * a.dinner] = gl[q].y;
+        }
+        if (half == 0) {
+            a.seg_ds[pb * a.dinner + d] = dsum;
+            a.seg_d0[pb * a.dinner + d] = dfirst;
+        }
+    }
+}
+
+// Shared memory of one backward warp: its stages, checkpoint tiles, per-step
+// scalars, partial sums and barriers.
+template <typename T, int NT, int DISC, bool GATE, int CW>
+__host__ __device__ constexpr size_t bwd_smem_bytes() {
+    constexpr int TC = kChunk;
+    constexpr int NTEN = GATE ? 5 : 3;
+    constexpr int NQN = DISC == 1 ? 3 : 2;
+    return kBwdStages * (NTEN * TC * CW + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
+           + kBwdStages * NT * CW * sizeof(float)      // checkpoint tiles
+           + 2 * TC * NT * sizeof(float)               // fp32 B|C (bf16 or unaligned B/C)
+           + 3 * TC * CW * sizeof(float)               // delta, delta*u, dy
+           + TC * NQN * 4 * CW * sizeof(float)         // state-sum partials
+           + (CW == 32 ? TC : 4) * 9 * NT * sizeof(float)   // dB or dC partials by channel group
+           + 2 * TC * CW * sizeof(float)               // sigmoid(delta_raw), sigmoid(z)
+           + kBwdStages * sizeof(uint64_t);
+}
+
 // CW = channels per CTA (one warp): 32 (each lane 4 channels) or 16 (each lane
 // 2 channels: half the work per warp and fewer registers, so twice the warps
 // when the problem has few channels).
-template <typename T, int NT, int DISC, bool GATE, int CW>
-__global__ void __launch_bounds__(32, CW == 16 ? kBwdMinBlocks16 : 1)
+//
+// CHUNKED: the a.nseg time segments of one channel tile are the warps of one
+// CTA.  Each warp but the first first walks its segment backwards from g = 0
+// (bwd_segsum_run) and leaves g at its first step, the sum of delta over its
+// later steps and delta at its first step in shared memory; after a CTA
+// barrier each warp but the last combines the segments after its own into its
+// carry (dL/dh and delta at the first step of the next segment), then runs its
+// segment as below.  Each warp has its own shared-memory region of
+// bwd_warp_bytes(); the exchange follows them.
+template <typename T, int NT, int DISC, bool GATE, int CW, bool CHUNKED = false>
+__global__ void __launch_bounds__(CHUNKED ? 32 * kBwdChunkWarps : 32,
+                                  CHUNKED ? kBwdMinBlocks16 / kBwdChunkWarps : (CW == 16 ? kBwdMinBlocks16 : 1))
 scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr int TC = kChunk;
     constexpr int S = kBwdStages;
@@ -91,7 +301,10 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     constexpr int PR = CW == 32 ? TC : 4;       // steps per dB/dC flush
     constexpr int PJ = 9 * NT;                  // padded partial row: conflict-free float4 sums
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_all[];
+    const int wid = CHUNKED ? static_cast<int>(threadIdx.x >> 5) : 0;
+    constexpr size_t warp_bytes = CHUNKED ? (bwd_smem_bytes<T, NT, DISC, GATE, CW>() + 127) / 128 * 128 : 0;
+    unsigned char* smem = smem_all + wid * warp_bytes;
     T* tiles = reinterpret_cast<T*>(smem);                               // [S][STAGE]
     float* cks = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T)); // [S][NT][CW]
     float* bcs = cks + S * NT * CW;                                      // [TC][NT] B | [TC][NT] C
@@ -104,15 +317,15 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     float* Psz = Psdr + TILE;                                            // [TC][CW] sigmoid(z)
     uint64_t* full = reinterpret_cast<uint64_t*>(Psz + TILE);            // [S]
 
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const int cg = lane >> 2, ng = lane & 3;     // channel group (CPL channels), state group (NS states)
     const int cbase = cg * CPL;
     const int c0 = blockIdx.x * CW;
     const int b = blockIdx.y;
     const int L = a.seqlen, N = a.dstate, Dn = a.dinner;
     const int nchunks = (L + TC - 1) / TC;
-    // this CTA's time segment: chunks [kcb, kce), walked last to first
-    const int sg = blockIdx.z;
+    // this CTA's (warp's) time segment: chunks [kcb, kce), walked last to first
+    const int sg = CHUNKED ? wid : static_cast<int>(blockIdx.z);
     const int kcb = sg * a.seg_chunks;
     const int kce = min(nchunks, kcb + a.seg_chunks);
     const int nit = kce - kcb;
@@ -173,6 +386,59 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         if (kc > 0)
             tma_load_2d(cks + s * NT * CW, &maps.ck, &full[s], c0, (b * a.nck + kc - 1) * NT);
     };
+    // CHUNKED: the segment pass of the warps after the first, the exchange and
+    // this warp's carry ([NT][CW] dL/dh, then [CW] delta) in shared memory
+    float* xcarry = nullptr;
+    if constexpr (CHUNKED) {
+        constexpr int SNL = NT * CW / 32, SNQ = SNL / 2;
+        const int nw = static_cast<int>(blockDim.x >> 5);
+        float* xg = reinterpret_cast<float*>(smem_all + nw * warp_bytes);    // [nseg][NT][CW]
+        float* xds = xg + nw * NT * CW;                                       // [nseg][CW]
+        float* xd0 = xds + nw * CW;                                           // [nseg][CW]
+        xcarry = xd0 + nw * CW + wid * (NT + 1) * CW;                         // [nseg][NT + 1][CW]
+        const int sc = lane % CW, shalf = lane / CW, snb = shalf * SNL;
+        if (sg >= 1) {
+            float2 gl[SNQ];
+            float dsum, dfirst;
+            bwd_segsum_run<T, NT, GATE, CW>(maps, a, smem, c0, b, sg, lane, gl, dsum, dfirst);
+            if (lane == 0)
+                for (int s2 = 0; s2 < S; ++s2)
+                    mbar_inval(reinterpret_cast<uint64_t*>(smem + bwd_segsum_smem_bytes<T, NT, GATE, CW>() -
+                                                           S * sizeof(uint64_t)) + s2);
+#pragma unroll
+            for (int q = 0; q < SNQ; ++q) {
+                xg[(sg * NT + snb + 2 * q) * CW + sc] = gl[q].x;
+                xg[(sg * NT + snb + 2 * q + 1) * CW + sc] = gl[q].y;
+            }
+            if (shalf == 0) {
+                xds[sg * CW + sc] = dsum;
+                xd0[sg * CW + sc] = dfirst;
+            }
+        }
+        fence_proxy_async_smem();   // the stages are TMA destinations again below
+        __syncthreads();
+        if (sg + 1 < a.nseg) {
+            // carry = true g at the first step of segment sg + 1, walking the
+            // segments last to first as the global combine does
+            const int dd = c0 + sc;
+#pragma unroll
+            for (int q = 0; q < SNL; ++q) {
+                const int n = snb + q;
+                const float A2 = (dd < Dn && n < N) ? a2_from_alog(a.A_log[static_cast<size_t>(dd) * N + n]) : 0.0f;
+                float carry = 0.0f;
+                for (int s2 = a.nseg - 1; s2 > sg; --s2) {
+                    float gstart = xg[(s2 * NT + n) * CW + sc];
+                    if (s2 + 1 < a.nseg)
+                        gstart = fmaf(ex2(A2 * (xds[s2 * CW + sc] + xd0[(s2 + 1) * CW + sc])), carry, gstart);
+                    carry = gstart;
+                }
+                xcarry[n * CW + sc] = carry;
+            }
+            if (shalf == 0) xcarry[NT * CW + sc] = xd0[(sg + 1) * CW + sc];
+        }
+        __syncwarp();
+    }
+
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
@@ -219,7 +485,13 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             const int d = c0 + cbase + i;
-            if (d < Dn) {
+            if (d < Dn && CHUNKED) {
+                dl_next[i] = xcarry[NT * CW + cbase + i];
+#pragma unroll
+                for (int p = 0; p < NS / 2; ++p)
+                    g[i][p] = make_float2(xcarry[(ng * NS + 2 * p) * CW + cbase + i],
+                                          xcarry[(ng * NS + 2 * p + 1) * CW + cbase + i]);
+            } else if (d < Dn) {
                 dl_next[i] = a.carry_dl[plane_b * Dn + d];
 #pragma unroll
                 for (int p = 0; p < NS / 2; ++p) {
@@ -773,167 +1045,6 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
     }
 }
 
-// Segment pass of the time-parallel backward: for segment sg >= 1 of batch
-// row b, walk its steps last to first with g = 0 after its last step,
-//   g_t = C_t dy_t + a_{t+1} g_{t+1},
-// and keep g at its first step, the sum of delta over its steps after the
-// first, and delta at its first step.  Because the product of a_s over steps
-// t0+1 .. t1+1 is exp(A (that sum + delta at t1+1)), the true g at the first
-// step of a segment is its zero-carry value plus that product times the true
-// g at the first step of the next segment (scan_bwd_combine_kernel).  A lane
-// owns NT * CW / 32 states of one channel.
-template <typename T, int NT, bool GATE, int CW>
-__global__ void __launch_bounds__(32, 1)
-scan_bwd_segsum_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
-    constexpr int TC = kChunk;
-    constexpr int S = kBwdStages;
-    constexpr int SPL = 32 / CW;                 // lanes per channel
-    constexpr int NL = NT / SPL;                 // states per lane
-    constexpr int NQ = NL / 2;
-    constexpr int TILE = TC * CW;
-    constexpr int BCT = TC * NT;
-    constexpr int NTEN = GATE ? 3 : 2;           // delta_raw, dout, [z]
-    constexpr int STAGE = NTEN * TILE + BCT;     // + C
-    constexpr uint32_t kActBytes = NTEN * TILE * sizeof(T);
-    constexpr uint32_t kCBytes = BCT * sizeof(T);
-    static_assert((STAGE * sizeof(T)) % 128 == 0, "stages stay 128-byte aligned");
-
-    extern __shared__ __align__(128) unsigned char smem[];
-    T* tiles = reinterpret_cast<T*>(smem);                                   // [S][STAGE]
-    float* csm = reinterpret_cast<float*>(smem + S * STAGE * sizeof(T));    // [TC][NT] fp32 C
-    uint64_t* full = reinterpret_cast<uint64_t*>(csm + BCT);                 // [S]
-
-    const int lane = threadIdx.x;
-    const int c = lane % CW, half = lane / CW;
-    const int nbase = half * NL;
-    const int c0 = blockIdx.x * CW;
-    const int b = blockIdx.y;
-    const int sg = blockIdx.z + 1;               // segments 1 .. nseg-1
-    const int d = c0 + c;
-    const bool active = d < a.dinner;
-    const int L = a.seqlen, N = a.dstate;
-    const int nchunks = (L + TC - 1) / TC;
-    const int kcb = sg * a.seg_chunks;
-    const int kce = min(nchunks, kcb + a.seg_chunks);
-    const int nit = kce - kcb;
-    const size_t row0 = static_cast<size_t>(b) * L;
-    const bool bc_tma = a.bc_tma != 0;
-
-    float2 A2[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        float v[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = nbase + 2 * q + e;
-            const bool ok = active && n < N;
-            v[e] = ok ? a2_from_alog(a.A_log[static_cast<size_t>(d) * N + n]) : 0.0f;
-        }
-        A2[q] = make_float2(v[0], v[1]);
-    }
-    float2 gl[NQ], an[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) gl[q] = an[q] = make_float2(0.0f, 0.0f);
-    float dsum = 0.0f, dfirst = 0.0f;
-
-    const T* Cp = static_cast<const T*>(a.C);
-    auto issue = [&](int it) {
-        const int kc = kce - 1 - it;
-        const int s = it % S;
-        T* dst = tiles + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], kActBytes + (bc_tma ? kCBytes : 0u));
-        tma_load_3d(dst, &maps.dr, &full[s], c0, kc * TC, b);
-        tma_load_3d(dst + TILE, &maps.dout, &full[s], c0, kc * TC, b);
-        if (GATE) tma_load_3d(dst + 2 * TILE, &maps.z, &full[s], c0, kc * TC, b);
-        if (bc_tma) tma_load_3d(dst + NTEN * TILE, &maps.C, &full[s], 0, kc * TC, b);
-    };
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    if (lane == 0)
-        for (int it = 0; it < S && it < nit; ++it) issue(it);
-
-    int it = 0;
-    for (; it < nit; ++it) {
-        const int kc = kce - 1 - it;
-        const int s = it % S;
-        bool ok = mbar_wait(&full[s], (it / S) & 1, kFaultBwdWait);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const T* tr = tiles + s * STAGE;
-        const T* tg = tr + TILE;
-        const T* tz = tr + 2 * TILE;
-        const T* tc = tr + NTEN * TILE;
-        const float* Cf;
-        if (bc_tma && sizeof(T) == 4) {
-            Cf = reinterpret_cast<const float*>(tc);
-        } else {
-            for (int e = lane; e < BCT; e += 32) {
-                float v;
-                if (bc_tma) {
-                    v = Act<T>::to_f(tc[e]);
-                } else {
-                    const int j = e / NT, n = e % NT, t = kc * TC + j;
-                    v = (n < N && t < L) ? Act<T>::load(Cp + (row0 + t) * a.ld_C + n) : 0.0f;
-                }
-                csm[e] = v;
-            }
-            Cf = csm;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = TC - 1; j >= 0; --j) {
-            const int t = kc * TC + j;
-            const float xr = Act<T>::to_f(tr[j * CW + c]);
-            const float go = Act<T>::to_f(tg[j * CW + c]);
-            float dt, dy = go;
-            if (GATE) {
-                const float zv = Act<T>::to_f(tz[j * CW + c]);
-                float sz;
-                softplus_sigmoid(xr, zv, dt, sz);
-                dy = go * zv * sz;
-            } else {
-                float e;
-                dt = softplus_e(xr, e);
-            }
-            // past seqlen the tiles are zero: dy = 0 keeps g at 0 there
-            const float2 dy2 = f2(dy), dt2 = f2(dt);
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float2 Cq = *reinterpret_cast<const float2*>(Cf + j * NT + nbase + 2 * q);
-                gl[q] = fma2(an[q], gl[q], mul2(Cq, dy2));
-                const float2 x = mul2(dt2, A2[q]);
-                an[q] = make_float2(ex2(x.x), ex2(x.y));
-            }
-            if (t < L) {
-                if (t == kcb * TC) dfirst = dt;
-                else dsum += dt;
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && it + S < nit) issue(it + S);
-    }
-    if (it < nit && lane == 0) {
-        for (int k2 = it; k2 < nit && k2 < it + S; ++k2)
-            mbar_wait(&full[k2 % S], (k2 / S) & 1, kFaultDrain);
-    }
-    if (active && it == nit) {
-        const size_t pb = static_cast<size_t>(b) * a.nseg + sg;
-        float* gp = a.seg_g + (pb * NT + nbase) * a.dinner + d;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            gp[static_cast<size_t>(2 * q) * a.dinner] = gl[q].x;
-            gp[static_cast<size_t>(2 * q + 1) * a.dinner] = gl[q].y;
-        }
-        if (half == 0) {
-            a.seg_ds[pb * a.dinner + d] = dsum;
-            a.seg_d0[pb * a.dinner + d] = dfirst;
-        }
-    }
-}
-
 // Combine of the backward's time segments: one thread per (batch row, state,
 // channel) walks the segments last to first and writes the carry (true dL/dh
 // and delta at the first step of the next segment) of every segment but the
@@ -1007,27 +1118,38 @@ __global__ void scan_reduce_kernel(const ScanReduceArgs a) {
     }
 }
 
-template <typename T, int NT, int DISC, bool GATE, int CW>
-static size_t bwd_smem_bytes() {
-    constexpr int TC = kChunk;
-    constexpr int NTEN = GATE ? 5 : 3;
-    constexpr int NQN = DISC == 1 ? 3 : 2;
-    return kBwdStages * (NTEN * TC * CW + 2 * TC * NT) * sizeof(T)   // activation, B, C tiles
-           + kBwdStages * NT * CW * sizeof(float)      // checkpoint tiles
-           + 2 * TC * NT * sizeof(float)               // fp32 B|C (bf16 or unaligned B/C)
-           + 3 * TC * CW * sizeof(float)               // delta, delta*u, dy
-           + TC * NQN * 4 * CW * sizeof(float)         // state-sum partials
-           + (CW == 32 ? TC : 4) * 9 * NT * sizeof(float)   // dB or dC partials by channel group
-           + 2 * TC * CW * sizeof(float)               // sigmoid(delta_raw), sigmoid(z)
-           + kBwdStages * sizeof(uint64_t);
-}
 
 template <typename T, int NT, int DISC, bool GATE, int CW>
 static cudaError_t launch_bwd_cw(const BwdMaps& maps, const ScanBwdArgs& a, cudaStream_t st) {
     const size_t smem = bwd_smem_bytes<T, NT, DISC, GATE, CW>();
+    cudaError_t e;
+    if constexpr (CW == 16) {
+        if (a.nseg > 1 && a.nseg <= kBwdChunkWarps) {
+            // the segments as the warps of one CTA per (channel tile, batch row),
+            // when those CTAs all fit at once
+            auto kc = scan_bwd_kernel<T, NT, DISC, GATE, CW, true>;
+            const size_t wb = (smem + 127) / 128 * 128;
+            auto bytes = [&](int nw) {
+                return nw * wb + static_cast<size_t>(nw) * (NT * CW + 2 * CW + (NT + 1) * CW) * sizeof(float);
+            };
+            e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(bytes(kBwdChunkWarps)));
+            if (e != cudaSuccess) return e;
+            int dev = 0, nsm = 0, per_sm = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, 32 * a.nseg, bytes(a.nseg));
+            if (e != cudaSuccess) return e;
+            if (static_cast<long long>(a.ncl) * a.batch <= static_cast<long long>(nsm) * per_sm) {
+                kc<<<dim3(static_cast<unsigned>(a.ncl), static_cast<unsigned>(a.batch), 1), 32 * a.nseg,
+                     bytes(a.nseg), st>>>(maps, a);
+                return cudaGetLastError();
+            }
+        }
+    }
     auto kern = scan_bwd_kernel<T, NT, DISC, GATE, CW>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (a.nseg > 1) {
         // segment pass (segments 1 .. nseg-1), then the combine of the carries
