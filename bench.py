@@ -286,7 +286,8 @@ def cpu_oracle_sample(cfg, inp, target_s=12.0, threads=1):
     (channel blocks).  Returns (Mtokens/s, sample text, seconds)."""
     import numpy as np
     import oracle
-    L, D, Bn = cfg["seqlen"], cfg["dinner"], cfg["batch"]
+    L, D = cfg["seqlen"], cfg["dinner"]
+    Bn = min(cfg["batch"], inp["u"].shape[0] // L)   # batch rows the inputs hold
 
     def run(nb, dsub):
         sl, rows = slice(0, dsub), slice(0, nb * L)
@@ -977,7 +978,7 @@ def run_reference(args):
         return
     from selective_state_space_ssm_gb300 import workloads
     cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
-    inp = workloads.named_scan_inputs(WORKLOAD, batch=1)
+    inp = workloads.named_scan_inputs(WORKLOAD)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     ncores = host_cores()
     vals, secs = [], []

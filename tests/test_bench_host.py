@@ -38,3 +38,15 @@ def test_alu_roofline_counts_the_recurrences_minimal_fp32_work():
     assert abs(r["fwd_frac"] - 4 * el / peak / 1e-3) < 1e-4
     assert abs(r["bwd_frac"] - 12 * el / peak / 3e-3) < 1e-4
     assert abs(r["step_frac"] - 16 * el / peak / 4e-3) < 1e-4
+
+
+def test_cpu_sample_counts_only_rows_it_has():
+    """The CPU oracle sample never counts batch rows its inputs do not hold:
+    with one batch row of data it runs and counts one row, whatever the
+    workload's batch."""
+    from selective_state_space_ssm_gb300 import workloads
+    cfg = dict(batch=8, seqlen=16, dinner=64, dstate=4)
+    inp = workloads.scan_inputs(1, 16, 64, 4, seed=1)
+    v, sample, secs = bench.cpu_oracle_sample(cfg, inp, target_s=0.5, threads=1)
+    assert sample.startswith("batch rows [0, 1)")
+    assert v > 0 and secs > 0
