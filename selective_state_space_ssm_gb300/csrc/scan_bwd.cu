@@ -448,10 +448,13 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
         for (int it = 0; it < S && it < nit; ++it) issue(it);
     __syncwarp();
 
-    // The carries of the reverse recurrence (g) and the dA accumulators live in
-    // registers only during the reverse pass and epilogue; between chunks they
-    // are parked in the (then idle) state-sum buffer, so pass B can hold the
-    // chunk's a h_{t-1} values in registers.
+    // The carries of the reverse recurrence (g) and the dA accumulators: with
+    // ZOH B, and in 16-channel CTAs held to 128 registers, they live in
+    // registers only during the reverse pass and epilogue and are parked in the
+    // (then idle) state-sum buffer between chunks, so pass B can hold the
+    // chunk's a h_{t-1} values in registers without spilling; otherwise they
+    // stay in registers throughout (no shared-memory round trip per chunk).
+    constexpr bool kPark = DISC == 1 || (CW == 16 && !CHUNKED);
     float* stash = part;
     static_assert(2 * CPL * NS * 32 <= TC * NQN * 4 * CW, "stash fits in the partials buffer");
     float2 dA[CPL][NS / 2], g[CPL][NS / 2];
@@ -460,6 +463,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
 #pragma unroll
         for (int p = 0; p < NS / 2; ++p) dA[i][p] = g[i][p] = make_float2(0.f, 0.f);
     auto park = [&]() {
+        if constexpr (!kPark) return;
 #pragma unroll
         for (int i = 0; i < CPL; ++i)
 #pragma unroll
@@ -469,6 +473,7 @@ scan_bwd_kernel(const __grid_constant__ BwdMaps maps, const ScanBwdArgs a) {
             }
     };
     auto unpark = [&]() {
+        if constexpr (!kPark) return;
 #pragma unroll
         for (int i = 0; i < CPL; ++i)
 #pragma unroll
