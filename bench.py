@@ -237,6 +237,42 @@ class ClockSampler:
         return res
 
 
+def graph_kernel_count(run, dev):
+    """Kernel launches of one call sequence: `run(stream)` captured once into a
+    CUDA graph (outside any timed region, never replayed) and the graph's
+    kernel nodes counted through the driver API.  Returns (count, note); count
+    is None when the capture or the count is not available."""
+    import ctypes
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        return None, "this PyTorch cannot keep a captured graph"
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    try:
+        with torch.cuda.graph(g, stream=s):
+            run(s)
+        torch.cuda.synchronize(dev)
+        cu = ctypes.CDLL("libcuda.so.1")
+        graph = ctypes.c_void_p(g.raw_cuda_graph())
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
+            return None, "cuGraphGetNodes failed"
+        nodes = (ctypes.c_void_p * max(n.value, 1))()
+        if cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
+            return None, "cuGraphGetNodes failed"
+        kind = ctypes.c_int(-1)
+        kernels = 0
+        for i in range(n.value):
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(kind)) != 0:
+                return None, "cuGraphNodeGetType failed"
+            kernels += kind.value == 0          # CU_GRAPH_NODE_TYPE_KERNEL
+        return kernels, f"kernel nodes of one step captured in a CUDA graph ({n.value} nodes in all)"
+    except Exception as e:                      # capture refused by a call of the step
+        return None, f"capture failed: {type(e).__name__}"
+
+
 def clock_soak(step, sync, t_start, min_span=CLOCK_WINDOW_S):
     """Repeat `step` (untimed) until at least min_span seconds have passed
     since t_start, so that a short timed region still gets clock samples of
@@ -646,6 +682,12 @@ def run_block(args):
     t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     t_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms_step = t_fwd + t_bwd
+
+    def step_on(s):
+        ssm.ssm_block_fwd(desc, x, w, out, ctx, wsb, s)
+        ssm.ssm_block_bwd(desc, x, w, dout, ctx, dx, grads, wsb, s)
+
+    per_step, launch_note = graph_kernel_count(step_on, dev)
     M = dims["batch"] * dims["seqlen"]
     f_fwd, f_bwd = block_flops(dims)
     peaks, peak_kind = measured_peaks()
@@ -670,7 +712,8 @@ def run_block(args):
                      "note": "fp32 products as three TF32 passes: the tensor cores run 3x these "
                              "flops, so 1/3 is this figure's ceiling",
                      "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4)},
-        "gpu_launches": None, "clocks": clk,
+        "gpu_launches": None if per_step is None else per_step * K,
+        "gpu_launches_per_step": per_step, "gpu_launches_source": launch_note, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 
