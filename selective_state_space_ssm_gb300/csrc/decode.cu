@@ -37,8 +37,9 @@ __device__ __forceinline__ float silu_f(float x) { return x * rcp(1.0f + ex2(-x 
 // One thread = one channel, all dstate states of it (in packed pairs), for the
 // kStepRows batch rows of its CTA (a 64 x 4096 batch: 1024 CTAs of 128
 // threads, 7 per SM by the 72-register budget).  A log2(e) of the channel is computed once
-// into shared memory; the next row's states are loaded while the current row
-// is computed and stored.  FULL: dstate == NT.
+// into shared memory; the first two rows' states are both loaded before that
+// set-up (more bytes in flight from the start), and each later row while the
+// one before it is computed and stored.  FULL: dstate == NT.
 template <typename T, int NT, int DISC, bool GATE, bool FULL>
 __global__ void __launch_bounds__(kStepThreads, 7)
 scan_step_kernel(const ScanStepArgs a) {
@@ -70,6 +71,7 @@ scan_step_kernel(const ScanStepArgs a) {
     };
     Row cur, nxt;
     if (active) load_row(cur, b0);                 // the longest loads first
+    if (active && nrow > 1) load_row(nxt, b0 + 1);
 
     // the rows' B and C, zero past dstate so that packed pairs need no guard
     for (int i = threadIdx.x; i < nrow * NT; i += kStepThreads) {
@@ -104,7 +106,7 @@ scan_step_kernel(const ScanStepArgs a) {
     for (int r = 0; r < RB; ++r) {
         if (r >= nrow) break;
         const int b = b0 + r;
-        if (r + 1 < nrow) load_row(nxt, b + 1);   // next row in flight during this one
+        if (r > 0 && r + 1 < nrow) load_row(nxt, b + 1);   // next row in flight during this one
 
         float dt, gz = 1.0f;
         if (GATE) {
