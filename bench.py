@@ -314,32 +314,32 @@ def recorded_traffic():
 
 # ----------------------------------------------------------------- CPU oracle leg
 
-def cpu_oracle_sample(cfg, inp, target_s=12.0, threads=1):
-    """Time the fp64 oracle (scan fwd + bwd) on a slice of the workload: the
-    first `nb` batch rows, all seqlen steps, the first `dsub` channels, grown
-    until it takes about target_s.  dB/dC/dA_log/dD over the slice are part of
-    the work.  threads > 1 runs the oracle's chains on that many host threads
-    (channel blocks).  Returns (Mtokens/s, sample text, seconds)."""
+def oracle_slice_seconds(inp, L, nb, dsub, threads):
+    """Seconds the fp64 oracle (scan fwd + bwd) takes on the first nb batch rows
+    (all L steps) and the first dsub channels of the workload's inputs."""
     import numpy as np
     import oracle
+    sl, rows = slice(0, dsub), slice(0, nb * L)
+    u, dr, z, dout = (inp[k][rows, sl].astype(np.float64) for k in ("u", "delta_raw", "z", "dout"))
+    B, C = inp["B"][rows].astype(np.float64), inp["C"][rows].astype(np.float64)
+    Al, Dv = inp["A_log"][sl].astype(np.float64), inp["D"][sl].astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.scan_fwd(u, dr, Al, B, C, Dv, z, 0, batch=nb, threads=threads)
+    oracle.scan_bwd(u, dr, Al, B, C, Dv, z, dout, 0, batch=nb, threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_slice(cfg, inp, target_s, threads):
+    """The slice of the workload the oracle covers in about target_s: grown
+    from one batch row and a few channels (channels first, then batch rows).
+    Returns (nb, dsub, seconds of the last run)."""
+    import oracle
+    oracle.build()
     L, D = cfg["seqlen"], cfg["dinner"]
     Bn = min(cfg["batch"], inp["u"].shape[0] // L)   # batch rows the inputs hold
-
-    def run(nb, dsub):
-        sl, rows = slice(0, dsub), slice(0, nb * L)
-        u, dr, z, dout = (inp[k][rows, sl].astype(np.float64) for k in ("u", "delta_raw", "z",
-                                                                         "dout"))
-        B, C = inp["B"][rows].astype(np.float64), inp["C"][rows].astype(np.float64)
-        Al, Dv = inp["A_log"][sl].astype(np.float64), inp["D"][sl].astype(np.float64)
-        t0 = time.perf_counter()
-        oracle.scan_fwd(u, dr, Al, B, C, Dv, z, 0, batch=nb, threads=threads)
-        oracle.scan_bwd(u, dr, Al, B, C, Dv, z, dout, 0, batch=nb, threads=threads)
-        return time.perf_counter() - t0
-
-    oracle.build()
     nb, dsub = 1, min(D, max(16, 8 * threads))
-    t = run(nb, dsub)
-    for _ in range(4):                 # grow the slice until it takes about target_s
+    t = oracle_slice_seconds(inp, L, nb, dsub, threads)
+    for _ in range(4):
         if t >= 0.7 * target_s or (dsub >= D and nb >= Bn):
             break
         scale = target_s / max(t, 1e-3)
@@ -347,9 +347,27 @@ def cpu_oracle_sample(cfg, inp, target_s=12.0, threads=1):
             dsub = max(8, int(min(D, max(dsub + 8, dsub * scale))) // 8 * 8)
         else:
             nb = int(min(Bn, max(nb + 1, math.floor(nb * scale))))
-        t = run(nb, dsub)
+        t = oracle_slice_seconds(inp, L, nb, dsub, threads)
+    return nb, dsub, t
+
+
+def oracle_rate(cfg, nb, dsub, t):
+    """Mtokens/s of the full-width problem that a slice timed at t seconds is
+    worth, and the slice's description."""
+    L, D = cfg["seqlen"], cfg["dinner"]
     tokens = nb * L * dsub / D       # rows of the full-width problem this slice is worth
-    return tokens / t / 1e6, f"batch rows [0, {nb}), {L} steps, channels [0, {dsub}) of {D}", t
+    return tokens / t / 1e6, f"batch rows [0, {nb}), {L} steps, channels [0, {dsub}) of {D}"
+
+
+def cpu_oracle_sample(cfg, inp, target_s=12.0, threads=1):
+    """Time the fp64 oracle (scan fwd + bwd) on a slice of the workload: the
+    first `nb` batch rows, all seqlen steps, the first `dsub` channels, grown
+    until it takes about target_s.  dB/dC/dA_log/dD over the slice are part of
+    the work.  threads > 1 runs the oracle's chains on that many host threads
+    (channel blocks).  Returns (Mtokens/s, sample text, seconds)."""
+    nb, dsub, t = oracle_slice(cfg, inp, target_s, threads)
+    v, sample = oracle_rate(cfg, nb, dsub, t)
+    return v, sample, t
 
 
 def host_cores():
@@ -1022,12 +1040,16 @@ def run_reference(args):
     from selective_state_space_ssm_gb300 import workloads
     cfg = dict(workloads.SCAN_WORKLOADS[WORKLOAD])
     inp = workloads.named_scan_inputs(WORKLOAD)
-    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    # the slice is sized once (about 60 s of oracle work over all steps), then
+    # every warm-up and timed step runs that same slice
+    per_step = max(0.25, 60.0 / max(1, args.steps + args.warmup))
     ncores = host_cores()
+    nb, dsub, _ = oracle_slice(cfg, inp, per_step, ncores)
     vals, secs = [], []
     sample = ""
     for i in range(args.warmup + args.steps):
-        v, sample, s = cpu_oracle_sample(cfg, inp, target_s=per_step, threads=ncores)
+        s = oracle_slice_seconds(inp, cfg["seqlen"], nb, dsub, ncores)
+        v, sample = oracle_rate(cfg, nb, dsub, s)
         if i >= args.warmup:
             vals.append(v)
             secs.append(s)

@@ -50,3 +50,31 @@ def test_cpu_sample_counts_only_rows_it_has():
     v, sample, secs = bench.cpu_oracle_sample(cfg, inp, target_s=0.5, threads=1)
     assert sample.startswith("batch rows [0, 1)")
     assert v > 0 and secs > 0
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the metric, unit and config of the GPU arm, a cpu_baseline and an
+    e2e object with zero host-device bytes; every step times the same slice,
+    sized once."""
+    import json
+    import types
+    monkeypatch.setattr(bench, "WORKLOAD", "tiny_scan_fp32")
+    calls = []
+    real = bench.oracle_slice_seconds
+
+    def counted(inp, L, nb, dsub, threads):
+        calls.append((nb, dsub))
+        return real(inp, L, nb, dsub, threads)
+
+    monkeypatch.setattr(bench, "oracle_slice_seconds", counted)
+    args = types.SimpleNamespace(steps=3, warmup=2)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "Mtokens/s" and line["steps"] == 3 and line["warmup"] == 2
+    assert line["config"]["workload"].startswith("tiny_scan_fp32")
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the 5 steps all ran the slice that the sizing ended on
+    assert len(set(calls[-5:])) == 1
