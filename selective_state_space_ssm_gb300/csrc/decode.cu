@@ -25,7 +25,7 @@ namespace {
 
 constexpr int kStepThreads = 128;
 constexpr int kStepRows = 2;     // batch rows per decode-step CTA
-constexpr int kConvRows = 4;     // batch rows per conv-step thread
+constexpr int kConvRows = 2;     // batch rows per conv-step thread
 
 __device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4f(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -185,10 +185,29 @@ conv_step_kernel(const ConvStepArgs a) {
     const float4 bias = a.bias ? ld4f(a.bias + d0) : make_float4(0.f, 0.f, 0.f, 0.f);
     float wt[4][K];
     const float* w = a.w + static_cast<size_t>(d0) * K;
+    if constexpr (K == 4) {
+        // the 4 channels' taps are 16 contiguous floats: four 16-byte loads
+        if ((reinterpret_cast<uintptr_t>(w) & 15u) == 0) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                const float4 q = ld4f(w + 4 * c);
+                wt[c][0] = q.x;
+                wt[c][1] = q.y;
+                wt[c][2] = q.z;
+                wt[c][3] = q.w;
+            }
+        } else {
 #pragma unroll
-        for (int k = 0; k < K; ++k) wt[c][k] = w[c * K + k];
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < K; ++k) wt[c][k] = w[c * K + k];
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < K; ++k) wt[c][k] = w[c * K + k];
+    }
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
         if (r >= nrow) break;
