@@ -70,6 +70,9 @@ def parse():
     p.add_argument("--decode", action="store_true",
                    help="time single-token decode (conv1d+SiLU step + scan step per layer) on "
                         "the decode workload instead of the scan step")
+    p.add_argument("--conv", action="store_true",
+                   help="time the causal depthwise conv1d + SiLU (forward + backward) on the "
+                        "block workload's shape instead of the scan step")
     p.add_argument("--measure-pipes", metavar="OUT_JSON", default=None,
                    help="measure the MUFU ex2 and fp32 FFMA / FFMA2 rates of the GPU with the "
                         "library's probe kernels (CUDA events + sampled SM clock), write them "
@@ -738,6 +741,144 @@ def run_block(args):
 
 # ----------------------------------------------------------------- decode leg
 
+CONV_METRIC = "Mamba-1 conv1d+SiLU fwd+bwd Mtokens/s; achieved % of the HBM roofline"
+
+
+def conv_bytes(M, D, K):
+    """Algorithmic HBM bytes of the conv, fp32: forward x in, out out (plus
+    the taps and bias); backward x and dout in, dx out (plus taps and bias
+    in, dw and dbias out)."""
+    params = D * (K + 1) * 4
+    return M * D * 8 + params, M * D * 12 + 2 * params
+
+
+def conv_cpu_sample(x, w, bias, dout, batch, target_s=8.0):
+    """The fp64 oracle's conv forward + backward on the first dsub channels,
+    grown until it takes about target_s; scaled to Mtokens/s of the full
+    width."""
+    import oracle
+    oracle.build()
+    D = x.shape[1]
+    M = x.shape[0]
+    dsub = 8
+    while True:
+        sl = slice(0, dsub)
+        t0 = time.perf_counter()
+        oracle.conv1d_silu_fwd(x[:, sl], w[sl], bias[sl], batch=batch)
+        oracle.conv1d_silu_bwd(x[:, sl], w[sl], bias[sl], dout[:, sl], batch=batch)
+        t = time.perf_counter() - t0
+        if t >= 0.5 * target_s or dsub >= D:
+            break
+        dsub = int(min(D, max(2 * dsub, dsub * target_s / max(t, 1e-3))))
+    return M * dsub / D / t / 1e6, f"all {M} rows, channels [0, {dsub}) of {D}", t
+
+
+def run_conv(args):
+    """The causal depthwise conv1d + SiLU on the block workload's shape (its x
+    a column view of the in_proj output, as in the block), forward and
+    backward, each against the measured HBM bandwidth."""
+    import numpy as np
+    import torch
+    import selective_state_space_ssm_gb300 as ssm
+    from selective_state_space_ssm_gb300 import build as ssm_build, workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        raise SystemExit("--conv runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm_build.build()
+    ssm.load()
+    bcfg = workloads.BLOCK_WORKLOADS[BLOCK_WORKLOAD]
+    Bn, L, D, K = bcfg["batch"], bcfg["seqlen"], bcfg["dinner"], bcfg["dconv"]
+    if args.batch:
+        Bn = args.batch
+    if args.seqlen:
+        L = args.seqlen
+    M = Bn * L
+    inp = workloads.conv_inputs(Bn, L, D, K, seed=bcfg["seed"])
+    xz = torch.zeros((M, 2 * D), dtype=torch.float32, device=dev)
+    xz[:, :D] = torch.from_numpy(inp["x"]).to(dev)
+    x = xz[:, :D]                                   # the in_proj output's x half
+    w = torch.from_numpy(inp["w"]).to(dev)
+    b = torch.from_numpy(inp["bias"]).to(dev)
+    dout = torch.from_numpy(inp["dout"]).to(dev)
+    out = torch.empty((M, D), dtype=torch.float32, device=dev)
+    dxz = torch.empty((M, 2 * D), dtype=torch.float32, device=dev)
+    dx = dxz[:, :D]
+    dw, db = torch.empty_like(w), torch.empty_like(b)
+    wsb = torch.empty(ssm.ssm_conv1d_silu_bwd_workspace_bytes(Bn, L, D, K), dtype=torch.uint8,
+                      device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ssm.ssm_conv1d_silu(Bn, x, w, b, out, stream)
+
+    def bwd():
+        ssm.ssm_conv1d_silu_bwd(Bn, x, w, b, dout, dx, dw, db, wsb, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    K2 = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    h0 = time.perf_counter()
+    for i in range(K2):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    h1 = time.perf_counter()
+
+    def step_untimed():
+        fwd()
+        bwd()
+
+    h2 = clock_soak(step_untimed, torch.cuda.synchronize, h0)
+    clocks.window(h0, h2, timed=(h0, h1))
+    clk = clocks.stop()
+    t_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_step = t_fwd + t_bwd
+    by_f, by_b = conv_bytes(M, D, K)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ach_f = by_f / (t_fwd * 1e-3) / 1e9
+    ach_b = by_b / (t_bwd * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        v, sample, secs = conv_cpu_sample(inp["x"], inp["w"], inp["bias"], inp["dout"], Bn)
+        cpu = {"value": round(v, 6), "unit": "Mtokens/s", "cores": 1, "kind": "oracle",
+               "sample": sample, "seconds": round(secs, 2)}
+    line = {
+        "metric": CONV_METRIC, "value": round(M / (ms_step * 1e-3) / 1e6, 4), "unit": "Mtokens/s",
+        "n_gpus": 1, "steps": K2, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; the workload's distributions)",
+        "config": {"workload": f"mamba_block_fp32 conv: batch {Bn}, seqlen {L}, dinner {D}, "
+                               f"kconv {K}, fp32, x and dx column views of (M, 2 dinner)",
+                   "global_batch": Bn, "seq_len": L,
+                   "l2": "inputs larger than L2 (2 x 100 MB per pass), no flush"},
+        "roofline": {"kernel": "conv1d_silu_bwd_kernel + conv1d_reduce_kernel (ssm_conv1d_silu_bwd)",
+                     "bound": "hbm", "achieved": round(ach_b, 1), "peak": round(hbm, 1),
+                     "unit": "GB/s", "frac": round(ach_b / hbm, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": by_b, "fwd_bytes": by_f,
+                     "fwd_ms": round(t_fwd, 4), "bwd_ms": round(t_bwd, 4),
+                     "fwd_frac": round(ach_f / hbm, 4), "bwd_frac": round(ach_b / hbm, 4)},
+        "cpu_baseline": cpu, "e2e": None,
+        "e2e_note": "inside the block the conv's input and output stay on the device",
+        "gpu_launches": 3 * K2, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 DECODE_WORKLOAD = "mamba1p4b_decode_fp32"
 DECODE_METRIC = ("Mamba-1 decode (conv1d+SiLU step + scan step per layer) tokens/s; "
                  "achieved % of the HBM roofline")
@@ -1081,6 +1222,8 @@ def main():
         run_block(args)
     elif args.decode:
         run_decode(args)
+    elif args.conv:
+        run_conv(args)
     else:
         run_gb300(args)
 

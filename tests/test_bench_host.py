@@ -78,3 +78,12 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     # the 5 steps all ran the slice that the sizing ended on
     assert len(set(calls[-5:])) == 1
+
+
+def test_conv_bytes():
+    """The conv's algorithmic bytes: 8 per element forward (x in, out out), 12
+    backward (x, dout in; dx out), plus the taps and bias (and, backward,
+    their gradients)."""
+    fwd, bwd = bench.conv_bytes(16384, 1536, 4)
+    assert fwd == 16384 * 1536 * 8 + 1536 * 5 * 4
+    assert bwd == 16384 * 1536 * 12 + 2 * 1536 * 5 * 4
