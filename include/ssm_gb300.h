@@ -138,14 +138,15 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc,
  * x and out are (M, dinner) fp32 with row strides ld_x, ld_out (0 = packed);
  * w is (dinner, kconv) fp32 with tap k = 0 on the CURRENT step (the reverse of
  * torch.nn.Conv1d's weight order); bias (dinner) fp32 may be NULL.
- * 1 <= kconv <= 8. */
+ * 1 <= kconv <= 8.  out must not overlap x (a thread reads rows that another
+ * thread's run writes). */
 ssm_status ssm_conv1d_silu(int32_t batch, int32_t seqlen, int32_t dinner, int32_t kconv,
                            const float* x, int64_t ld_x, const float* w, const float* bias,
                            float* out, int64_t ld_out, cudaStream_t stream);
 
 /* Backward of ssm_conv1d_silu (mamba1_cpu.ts backward steps 5-4): given
  * dout = dL/d(out) (ld_dout), writes dx (ld_dx), dw (dinner, kconv) and dbias
- * (dinner; may be NULL).  workspace must hold
+ * (dinner; may be NULL).  dx must not overlap x or dout.  workspace must hold
  * ssm_conv1d_silu_bwd_workspace_bytes(...) bytes. */
 size_t ssm_conv1d_silu_bwd_workspace_bytes(int32_t batch, int32_t seqlen, int32_t dinner,
                                            int32_t kconv);
