@@ -196,6 +196,16 @@ struct Run {
         return o;
     }
 
+    // x (rows, cols) transposed into buf as a GEMM operand, with the column sums
+    // of x written to colsum from the same pass (ws: colsum_ws_floats floats).
+    Op operand_t_colsum(const float* x, int64_t ldx, int rows, int cols, float* buf, float* colsum,
+                        float* ws) {
+        Op o{buf, cols, rows, 0};
+        o.ld = round4(o.cols);
+        if (ok()) cuda(ssm::launch_operand_copy_t_colsum(x, ldx, rows, cols, buf, o.ld, colsum, ws, st));
+        return o;
+    }
+
     // C (A.rows, B.rows) = A B^T (+ bias) (+ R); A.cols == B.cols.
     void gemm(const Op& A, const Op& B, float* C, int64_t ldc, const float* bias, const float* R,
               int64_t ldr) {
@@ -613,10 +623,9 @@ ssm_status ssm_block_bwd(const ssm_block_desc* d, const float* x, const ssm_bloc
             Op Wt = run.operand(W, k, nout, k, true, whi);   // (k, nout)
             run.gemm(A, Wt, dX, lddx, nullptr, accumulate ? dX : nullptr, lddx);
         }
-        Op At = run.operand(dY, lddy, M, nout, true, ahi);   // (nout, M)
-        Op Xt = run.operand(X, ldx, M, k, true, bhi);        // (k, M)
+        Op At = run.operand_t_colsum(dY, lddy, M, nout, ahi, db, red);   // (nout, M); db
+        Op Xt = run.operand(X, ldx, M, k, true, bhi);                     // (k, M)
         run.gemm(At, Xt, dW, k, nullptr, nullptr, 0);
-        if (run.ok()) run.cuda(ssm::launch_colsum(dY, lddy, M, nout, db, red, stream));
     };
 
     // 10. out_proj (the residual's share of dx is added at step 1)

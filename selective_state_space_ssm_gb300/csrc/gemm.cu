@@ -585,10 +585,15 @@ __global__ void transpose_kernel(const float* __restrict__ x, int64_t ldx, int r
 
 // Transpose of 64 x 64 tiles with 16-byte loads and stores (x, out 16-byte
 // aligned, ldx and ldo multiples of 4); tiles cut by the matrix edge take
-// single-element accesses.  256 threads, 4 float4 each way per thread.
+// single-element accesses.  256 threads, 4 float4 each way per thread.  With
+// csum non-null the tile's column sums (over its 64 rows, in a fixed order)
+// are also written to csum[blockIdx.y][column]: the column sums of x come out
+// of the same pass over it.
 __global__ void __launch_bounds__(256) transpose64_kernel(const float* __restrict__ x, int64_t ldx, int rows,
-                                                          int cols, float* __restrict__ out, int64_t ldo) {
+                                                          int cols, float* __restrict__ out, int64_t ldo,
+                                                          float* __restrict__ csum) {
     __shared__ float tile[64][65];
+    __shared__ float qsum[4][64];
     const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
     const int t = threadIdx.x;
     const bool full = r0 + 64 <= rows && c0 + 64 <= cols;
@@ -615,6 +620,14 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const float* __restric
         tile[rr][cc + 3] = v[i].w;
     }
     __syncthreads();
+    if (csum) {
+        // column t % 64 over rows 16 (t / 64) .. + 15 (zeros past the edge)
+        const int c = t & 63, q = t >> 6;
+        float sacc = 0.0f;
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) sacc += tile[16 * q + rr][c];
+        qsum[q][c] = sacc;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int idx = t + 256 * i, cr = idx >> 4, rc = (idx & 15) * 4;
@@ -629,6 +642,12 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const float* __restric
                 if (r0 + rc + k < rows) dst[k] = e[k];
         }
     }
+    if (csum) {
+        __syncthreads();
+        if (t < 64 && c0 + t < cols)
+            csum[static_cast<int64_t>(blockIdx.y) * cols + c0 + t] =
+                ((qsum[0][t] + qsum[1][t]) + qsum[2][t]) + qsum[3][t];
+    }
 }
 
 cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols, int transpose,
@@ -638,7 +657,7 @@ cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols,
                      ldx % 4 == 0 && ldo % 4 == 0;
     if (transpose && vec) {
         dim3 grid((cols + 63) / 64, (rows + 63) / 64);
-        transpose64_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
+        transpose64_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo, nullptr);
     } else if (transpose) {
         dim3 grid((cols + 31) / 32, (rows + 31) / 32);
         transpose_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo);
@@ -683,8 +702,52 @@ __global__ void colsum_final_kernel(const float* __restrict__ part, int nparts, 
     out[c] = s;
 }
 
+// Sum of nparts partial rows of cols columns: a CTA per 32 columns, its 8
+// warps each adding every 8th partial (lane = column), then the 8 warp sums
+// in a fixed order.
+__global__ void __launch_bounds__(256) colsum_final8_kernel(const float* __restrict__ part, int nparts,
+                                                            int cols, float* __restrict__ out) {
+    __shared__ float red[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
+    float s = 0.0f;
+    if (c < cols)
+        for (int p = w; p < nparts; p += 8) s += part[static_cast<int64_t>(p) * cols + c];
+    red[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && c < cols) {
+        float t = red[0][lane];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) t += red[k][lane];
+        out[c] = t;
+    }
+}
+
+// Partials of the 64-row tiles of the transposing copy, or of kColsumRows-row
+// slabs: the larger count.
 size_t colsum_ws_floats(int rows, int cols) {
-    return static_cast<size_t>((rows + kColsumRows - 1) / kColsumRows) * cols;
+    return static_cast<size_t>((rows + 63) / 64) * cols;
+}
+
+cudaError_t launch_operand_copy_t_colsum(const float* x, int64_t ldx, int rows, int cols, float* out,
+                                         int64_t ldo, float* colsum, float* ws, cudaStream_t st) {
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
+                     ldx % 4 == 0 && ldo % 4 == 0;
+    if (!colsum || !vec) {
+        cudaError_t e = launch_operand_copy(x, ldx, rows, cols, 1, out, ldo, st);
+        if (e != cudaSuccess || !colsum) return e;
+        return launch_colsum(x, ldx, rows, cols, colsum, ws, st);
+    }
+    if (cols == 0) return cudaSuccess;
+    const int nparts = (rows + 63) / 64;
+    if (nparts > 0) {
+        dim3 grid((cols + 63) / 64, nparts);
+        transpose64_kernel<<<grid, 256, 0, st>>>(x, ldx, rows, cols, out, ldo, ws);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    colsum_final8_kernel<<<(cols + 31) / 32, 256, 0, st>>>(ws, nparts, cols, colsum);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_colsum(const float* x, int64_t ldx, int rows, int cols, float* out, float* ws,

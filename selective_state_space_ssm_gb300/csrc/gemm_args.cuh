@@ -72,6 +72,11 @@ cudaError_t launch_operand_copy(const float* x, int64_t ldx, int rows, int cols,
 size_t colsum_ws_floats(int rows, int cols);
 cudaError_t launch_colsum(const float* x, int64_t ldx, int rows, int cols, float* out, float* ws,
                           cudaStream_t st);
+// The transposed operand copy of launch_operand_copy (transpose = 1) that also
+// writes colsum[n] = sum_m x[m, n] (null: the copy only) from the same pass
+// over x when the copy takes 16-byte accesses; ws as for launch_colsum.
+cudaError_t launch_operand_copy_t_colsum(const float* x, int64_t ldx, int rows, int cols, float* out,
+                                         int64_t ldo, float* colsum, float* ws, cudaStream_t st);
 
 // RMSNorm of cpu_ops.ts: inv[r] = 1/sqrt(mean_i x[r,i]^2 + eps); y = x inv w.
 cudaError_t launch_rmsnorm_fwd(const float* x, const float* w, int rows, int dm, float eps,
