@@ -40,6 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "Mamba-1 selective scan fwd+bwd Mtokens/s; achieved % of HBM/SFU roofline"
+E2E_SETS = 3   # device buffer sets of the end-to-end leg (uploads / compute / read-backs in flight)
 WORKLOAD = "mamba1p4b_scan_bf16"
 BLOCK_WORKLOAD = "mamba_block_fp32"
 SM_COUNT = 152
@@ -528,28 +529,30 @@ def run_gb300(args):
         "bwd_frac": round(bound_bwd / (t_bwd * 1e-3), 4),
     }
 
-    # ---- end to end: host buffers, copies inside the timed region.  Two device
-    # buffer sets: step i uses set i % 2, so the upload of step i+1 and the
-    # read-back of step i-1 run on their own streams while step i computes.
+    # ---- end to end: host buffers, copies inside the timed region.  E2E_SETS
+    # device buffer sets: step i uses set i % E2E_SETS, so the uploads of the
+    # next steps and the read-backs of the previous ones run on their own
+    # streams while step i computes.
     e2e = None
     if not args.no_e2e:
         pin = {k: v.pin_memory() for k, v in host.items()}
         outs = {"out": out, "du": du, "ddelta": ddr, "dz": dz, "dB": dB, "dC": dC, "dA_log": dA,
                 "dD": dD}
-        ins = [t, {k: torch.empty_like(v) for k, v in t.items()}]
-        osets = [outs, {k: torch.empty_like(v) for k, v in outs.items()}]
+        ins = [t] + [{k: torch.empty_like(v) for k, v in t.items()} for _ in range(E2E_SETS - 1)]
+        osets = [outs] + [{k: torch.empty_like(v) for k, v in outs.items()}
+                          for _ in range(E2E_SETS - 1)]
         hout = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
-                for _ in range(2)]
+                for _ in range(E2E_SETS)]
         h2d = sum(v.numel() * v.element_size() for v in pin.values())
         d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
-        K2 = max(2, min(K, 10))
+        K2 = max(E2E_SETS, min(K, 20))
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        computed = [torch.cuda.Event() for _ in range(2)]
-        read_back = [torch.cuda.Event() for _ in range(2)]
+        in_ready = [torch.cuda.Event() for _ in range(E2E_SETS)]
+        computed = [torch.cuda.Event() for _ in range(E2E_SETS)]
+        read_back = [torch.cuda.Event() for _ in range(E2E_SETS)]
 
         def e2e_step(i):
-            j = i % 2
+            j = i % E2E_SETS
             T, O = ins[j], osets[j]
             s_in.wait_event(computed[j])            # set j's inputs no longer read
             with torch.cuda.stream(s_in):
@@ -570,7 +573,7 @@ def run_gb300(args):
                     hout[j][k].copy_(v, non_blocking=True)
                 read_back[j].record(s_out)
 
-        for i in range(2):
+        for i in range(E2E_SETS):
             e2e_step(i)
         torch.cuda.synchronize()
         barrier()
@@ -587,8 +590,8 @@ def run_gb300(args):
         e2e = {"value": round(whole_job_rate(M, ws, ms_e2e), 4), "unit": "Mtokens/s",
                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": K2,
-               "overlap": "uploads and read-backs on their own streams, double-buffered, "
-                          "overlapping the compute of the neighbouring steps"}
+               "overlap": f"uploads and read-backs on their own streams, {E2E_SETS} device buffer "
+                          "sets, overlapping the compute of the neighbouring steps"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
