@@ -55,8 +55,9 @@ def test_benchmark_workload_runs_one_segment_with_32_channel_backward(table):
 
 
 def test_few_channel_workloads(table):
-    # B8 L1024 D1536: 16-channel backward CTAs (twice the warps), no segments
-    assert table[(8, 1024, 1536)] == (16, 1, 1)
+    # B8 L1024 D1536: 16-channel backward CTAs (twice the warps: 768, 5 per
+    # SM) and 2 backward time segments; the forward (384 warps) is not split
+    assert table[(8, 1024, 1536)] == (16, 1, 2)
     # B1 L65536 D2048: time segments in both passes (15 forward, 8 backward)
     assert table[(1, 65536, 2048)] == (16, 15, 8)
     # the tiny problem: too short to split

@@ -4,9 +4,9 @@ uses 32-channel CTAs when batch * ceil(dinner / 32) >= 912 and 16-channel CTAs
 otherwise; the wide cases below (short sequences, many channels) run the
 32-channel kernel, the rest the 16-channel one.  The forward scans time
 segments in parallel when batch * ceil(dinner / 32) < 304 and seqlen >= 512
-(the B2 L1000 case and the three marked below): up to 4 segments as the
-warps of one CTA when those CTAs fit on the GPU at once, else one CTA per
-segment."""
+(the B2 L1000 case and the ones marked below), the backward when its warps
+number fewer than 912 and seqlen >= 512: up to 4 segments as the warps of
+one CTA when those CTAs fit on the GPU at once, else one CTA per segment."""
 import numpy as np
 import pytest
 
@@ -37,6 +37,9 @@ CASES = [
     (4, 40, 8192, 16, "bf16", 0, True, 0.5, 0.02),
     (4, 21, 8192, 16, "f32", 1, True, 0.5, 0.02),
     (8, 17, 3680, 6, "f32", 0, False, 0.3, 0.0),    # NT = 8
+    # 304 16-channel backward warps (fewer than 6 per SM): 2 backward time
+    # segments as the warps of one CTA; the forward too splits in 2
+    (4, 600, 1216, 16, "f32", 0, True, 0.3, 0.02),
     # dinner not a multiple of 32: a ragged last 32-channel tile (8 and 4 channels)
     (8, 19, 3688, 16, "bf16", 0, True, 0.3, 0.02),
     (8, 23, 3684, 16, "f32", 1, True, 0.3, 0.02),
