@@ -9,8 +9,13 @@ import parity
 
 pytestmark = pytest.mark.gpu
 
+# (batch, seqlen, dinner, kconv, bias): rows are walked in runs of 64 and
+# loaded in groups (4 forward, 8 backward, 4 backward for kconv > 4), so the
+# cases cover ragged groups and runs, halos across run boundaries, seqlen <
+# kconv and every kconv from 1 to 8
 CASES = [(2, 37, 24, 4, True), (1, 100, 64, 3, False), (3, 5, 8, 1, True), (2, 70, 32, 8, True),
-         (1, 130, 1536, 4, True)]
+         (1, 130, 1536, 4, True), (2, 3, 16, 6, True), (1, 129, 40, 7, True), (2, 66, 24, 5, False),
+         (2, 9, 8, 2, True)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}L{}D{}K{}{}".format(*c[:4], "" if c[4] else "-nobias"))
@@ -52,3 +57,27 @@ def test_conv_strided_views(lib):
     ref, _ = oracle.conv1d_silu_fwd(inp["x"], inp["w"], inp["bias"], batch=Bt)
     assert parity.rel_l2(out.cpu().numpy(), ref) <= parity.TOL_FWD_F32
     assert torch.count_nonzero(out_wide[:, :D]) == 0 and torch.count_nonzero(out_wide[:, 2 * D:]) == 0
+
+
+def test_conv_unaligned_taps(lib):
+    """Taps whose rows do not start on 16 bytes (a view one float into a
+    buffer) take the scalar tap loads; same result as the oracle."""
+    import torch
+    Bt, L, D, K = 2, 75, 32, 4
+    inp = workloads.conv_inputs(Bt, L, D, K, seed=11)
+    buf = torch.zeros(D * K + 1, device="cuda")
+    buf[1:] = torch.from_numpy(inp["w"]).cuda().reshape(-1)
+    w = buf[1:].view(D, K)
+    assert w.data_ptr() % 16 != 0
+    x = torch.from_numpy(inp["x"]).cuda()
+    b = torch.from_numpy(inp["bias"]).cuda()
+    dout = torch.from_numpy(inp["dout"]).cuda()
+    out = lib.conv1d_silu(x, w, b, batch=Bt)
+    dx, dw, db = lib.conv1d_silu_bwd(x, w, b, dout, batch=Bt)
+    torch.cuda.synchronize()
+    ref_out, _ = oracle.conv1d_silu_fwd(inp["x"], inp["w"], inp["bias"], batch=Bt)
+    rdx, rdw, rdb = oracle.conv1d_silu_bwd(inp["x"], inp["w"], inp["bias"], inp["dout"], batch=Bt)
+    assert parity.rel_l2(out.cpu().numpy(), ref_out) <= parity.TOL_FWD_F32
+    assert parity.rel_l2(dx.cpu().numpy(), rdx) <= parity.TOL_GRAD_F32
+    assert parity.rel_l2(dw.cpu().numpy(), rdw) <= parity.TOL_GRAD_F32
+    assert parity.rel_l2(db.cpu().numpy(), rdb) <= parity.TOL_GRAD_F32

@@ -178,3 +178,25 @@ def test_conv_step(lib, K):
         for t in range(P, L):
             o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, cst)
             assert parity.rel_l2(_f64(o), ref[:, t]) <= parity.TOL_FWD_F32, (P, t)
+
+
+def test_conv_step_unaligned_taps(lib):
+    """Taps whose rows do not start on 16 bytes (a view one float into a
+    buffer) take the scalar tap loads of the conv step: same steps as the
+    whole-sequence oracle; an odd batch leaves a thread with one row."""
+    import torch
+    Bt, L, D, K = 3, 9, 40, 4
+    cin = workloads.conv_inputs(Bt, L, D, K, seed=91)
+    ref, _ = oracle.conv1d_silu_fwd(cin["x"], cin["w"], cin["bias"], batch=Bt)
+    ref = ref.reshape(Bt, L, D)
+    xs = cin["x"].reshape(Bt, L, D)
+    buf = torch.zeros(D * K + 1, device="cuda")
+    buf[1:] = _gpu(cin["w"]).reshape(-1)
+    w = buf[1:].view(D, K)
+    assert w.data_ptr() % 16 != 0
+    bias = _gpu(cin["bias"])
+    cst = torch.zeros((Bt, K - 1, D), dtype=torch.float32, device="cuda")
+    for t in range(L):
+        o = lib.conv1d_silu_step(_gpu(xs[:, t]), w, bias, cst)
+        torch.cuda.synchronize()
+        assert parity.rel_l2(_f64(o), ref[:, t]) <= parity.TOL_FWD_F32, t
