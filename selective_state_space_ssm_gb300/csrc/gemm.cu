@@ -169,6 +169,12 @@ struct GemmTile {
 // running sums per thread, so the other three warpgroups hand it registers
 // (setmaxnreg): 128 x (kGemmRegsSmall + 2 x kGemmRegsConv + kGemmRegsEpi) must not exceed the
 // 512 x (launch registers) the CTA starts with, which the launcher checks.
+//
+// RES: the launch adds a residual R (ksplit 1); its epilogue loads each
+// sub-tile's residual one sub-tile ahead, so that the loads' latency overlaps
+// the previous sub-tile's stores (GEMMs with a short K are bound by it).  The
+// launches without a residual keep the plain epilogue.
+template <bool RES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     constexpr int S = kGemmStages;
@@ -400,6 +406,21 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         for (int t = blockIdx.x; t < ntiles && got; t += gridDim.x) {
             const GemmTile x = tile_of(t);
             const int ng = (x.nk + G - 1) / G;
+            // RES: the residual rows of the sub-tile stored next (column x.n0 +
+            // c0 + lane, rows x.m0 + 32 q ..), loaded one sub-tile ahead
+            const int rb = x.m0 + 32 * q;
+            const int nrows = min(32, a.M - rb);
+            float resn[RES ? 32 : 1];
+            auto load_res = [&](int c0) {
+                if constexpr (RES) {
+                    const int col = x.n0 + c0 + lane;
+                    const bool ld = col < a.N && nrows > 0;
+                    const float* Rp = ld ? a.R + static_cast<size_t>(rb) * a.ldr + col : nullptr;
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr)
+                        resn[rr] = ld ? ld_global_f32(Rp + static_cast<size_t>(min(rr, nrows - 1)) * a.ldr) : 0.0f;
+                }
+            };
             for (int gi = 0; gi < ng && got; ++gi, ++gg) {
                 const int buf = gg & 1;
                 got = mbar_wait(&acc_full[buf], (gg >> 1) & 1, kFaultGemm) && got;
@@ -420,6 +441,7 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (lane == 0) mbar_arrive(&acc_empty[buf]);
             }
             if (!got) break;
+            load_res(0);
             // each warp turns its 32 x 32 sub-tiles around through its slice of
             // ebuf so that global stores run along rows
 #pragma unroll
@@ -433,6 +455,11 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 #pragma unroll
                 for (int rr = 0; rr < 32; ++rr) v[rr] = tile[rr * 33 + lane];
                 __syncwarp();
+                if constexpr (RES) {
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) v[rr] += resn[rr];
+                    if (c0 + 32 < kGemmBN) load_res(c0 + 32);
+                }
                 const int col = x.n0 + c0 + lane;
                 const int rbase = x.m0 + 32 * q;
                 const int rows = min(32, a.M - rbase);
@@ -445,7 +472,7 @@ gemm_tf32x3_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                             if (rr < rows) st_global_f32(P + static_cast<size_t>(rr) * a.N, v[rr]);
                     } else {
                         const float bv = a.bias ? a.bias[col] : 0.0f;
-                        if (a.R) {
+                        if (!RES && a.R) {
                             const float* Rp = a.R + static_cast<size_t>(rbase) * a.ldr + col;
                             float res[32];
 #pragma unroll
@@ -522,19 +549,21 @@ cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStre
     if (a.ksplit < 1 || (a.ksplit > 1 && !a.part)) return cudaErrorInvalidValue;
     const size_t smem = kGemmStages * kPairBytes + kGemmLoBufs * kOpTileBytes + 4 * 32 * 33 * 4 +
                         (2 * kGemmStages + kGemmLoBufs + 4) * 8 + 16 + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool res = a.R && a.ksplit == 1;
+    auto kern = res ? gemm_tf32x3_kernel<true> : gemm_tf32x3_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // The warpgroups' register split must fit in what the CTA is launched
     // with (otherwise the epilogue's setmaxnreg.inc could never be granted).
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
+    static int launch_regs[2] = {-1, -1};
+    if (launch_regs[res] < 0) {
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm_tf32x3_kernel);
+        e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
-        launch_regs = fa.numRegs;
+        launch_regs[res] = fa.numRegs;
     }
-    if (kGemmThreads * launch_regs < 128 * (kGemmRegsSmall + 2 * kGemmRegsConv + kGemmRegsEpi))
+    if (kGemmThreads * launch_regs[res] < 128 * (kGemmRegsSmall + 2 * kGemmRegsConv + kGemmRegsEpi))
         return cudaErrorInvalidConfiguration;
     // persistent: one CTA per SM (shared memory allows no more), each walking
     // its share of the output tiles
@@ -545,7 +574,7 @@ cudaError_t launch_gemm_tf32x3(const GemmMaps& maps, const GemmArgs& a, cudaStre
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(std::min<long long>(ntiles, std::max(nsm, 1)));
-    gemm_tf32x3_kernel<<<grid, kGemmThreads, smem, st>>>(maps, a);
+    kern<<<grid, kGemmThreads, smem, st>>>(maps, a);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.ksplit == 1) return e;
     const size_t total = static_cast<size_t>(a.M) * a.N;
